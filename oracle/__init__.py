@@ -1,0 +1,147 @@
+"""CPU oracle for ragged paged attention -- TEST INFRASTRUCTURE ONLY.
+
+The plain definition of the attention step that the GPU library is checked
+against (see ``rpa_oracle.cpp`` for the definition and its sources).  Only the
+test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may
+import this package.  It shares no code with ``ragged_paged_attention_rpa_gb300``
+and imports nothing from it.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rpa_oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle_rpa.so")
+
+_libs = {}
+
+CXXFLAGS = ["-O2", "-std=c++17", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC"]
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile the oracle source into a shared library (default: next to it)."""
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    tmp = out + ".tmp.%d" % os.getpid()
+    subprocess.run(["g++"] + CXXFLAGS + ["-o", tmp, src], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _load(lib_path=None):
+    """Load the oracle library (``lib_path`` selects another build of it)."""
+    key = lib_path or _LIB
+    if key not in _libs:
+        lib = ctypes.CDLL(build() if lib_path is None else lib_path)
+        i32, i64, dbl, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+        common = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, i32, vp, vp, vp, i32,
+                  i32, i32, i32, i32, i32, dbl]
+        lib.rpa_oracle_rows.argtypes = common + [vp, i64, vp, vp, ctypes.c_int]
+        lib.rpa_oracle_rows.restype = ctypes.c_int
+        lib.rpa_oracle_prow.argtypes = common + [i64, vp, vp, vp]
+        lib.rpa_oracle_prow.restype = ctypes.c_int
+        lib.rpa_oracle_round_bf16.argtypes = [vp, vp, i64]
+        lib.rpa_oracle_round_bf16.restype = None
+        _libs[key] = lib
+    return _libs[key]
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _as_inputs(q, k_pages, v_pages):
+    """Accept uint16 arrays (bf16 bit patterns) or float32 arrays."""
+    arrs = [np.ascontiguousarray(x) for x in (q, k_pages, v_pages)]
+    dt = arrs[0].dtype
+    if any(a.dtype != dt for a in arrs):
+        raise TypeError("q, k_pages and v_pages must share a dtype")
+    if dt == np.uint16:
+        return 0, arrs
+    if dt == np.float32:
+        return 1, arrs
+    raise TypeError("inputs must be uint16 (bf16 bits) or float32, got %s" % dt)
+
+
+def _meta(page_table, cu_q_lens, kv_lens, window):
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    cu = np.ascontiguousarray(cu_q_lens, dtype=np.int32)
+    kl = np.ascontiguousarray(kv_lens, dtype=np.int32)
+    win = None if window is None else np.ascontiguousarray(window, dtype=np.int32)
+    return pt, cu, kl, win
+
+
+def attention(q, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window,
+              sm_scale, rows=None, precision=32, threads=0, with_bf16=False,
+              lib_path=None):
+    """Run the oracle.
+
+    q: [total_q, Hq, D]; k_pages/v_pages: [num_pages, P, Hkv, D], as uint16 bf16
+    bits or float32.  page_table: [num_seqs, max_pages_per_seq] int32.
+    window: None, or int32 [num_seqs] (<= 0: full causal).
+    rows: None for every row, else int64 indices r = token * Hq + head.
+    Returns float64 [n_rows, D] (and the bf16-rounded uint16 copy if asked).
+    """
+    lib = _load(lib_path)
+    in_dtype, (q, k, v) = _as_inputs(q, k_pages, v_pages)
+    total_q, hq, d = q.shape
+    num_pages, p, hkv, d2 = k.shape
+    assert d2 == d and v.shape == k.shape
+    pt, cu, kl, win = _meta(page_table, cu_q_lens, kv_lens, window)
+    num_seqs = kl.shape[0]
+    assert cu.shape[0] == num_seqs + 1 and pt.shape[0] == num_seqs
+    if rows is None:
+        n = total_q * hq
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n = rows_arr.shape[0]
+    out = np.empty((n, d), dtype=np.float64)
+    out16 = np.empty((n, d), dtype=np.uint16) if with_bf16 else None
+    rc = lib.rpa_oracle_rows(precision, in_dtype, _ptr(q), _ptr(k), _ptr(v), _ptr(pt),
+                             pt.shape[1], _ptr(cu), _ptr(kl), _ptr(win), num_seqs, hq,
+                             hkv, d, p, num_pages, float(sm_scale), _ptr(rows_arr), n,
+                             _ptr(out), _ptr(out16), threads)
+    if rc != 0:
+        raise ValueError("oracle rejected the problem (code %d)" % rc)
+    return (out, out16) if with_bf16 else out
+
+
+def softmax_row(q, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window,
+                sm_scale, row, precision=32, lib_path=None):
+    """Normalised softmax probabilities of one output row over its visible keys.
+
+    Returns (p, lo, hi): p[j - lo] for visible keys lo..hi inclusive.
+    """
+    lib = _load(lib_path)
+    in_dtype, (q, k, v) = _as_inputs(q, k_pages, v_pages)
+    total_q, hq, d = q.shape
+    num_pages, p_sz, hkv, _ = k.shape
+    pt, cu, kl, win = _meta(page_table, cu_q_lens, kv_lens, window)
+    num_seqs = kl.shape[0]
+    buf = np.zeros(max(1, int(kl.max()) if num_seqs else 1), dtype=np.float64)
+    lo = np.zeros(1, dtype=np.int64)
+    hi = np.zeros(1, dtype=np.int64)
+    rc = lib.rpa_oracle_prow(precision, in_dtype, _ptr(q), _ptr(k), _ptr(v), _ptr(pt),
+                             pt.shape[1], _ptr(cu), _ptr(kl), _ptr(win), num_seqs, hq,
+                             hkv, d, p_sz, num_pages, float(sm_scale), int(row),
+                             _ptr(buf), _ptr(lo), _ptr(hi))
+    if rc != 0:
+        raise ValueError("oracle rejected the problem (code %d)" % rc)
+    return buf[: int(hi[0] - lo[0]) + 1].copy(), int(lo[0]), int(hi[0])
+
+
+def round_bf16(x):
+    """float32 -> bf16 bit patterns (uint16), round to nearest even."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib.rpa_oracle_round_bf16(_ptr(x), _ptr(out), x.size)
+    return out
