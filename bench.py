@@ -1,0 +1,507 @@
+#!/usr/bin/env python
+"""Benchmark of ragged paged attention (librpa) on one GB300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
+    python bench.py --impl reference ...      # the CPU oracle as the reference arm
+
+A step is one rpa_forward over one seeded synthetic batch (every kernel of the
+hot path for that batch: split-KV decode + log-sum-exp combine for decode
+sequences, prefill for the rest), with q, the KV pages and the metadata
+resident in HBM and the plan built once for the batch, as a serving step
+reuses one plan for every layer.  L2 is flushed (a 256 MiB write) before every
+timed step; each step is bracketed by CUDA events on the launching stream.
+The host enqueues the timed loop behind a GPU sleep so that launch latency does
+not leak into the device timing.
+
+The default workload is the decode batch: 128 sequences with one query each,
+KV lengths uniform in [128, 2048], 8 query heads sharing one KV head of
+dimension 256, 128-token pages from a shuffled pool of 4096.
+
+Besides `value` (device-timed query tokens/s) the JSON line carries:
+  e2e        the same metric through the public API with host buffers: per step
+             the pinned host->device copy of q and the metadata, rpa_plan on the
+             host metadata, rpa_forward, and the device->host copy of out (the
+             KV pages are the device-resident cache);
+  roofline   the dominant kernel's algorithmic bytes (or flops) per launch over
+             its average launch time, measured with library trace events;
+  cpu_baseline  the CPU oracle timed on this host's cores on a bounded sample.
+With torchrun (N > 1) every rank runs an independent replica (the path has no
+exchange step); the timing is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention tokens/s and % roofline (TFLOP/s prefill, HBM GB/s decode) on 1 GB300"
+NOMINAL_TFLOPS = 2250.0   # the roofline constants the metric is quoted against
+NOMINAL_GBS = 8000.0
+FALLBACK_GBS = 6800.0
+FALLBACK_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------- workload
+
+
+def algorithmic_counts(b):
+    """Visible (query, key) pairs, flops and bytes of one step.
+
+    Pairs: for query i of sequence s at pos = L - q_len + i, keys
+    max(0, pos - W + 1) .. pos.  FLOPs = 4 * D * Hq * pairs (QK^T and PV).
+    Bytes: each visible KV token of each KV head once (K and V), q read once,
+    out written once, plus the page-table entries of visible pages and the
+    per-sequence metadata.  Counted from the realised lengths.
+    """
+    esz = 2 if b.dtype == "bf16" else 4
+    hq, hkv, d, p = b.num_q_heads, b.num_kv_heads, b.head_dim, b.page_size
+    pairs = kv_tokens = pages = 0
+    for s in range(b.num_seqs):
+        ql = int(b.cu_q_lens[s + 1] - b.cu_q_lens[s])
+        if ql == 0:
+            continue
+        L = int(b.kv_lens[s])
+        w = 0 if b.window is None else int(b.window[s])
+        pos = np.arange(L - ql, L, dtype=np.int64)
+        lo = np.maximum(0, pos - w + 1) if w > 0 else np.zeros_like(pos)
+        pairs += int((pos - lo + 1).sum())
+        first = int(lo[0])
+        kv_tokens += L - first
+        pages += (L - 1) // p - first // p + 1
+    flops = 4.0 * d * hq * pairs
+    meta = (2 * b.num_seqs + 1 + (b.num_seqs if b.window is not None else 0)) * 4
+    byts = (kv_tokens * hkv * d * 2 * esz + 2 * b.total_q * hq * d * esz + pages * 4 + meta)
+    return dict(pairs=pairs, kv_tokens=kv_tokens, flops=flops, bytes=float(byts))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+    except (OSError, ValueError):
+        return dict(hbm_gbs=FALLBACK_GBS, bf16_tflops=FALLBACK_TFLOPS,
+                    bf16_tflops_sustained=1700.0, source="fallback")
+
+    def num(*keys):
+        for k in keys:
+            v = pk.get(k)
+            if isinstance(v, (int, float)):
+                return float(v)
+            if isinstance(v, dict):
+                for kk in ("value", "gbs", "tflops", "median", "max"):
+                    if isinstance(v.get(kk), (int, float)):
+                        return float(v[kk])
+        return None
+
+    hbm = num("hbm_gbs", "hbm_copy_gbs", "hbm")
+    tf = num("bf16_tflops", "bf16_tflops_burst")
+    tfs = num("bf16_tflops_sustained")
+    return dict(hbm_gbs=hbm or FALLBACK_GBS, bf16_tflops=tf or FALLBACK_TFLOPS,
+                bf16_tflops_sustained=tfs or tf or 1700.0,
+                source="measured" if hbm else "fallback")
+
+
+def profile_traffic(kernel: str, workload: str, src_file: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when absent
+    or taken on a different version of the kernel source."""
+    path = os.path.join(ROOT, "profiles", "%s.%s.txt" % (kernel, workload))
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    kv = {}
+    for ln in lines:
+        if ":" in ln and not ln.startswith(" "):
+            k, v = ln.split(":", 1)
+            kv[k.strip()] = v.strip()
+    want = hashlib.sha256(open(os.path.join(ROOT, src_file), "rb").read()).hexdigest()[:16]
+    if kv.get("source_sha256_16") != want:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons) while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        time.sleep(0.25)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO("\n".join(self.lines))):
+            if len(row) < 7:
+                continue
+            try:
+                sm.append(float(row[0]))
+                mx.append(float(row[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, row[3:7]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+
+def oracle_sample_rows(b, n_tokens, start=0):
+    """Rows (all heads) of n_tokens query tokens, cycling through the batch."""
+    toks = (start + np.arange(n_tokens)) % b.total_q
+    return (toks[:, None] * b.num_q_heads + np.arange(b.num_q_heads)[None, :]).reshape(-1)
+
+
+def cpu_oracle_rate(b, seconds: float, threads: int):
+    """Query tokens/s of the CPU oracle (fp32) on this host: whole query tokens
+    (every head) taken round-robin from the batch until `seconds` have passed."""
+    import oracle
+    oracle.build()
+    done = 0
+    t0 = time.perf_counter()
+    chunk = max(1, min(b.total_q, 64))
+    while True:
+        rows = oracle_sample_rows(b, chunk, done)
+        oracle.attention(b.q, b.k_pages, b.v_pages, b.page_table, b.cu_q_lens, b.kv_lens,
+                         b.window, b.sm_scale, rows=rows, precision=32, threads=threads)
+        done += chunk
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return done / el, done, el
+
+
+# ----------------------------------------------------------------- main
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["rpa", "reference"], default="rpa")
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "tiny_prefill", "swa_prefill", "causal_prefill", "mixed"])
+    ap.add_argument("--seed", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--q-block", type=int, default=0)
+    ap.add_argument("--kv-split", type=int, default=0)
+    return ap.parse_args()
+
+
+def make_workload(args):
+    from ragged_paged_attention_rpa_gb300 import workloads
+    fn = workloads.WORKLOADS[args.workload]
+    return fn() if args.seed is None else fn(seed=args.seed)
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+    return world, rank, local, pg
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle, as it stands, on this host's cores."""
+    if rank != 0:
+        return
+    b = make_workload(args)
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    per_step = 1                      # query tokens (all heads) per reference step
+    for w in range(args.warmup):
+        rows = oracle_sample_rows(b, per_step, w)
+        oracle.attention(b.q, b.k_pages, b.v_pages, b.page_table, b.cu_q_lens, b.kv_lens,
+                         b.window, b.sm_scale, rows=rows, precision=32, threads=cores)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        rows = oracle_sample_rows(b, per_step, args.warmup + k)
+        oracle.attention(b.q, b.k_pages, b.v_pages, b.page_table, b.cu_q_lens, b.kv_lens,
+                         b.window, b.sm_scale, rows=rows, precision=32, threads=cores)
+    el = time.perf_counter() - t0
+    value = args.steps * per_step / el
+    sample = ("%d query tokens (all %d heads) of the %s batch, one per step, "
+              "round-robin" % (args.steps * per_step, b.num_q_heads, b.name))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": b.name, "oracle": "C++ CPU oracle, fp32 accumulation"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local, dist = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    from ragged_paged_attention_rpa_gb300 import binding, build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    build.build()
+    b = make_workload(args)
+    counts = algorithmic_counts(b)
+    db = binding.Batch(b)
+    plan = db.plan(q_block=args.q_block, kv_split=args.kv_split)
+    info = plan.info()
+    ws = binding.alloc_workspace(plan)
+    fwd = db.call(plan, ws)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    flushes = [0]
+
+    def flush_l2():
+        flushes[0] += 1
+        flush.fill_(flushes[0] & 0x7F)
+
+    # Warm-up (untimed).
+    for _ in range(max(3, args.warmup)):
+        flush_l2()
+        fwd()
+    torch.cuda.synchronize()
+    if binding.rpa_get_device_error(ws) != 0:
+        raise SystemExit("device error word set during warm-up")
+
+    # Timed region: K steps, each bracketed by events; enqueued behind a sleep.
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    with ClockSampler(gpu_index) as clocks:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(int(2e6))
+        for k in range(K):
+            flush_l2()
+            ev[k][0].record(stream)
+            fwd()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+    step_ms = [a.elapsed_time(e) for a, e in ev]
+    total_ms = float(sum(step_ms))
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if binding.rpa_get_device_error(ws) != 0:
+        raise SystemExit("device error word set during the timed region")
+
+    # Kernel durations from the library's trace events (a separate pass of the
+    # same loop, so the events do not touch the headline timing).
+    n_trace = min(K, 500)
+    binding.rpa_trace_begin(8 * n_trace)
+    torch.cuda._sleep(int(2e6))
+    for _ in range(n_trace):
+        flush_l2()
+        fwd()
+    torch.cuda.synchronize()
+    recs = binding.rpa_trace_end(8 * n_trace)
+    per_kernel = {}
+    for name, ms in recs:
+        per_kernel.setdefault(name, []).append(ms)
+    launches_per_step = len(recs) / n_trace
+    kernels = {k: {"launches_per_step": len(v) / n_trace, "avg_us": 1e3 * statistics.mean(v)}
+               for k, v in per_kernel.items()}
+
+    # End to end through the public API with host buffers.
+    e2e = run_e2e(args, b, db, plan, flush_l2, binding, torch)
+
+    peaks = load_peaks()
+    tokens = b.total_q
+    ms_per_step = total_ms / K
+    value = world * tokens * K / (total_ms / 1e3)
+    decode_heavy = info["num_prefill_seqs"] == 0 or args.workload in ("decode", "mixed")
+    dom = max(kernels, key=lambda k: kernels[k]["avg_us"] * kernels[k]["launches_per_step"])
+    dom_us = kernels[dom]["avg_us"]
+    if decode_heavy:
+        achieved = counts["bytes"] / (dom_us * 1e-6) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak}
+        src = {"decode_split": "ragged_paged_attention_rpa_gb300/csrc/decode.cu",
+               "simt": "ragged_paged_attention_rpa_gb300/csrc/simt.cu"}.get(
+                   dom, "ragged_paged_attention_rpa_gb300/csrc/decode.cu")
+    else:
+        achieved = counts["flops"] / (dom_us * 1e-6) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak}
+        src = {"prefill_tc": "ragged_paged_attention_rpa_gb300/csrc/prefill_tc.cu",
+               "simt": "ragged_paged_attention_rpa_gb300/csrc/simt.cu"}.get(
+                   dom, "ragged_paged_attention_rpa_gb300/csrc/prefill_tc.cu")
+    roof["kernel"] = dom
+    roof["peak_source"] = "of %s (%s)" % (peaks["source"], "MEASURED_PEAKS.json"
+                                          if peaks["source"] == "measured" else
+                                          "6.8 TB/s, 1.9 PFLOP/s")
+    roof["traffic"] = profile_traffic(dom, args.workload, src)
+    step_s = ms_per_step / 1e3
+    nominal_frac = max(counts["flops"] / (NOMINAL_TFLOPS * 1e12),
+                       counts["bytes"] / (NOMINAL_GBS * 1e9)) / step_s
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = len(os.sched_getaffinity(0))
+        rate, n_tok, el = cpu_oracle_rate(b, args.cpu_seconds, cores)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": "%d query tokens (all %d heads) of the %s batch, round-robin, "
+                         "%.1f s" % (n_tok, b.num_q_heads, b.name, el)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if b.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": b.name, "seed": b.seed,
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "plan": info},
+        "achieved_gbs": counts["bytes"] / step_s / 1e9,
+        "achieved_tflops": counts["flops"] / step_s / 1e12,
+        "roofline_frac_nominal": nominal_frac,
+        "algorithmic": counts,
+        "kernels": kernels,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(round(launches_per_step * K)),
+        "clocks": clocks.summary(),
+        "step_ms_p50": statistics.median(step_ms),
+        "step_ms_min": min(step_ms),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, b, db, plan_dev, flush_l2, binding, torch):
+    """Per step: pinned H2D of q + metadata, rpa_plan on host metadata,
+    rpa_forward, D2H of out; timed with events around the whole sequence."""
+    stream = torch.cuda.current_stream()
+    hq = torch.from_numpy(np.ascontiguousarray(b.q)).pin_memory()
+    host_meta = [np.ascontiguousarray(x) for x in (b.page_table, b.cu_q_lens, b.kv_lens)]
+    if b.window is not None:
+        host_meta.append(np.ascontiguousarray(b.window))
+    hmeta = [torch.from_numpy(x).pin_memory() for x in host_meta]
+    dq = torch.empty(hq.shape, dtype=torch.int16 if b.dtype == "bf16" else torch.float32,
+                     device="cuda")
+    dmeta = [torch.empty(x.shape, dtype=torch.int32, device="cuda") for x in hmeta]
+    hout = torch.empty(tuple(db.out.shape), dtype=db.out.dtype).pin_memory()
+    qv = dq.view(torch.bfloat16) if b.dtype == "bf16" else dq
+    win_d = dmeta[3] if b.window is not None else None
+    ws = binding.alloc_workspace(plan_dev)
+    h2d = hq.numel() * hq.element_size() + sum(x.numel() * 4 for x in hmeta)
+    d2h = hout.numel() * hout.element_size()
+    n = args.e2e_steps
+    times = []
+    for k in range(n + 3):
+        flush_l2()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dq.copy_(hq.view(dq.dtype), non_blocking=True)
+        for d, h in zip(dmeta, hmeta):
+            d.copy_(h, non_blocking=True)
+        plan = binding.rpa_plan(b.cu_q_lens, b.kv_lens, b.window, b.num_q_heads,
+                                b.num_kv_heads, b.head_dim, b.page_size,
+                                b.max_pages_per_seq, b.num_pages,
+                                dtype=db.dtype)
+        if plan.workspace_bytes > ws.numel():
+            raise RuntimeError("workspace too small for the per-step plan")
+        binding.rpa_forward(qv, db.k_pages, db.v_pages, dmeta[0], dmeta[1], dmeta[2], win_d,
+                            b.sm_scale, db.out, plan, ws)
+        hout.copy_(db.out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if k >= 3:
+            times.append(e0.elapsed_time(e1))
+    ms = statistics.mean(times)
+    return {"value": b.total_q / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "includes": "H2D q+metadata (pinned), rpa_plan, rpa_forward, D2H out"}
+
+
+if __name__ == "__main__":
+    main()

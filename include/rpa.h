@@ -1,0 +1,230 @@
+/*
+ * librpa: ragged paged attention on one NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (sources named by page title and section):
+ *
+ *  - "TPU Deep Dive" slides, chapter 8, "Continuous batching with static
+ *    shapes": a serving step flattens every query token of every sequence into
+ *    one array, and per-sequence metadata carries the ragged structure.  Here
+ *    that is q[total_q, Hq, D] with cu_q_lens[num_seqs + 1] (prefix sums of the
+ *    per-sequence query counts) and kv_lens[num_seqs].
+ *  - Same deck, chapter 8, "KV cache layout", and "Pallas kernel / vLLM on TPU
+ *    ... 19,511 tokens per second", section "Strategy 3": the KV cache is
+ *    paged in fixed-size blocks (128 tokens there); each sequence reaches its
+ *    blocks through a page table.  Here k_pages / v_pages are
+ *    [num_pages, page_size, Hkv, D] and page_table is
+ *    [num_seqs, max_pages_per_seq] int32 holding physical page ids.
+ *  - "Chasing speed of light on TPU v6e", section "Attention" and footnote 5:
+ *    the result is exact softmax attention over every key a query may see;
+ *    sliding-window layers let a key be seen by the W queries that follow it
+ *    (itself included).  Footnote 6: softmax accumulators are fp32.
+ *  - "Pallas kernel / vLLM on TPU ...", section "Strategy 3": several query
+ *    heads share one KV head (GQA/MQA); query head h reads KV head
+ *    h / (Hq / Hkv).
+ *
+ * For sequence s with q_len = cu_q_lens[s+1] - cu_q_lens[s] and L = kv_lens[s],
+ * query i (token t = cu_q_lens[s] + i) sits at position pos = L - q_len + i: the
+ * new tokens are the last q_len entries of the cache, already written there by
+ * the caller.  Key j is visible iff j <= pos and, when window[s] > 0,
+ * pos - j < window[s].  For every query head h:
+ *     out[t][h] = sum_j softmax_j(sm_scale * q[t][h] . k_j) v_j
+ * accumulated in fp32 and stored in the output dtype (bf16: round to nearest
+ * even).
+ *
+ * Ownership and threading.  The caller owns every device buffer (q, pages,
+ * metadata, out, workspace) and the CUDA stream.  rpa_forward allocates no
+ * device memory, never synchronises, and enqueues its work on `stream` only.
+ * A plan is a host object owned by the library between rpa_plan and
+ * rpa_plan_destroy; it is read-only after creation, so one plan may serve many
+ * rpa_forward calls (for instance every layer of a model step).  Two calls
+ * that share a workspace must not overlap on the GPU.
+ *
+ * Errors.  Every entry point returns an rpa_status_t.  Shapes, dtypes,
+ * pointer alignment and the plan/argument match are checked on the host before
+ * anything is enqueued; a failed check enqueues nothing.  Problems only the GPU
+ * can see (a page id outside [0, num_pages), lengths that disagree with the
+ * plan) are never trapped: the kernel skips the bad access, writes a code into
+ * the workspace error word and carries on; rpa_get_device_error reads it.
+ */
+#ifndef RPA_H_
+#define RPA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that this header needs no CUDA
+ * header.  NULL means the legacy default stream. */
+typedef struct CUstream_st* rpa_stream_t;
+
+typedef int32_t rpa_status_t;
+enum {
+  RPA_OK = 0,
+  RPA_ERR_INVALID_ARG = -1,          /* null pointer, bad shape or metadata   */
+  RPA_ERR_UNSUPPORTED = -2,          /* head_dim / page_size / dtype / ratio  */
+  RPA_ERR_WORKSPACE_TOO_SMALL = -3,  /* workspace_bytes below the plan's need */
+  RPA_ERR_CUDA = -4,                 /* a CUDA runtime call failed            */
+  RPA_ERR_DEVICE = -5,               /* the device error word is set          */
+  RPA_ERR_PLAN_MISMATCH = -6         /* forward arguments differ from plan's  */
+};
+
+/* Element types of q, k_pages, v_pages and out (all four share one). */
+enum { RPA_DTYPE_BF16 = 0, RPA_DTYPE_F32 = 1 };
+
+/* Codes written into the workspace error word by the kernels. */
+enum {
+  RPA_DEVERR_NONE = 0,
+  RPA_DEVERR_PAGE_ID = 1,    /* a page-table entry outside [0, num_pages)       */
+  RPA_DEVERR_LENGTHS = 2,    /* device lengths disagree with the plan's copies  */
+  RPA_DEVERR_PLAN = 3,       /* the work list in the workspace is not this plan */
+  RPA_DEVERR_TIMEOUT = 4     /* a bounded wait inside a kernel gave up          */
+};
+
+/* Kernel paths a plan may use. */
+enum {
+  RPA_PATH_AUTO = 0,   /* tensor-core prefill + split-KV decode where supported */
+  RPA_PATH_SIMT = 1,   /* plain fp32 CUDA-core kernel for every sequence        */
+  RPA_PATH_TC = 2      /* tensor-core paths; RPA_ERR_UNSUPPORTED if impossible  */
+};
+
+/* Optional knobs for rpa_plan.  Zero-initialise and set struct_size. */
+typedef struct rpa_plan_options {
+  int32_t struct_size;      /* sizeof(rpa_plan_options)                         */
+  int32_t path;             /* RPA_PATH_*                                       */
+  int32_t q_block;          /* prefill query block, tokens (0: choose)          */
+  int32_t kv_split;         /* decode split length, tokens (0: choose)          */
+  int32_t num_sms;          /* SMs to plan for (0: ask the current device, else 152) */
+} rpa_plan_options;
+
+/* What a plan chose; filled by rpa_plan_get_info. */
+typedef struct rpa_plan_info {
+  int32_t path;             /* RPA_PATH_SIMT or RPA_PATH_TC                     */
+  int32_t num_decode_seqs;  /* sequences with q_len == 1                        */
+  int32_t num_prefill_seqs; /* sequences with q_len > 1                         */
+  int32_t q_block;          /* prefill query block in tokens                    */
+  int32_t kv_split;         /* decode split length in tokens                    */
+  int32_t max_splits;       /* largest split count of any decode sequence       */
+  int32_t num_prefill_items;/* (sequence, query block, kv head) work items      */
+  int32_t prefill_ctas;     /* persistent prefill CTAs launched                 */
+  int64_t workspace_bytes;  /* bytes rpa_forward needs                          */
+} rpa_plan_info;
+
+typedef struct rpa_plan rpa_plan_t;
+
+/*
+ * Build a plan from HOST copies of the ragged metadata (the scheduler).
+ *
+ * It classifies each sequence as decode (q_len == 1) or prefill (q_len > 1;
+ * q_len == 0 contributes nothing), picks the decode split length and the
+ * prefill query block, orders the prefill work items longest first over a
+ * persistent grid, and sizes the workspace.  Host only: it launches nothing
+ * and touches no device memory.
+ *
+ *   cu_q_lens_host [num_seqs+1], kv_lens_host [num_seqs]: host int32 arrays
+ *       (cu_q_lens_host[0] == 0, non-decreasing; q_len <= kv_len).
+ *   window_host: host int32 [num_seqs] (<= 0: full causal), or NULL (all
+ *       full causal).  It must match what is later passed to rpa_forward.
+ *   num_q_heads % num_kv_heads == 0.  head_dim in {64, 128, 256}; page_size
+ *       a power of two in [1, 256] (the tensor-core prefill needs >= 16);
+ *       dtype RPA_DTYPE_BF16 or RPA_DTYPE_F32 (F32 always takes the SIMT path,
+ *       the fp32 debug build).
+ *   max_pages_per_seq: row length of the page table; every sequence needs
+ *       ceil(kv_len / page_size) <= max_pages_per_seq.
+ *   num_pages: pages in the pool (page ids must lie in [0, num_pages)).
+ *   opts: NULL for defaults.
+ *   *plan receives a new plan (free with rpa_plan_destroy); *workspace_bytes
+ *       (may be NULL) the device workspace rpa_forward needs.
+ * Returns RPA_OK, RPA_ERR_INVALID_ARG or RPA_ERR_UNSUPPORTED; on error *plan
+ * is set to NULL.
+ */
+rpa_status_t rpa_plan(rpa_plan_t** plan, const int32_t* cu_q_lens_host,
+                      const int32_t* kv_lens_host, const int32_t* window_host,
+                      int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t page_size, int32_t max_pages_per_seq,
+                      int32_t num_pages, int32_t dtype, const rpa_plan_options* opts,
+                      size_t* workspace_bytes);
+
+/* Free a plan (NULL is a no-op).  Must not race with rpa_forward on it. */
+rpa_status_t rpa_plan_destroy(rpa_plan_t* plan);
+
+/* Copy out what the plan chose. */
+rpa_status_t rpa_plan_get_info(const rpa_plan_t* plan, rpa_plan_info* info);
+
+/*
+ * Ragged paged attention for the batch the plan was built for.
+ *
+ * Device pointers (all on the current device, contiguous, row-major):
+ *   q        [total_q, num_q_heads, head_dim]            dtype, 16-B aligned
+ *   k_pages, v_pages [num_pages, page_size, num_kv_heads, head_dim]
+ *                                                       dtype, 128-B aligned
+ *   page_table [num_seqs, max_pages_per_seq] int32; entries past a sequence's
+ *            last page are never read
+ *   cu_q_lens [num_seqs+1] int32, kv_lens [num_seqs] int32: the same values
+ *            the plan was built from
+ *   window   [num_seqs] int32 (<= 0: full causal) or NULL (all full causal);
+ *            NULL-ness and values must match the plan's window_host
+ *   out      [total_q, num_q_heads, head_dim]            dtype, 16-B aligned
+ *   workspace: at least the plan's workspace_bytes, 256-B aligned; scratch
+ *            owned by the call while it runs (the error word lives at its
+ *            start and is sticky until rpa_get_device_error clears it)
+ * The scalar arguments must equal the plan's, else RPA_ERR_PLAN_MISMATCH.
+ * sm_scale multiplies q.k before the softmax (1/sqrt(head_dim) is usual).
+ * Enqueues at most a small host-to-device copy of the plan's work list and
+ * three kernels on `stream`; returns without waiting for them.
+ */
+rpa_status_t rpa_forward(const void* q, const void* k_pages, const void* v_pages,
+                         const int32_t* page_table, const int32_t* cu_q_lens,
+                         const int32_t* kv_lens, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                         const int32_t* window, float sm_scale, void* out,
+                         rpa_stream_t stream, const rpa_plan_t* plan, void* workspace,
+                         size_t workspace_bytes);
+
+/*
+ * Read the device error word at the start of `workspace` after everything
+ * enqueued on `stream` so far (this call synchronises `stream`), store it in
+ * *err (an RPA_DEVERR_* code) and reset it to RPA_DEVERR_NONE.
+ */
+rpa_status_t rpa_get_device_error(void* workspace, rpa_stream_t stream, int32_t* err);
+
+/* Zero the workspace error word (enqueued on `stream`, no synchronisation). */
+rpa_status_t rpa_clear_device_error(void* workspace, rpa_stream_t stream);
+
+/*
+ * Kernel tracing (off by default).  Between rpa_trace_begin and rpa_trace_end,
+ * every rpa_forward call records a CUDA event on its stream before its first
+ * kernel and after each kernel it launches, so that the device time of each
+ * launch can be read back.  Tracing state is process-wide and not thread-safe;
+ * tracing adds one event record per launch to the stream.
+ *
+ * rpa_trace_begin: start recording up to `capacity` launches (1..65536).
+ * rpa_trace_end: synchronise on the recorded events, write up to *count
+ *     records (kernel id, device milliseconds) to `records`, set *count to the
+ *     number written, and stop tracing.  Launches beyond `capacity` are not
+ *     recorded.
+ */
+enum {
+  RPA_KERNEL_DECODE_SPLIT = 0,   /* split-KV decode                   */
+  RPA_KERNEL_DECODE_COMBINE = 1, /* log-sum-exp merge of decode splits */
+  RPA_KERNEL_PREFILL_TC = 2,     /* tensor-core prefill               */
+  RPA_KERNEL_SIMT = 3            /* CUDA-core (fp32) path             */
+};
+typedef struct rpa_trace_record {
+  int32_t kernel; /* RPA_KERNEL_* */
+  float ms;       /* device time from the previous mark of the same call */
+} rpa_trace_record;
+
+rpa_status_t rpa_trace_begin(int32_t capacity);
+rpa_status_t rpa_trace_end(rpa_trace_record* records, int32_t* count);
+
+/* A static, human-readable name for a status code. */
+const char* rpa_status_string(rpa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RPA_H_ */

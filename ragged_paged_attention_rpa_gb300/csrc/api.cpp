@@ -1,0 +1,195 @@
+// The C ABI of librpa (include/rpa.h): argument checks, plan objects and the
+// launch sequence of rpa_forward.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "rpa.h"
+#include "rpa_internal.h"
+
+struct rpa_plan {
+  rpa::Plan p;
+};
+
+namespace {
+
+bool is_pow2(int32_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+bool aligned(const void* ptr, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0;
+}
+
+int32_t device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+rpa_status_t rpa_plan(rpa_plan_t** plan, const int32_t* cu_q_lens_host,
+                      const int32_t* kv_lens_host, const int32_t* window_host,
+                      int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t page_size, int32_t max_pages_per_seq,
+                      int32_t num_pages, int32_t dtype, const rpa_plan_options* opts,
+                      size_t* workspace_bytes) {
+  if (plan == nullptr) return RPA_ERR_INVALID_ARG;
+  *plan = nullptr;
+  if (cu_q_lens_host == nullptr || (num_seqs > 0 && kv_lens_host == nullptr))
+    return RPA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      page_size <= 0 || max_pages_per_seq < 0 || num_pages < 0)
+    return RPA_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads != 0) return RPA_ERR_INVALID_ARG;
+  if (dtype != RPA_DTYPE_BF16 && dtype != RPA_DTYPE_F32) return RPA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return RPA_ERR_UNSUPPORTED;
+  if (!is_pow2(page_size) || page_size > 256) return RPA_ERR_UNSUPPORTED;
+  rpa_plan_options o{};
+  o.struct_size = sizeof(rpa_plan_options);
+  if (opts != nullptr) {
+    if (opts->struct_size < static_cast<int32_t>(sizeof(int32_t)) ||
+        opts->struct_size > static_cast<int32_t>(sizeof(rpa_plan_options)))
+      return RPA_ERR_INVALID_ARG;
+    std::memcpy(&o, opts, static_cast<size_t>(opts->struct_size));
+  }
+  if (o.q_block < 0 || o.kv_split < 0 || o.num_sms < 0) return RPA_ERR_INVALID_ARG;
+  rpa_status_t st = rpa::validate_metadata(cu_q_lens_host, kv_lens_host, num_seqs,
+                                           page_size, max_pages_per_seq);
+  if (st != RPA_OK) return st;
+
+  struct rpa_plan* pl = new (std::nothrow) struct rpa_plan();
+  if (pl == nullptr) return RPA_ERR_INVALID_ARG;
+  rpa::Plan& p = pl->p;
+  p.num_seqs = num_seqs;
+  p.hq = num_q_heads;
+  p.hkv = num_kv_heads;
+  p.d = head_dim;
+  p.p = page_size;
+  p.mpps = max_pages_per_seq;
+  p.num_pages = num_pages;
+  p.dtype = dtype;
+  p.has_window = window_host != nullptr;
+  p.total_q = cu_q_lens_host[num_seqs];
+  int32_t sms = o.num_sms;
+  if (sms == 0) sms = device_sm_count();
+  p.num_sms = sms > 0 ? sms : 152;
+  st = rpa::build_schedule(p, cu_q_lens_host, kv_lens_host, window_host, o);
+  if (st != RPA_OK) {
+    delete pl;
+    return st;
+  }
+  *plan = pl;
+  if (workspace_bytes) *workspace_bytes = p.ws_bytes;
+  return RPA_OK;
+}
+
+rpa_status_t rpa_plan_destroy(rpa_plan_t* plan) {
+  delete plan;
+  return RPA_OK;
+}
+
+rpa_status_t rpa_plan_get_info(const rpa_plan_t* plan, rpa_plan_info* info) {
+  if (plan == nullptr || info == nullptr) return RPA_ERR_INVALID_ARG;
+  const rpa::Plan& p = plan->p;
+  info->path = p.path;
+  info->num_decode_seqs = p.num_decode;
+  info->num_prefill_seqs = p.num_prefill;
+  info->q_block = p.q_block;
+  info->kv_split = p.kv_split;
+  info->max_splits = p.max_splits;
+  info->num_prefill_items = static_cast<int32_t>(p.items.size());
+  info->prefill_ctas = p.prefill_ctas;
+  info->workspace_bytes = static_cast<int64_t>(p.ws_bytes);
+  return RPA_OK;
+}
+
+rpa_status_t rpa_forward(const void* q, const void* k_pages, const void* v_pages,
+                         const int32_t* page_table, const int32_t* cu_q_lens,
+                         const int32_t* kv_lens, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                         const int32_t* window, float sm_scale, void* out,
+                         rpa_stream_t stream, const rpa_plan_t* plan, void* workspace,
+                         size_t workspace_bytes) {
+  if (plan == nullptr) return RPA_ERR_INVALID_ARG;
+  const rpa::Plan& p = plan->p;
+  if (num_seqs != p.num_seqs || num_q_heads != p.hq || num_kv_heads != p.hkv ||
+      head_dim != p.d || page_size != p.p || (window != nullptr) != p.has_window)
+    return RPA_ERR_PLAN_MISMATCH;
+  if (workspace == nullptr || !aligned(workspace, 256)) return RPA_ERR_INVALID_ARG;
+  if (workspace_bytes < p.ws_bytes) return RPA_ERR_WORKSPACE_TOO_SMALL;
+  if (p.total_q == 0) return RPA_OK;  // nothing to compute
+  if (q == nullptr || k_pages == nullptr || v_pages == nullptr || page_table == nullptr ||
+      cu_q_lens == nullptr || kv_lens == nullptr || out == nullptr)
+    return RPA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_pages, 128) ||
+      !aligned(v_pages, 128) || !aligned(page_table, 4) || !aligned(cu_q_lens, 4) ||
+      !aligned(kv_lens, 4) || !aligned(window, 4))
+    return RPA_ERR_INVALID_ARG;
+
+  rpa::Args a{q, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window, sm_scale,
+              out, static_cast<unsigned char*>(workspace)};
+  int err = 0;
+  rpa::trace_start(stream);
+  if (p.num_decode > 0 && !p.simt_decode) {
+    err = rpa::launch_decode(p, a, stream);
+    if (err) return RPA_ERR_CUDA;
+  }
+  if (!p.items.empty()) {
+    err = rpa::launch_prefill_tc(p, a, stream);
+    if (err) return RPA_ERR_CUDA;
+  }
+  if (p.simt_decode || p.simt_prefill) {
+    err = rpa::launch_simt(p, a, stream);
+    if (err) return RPA_ERR_CUDA;
+  }
+  return RPA_OK;
+}
+
+rpa_status_t rpa_get_device_error(void* workspace, rpa_stream_t stream, int32_t* err) {
+  if (workspace == nullptr || err == nullptr) return RPA_ERR_INVALID_ARG;
+  int32_t v = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return RPA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RPA_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, 2 * sizeof(int32_t), s) != cudaSuccess)
+    return RPA_ERR_CUDA;
+  *err = v;
+  return v == RPA_DEVERR_NONE ? RPA_OK : RPA_ERR_DEVICE;
+}
+
+rpa_status_t rpa_clear_device_error(void* workspace, rpa_stream_t stream) {
+  if (workspace == nullptr) return RPA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, 2 * sizeof(int32_t), s) != cudaSuccess)
+    return RPA_ERR_CUDA;
+  return RPA_OK;
+}
+
+const char* rpa_status_string(rpa_status_t status) {
+  switch (status) {
+    case RPA_OK: return "RPA_OK";
+    case RPA_ERR_INVALID_ARG: return "RPA_ERR_INVALID_ARG: bad pointer, shape or metadata";
+    case RPA_ERR_UNSUPPORTED: return "RPA_ERR_UNSUPPORTED: shape or dtype not supported";
+    case RPA_ERR_WORKSPACE_TOO_SMALL: return "RPA_ERR_WORKSPACE_TOO_SMALL";
+    case RPA_ERR_CUDA: return "RPA_ERR_CUDA: a CUDA runtime call failed";
+    case RPA_ERR_DEVICE: return "RPA_ERR_DEVICE: a kernel reported an error";
+    case RPA_ERR_PLAN_MISMATCH: return "RPA_ERR_PLAN_MISMATCH: arguments differ from the plan";
+    default: return "unknown rpa status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,95 @@
+// Internal declarations shared by the host API, the scheduler and the kernel
+// launchers of librpa.  Not part of the public interface (include/rpa.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "rpa.h"
+
+namespace rpa {
+
+// Workspace layout: a 256-byte header (error word first), then the decode
+// split partials.  Offsets are multiples of 256 bytes.
+constexpr size_t kHeaderBytes = 256;
+
+// One prefill work item: query block `qb` (of plan.q_block tokens) of
+// sequence `seq`, for KV head `head`.  Ordered longest first in the plan.
+struct PrefillItem {
+  int32_t seq;
+  int32_t qb_head;  // (query block index << 8) | kv head
+};
+
+// Most work items one tensor-core prefill launch carries in its parameters;
+// longer lists are split over several launches.
+constexpr int kMaxItemsPerLaunch = 3072;
+
+struct Plan {
+  // Problem description (checked against every rpa_forward call).
+  int32_t num_seqs = 0, hq = 0, hkv = 0, d = 0, p = 0, mpps = 0, num_pages = 0;
+  int32_t dtype = RPA_DTYPE_BF16;
+  bool has_window = false;
+  int64_t total_q = 0;
+
+  int32_t path = RPA_PATH_SIMT;     // path actually used
+  bool simt_decode = false;          // decode sequences handled by the SIMT kernel
+  bool simt_prefill = false;         // prefill sequences handled by the SIMT kernel
+  int32_t num_sms = 152;
+
+  // Decode (q_len == 1) on the split-KV kernel.
+  int32_t num_decode = 0;
+  int32_t kv_split = 0;   // tokens per split (multiple of 64)
+  int32_t max_splits = 0;
+  int64_t decode_ctas = 0;  // non-empty (seq, split, kv head) CTAs
+
+  // Prefill (q_len > 1).
+  int32_t num_prefill = 0;
+  int32_t q_block = 0;
+  std::vector<PrefillItem> items;  // longest first
+  int32_t prefill_ctas = 0;
+
+  // Workspace.
+  size_t off_partial_o = 0, off_partial_lse = 0, ws_bytes = kHeaderBytes;
+};
+
+// Scheduler (plan.cpp): fills everything but the problem description, which
+// the caller has set and validated.
+rpa_status_t build_schedule(Plan& plan, const int32_t* cu_q_lens, const int32_t* kv_lens,
+                            const int32_t* window, const rpa_plan_options& opts);
+
+// Host-side checks of the metadata (plan.cpp).
+rpa_status_t validate_metadata(const int32_t* cu_q_lens, const int32_t* kv_lens,
+                               int32_t num_seqs, int32_t page_size,
+                               int32_t max_pages_per_seq);
+
+// Arguments every kernel launcher receives.
+struct Args {
+  const void* q;
+  const void* k_pages;
+  const void* v_pages;
+  const int32_t* page_table;
+  const int32_t* cu_q_lens;
+  const int32_t* kv_lens;
+  const int32_t* window;
+  float sm_scale;
+  void* out;
+  unsigned char* workspace;
+};
+
+// Kernel launchers; each returns cudaError_t as int (0 = success).
+int launch_simt(const Plan& plan, const Args& a, void* stream);
+int launch_decode(const Plan& plan, const Args& a, void* stream);
+int launch_prefill_tc(const Plan& plan, const Args& a, void* stream);
+
+// Tracing hooks (trace.cpp): trace_start before a call's first launch,
+// trace_mark after each launch (no-ops unless tracing is on).
+void trace_start(void* stream);
+void trace_mark(int kernel, void* stream);
+
+// Whether the tensor-core prefill supports this shape (prefill_tc.cu).
+bool prefill_tc_supported(int32_t head_dim, int32_t page_size, int32_t group);
+// Whether the split-KV decode supports this shape (decode.cu).
+bool decode_supported(int32_t head_dim, int32_t group);
+
+}  // namespace rpa

@@ -77,7 +77,12 @@ class Batch:
         return np.diff(self.cu_q_lens).astype(np.int32)
 
 
-def _normal(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
+def _normal(rng: np.random.Generator, shape, dtype: str, meta_only: bool = False) -> np.ndarray:
+    if meta_only:
+        # Shape only (zero-stride, no memory): for scheduling tests that never
+        # read the values.
+        return np.broadcast_to(np.zeros((), np.uint16 if dtype == "bf16" else np.float32),
+                               shape)
     x = rng.standard_normal(size=shape, dtype=np.float32)
     if dtype == "f32":
         return x
@@ -91,7 +96,7 @@ def make_batch(q_lens: Sequence[int], kv_lens: Sequence[int], *, num_q_heads: in
                windows: Optional[Sequence[int]] = None, seed: int = 0,
                pool_pages: Optional[int] = None, dtype: str = "bf16",
                sm_scale: Optional[float] = None, name: str = "batch",
-               max_pages_per_seq: Optional[int] = None) -> Batch:
+               max_pages_per_seq: Optional[int] = None, meta_only: bool = False) -> Batch:
     """A ragged batch whose pages are drawn without replacement from a shuffled pool.
 
     Sequence s owns ceil(kv_lens[s] / page_size) pages; its page-table row is
@@ -124,9 +129,9 @@ def make_batch(q_lens: Sequence[int], kv_lens: Sequence[int], *, num_q_heads: in
     cu = np.zeros(len(kv) + 1, dtype=np.int32)
     cu[1:] = np.cumsum(q_lens)
     total_q = int(cu[-1])
-    q = _normal(r_q, (total_q, num_q_heads, head_dim), dtype)
-    k = _normal(r_k, (pool, page_size, num_kv_heads, head_dim), dtype)
-    v = _normal(r_v, (pool, page_size, num_kv_heads, head_dim), dtype)
+    q = _normal(r_q, (total_q, num_q_heads, head_dim), dtype, meta_only)
+    k = _normal(r_k, (pool, page_size, num_kv_heads, head_dim), dtype, meta_only)
+    v = _normal(r_v, (pool, page_size, num_kv_heads, head_dim), dtype, meta_only)
     win = None if windows is None else np.asarray(windows, dtype=np.int32)
     scale = 1.0 / math.sqrt(head_dim) if sm_scale is None else float(sm_scale)
     return Batch(name, q, k, v, table, cu, kv.astype(np.int32), win, scale, seed)
@@ -146,19 +151,19 @@ def tiny_prefill(seed: int = 0) -> Batch:
 
 
 def decode_batch(seed: int = 1, num_seqs: int = 128, lo: int = 128, hi: int = 2048,
-                 pool_pages: int = 4096) -> Batch:
+                 pool_pages: int = 4096, meta_only: bool = False) -> Batch:
     """128 decoding sequences (1 query each), KV length uniform in [128, 2048];
     8 q / 1 kv heads (MQA), D 256; 128-token pages from a shuffled pool of 4096."""
     rng = np.random.default_rng(np.random.SeedSequence([seed, 101]))
     kv = rng.integers(lo, hi + 1, size=num_seqs)
     return make_batch(np.ones(num_seqs, dtype=np.int64), kv, num_q_heads=8,
                       num_kv_heads=1, head_dim=256, page_size=128,
-                      pool_pages=pool_pages, seed=seed,
+                      pool_pages=pool_pages, seed=seed, meta_only=meta_only,
                       name="decode_b%d_l%d-%d_h8kv1_d256_p128" % (num_seqs, lo, hi))
 
 
 def prefill_8k(seed: int = 2, window: int = 1024, tokens: int = 8192,
-               num_q_heads: int = 32, num_kv_heads: int = 16) -> Batch:
+               num_q_heads: int = 32, num_kv_heads: int = 16, meta_only: bool = False) -> Batch:
     """One 8192-token sequence attending causally to itself; 32 q / 16 kv heads,
     D 256, 128-token pages randomly permuted.  window <= 0: global causal."""
     pages = (tokens + 127) // 128
@@ -166,11 +171,12 @@ def prefill_8k(seed: int = 2, window: int = 1024, tokens: int = 8192,
         "_prefill_%d_h%dkv%d_d256_p128" % (tokens, num_q_heads, num_kv_heads)
     return make_batch([tokens], [tokens], num_q_heads=num_q_heads,
                       num_kv_heads=num_kv_heads, head_dim=256, page_size=128,
-                      windows=[window], pool_pages=pages, seed=seed, name=name)
+                      windows=[window], pool_pages=pages, seed=seed, name=name,
+                      meta_only=meta_only)
 
 
 def mixed_batch(seed: int = 4, num_decode: int = 512, num_prefill: int = 4,
-                chunk: int = 2048) -> Batch:
+                chunk: int = 2048, meta_only: bool = False) -> Batch:
     """512 decoding sequences (KV length uniform in [256, 4096]) followed by 4
     chunked-prefill sequences of 2048 new tokens appended to a prior length
     uniform in [0, 4096]; 8 q / 1 kv heads, D 256, 128-token pages, random
@@ -187,14 +193,14 @@ def mixed_batch(seed: int = 4, num_decode: int = 512, num_prefill: int = 4,
     need = int(((kv + 127) // 128).sum())
     return make_batch(ql, kv, num_q_heads=8, num_kv_heads=1, head_dim=256,
                       page_size=128, windows=win, pool_pages=need, seed=seed,
-                      name="mixed_d%d_p%dx%d_h8kv1_d256_p128" % (num_decode, num_prefill,
+                      meta_only=meta_only, name="mixed_d%d_p%dx%d_h8kv1_d256_p128" % (num_decode, num_prefill,
                                                                   chunk))
 
 
 WORKLOADS = {
     "tiny_prefill": tiny_prefill,
     "decode": decode_batch,
-    "swa_prefill": lambda seed=2: prefill_8k(seed=seed, window=1024),
-    "causal_prefill": lambda seed=3: prefill_8k(seed=seed, window=0),
+    "swa_prefill": lambda seed=2, **kw: prefill_8k(seed=seed, window=1024, **kw),
+    "causal_prefill": lambda seed=3, **kw: prefill_8k(seed=seed, window=0, **kw),
     "mixed": mixed_batch,
 }

@@ -1,0 +1,221 @@
+"""GPU parity: librpa (through its C ABI) against the CPU oracle.
+
+Tolerances:
+  * bf16 in/out: max |gpu - oracle| <= 2e-2 and mean |gpu - oracle| <= 2e-3 over
+    the compared outputs, the oracle in fp32 accumulation, unrounded;
+  * fp32 debug build: max |gpu - oracle| / max |oracle| <= 1e-5 (normwise; an
+    elementwise relative bound is meaningless near zero outputs).
+Small cases compare every output; the full-size workloads compare every decode
+row and a fixed sample of prefill rows (first, last and window-edge tokens plus
+seeded random ones), which the oracle computes one by one.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from ragged_paged_attention_rpa_gb300 import binding, build, workloads
+from ragged_paged_attention_rpa_gb300.binding import RPA_PATH_SIMT, RPA_PATH_TC
+
+pytestmark = pytest.mark.gpu
+
+BF16_MAX, BF16_MEAN, F32_NORMWISE = 2e-2, 2e-3, 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build.build()
+
+
+def run_gpu(b, **plan_kw):
+    db = binding.Batch(b)
+    plan = db.plan(**plan_kw)
+    ws = binding.alloc_workspace(plan)
+    out = db.forward(plan, ws)
+    err = binding.rpa_get_device_error(ws)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().reshape(-1, b.head_dim).astype(np.float64), err, plan
+
+
+def oracle_rows(b, rows=None):
+    return oracle.attention(b.q, b.k_pages, b.v_pages, b.page_table, b.cu_q_lens,
+                            b.kv_lens, b.window, b.sm_scale, rows=rows, precision=32)
+
+
+def assert_bf16_close(got, ref, what=""):
+    e = np.abs(got - ref)
+    assert np.isfinite(got).all(), what + ": non-finite output"
+    assert e.max() <= BF16_MAX and e.mean() <= BF16_MEAN, \
+        "%s: max %.3g mean %.3g" % (what, e.max(), e.mean())
+
+
+def sample_rows(b, n_random=512, seed=0):
+    """Every row of decode tokens; for prefill sequences their first and last
+    tokens, tokens at the window edge, and seeded random tokens (all heads)."""
+    hq = b.num_q_heads
+    toks = set()
+    rng = np.random.default_rng(seed)
+    for s in range(b.num_seqs):
+        t0, t1 = int(b.cu_q_lens[s]), int(b.cu_q_lens[s + 1])
+        if t1 - t0 == 0:
+            continue
+        if t1 - t0 == 1:
+            toks.add(t0)
+            continue
+        toks.update([t0, t0 + 1, t1 - 1, t1 - 2])
+        w = 0 if b.window is None else int(b.window[s])
+        if w > 0:
+            L = int(b.kv_lens[s])
+            for pos in (w - 1, w, w + 1, w + 127, 2 * w):
+                t = t0 + pos - (L - (t1 - t0))
+                if t0 <= t < t1:
+                    toks.add(t)
+        toks.update(int(x) for x in rng.integers(t0, t1, size=min(n_random, t1 - t0)))
+    toks = np.array(sorted(toks), dtype=np.int64)
+    return (toks[:, None] * hq + np.arange(hq)[None, :]).reshape(-1)
+
+
+# ---------------------------------------------------------------- small cases
+
+SMALL = [
+    # (q_lens, kv_lens, Hq, Hkv, D, P, windows)
+    ([5, 1, 0, 17, 1, 33], [9, 33, 4, 40, 1, 300], 4, 2, 64, 16, [0, 5, 0, 7, 1, 64]),
+    ([1] * 9, [1, 2, 15, 16, 17, 127, 128, 129, 700], 8, 1, 256, 128, None),
+    ([1] * 6 + [20], [3, 64, 65, 200, 1000, 5, 40], 8, 2, 128, 32, [0, 16, 0, 100, 0, 2, 9]),
+    ([1, 1, 1, 70], [2000, 37, 513, 90], 2, 2, 256, 16, [1000, 0, 64, 0]),
+    ([1, 1, 64, 1], [129, 4097, 64, 1], 16, 2, 64, 64, None),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_small_ragged_bf16(case):
+    ql, kv, hq, hkv, d, p, win = SMALL[case]
+    b = workloads.make_batch(ql, kv, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                             page_size=p, windows=win, pool_pages=None, seed=100 + case)
+    got, err, plan = run_gpu(b)
+    assert err == 0
+    assert_bf16_close(got, oracle_rows(b), "case %d" % case)
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_small_ragged_f32_debug(case):
+    ql, kv, hq, hkv, d, p, win = SMALL[case]
+    b = workloads.make_batch(ql, kv, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                             page_size=p, windows=win, seed=200 + case, dtype="f32")
+    got, err, plan = run_gpu(b)
+    assert err == 0 and plan.info()["path"] == RPA_PATH_SIMT
+    ref = oracle_rows(b)
+    nw = np.abs(got - ref).max() / np.abs(ref).max()
+    assert nw <= F32_NORMWISE, nw
+
+
+def test_simt_path_bf16_matches_oracle():
+    ql, kv, hq, hkv, d, p, win = SMALL[2]
+    b = workloads.make_batch(ql, kv, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                             page_size=p, windows=win, seed=300)
+    got, err, plan = run_gpu(b, path=RPA_PATH_SIMT)
+    assert err == 0 and plan.info()["path"] == RPA_PATH_SIMT
+    assert_bf16_close(got, oracle_rows(b))
+
+
+def test_tiny_prefill_workload():
+    b = workloads.tiny_prefill(seed=0)
+    got, err, _ = run_gpu(b)
+    assert err == 0
+    assert_bf16_close(got, oracle_rows(b), "tiny prefill")
+
+
+def test_empty_batch_is_a_no_op():
+    b = workloads.make_batch([0, 0], [5, 0], num_q_heads=8, num_kv_heads=1, head_dim=256,
+                             page_size=128, seed=1)
+    db = binding.Batch(b)
+    plan = db.plan()
+    ws = binding.alloc_workspace(plan)
+    db.forward(plan, ws)
+    assert binding.rpa_get_device_error(ws) == 0
+
+
+# ---------------------------------------------------------------- decode
+
+
+@pytest.fixture(scope="module")
+def decode_case():
+    b = workloads.decode_batch(seed=1)
+    return b, oracle_rows(b)
+
+
+def test_decode_workload_full(decode_case):
+    b, ref = decode_case
+    got, err, plan = run_gpu(b)
+    assert err == 0 and plan.info()["path"] == RPA_PATH_TC
+    assert_bf16_close(got, ref, "decode")
+
+
+@pytest.mark.parametrize("split", [64, 128, 448, 2048])
+def test_decode_split_invariance(decode_case, split):
+    """The split length changes scheduling, not the result."""
+    b, ref = decode_case
+    got, err, plan = run_gpu(b, kv_split=split)
+    assert err == 0 and plan.info()["kv_split"] == split
+    assert_bf16_close(got, ref, "split %d" % split)
+
+
+def test_decode_simt_and_tc_agree(decode_case):
+    b, ref = decode_case
+    simt, err, _ = run_gpu(b, path=RPA_PATH_SIMT)
+    assert err == 0
+    assert_bf16_close(simt, ref, "simt decode")
+
+
+def test_page_permutation_is_bitwise_invisible():
+    b = workloads.decode_batch(seed=5, num_seqs=32, pool_pages=600)
+    got, _, _ = run_gpu(b)
+    perm = np.random.default_rng(9).permutation(b.num_pages)
+    k2 = np.empty_like(b.k_pages)
+    v2 = np.empty_like(b.v_pages)
+    k2[perm] = b.k_pages
+    v2[perm] = b.v_pages
+    pt2 = np.where(b.page_table >= 0, perm[np.maximum(b.page_table, 0)], -1).astype(np.int32)
+    b2 = workloads.Batch(**{**b.__dict__, "k_pages": k2, "v_pages": v2, "page_table": pt2})
+    got2, _, _ = run_gpu(b2)
+    assert np.array_equal(got, got2)
+
+
+def test_bad_page_id_sets_the_error_word_without_faulting():
+    b = workloads.decode_batch(seed=6, num_seqs=8, pool_pages=160)
+    db = binding.Batch(b)
+    plan = db.plan()
+    ws = binding.alloc_workspace(plan)
+    pt = db.page_table.clone()
+    pt[3, 0] = b.num_pages + 7          # outside the pool: the kernel must skip it
+    binding.rpa_forward(db.q, db.k_pages, db.v_pages, pt, db.cu_q_lens, db.kv_lens,
+                        db.window, b.sm_scale, db.out, plan, ws)
+    assert binding.rpa_get_device_error(ws) == binding.RPA_DEVERR_PAGE_ID
+    # The error word was cleared by the read, and a good call still works.
+    db.forward(plan, ws)
+    assert binding.rpa_get_device_error(ws) == 0
+    got = db.out.float().cpu().numpy().reshape(-1, b.head_dim).astype(np.float64)
+    assert_bf16_close(got, oracle_rows(b))
+
+
+# ---------------------------------------------------------------- prefill, mixed
+
+
+@pytest.mark.parametrize("name", ["swa_prefill", "causal_prefill"])
+def test_prefill_workloads_sampled(name):
+    b = workloads.WORKLOADS[name]()
+    got, err, _ = run_gpu(b)
+    assert err == 0
+    rows = sample_rows(b, n_random=96)
+    assert_bf16_close(got[rows], oracle_rows(b, rows), name)
+
+
+def test_mixed_workload_sampled():
+    b = workloads.mixed_batch(seed=4)
+    got, err, plan = run_gpu(b)
+    assert err == 0
+    rows = sample_rows(b, n_random=64)
+    assert_bf16_close(got[rows], oracle_rows(b, rows), "mixed")
