@@ -129,8 +129,9 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
 void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t* win,
                   int32_t forced_q_block) {
   const int32_t group = plan.hq / plan.hkv;
-  int32_t qb = prefill_tokens_per_block(plan.d, group);
-  if (forced_q_block > 0) qb = forced_q_block;
+  const int32_t max_qb = prefill_tokens_per_block(plan.d, group);
+  int32_t qb = max_qb;
+  if (forced_q_block > 0) qb = std::min(forced_q_block, max_qb);
   plan.q_block = qb;
   struct Cost {
     int64_t cost;

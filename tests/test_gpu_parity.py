@@ -138,6 +138,51 @@ def test_empty_batch_is_a_no_op():
     assert binding.rpa_get_device_error(ws) == 0
 
 
+# ---------------------------------------------------------------- prefill (tensor cores)
+
+PREFILL = [
+    # (q_lens, kv_lens, Hq, Hkv, D, P, windows)
+    ([200, 129, 64], [300, 129, 1000], 4, 4, 128, 128, [100, 0, 0]),      # G = 1
+    ([1000], [1000], 4, 2, 256, 128, [0]),                                 # G = 2 causal
+    ([1000], [1000], 4, 2, 256, 128, [256]),                               # G = 2 window
+    ([100, 1, 37], [400, 50, 37], 8, 1, 256, 128, [64, 0, 1024]),          # G = 8, chunked
+    ([70, 33, 2], [70, 90, 2], 8, 2, 64, 16, [0, 20, 0]),                  # G = 4, P = 16
+    ([45, 80], [45, 300], 6, 2, 128, 64, [0, 33]),                         # G = 3
+    ([40, 17], [100, 17], 16, 1, 64, 32, [0, 5]),                          # G = 16
+    ([130, 65], [130, 2000], 2, 2, 256, 16, [0, 0]),                       # G = 1, P = 16
+]
+
+
+@pytest.mark.parametrize("case", range(len(PREFILL)))
+def test_prefill_tc_small(case):
+    ql, kv, hq, hkv, d, p, win = PREFILL[case]
+    b = workloads.make_batch(ql, kv, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                             page_size=p, windows=win, seed=400 + case)
+    got, err, plan = run_gpu(b)
+    info = plan.info()
+    assert err == 0 and info["path"] == RPA_PATH_TC and info["num_prefill_items"] > 0
+    assert_bf16_close(got, oracle_rows(b), "prefill case %d" % case)
+
+
+@pytest.mark.parametrize("q_block", [64, 32, 16, 8])
+def test_prefill_q_block_invariance(q_block):
+    """The query block changes scheduling, not the result."""
+    b = workloads.make_batch([700, 300], [700, 900], num_q_heads=4, num_kv_heads=2,
+                             head_dim=256, page_size=128, windows=[0, 128], seed=77)
+    got, err, plan = run_gpu(b, q_block=q_block)
+    assert err == 0 and plan.info()["q_block"] == q_block
+    assert_bf16_close(got, oracle_rows(b), "q_block %d" % q_block)
+
+
+def test_prefill_tc_and_simt_agree():
+    b = workloads.make_batch([300], [500], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                             page_size=64, windows=[200], seed=78)
+    tc, err1, _ = run_gpu(b, path=RPA_PATH_TC)
+    simt, err2, _ = run_gpu(b, path=RPA_PATH_SIMT)
+    assert err1 == 0 and err2 == 0
+    assert np.abs(tc - simt).max() <= 2 * BF16_MAX
+
+
 # ---------------------------------------------------------------- decode
 
 
