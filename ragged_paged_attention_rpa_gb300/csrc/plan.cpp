@@ -15,6 +15,8 @@
 //    each key is read once per query block that wants it, so the query block
 //    grows with the head-group ratio (the MMA rows are q-block x group).
 #include <algorithm>
+#include <cmath>
+#include <cstdlib>
 #include <cstdint>
 #include <functional>
 #include <numeric>
@@ -92,13 +94,34 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
   } else {
     candidates = {64, 128, 192, 256, 320, 384, 512, 640, 768, 1024, 1536, 2048, 3072, 4096};
   }
+  // Evaluate the candidate nearest to two waves first so that the lower bound
+  // below prunes most of the others without simulating them.
+  int64_t total_vis = 0, max_vis = 0;
+  for (int64_t n : vis) {
+    total_vis += n;
+    max_vis = std::max(max_vis, n);
+  }
+  const double two_waves = static_cast<double>(total_vis) * plan.hkv / (2.0 * slots);
+  std::stable_sort(candidates.begin(), candidates.end(), [&](int32_t a, int32_t b) {
+    return std::abs(a - two_waves) < std::abs(b - two_waves);
+  });
   double best = -1.0;
   int32_t best_split = candidates.front();
+  std::vector<double> costs;
   for (int32_t split : candidates) {
+    // Lower bound: total work over the slots, or the longest CTA.
+    int64_t ctas = 0;
+    for (int64_t n : vis) ctas += ceil_div(n, split);
+    ctas *= plan.hkv;
+    const double lb = std::max(
+        (static_cast<double>(total_vis) * plan.hkv + kCtaOverheadTokens * ctas) / slots,
+        kCtaOverheadTokens + static_cast<double>(std::min<int64_t>(split, max_vis)));
+    if (best >= 0 && lb >= best) continue;
     // Grid order: x = sequence (fastest), y = split, z = kv head.
     int64_t max_n = 0;
     for (int64_t n : vis) max_n = std::max(max_n, ceil_div(n, split));
-    std::vector<double> costs;
+    costs.clear();
+    costs.reserve(static_cast<size_t>(ctas));
     bool any_multi = false;
     for (int32_t h = 0; h < plan.hkv; ++h)
       for (int64_t c = 0; c < max_n; ++c)
@@ -111,7 +134,7 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
           costs.push_back(kCtaOverheadTokens + tok + (n > 1 ? 2.0 * group : 0.0));
         }
     double t = list_schedule(costs, slots) + (any_multi ? kCombineLaunchTokens : 0.0);
-    if (best < 0 || t < best - 1e-9) {
+    if (best < 0 || t < best - 1e-9 || (std::abs(t - best) <= 1e-9 && split > best_split)) {
       best = t;
       best_split = split;
     }
