@@ -23,7 +23,11 @@
 //                                          warp-level 8x8 transpose)
 // keeping an online softmax per head.  The warps merge through shared memory
 // at the end.  One split writes the output; several write fp32 partials
-// (O / l and log2-sum-exp) that the combine kernel merges.
+// (O / l and log2-sum-exp), and the split that finishes last for a sequence
+// (a per-sequence arrival counter in the workspace, reset by that split)
+// merges them: out = sum_c 2^(lse_c - M) O_c / sum_c 2^(lse_c - M).
+// The page ids of a split are read into shared memory once, before the copy
+// pipeline starts, so no copy waits on a page-table load.
 #include "common.cuh"
 #include "rpa_internal.h"
 
@@ -33,6 +37,7 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kBlk = 16;  // keys per warp block (the MMA's M)
+constexpr int kMaxMergeSplits = 64;
 
 constexpr int stages_for(int D) { return D >= 256 ? 3 : 4; }
 
@@ -48,6 +53,7 @@ struct DecodeParams {
   unsigned char* ws;
   float* part_o;
   float* part_lse;
+  int32_t* arrivals;  // [num_seqs * hkv], zero between calls
   int32_t num_seqs, hq, hkv, group, page_shift, mpps, num_pages;
   int32_t kv_split, max_splits;
   float scale_log2;  // sm_scale * log2(e)
@@ -135,39 +141,41 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(DecodePara
   const int32_t* pt = p.page_table + static_cast<int64_t>(s) * p.mpps;
   const int32_t psize = 1 << p.page_shift;
 
-  // Q^T as the B operand: lane holds head lane/4, dims 2(lane%4)+{0,1} (+8).
-  uint32_t qf[KT][2];
-  {
-    const int h = lane >> 2;
-    const bool hv = h < G;
-    const __nv_bfloat16* qr = p.q + (static_cast<int64_t>(q0) * p.hq + g * G + (hv ? h : 0)) * D;
-#pragma unroll
-    for (int kt = 0; kt < KT; ++kt) {
-      const int d0 = kt * 16 + 2 * (lane & 3);
-      qf[kt][0] = hv ? *reinterpret_cast<const uint32_t*>(qr + d0) : 0u;
-      qf[kt][1] = hv ? *reinterpret_cast<const uint32_t*>(qr + d0 + 8) : 0u;
+  // Page ids of this split, read once (coalesced) into shared memory.
+  __shared__ int32_t s_pages[kMaxSplitPages];
+  const int32_t slot0 = kb >> p.page_shift;
+  const int32_t npg = ((ke - 1) >> p.page_shift) - slot0 + 1;
+  for (int i = threadIdx.x; i < npg && i < kMaxSplitPages; i += kWarps * 32) {
+    const int32_t slot = slot0 + i;
+    int32_t page = -1;
+    if (slot >= p.mpps) {
+      report_error(p.ws, RPA_DEVERR_LENGTHS, s);
+    } else {
+      page = __ldg(pt + slot);
+      if (page < 0 || page >= p.num_pages) {
+        report_error(p.ws, RPA_DEVERR_PAGE_ID, s);
+        page = -1;
+      }
     }
+    s_pages[i] = page;
   }
+  if (npg > kMaxSplitPages && threadIdx.x == 0) report_error(p.ws, RPA_DEVERR_LENGTHS, s);
+  __syncthreads();
 
   __nv_bfloat16* ring = smem + warp * S * 2 * TILE;  // this warp's S stages of K then V
   // Issue the copies of this warp's i-th block into stage st (always commits).
   auto issue = [&](int i, int st) {
     if (i < my_blocks) {
       const int32_t key0 = kb + (warp + i * kWarps) * kBlk;
-      // Lanes 0..15 resolve the page of one key each.
+      // Lanes 0..15 look up the page of one key each.
       int32_t page = 0;
       bool ok = false;
       if (lane < kBlk) {
         const int32_t key = key0 + lane;
-        if (key < ke) {
-          const int32_t slot = key >> p.page_shift;
-          if (slot >= p.mpps) {
-            report_error(p.ws, RPA_DEVERR_LENGTHS, s);
-          } else {
-            page = __ldg(pt + slot);
-            ok = page >= 0 && page < p.num_pages;
-            if (!ok) report_error(p.ws, RPA_DEVERR_PAGE_ID, s);
-          }
+        const int32_t idx = (key >> p.page_shift) - slot0;
+        if (key < ke && idx < kMaxSplitPages) {
+          page = s_pages[idx];
+          ok = page >= 0;
         }
       }
       const uint32_t vmask = __ballot_sync(0xffffffffu, ok);
@@ -183,28 +191,35 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(DecodePara
         const int32_t key = key0 + r;
         const int64_t off =
             ((static_cast<int64_t>(pg) * psize + (key & (psize - 1))) * p.hkv + g) * D + ch * 8;
-        if (r < kBlk) {
-          cp_async16(smem_u32(kt + swz<D>(r, ch)), v ? p.k + off : p.k, v);
-          cp_async16(smem_u32(vt + swz<D>(r, ch)), v ? p.v + off : p.v, v);
-        }
-#pragma unroll
-        for (int c2 = 32; c2 < CPR; c2 += 32) {  // D > 256 never happens; kept general
-          cp_async16(smem_u32(kt + swz<D>(r, ch + c2)), v ? p.k + off + c2 * 8 : p.k, v);
-          cp_async16(smem_u32(vt + swz<D>(r, ch + c2)), v ? p.v + off + c2 * 8 : p.v, v);
-        }
+        cp_async16(smem_u32(kt + swz<D>(r, ch)), v ? p.k + off : p.k, v);
+        cp_async16(smem_u32(vt + swz<D>(r, ch)), v ? p.v + off : p.v, v);
       }
     }
     cp_async_commit();
   };
+#pragma unroll
+  for (int i = 0; i < S - 1; ++i) issue(i, i);
+
+  // Q^T as the B operand: lane holds head lane/4, dims 2(lane%4)+{0,1} (+8).
+  // Loaded after the first copies are in flight.
+  uint32_t qf[KT][2];
+  {
+    const int h = lane >> 2;
+    const bool hv = h < G;
+    const __nv_bfloat16* qr = p.q + (static_cast<int64_t>(q0) * p.hq + g * G + (hv ? h : 0)) * D;
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt) {
+      const int d0 = kt * 16 + 2 * (lane & 3);
+      qf[kt][0] = hv ? *reinterpret_cast<const uint32_t*>(qr + d0) : 0u;
+      qf[kt][1] = hv ? *reinterpret_cast<const uint32_t*>(qr + d0 + 8) : 0u;
+    }
+  }
 
   float m[2] = {-INFINITY, -INFINITY};  // running max (log2 domain), heads 2(lane%4)+j
   float l[2] = {0.f, 0.f};              // this lane's share of the running sum
   float o[KT][4];
 #pragma unroll
   for (int mt = 0; mt < KT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-
-#pragma unroll
-  for (int i = 0; i < S - 1; ++i) issue(i, i);
 
   for (int i = 0; i < my_blocks; ++i) {
     issue(i + S - 1, (i + S - 1) % S);
@@ -348,32 +363,32 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(DecodePara
       if (d == 0) p.part_lse[row] = M + __log2f(Lsum);
     }
   }
-}
+  if (nsplit == 1) return;
 
-// Merge the splits of each decode sequence: weights 2^(lse_c - max lse).
-template <int D>
-__global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams p) {
-  const int s = blockIdx.x, g = blockIdx.y;
-  const int32_t q0 = __ldg(p.cu_q_lens + s);
-  if (__ldg(p.cu_q_lens + s + 1) - q0 != 1) return;
-  const int32_t L = __ldg(p.kv_lens + s);
-  const int32_t W = p.window ? __ldg(p.window + s) : 0;
-  const int32_t lo = (W > 0 && L - W > 0) ? L - W : 0;
-  const int32_t nsplit = min((L - lo + p.kv_split - 1) / p.kv_split, p.max_splits);
-  if (nsplit <= 1) return;
-  const int G = p.group;
-  for (int e = threadIdx.x * 4; e < G * D; e += blockDim.x * 4) {
+  // Arrival: the last split of (sequence, KV head) to finish merges them all.
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(p.arrivals + s * p.hkv + g, 1) == nsplit - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int ns = min(nsplit, kMaxMergeSplits);
+  float* s_lse = reinterpret_cast<float*>(smem_raw);  // [ns][G], ring is free
+  const int64_t row0 = static_cast<int64_t>(s) * p.max_splits * p.hq + g * G;
+  for (int i = threadIdx.x; i < ns * G; i += kWarps * 32)
+    s_lse[i] = __ldcg(p.part_lse + row0 + static_cast<int64_t>(i / G) * p.hq + i % G);
+  __syncthreads();
+  for (int e = threadIdx.x * 4; e < G * D; e += kWarps * 32 * 4) {
     const int h = e / D, d = e % D;
-    const int hq_idx = g * G + h;
-    const int64_t row0 = static_cast<int64_t>(s) * p.max_splits * p.hq + hq_idx;
     float M = -INFINITY;
-    for (int c = 0; c < nsplit; ++c) M = fmaxf(M, p.part_lse[row0 + static_cast<int64_t>(c) * p.hq]);
+    for (int k = 0; k < ns; ++k) M = fmaxf(M, s_lse[k * G + h]);
     float wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = 0; c < nsplit; ++c) {
-      const int64_t row = row0 + static_cast<int64_t>(c) * p.hq;
-      const float w = fast_exp2(p.part_lse[row] - M);
-      const float4 u = *reinterpret_cast<const float4*>(p.part_o + row * D + d);
+    for (int k = 0; k < ns; ++k) {
+      const float w = fast_exp2(s_lse[k * G + h] - M);
+      const float4 u = __ldcg(reinterpret_cast<const float4*>(
+          p.part_o + (row0 + static_cast<int64_t>(k) * p.hq + h) * D + d));
       wsum += w;
       acc.x += w * u.x; acc.y += w * u.y; acc.z += w * u.z; acc.w += w * u.w;
     }
@@ -381,8 +396,9 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeParams p) {
     uint2 pk;
     pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
     pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(q0) * p.hq + hq_idx) * D + d) = pk;
+    *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(q0) * p.hq + g * G + h) * D + d) = pk;
   }
+  if (threadIdx.x == 0) p.arrivals[s * p.hkv + g] = 0;  // ready for the next call
 }
 
 template <int D>
@@ -393,6 +409,7 @@ constexpr size_t decode_smem() {
 template <int D>
 int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   static_assert(decode_smem<D>() >= kWarps * 8 * D * sizeof(float), "merge buffer fits");
+  static_assert(decode_smem<D>() >= kMaxMergeSplits * 8 * sizeof(float), "lse buffer fits");
   constexpr size_t smem = decode_smem<D>();
   static bool configured = false;
   if (!configured) {
@@ -414,6 +431,7 @@ int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   p.ws = a.workspace;
   p.part_o = plan.max_splits > 1 ? reinterpret_cast<float*>(a.workspace + plan.off_partial_o) : nullptr;
   p.part_lse = plan.max_splits > 1 ? reinterpret_cast<float*>(a.workspace + plan.off_partial_lse) : nullptr;
+  p.arrivals = plan.max_splits > 1 ? reinterpret_cast<int32_t*>(a.workspace + plan.off_arrivals) : nullptr;
   p.num_seqs = plan.num_seqs;
   p.hq = plan.hq;
   p.hkv = plan.hkv;
@@ -431,12 +449,7 @@ int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return static_cast<int>(e);
   trace_mark(RPA_KERNEL_DECODE_SPLIT, stream);
-  if (plan.max_splits > 1) {
-    decode_combine_kernel<D><<<dim3(plan.num_seqs, plan.hkv), 256, 0, stream>>>(p);
-    e = cudaGetLastError();
-    if (e == cudaSuccess) trace_mark(RPA_KERNEL_DECODE_COMBINE, stream);
-  }
-  return static_cast<int>(e);
+  return 0;
 }
 
 }  // namespace

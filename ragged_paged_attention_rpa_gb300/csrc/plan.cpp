@@ -89,10 +89,22 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
   const int slots = plan.num_sms * decode_ctas_per_sm(plan.d);
   const int32_t group = plan.hq / plan.hkv;
   std::vector<int32_t> candidates;
+  // A split's page ids must fit the kernel's shared-memory table, and a
+  // sequence may have at most kMaxSplits splits.
+  const int64_t max_split_len = std::max<int64_t>(64, (kMaxSplitPages - 2) / 64 * 64 * plan.p);
+  int64_t max_vis0 = 1;
+  for (int64_t n : vis) max_vis0 = std::max(max_vis0, n);
+  const int64_t min_split_len = ceil_div(ceil_div(max_vis0, kMaxSplits), 64) * 64;
+  auto clamp_split = [&](int64_t x) {
+    x = std::max<int64_t>(x, min_split_len);
+    x = std::min<int64_t>(x, max_split_len);
+    return static_cast<int32_t>(std::max<int64_t>(64, x));
+  };
   if (forced_split > 0) {
-    candidates.push_back(static_cast<int32_t>(ceil_div(forced_split, 64) * 64));
+    candidates.push_back(clamp_split(ceil_div(forced_split, 64) * 64));
   } else {
-    candidates = {64, 128, 192, 256, 320, 384, 512, 640, 768, 1024, 1536, 2048, 3072, 4096};
+    for (int32_t c : {64, 128, 192, 256, 320, 384, 512, 640, 768, 1024, 1536, 2048, 3072, 4096})
+      candidates.push_back(clamp_split(c));
   }
   // Evaluate the candidate nearest to two waves first so that the lower bound
   // below prunes most of the others without simulating them.
@@ -246,6 +258,8 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
     off += (rows * plan.d * sizeof(float) + 255) / 256 * 256;
     plan.off_partial_lse = off;
     off += (rows * sizeof(float) + 255) / 256 * 256;
+    plan.off_arrivals = off;
+    off += (static_cast<size_t>(plan.num_seqs) * plan.hkv * sizeof(int32_t) + 255) / 256 * 256;
   }
   plan.ws_bytes = off;
   return RPA_OK;

@@ -25,6 +25,11 @@ struct PrefillItem {
 // longer lists are split over several launches.
 constexpr int kMaxItemsPerLaunch = 3072;
 
+// Most pages one decode split may touch (its page ids sit in shared memory),
+// and most splits per sequence.
+constexpr int kMaxSplitPages = 1024;
+constexpr int kMaxSplits = 64;
+
 struct Plan {
   // Problem description (checked against every rpa_forward call).
   int32_t num_seqs = 0, hq = 0, hkv = 0, d = 0, p = 0, mpps = 0, num_pages = 0;
@@ -50,7 +55,7 @@ struct Plan {
   int32_t prefill_ctas = 0;
 
   // Workspace.
-  size_t off_partial_o = 0, off_partial_lse = 0, ws_bytes = kHeaderBytes;
+  size_t off_partial_o = 0, off_partial_lse = 0, off_arrivals = 0, ws_bytes = kHeaderBytes;
 };
 
 // Scheduler (plan.cpp): fills everything but the problem description, which

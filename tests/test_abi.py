@@ -66,10 +66,12 @@ def test_decode_plan_covers_every_key():
     assert split % 64 == 0 and split > 0
     nsplit = [ceil_div(int(L), split) for L in b.kv_lens]
     assert info["max_splits"] == max(nsplit)
-    # Workspace: 256-byte header, fp32 partial O and LSE for every split slot.
+    # Workspace: 256-byte header, fp32 partial O and LSE for every split slot,
+    # one int32 arrival counter per (sequence, KV head).
     if info["max_splits"] > 1:
         rows = b.num_seqs * info["max_splits"] * b.num_q_heads
-        want = 256 + ceil_div(rows * b.head_dim * 4, 256) * 256 + ceil_div(rows * 4, 256) * 256
+        want = (256 + ceil_div(rows * b.head_dim * 4, 256) * 256 + ceil_div(rows * 4, 256) * 256
+                + ceil_div(b.num_seqs * b.num_kv_heads * 4, 256) * 256)
     else:
         want = 256
     assert info["workspace_bytes"] == p.workspace_bytes == want
@@ -92,6 +94,15 @@ def test_decode_split_respects_window():
 def test_forced_split_is_rounded_to_64():
     b = workloads.decode_batch(seed=1, meta_only=True)
     assert plan_of(b, kv_split=100).info()["kv_split"] == 128
+
+
+def test_split_count_is_capped():
+    # 64 splits at most per sequence: a 64-token split of a 100k-token context
+    # is raised to ceil(100000 / 64) rounded up to 64.
+    b = workloads.make_batch([1], [100000], num_q_heads=8, num_kv_heads=1, head_dim=256,
+                             page_size=128, meta_only=True)
+    info = plan_of(b, kv_split=64).info()
+    assert info["max_splits"] <= 64 and info["kv_split"] == 1600
 
 
 def test_f32_takes_the_simt_path():
