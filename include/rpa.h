@@ -199,6 +199,40 @@ rpa_status_t rpa_get_device_error(void* workspace, rpa_stream_t stream, int32_t*
 rpa_status_t rpa_clear_device_error(void* workspace, rpa_stream_t stream);
 
 /*
+ * Decode without a caller-supplied workspace: rpa_forward_decode_noalloc.
+ *
+ * For callers that cannot allocate device memory when they run attention:
+ * code that executes inside a framework whose device memory is entirely owned
+ * by another allocator, embedded or real-time serving loops that must not
+ * call cudaMalloc (it can synchronise the device), and plug-ins that receive
+ * only the tensors they work on.  The paper has no counterpart; this is a
+ * deployment convenience.
+ *
+ * Same arguments as rpa_forward without the workspace.  The plan must hold
+ * decode sequences only (q_len <= 1) on the split-KV decode kernel, else
+ * RPA_ERR_UNSUPPORTED; a plan whose workspace_bytes exceeds
+ * RPA_NOALLOC_SCRATCH_BYTES is rejected with RPA_ERR_WORKSPACE_TOO_SMALL.
+ * The scratch is one fixed array inside the library (every GPU that loads the
+ * library holds it until the process exits), shared by every call: each call
+ * clears the parts that must start at zero, and calls that overlap on the GPU
+ * (for example on two streams) race on it.  The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  No device memory
+ * is allocated or freed.  The device error word of this scratch is not
+ * exposed; the call returns RPA_OK once its work is enqueued.
+ */
+#define RPA_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
+
+rpa_status_t rpa_forward_decode_noalloc(const void* q, const void* k_pages,
+                                        const void* v_pages, const int32_t* page_table,
+                                        const int32_t* cu_q_lens, const int32_t* kv_lens,
+                                        int32_t num_seqs, int32_t num_q_heads,
+                                        int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t page_size, const int32_t* window,
+                                        float sm_scale, void* out, rpa_stream_t stream,
+                                        const rpa_plan_t* plan);
+
+/*
  * Kernel tracing (off by default).  Between rpa_trace_begin and rpa_trace_end,
  * every rpa_forward call records a CUDA event on its stream before its first
  * kernel and after each kernel it launches, so that the device time of each

@@ -40,7 +40,7 @@ RPA_PATH_TC = 2
 
 EXPORTS = ["rpa_plan", "rpa_plan_destroy", "rpa_plan_get_info", "rpa_forward",
            "rpa_get_device_error", "rpa_clear_device_error", "rpa_trace_begin",
-           "rpa_trace_end", "rpa_status_string"]
+           "rpa_trace_end", "rpa_status_string", "rpa_forward_decode_noalloc"]
 
 RPA_KERNEL_NAMES = {0: "decode_split", 2: "prefill_tc", 3: "simt"}
 
@@ -95,6 +95,9 @@ def lib() -> ctypes.CDLL:
         L.rpa_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
                                   ctypes.c_float, vp, vp, vp, vp, sz]
         L.rpa_forward.restype = i32
+        L.rpa_forward_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                  i32, vp, ctypes.c_float, vp, vp, vp]
+        L.rpa_forward_decode_noalloc.restype = i32
         L.rpa_get_device_error.argtypes = [vp, vp, ctypes.POINTER(i32)]
         L.rpa_get_device_error.restype = i32
         L.rpa_clear_device_error.argtypes = [vp, vp]
@@ -218,6 +221,24 @@ def rpa_forward(q, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window,
         workspace.numel() * workspace.element_size())
     if st != RPA_OK:
         raise RpaError(st, "rpa_forward")
+
+
+def rpa_forward_decode_noalloc(q, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window,
+                               sm_scale: float, out, plan: Plan, stream=None) -> None:
+    """rpa_forward_decode_noalloc: decode with the library's fixed scratch
+    array instead of a caller workspace (see include/rpa.h)."""
+    import torch
+    m = plan.meta
+    dt = torch.bfloat16
+    st = lib().rpa_forward_decode_noalloc(
+        _dptr(q, "q", dt), _dptr(k_pages, "k_pages", dt), _dptr(v_pages, "v_pages", dt),
+        _dptr(page_table, "page_table", torch.int32), _dptr(cu_q_lens, "cu_q_lens", torch.int32),
+        _dptr(kv_lens, "kv_lens", torch.int32), m["num_seqs"], m["num_q_heads"],
+        m["num_kv_heads"], m["head_dim"], m["page_size"],
+        _dptr(window, "window", torch.int32), float(sm_scale), _dptr(out, "out", dt),
+        _stream_ptr(stream), plan.handle)
+    if st != RPA_OK:
+        raise RpaError(st, "rpa_forward_decode_noalloc")
 
 
 def rpa_get_device_error(workspace, stream=None) -> int:

@@ -158,6 +158,46 @@ rpa_status_t rpa_forward(const void* q, const void* k_pages, const void* v_pages
   return RPA_OK;
 }
 
+rpa_status_t rpa_forward_decode_noalloc(const void* q, const void* k_pages,
+                                        const void* v_pages, const int32_t* page_table,
+                                        const int32_t* cu_q_lens, const int32_t* kv_lens,
+                                        int32_t num_seqs, int32_t num_q_heads,
+                                        int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t page_size, const int32_t* window,
+                                        float sm_scale, void* out, rpa_stream_t stream,
+                                        const rpa_plan_t* plan) {
+  if (plan == nullptr) return RPA_ERR_INVALID_ARG;
+  const rpa::Plan& p = plan->p;
+  if (num_seqs != p.num_seqs || num_q_heads != p.hq || num_kv_heads != p.hkv ||
+      head_dim != p.d || page_size != p.p || (window != nullptr) != p.has_window)
+    return RPA_ERR_PLAN_MISMATCH;
+  if (p.num_prefill > 0 || p.simt_decode || p.dtype != RPA_DTYPE_BF16)
+    return RPA_ERR_UNSUPPORTED;
+  if (p.ws_bytes > RPA_NOALLOC_SCRATCH_BYTES) return RPA_ERR_WORKSPACE_TOO_SMALL;
+  if (p.total_q == 0) return RPA_OK;
+  if (q == nullptr || k_pages == nullptr || v_pages == nullptr || page_table == nullptr ||
+      cu_q_lens == nullptr || kv_lens == nullptr || out == nullptr)
+    return RPA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_pages, 128) ||
+      !aligned(v_pages, 128) || !aligned(page_table, 4) || !aligned(cu_q_lens, 4) ||
+      !aligned(kv_lens, 4) || !aligned(window, 4))
+    return RPA_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  if (rpa::noalloc_scratch(&scratch) != 0) return RPA_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // The error word and the arrival counters must start at zero.
+  if (cudaMemsetAsync(scratch, 0, rpa::kHeaderBytes, s) != cudaSuccess) return RPA_ERR_CUDA;
+  if (p.max_splits > 1 &&
+      cudaMemsetAsync(static_cast<unsigned char*>(scratch) + p.off_arrivals, 0,
+                      static_cast<size_t>(p.num_seqs) * p.hkv * sizeof(int32_t), s) != cudaSuccess)
+    return RPA_ERR_CUDA;
+  rpa::Args a{q, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window, sm_scale,
+              out, static_cast<unsigned char*>(scratch)};
+  rpa::trace_start(stream);
+  if (rpa::launch_decode(p, a, stream) != 0) return RPA_ERR_CUDA;
+  return RPA_OK;
+}
+
 rpa_status_t rpa_get_device_error(void* workspace, rpa_stream_t stream, int32_t* err) {
   if (workspace == nullptr || err == nullptr) return RPA_ERR_INVALID_ARG;
   int32_t v = 0;

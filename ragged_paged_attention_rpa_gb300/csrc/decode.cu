@@ -454,6 +454,37 @@ int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Fixed scratch for rpa_forward_decode_noalloc: the decode kernel's workspace
+// (error word, split partials, arrival counters) in a file-scope device array,
+// so that callers who cannot allocate device memory can still run decode.
+// Every GPU that loads this library holds the array until the process exits.
+// In host code `g_noalloc_scratch` names a host-side stand-in, never a device
+// address; the device address comes from cudaGetSymbolAddress, resolved once
+// per device (with that device current) on the first call on that device.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[RPA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+void* g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+int noalloc_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  if (dev < 0 || dev >= kMaxDevices) return static_cast<int>(cudaErrorInvalidDevice);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return 0;
+}
+
 bool decode_supported(int32_t head_dim, int32_t group) {
   return (head_dim == 64 || head_dim == 128 || head_dim == 256) && group >= 1 && group <= 8;
 }

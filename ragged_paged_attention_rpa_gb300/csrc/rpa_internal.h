@@ -94,6 +94,10 @@ void trace_mark(int kernel, void* stream);
 
 // Whether the tensor-core prefill supports this shape (prefill_tc.cu).
 bool prefill_tc_supported(int32_t head_dim, int32_t page_size, int32_t group);
+// Device address of the fixed no-allocation scratch array on the current
+// device (decode.cu); resolved on the first call per device.
+int noalloc_scratch(void** ptr);
+
 // Whether the split-KV decode supports this shape (decode.cu).
 bool decode_supported(int32_t head_dim, int32_t group);
 
