@@ -487,7 +487,7 @@ def run_e2e(args, b, db, plan_dev, flush_l2, binding, torch):
         plan = binding.rpa_plan(b.cu_q_lens, b.kv_lens, b.window, b.num_q_heads,
                                 b.num_kv_heads, b.head_dim, b.page_size,
                                 b.max_pages_per_seq, b.num_pages,
-                                dtype=db.dtype)
+                                dtype=db.dtype, q_block=args.q_block, kv_split=args.kv_split)
         if plan.workspace_bytes > ws.numel():
             raise RuntimeError("workspace too small for the per-step plan")
         binding.rpa_forward(qv, db.k_pages, db.v_pages, dmeta[0], dmeta[1], dmeta[2], win_d,

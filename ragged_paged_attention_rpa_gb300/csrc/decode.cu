@@ -1,5 +1,4 @@
-// Split-KV decode for sequences with one query token, and the log-sum-exp
-// combine of the splits.
+// Split-KV decode for sequences with one query token, on one balanced wave.
 //
 // Sources (page titles and sections):
 //  * "TPU Deep Dive" slides, chapter 4, "Attention: small share, wrong
@@ -8,26 +7,33 @@
 //    visible KV is read exactly once here.
 //  * "Pallas kernel / vLLM on TPU ... 19,511 tokens per second", section
 //    "Strategy 7": a KV block sized for long contexts wasted ~93% of its loads
-//    on short ones.  Here no load goes past a sequence's last key (or before
-//    its window), and the split length comes from the batch's real lengths.
+//    on short ones, and block size changes scheduling, not arithmetic.  Here no
+//    load goes past a sequence's last key (or before its window), and the work
+//    is cut by the batch's real lengths.
 //  * "Chasing speed of light on TPU v6e", footnote 6: fp32 softmax
 //    accumulators (m, l and O stay fp32; only P is rounded to bf16 for the
 //    tensor-core product, as any bf16 flash kernel does).
 //
-// CTA (s, c, g) streams keys [kb, ke) of split c of sequence s for KV head g.
-// Its four warps are independent: warp w takes blocks of 16 keys w, w+4, ...,
-// copies each block's K and V rows into its own shared-memory ring with
-// coalesced 16-byte cp.async loads through the page table, and runs
+// Schedule.  The visible keys of every (decode sequence, KV head) pair form a
+// "segment" of 16-key blocks; the segments are laid end to end and the block
+// stream is cut into equal contiguous ranges, one per CTA (one CTA per SM, a
+// single wave), so every CTA streams the same number of bytes whatever the
+// length mix.  A CTA's range may start or end inside a segment.
+//
+// CTA.  Four independent warps take the range's blocks round-robin (warp w:
+// blocks w, w+4, ... of each segment) and copy each block's K and V rows into
+// their own shared-memory ring with coalesced 16-byte cp.async loads through
+// the page table (the page ids of the whole range are read into shared memory
+// once, first).  Per block a warp runs
 //     S^T[16 keys x 8 heads] = K . Q^T     (mma.m16n8k16, bf16 -> fp32)
 //     O^T[D x 8 heads]     += V^T . P^T   (P^T rebuilt in registers by a
 //                                          warp-level 8x8 transpose)
-// keeping an online softmax per head.  The warps merge through shared memory
-// at the end.  One split writes the output; several write fp32 partials
-// (O / l and log2-sum-exp), and the split that finishes last for a sequence
-// (a per-sequence arrival counter in the workspace, reset by that split)
-// merges them: out = sum_c 2^(lse_c - M) O_c / sum_c 2^(lse_c - M).
-// The page ids of a split are read into shared memory once, before the copy
-// pipeline starts, so no copy waits on a page-table load.
+// with an online softmax per head.  The copy pipeline runs on across segment
+// boundaries.  At the end of each segment the warps merge in shared memory; a
+// segment wholly inside the range writes the output, a cut one writes an fp32
+// partial (O / l and log2-sum-exp).  The CTA that finishes a cut segment last
+// (a per-segment arrival counter in the workspace, reset by that CTA) merges
+// its partials: out = sum_c 2^(lse_c - M) O_c / sum_c 2^(lse_c - M).
 #include "common.cuh"
 #include "rpa_internal.h"
 
@@ -37,7 +43,6 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kBlk = 16;  // keys per warp block (the MMA's M)
-constexpr int kMaxMergeSplits = 64;
 
 constexpr int stages_for(int D) { return D >= 256 ? 3 : 4; }
 
@@ -51,12 +56,31 @@ struct DecodeParams {
   const int32_t* window;
   __nv_bfloat16* out;
   unsigned char* ws;
-  float* part_o;
-  float* part_lse;
-  int32_t* arrivals;  // [num_seqs * hkv], zero between calls
-  int32_t num_seqs, hq, hkv, group, page_shift, mpps, num_pages;
-  int32_t kv_split, max_splits;
-  float scale_log2;  // sm_scale * log2(e)
+  float* part_o;      // [2 * total CTAs][G][D]
+  float* part_lse;    // [2 * total CTAs][G]
+  int32_t* arrivals;  // [segments], zero between calls
+  int32_t hq, hkv, group, page_shift, mpps, num_pages;
+  float scale_log2;   // sm_scale * log2(e)
+};
+
+// One launch's share of the block stream.  seqhead[i] = (sequence << 8) | kv
+// head of segment i; blk0[i] = first block of segment i (blk0[n_seg] = total).
+template <int NSEG>
+struct DecodeSched {
+  int32_t n_seg, bpc, n_blocks, slot_base, seg_base;
+  int32_t seqhead[NSEG];
+  int32_t blk0[NSEG + 1];
+};
+
+struct SegInfo {
+  int32_t s, g, q0;      // sequence, kv head, its query token
+  int32_t kb, ke;        // keys [kb, ke) of this CTA's part
+  int32_t nb;            // 16-key blocks in this CTA's part
+  int32_t slot0, pg_off; // first page-table slot; offset in the shared page list
+  int32_t npg;           // pages of this part
+  int32_t whole;         // the segment lies entirely in this CTA's range
+  int32_t gseg;          // segment index in the launch
+  int32_t bad;           // device metadata disagree with the plan: skipped
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -109,71 +133,147 @@ __device__ __forceinline__ int swz(int row, int chunk) {
   return row * D + ((chunk ^ (row & 7)) << 3);
 }
 
+// Largest i in [0, n) with a[i] <= x (a sorted ascending, a[0] <= x).
+template <int NSEG>
+__device__ __forceinline__ int seg_of(const DecodeSched<NSEG>& sc, int32_t x) {
+  int lo = 0, hi = sc.n_seg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sc.blk0[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(DecodeParams p) {
-  constexpr int S = stages_for(D);
+struct DecodeSmem {
+  static constexpr int S = stages_for(D);
+  static constexpr int TILE = kBlk * D;                         // bf16 elements
+  static constexpr size_t kRing = size_t(kWarps) * S * 2 * TILE * 2;
+  static constexpr size_t kQ = 2 * 8 * D * 2;                   // two Q tiles (G <= 8)
+  static constexpr int kORow = D + 4;                           // padded row of the merge buffer
+  static constexpr size_t kO = 8 * kORow * 4;
+  static constexpr size_t kBytes = kRing + kQ + kO;
+};
+
+template <int D, int NSEG>
+__global__ void __launch_bounds__(kWarps * 32, 1)
+decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc) {
+  using L = DecodeSmem<D>;
+  constexpr int S = L::S;
   constexpr int KT = D / 16;        // k-steps of the score MMA, m-tiles of the PV MMA
   constexpr int CPR = D / 8;        // 16-byte chunks per row
   constexpr int RPI = 32 / CPR > 0 ? 32 / CPR : 1;  // rows per copy instruction
-  constexpr int TILE = kBlk * D;    // elements of one K (or V) block
+  constexpr int TILE = L::TILE;
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  __nv_bfloat16* smem = reinterpret_cast<__nv_bfloat16*>(smem_raw);
+  __nv_bfloat16* rings = reinterpret_cast<__nv_bfloat16*>(smem_raw);
+  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smem_raw + L::kRing);
+  float* so = reinterpret_cast<float*>(smem_raw + L::kRing + L::kQ);
+  __shared__ int32_t s_pages[kMaxCtaPages];
+  __shared__ SegInfo s_seg[kMaxCtaSegs];
   __shared__ uint32_t valid_mask[kWarps][S];
   __shared__ float wm[kWarps][8], wl[kWarps][8];
+  __shared__ int s_nseg, s_last;
 
-  const int s = blockIdx.x, c = blockIdx.y, g = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int32_t q0 = __ldg(p.cu_q_lens + s);
-  if (__ldg(p.cu_q_lens + s + 1) - q0 != 1) return;
-  const int32_t L = __ldg(p.kv_lens + s);
-  const int32_t W = p.window ? __ldg(p.window + s) : 0;
-  const int32_t lo = (W > 0 && L - W > 0) ? L - W : 0;
-  const int32_t n = L - lo;
-  const int32_t nsplit = (n + p.kv_split - 1) / p.kv_split;
-  if (nsplit > p.max_splits && c == 0 && g == 0 && threadIdx.x == 0)
-    report_error(p.ws, RPA_DEVERR_LENGTHS, s);
-  if (c >= nsplit) return;
-  const int32_t kb = lo + c * p.kv_split;
-  const int32_t ke = min(L, kb + p.kv_split);
-  const int32_t nblk = (ke - kb + kBlk - 1) / kBlk;
-  const int32_t my_blocks = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int G = p.group;
-  const int32_t* pt = p.page_table + static_cast<int64_t>(s) * p.mpps;
-  const int32_t psize = 1 << p.page_shift;
-
-  // Page ids of this split, read once (coalesced) into shared memory.
-  __shared__ int32_t s_pages[kMaxSplitPages];
-  const int32_t slot0 = kb >> p.page_shift;
-  const int32_t npg = ((ke - 1) >> p.page_shift) - slot0 + 1;
-  for (int i = threadIdx.x; i < npg && i < kMaxSplitPages; i += kWarps * 32) {
-    const int32_t slot = slot0 + i;
-    int32_t page = -1;
-    if (slot >= p.mpps) {
-      report_error(p.ws, RPA_DEVERR_LENGTHS, s);
-    } else {
-      page = __ldg(pt + slot);
-      if (page < 0 || page >= p.num_pages) {
-        report_error(p.ws, RPA_DEVERR_PAGE_ID, s);
-        page = -1;
-      }
-    }
-    s_pages[i] = page;
+  const int c = blockIdx.x;
+  const int32_t cb0 = c * sc.bpc;
+  const int32_t cb1 = min(cb0 + sc.bpc, sc.n_blocks);
+  if (cb0 >= cb1) return;
+  const int kfirst = seg_of(sc, cb0);
+  const int klast = seg_of(sc, cb1 - 1);
+  int nseg = klast - kfirst + 1;
+  if (nseg > kMaxCtaSegs) {
+    if (tid == 0) report_error(p.ws, RPA_DEVERR_LENGTHS, c);
+    nseg = kMaxCtaSegs;
   }
-  if (npg > kMaxSplitPages && threadIdx.x == 0) report_error(p.ws, RPA_DEVERR_LENGTHS, s);
+
+  // ---- Segment table of this CTA's range.
+  for (int t = tid; t < nseg; t += kWarps * 32) {
+    const int k = kfirst + t;
+    const int32_t sh = sc.seqhead[k];
+    SegInfo si;
+    si.s = sh >> 8;
+    si.g = sh & 255;
+    si.gseg = k;
+    si.q0 = __ldg(p.cu_q_lens + si.s);
+    const int32_t Lk = __ldg(p.kv_lens + si.s);
+    const int32_t W = p.window ? __ldg(p.window + si.s) : 0;
+    const int32_t lo = (W > 0 && Lk - W > 0) ? Lk - W : 0;
+    const int32_t nb_plan = sc.blk0[k + 1] - sc.blk0[k];
+    si.bad = (__ldg(p.cu_q_lens + si.s + 1) - si.q0 != 1 || (Lk - lo + kBlk - 1) / kBlk != nb_plan)
+                 ? 1 : 0;
+    if (si.bad) report_error(p.ws, RPA_DEVERR_LENGTHS, si.s);
+    const int32_t jb = max(cb0, sc.blk0[k]) - sc.blk0[k];
+    const int32_t je = min(cb1, sc.blk0[k + 1]) - sc.blk0[k];
+    si.kb = lo + kBlk * jb;
+    si.ke = min(Lk, lo + kBlk * je);
+    if (si.ke < si.kb) si.ke = si.kb;
+    si.nb = si.bad ? 0 : je - jb;
+    si.whole = (jb == 0 && je == nb_plan) ? 1 : 0;
+    si.slot0 = si.kb >> p.page_shift;
+    si.npg = (si.ke > si.kb) ? ((si.ke - 1) >> p.page_shift) - si.slot0 + 1 : 0;
+    si.pg_off = 0;
+    s_seg[t] = si;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int off = 0;
+    for (int t = 0; t < nseg; ++t) {
+      s_seg[t].pg_off = off;
+      off += s_seg[t].npg;
+    }
+    if (off > kMaxCtaPages) report_error(p.ws, RPA_DEVERR_LENGTHS, c);
+    s_nseg = nseg;
+  }
+  __syncthreads();
+  // ---- Page ids of the range, read once.
+  for (int t = 0; t < nseg; ++t) {
+    const SegInfo& si = s_seg[t];
+    const int n = si.npg;
+    const int32_t* pt = p.page_table + static_cast<int64_t>(si.s) * p.mpps;
+    for (int i = tid; i < n; i += kWarps * 32) {
+      const int32_t slot = si.slot0 + i;
+      int32_t page = -1;
+      if (slot >= p.mpps) {
+        report_error(p.ws, RPA_DEVERR_LENGTHS, si.s);
+      } else {
+        page = __ldg(pt + slot);
+        if (page < 0 || page >= p.num_pages) {
+          report_error(p.ws, RPA_DEVERR_PAGE_ID, si.s);
+          page = -1;
+        }
+      }
+      if (si.pg_off + i < kMaxCtaPages) s_pages[si.pg_off + i] = page;
+    }
+  }
+  // ---- Q of the first two segments; zero the merge buffer.
+  for (int t = 0; t < 2 && t < nseg; ++t) {
+    const SegInfo& si = s_seg[t];
+    if (si.bad) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.q + (static_cast<int64_t>(si.q0) * p.hq + si.g * G) * D);
+    uint4* dst = reinterpret_cast<uint4*>(qs + t * 8 * D);
+    for (int e = tid; e < G * D / 8; e += kWarps * 32) dst[e] = src[e];
+  }
+  for (int e = tid; e < 8 * L::kORow; e += kWarps * 32) so[e] = 0.f;
   __syncthreads();
 
-  __nv_bfloat16* ring = smem + warp * S * 2 * TILE;  // this warp's S stages of K then V
-  // Issue the copies of this warp's i-th block into stage st (always commits).
-  auto issue = [&](int i, int st) {
-    if (i < my_blocks) {
-      const int32_t key0 = kb + (warp + i * kWarps) * kBlk;
-      // Lanes 0..15 look up the page of one key each.
+  const int32_t psize = 1 << p.page_shift;
+  __nv_bfloat16* ring = rings + warp * S * 2 * TILE;
+  // Issue cursor over this warp's blocks: segment ist, local block isj.
+  int ist = 0, isj = warp;
+  while (ist < nseg && isj >= s_seg[ist].nb) { ++ist; isj = warp; }
+  auto issue = [&](int st) {
+    if (ist < nseg) {
+      const SegInfo& si = s_seg[ist];
+      const int32_t key0 = si.kb + isj * kBlk;
       int32_t page = 0;
       bool ok = false;
       if (lane < kBlk) {
         const int32_t key = key0 + lane;
-        const int32_t idx = (key >> p.page_shift) - slot0;
-        if (key < ke && idx < kMaxSplitPages) {
+        const int32_t idx = si.pg_off + (key >> p.page_shift) - si.slot0;
+        if (key < si.ke && idx < kMaxCtaPages) {
           page = s_pages[idx];
           ok = page >= 0;
         }
@@ -182,6 +282,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(DecodePara
       if (lane == 0) valid_mask[warp][st] = vmask;
       __nv_bfloat16* kt = ring + st * 2 * TILE;
       __nv_bfloat16* vt = kt + TILE;
+      const int g = si.g;
 #pragma unroll
       for (int r0 = 0; r0 < kBlk; r0 += RPI) {
         const int r = r0 + lane / CPR;
@@ -194,231 +295,269 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(DecodePara
         cp_async16(smem_u32(kt + swz<D>(r, ch)), v ? p.k + off : p.k, v);
         cp_async16(smem_u32(vt + swz<D>(r, ch)), v ? p.v + off : p.v, v);
       }
+      isj += kWarps;
+      while (ist < nseg && isj >= s_seg[ist].nb) { ++ist; isj = warp; }
     }
     cp_async_commit();
   };
 #pragma unroll
-  for (int i = 0; i < S - 1; ++i) issue(i, i);
+  for (int i = 0; i < S - 1; ++i) issue(i);
 
-  // Q^T as the B operand: lane holds head lane/4, dims 2(lane%4)+{0,1} (+8).
-  // Loaded after the first copies are in flight.
-  uint32_t qf[KT][2];
-  {
-    const int h = lane >> 2;
-    const bool hv = h < G;
-    const __nv_bfloat16* qr = p.q + (static_cast<int64_t>(q0) * p.hq + g * G + (hv ? h : 0)) * D;
-#pragma unroll
-    for (int kt = 0; kt < KT; ++kt) {
-      const int d0 = kt * 16 + 2 * (lane & 3);
-      qf[kt][0] = hv ? *reinterpret_cast<const uint32_t*>(qr + d0) : 0u;
-      qf[kt][1] = hv ? *reinterpret_cast<const uint32_t*>(qr + d0 + 8) : 0u;
-    }
-  }
-
-  float m[2] = {-INFINITY, -INFINITY};  // running max (log2 domain), heads 2(lane%4)+j
-  float l[2] = {0.f, 0.f};              // this lane's share of the running sum
-  float o[KT][4];
-#pragma unroll
-  for (int mt = 0; mt < KT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-
-  for (int i = 0; i < my_blocks; ++i) {
-    issue(i + S - 1, (i + S - 1) % S);
-    cp_async_wait<S - 1>();
-    __syncwarp();
-    const int st = i % S;
-    const __nv_bfloat16* kt = ring + st * 2 * TILE;
-    const __nv_bfloat16* vt = kt + TILE;
-    const uint32_t vmask = valid_mask[warp][st];
-
-    // Scores S^T = K Q^T for 16 keys x 8 heads (two chains for latency).
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+  int count = 0;  // blocks consumed by this warp
+  for (int t = 0; t < nseg; ++t) {
+    const SegInfo si = s_seg[t];
+    // Q^T as the B operand: lane holds head lane/4, dims 2(lane%4)+{0,1} (+8).
+    uint32_t qf[KT][2];
     {
-      const int row = lane & 15;
-      const int hi = lane >> 4;
+      const int h = lane >> 2;
+      const bool hv = h < G;
+      const __nv_bfloat16* qr = qs + (t & 1) * 8 * D + (hv ? h : 0) * D;
 #pragma unroll
-      for (int kt2 = 0; kt2 < KT; ++kt2) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(smem_u32(kt + swz<D>(row, 2 * kt2 + hi)), a0, a1, a2, a3);
-        if (kt2 & 1) mma_bf16(sb, a0, a1, a2, a3, qf[kt2][0], qf[kt2][1]);
-        else mma_bf16(sa, a0, a1, a2, a3, qf[kt2][0], qf[kt2][1]);
+      for (int kt = 0; kt < KT; ++kt) {
+        const int d0 = kt * 16 + 2 * (lane & 3);
+        qf[kt][0] = hv ? *reinterpret_cast<const uint32_t*>(qr + d0) : 0u;
+        qf[kt][1] = hv ? *reinterpret_cast<const uint32_t*>(qr + d0 + 8) : 0u;
       }
     }
-    // Row (key) validity: rows lane/4 and lane/4 + 8.
-    const int r_top = lane >> 2, r_bot = r_top + 8;
-    const bool v_top = (vmask >> r_top) & 1u, v_bot = (vmask >> r_bot) & 1u;
-    float x[4];
-    x[0] = v_top ? (sa[0] + sb[0]) * p.scale_log2 : -INFINITY;
-    x[1] = v_top ? (sa[1] + sb[1]) * p.scale_log2 : -INFINITY;
-    x[2] = v_bot ? (sa[2] + sb[2]) * p.scale_log2 : -INFINITY;
-    x[3] = v_bot ? (sa[3] + sb[3]) * p.scale_log2 : -INFINITY;
-    float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+    float m[2] = {-INFINITY, -INFINITY};  // running max (log2 domain), heads 2(lane%4)+j
+    float l[2] = {0.f, 0.f};              // this lane's share of the running sum
+    float o[KT][4];
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    // Every block holds at least one valid key, so the new max is finite.
-    const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-    const float al0 = fast_exp2(m[0] - mn0), al1 = fast_exp2(m[1] - mn1);
-    m[0] = mn0;
-    m[1] = mn1;
-    const float p0 = fast_exp2(x[0] - mn0), p1 = fast_exp2(x[1] - mn1);
-    const float p2 = fast_exp2(x[2] - mn0), p3 = fast_exp2(x[3] - mn1);
-    l[0] = l[0] * al0 + p0 + p2;
-    l[1] = l[1] * al1 + p1 + p3;
+    for (int mt = 0; mt < KT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    for (int j = warp; j < si.nb; j += kWarps, ++count) {
+      issue((count + S - 1) % S);
+      cp_async_wait<S - 1>();
+      __syncwarp();
+      const int st = count % S;
+      const __nv_bfloat16* kt = ring + st * 2 * TILE;
+      const __nv_bfloat16* vt = kt + TILE;
+      const uint32_t vmask = valid_mask[warp][st];
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int row = lane & 15;
+        const int hi = lane >> 4;
 #pragma unroll
-    for (int mt = 0; mt < KT; ++mt) {
-      o[mt][0] *= al0;
-      o[mt][1] *= al1;
-      o[mt][2] *= al0;
-      o[mt][3] *= al1;
-    }
-    // P^T as the B operand of O^T += V^T P^T.
-    const uint32_t b0 = transpose8x8(pack_bf16x2(p0, p1));
-    const uint32_t b1 = transpose8x8(pack_bf16x2(p2, p3));
-    {
-      const int row = (lane & 7) + ((lane >> 4) << 3);
-      const int hi = (lane >> 3) & 1;
+        for (int kt2 = 0; kt2 < KT; ++kt2) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(smem_u32(kt + swz<D>(row, 2 * kt2 + hi)), a0, a1, a2, a3);
+          if (kt2 & 1) mma_bf16(sb, a0, a1, a2, a3, qf[kt2][0], qf[kt2][1]);
+          else mma_bf16(sa, a0, a1, a2, a3, qf[kt2][0], qf[kt2][1]);
+        }
+      }
+      const int r_top = lane >> 2, r_bot = r_top + 8;
+      const bool v_top = (vmask >> r_top) & 1u, v_bot = (vmask >> r_bot) & 1u;
+      float x[4];
+      x[0] = v_top ? (sa[0] + sb[0]) * p.scale_log2 : -INFINITY;
+      x[1] = v_top ? (sa[1] + sb[1]) * p.scale_log2 : -INFINITY;
+      x[2] = v_bot ? (sa[2] + sb[2]) * p.scale_log2 : -INFINITY;
+      x[3] = v_bot ? (sa[3] + sb[3]) * p.scale_log2 : -INFINITY;
+      float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      // Every block holds at least one valid key, so the new max is finite.
+      const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+      const float al0 = fast_exp2(m[0] - mn0), al1 = fast_exp2(m[1] - mn1);
+      m[0] = mn0;
+      m[1] = mn1;
+      const float p0 = fast_exp2(x[0] - mn0), p1 = fast_exp2(x[1] - mn1);
+      const float p2 = fast_exp2(x[2] - mn0), p3 = fast_exp2(x[3] - mn1);
+      l[0] = l[0] * al0 + p0 + p2;
+      l[1] = l[1] * al1 + p1 + p3;
 #pragma unroll
       for (int mt = 0; mt < KT; ++mt) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(smem_u32(vt + swz<D>(row, 2 * mt + hi)), a0, a1, a2, a3);
-        mma_bf16(o[mt], a0, a1, a2, a3, b0, b1);
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+      const uint32_t b0 = transpose8x8(pack_bf16x2(p0, p1));
+      const uint32_t b1 = transpose8x8(pack_bf16x2(p2, p3));
+      {
+        const int row = (lane & 7) + ((lane >> 4) << 3);
+        const int hi = (lane >> 3) & 1;
+#pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(smem_u32(vt + swz<D>(row, 2 * mt + hi)), a0, a1, a2, a3);
+          mma_bf16(o[mt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+      __syncwarp();
+    }
+
+    // ---- Merge the four warps' states for segment t.
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+      l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+    }
+    if (lane < 4) {
+      wm[warp][2 * lane] = m[0];
+      wm[warp][2 * lane + 1] = m[1];
+      wl[warp][2 * lane] = l[0];
+      wl[warp][2 * lane + 1] = l[1];
+    }
+    __syncthreads();
+    // Q of segment t + 2 goes into the buffer segment t used.
+    uint4 qn[2];
+    const bool load_q = t + 2 < nseg && !s_seg[t + 2].bad;
+    const __nv_bfloat16* qsrc = nullptr;
+    if (load_q) {
+      const SegInfo& sn = s_seg[t + 2];
+      qsrc = p.q + (static_cast<int64_t>(sn.q0) * p.hq + sn.g * G) * D;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int e = tid + r * kWarps * 32;
+        if (e < G * D / 8) qn[r] = reinterpret_cast<const uint4*>(qsrc)[e];
       }
     }
-    __syncwarp();
+    {
+      const int h0 = 2 * (lane & 3);
+      float f[2];
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w][h0 + jj]);
+        f[jj] = (m[jj] == -INFINITY) ? 0.f : fast_exp2(m[jj] - M);
+      }
+      const bool h0v = h0 < G && f[0] != 0.f, h1v = h0 + 1 < G && f[1] != 0.f;
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        const int d = mt * 16 + (lane >> 2);
+        if (h0v) {
+          atomicAdd(so + h0 * L::kORow + d, o[mt][0] * f[0]);
+          atomicAdd(so + h0 * L::kORow + d + 8, o[mt][2] * f[0]);
+        }
+        if (h1v) {
+          atomicAdd(so + (h0 + 1) * L::kORow + d, o[mt][1] * f[1]);
+          atomicAdd(so + (h0 + 1) * L::kORow + d + 8, o[mt][3] * f[1]);
+        }
+      }
+    }
+    if (load_q) {
+      uint4* dst = reinterpret_cast<uint4*>(qs + (t & 1) * 8 * D);
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int e = tid + r * kWarps * 32;
+        if (e < G * D / 8) dst[e] = qn[r];
+      }
+    }
+    __syncthreads();
+    // Normalise; write the output (whole segment) or this CTA's partial.
+    const int slot = sc.slot_base + 2 * c + (t == 0 ? 0 : 1);
+    for (int e = tid * 4; e < (si.bad ? 0 : G * D); e += kWarps * 32 * 4) {
+      const int h = e / D, d = e % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w][h]);
+      float Lsum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w)
+        Lsum += (wm[w][h] == -INFINITY) ? 0.f : wl[w][h] * fast_exp2(wm[w][h] - M);
+      const float inv = 1.f / Lsum;
+      float* src = so + h * L::kORow + d;
+      const float4 u = make_float4(src[0] * inv, src[1] * inv, src[2] * inv, src[3] * inv);
+      src[0] = src[1] = src[2] = src[3] = 0.f;
+      if (si.whole) {
+        uint2 pk;
+        pk.x = pack_bf16x2(u.x, u.y);
+        pk.y = pack_bf16x2(u.z, u.w);
+        *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(si.q0) * p.hq + si.g * G + h) * D + d) = pk;
+      } else {
+        *reinterpret_cast<float4*>(p.part_o + (static_cast<int64_t>(slot) * G + h) * D + d) = u;
+        if (d == 0) p.part_lse[static_cast<int64_t>(slot) * G + h] = M + __log2f(Lsum);
+      }
+    }
+    __syncthreads();
   }
   cp_async_wait<0>();
 
-  // Reduce l over the lanes holding the same heads.
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
-    l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
-  }
-  if (lane < 4) {
-    wm[warp][2 * lane] = m[0];
-    wm[warp][2 * lane + 1] = m[1];
-    wl[warp][2 * lane] = l[0];
-    wl[warp][2 * lane + 1] = l[1];
-  }
-  __syncthreads();  // every warp is done with its ring: reuse it for the merge
-  float* so = reinterpret_cast<float*>(smem_raw);  // [kWarps][8][D]
-  {
-    // Scale this warp's O^T by exp2(m_w - M) before summing over warps.
-    const int h0 = 2 * (lane & 3);
-    float f[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
+  // ---- Arrivals for the cut segments (first and last of the range).
+  for (int which = 0; which < 2; ++which) {
+    const int t = which == 0 ? 0 : nseg - 1;
+    if (which == 1 && nseg == 1) break;
+    const SegInfo si = s_seg[t];
+    if (si.whole || si.bad) continue;
+    const int k = si.gseg;
+    const int ca = sc.blk0[k] / sc.bpc;
+    const int cb = (sc.blk0[k + 1] - 1) / sc.bpc;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0)
+      s_last = atomicAdd(p.arrivals + sc.seg_base + k, 1) == (cb - ca);
+    __syncthreads();
+    if (!s_last) continue;
+    __threadfence();
+    // Slots: the first CTA holds this segment in slot 0 if the segment starts
+    // its range, else in slot 1; every later CTA holds it in slot 0.
+    const int first_slot = (sc.blk0[k] != ca * sc.bpc) ? 1 : 0;
+    for (int e = tid * 4; e < G * D; e += kWarps * 32 * 4) {
+      const int h = e / D, d = e % D;
       float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w][h0 + j]);
-      f[j] = (m[j] == -INFINITY) ? 0.f : fast_exp2(m[j] - M);
+      for (int cc = ca; cc <= cb; ++cc) {
+        const int sl = sc.slot_base + 2 * cc + (cc == ca ? first_slot : 0);
+        M = fmaxf(M, __ldcg(p.part_lse + static_cast<int64_t>(sl) * G + h));
+      }
+      float wsum = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int cc = ca; cc <= cb; ++cc) {
+        const int sl = sc.slot_base + 2 * cc + (cc == ca ? first_slot : 0);
+        const float w = fast_exp2(__ldcg(p.part_lse + static_cast<int64_t>(sl) * G + h) - M);
+        const float4 u = __ldcg(reinterpret_cast<const float4*>(
+            p.part_o + (static_cast<int64_t>(sl) * G + h) * D + d));
+        wsum += w;
+        acc.x += w * u.x; acc.y += w * u.y; acc.z += w * u.z; acc.w += w * u.w;
+      }
+      const float inv = 1.f / wsum;
+      uint2 pk;
+      pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(si.q0) * p.hq + si.g * G + h) * D + d) = pk;
     }
-    float* base = so + warp * 8 * D;
-#pragma unroll
-    for (int mt = 0; mt < KT; ++mt) {
-      const int d = mt * 16 + (lane >> 2);
-      base[h0 * D + d] = o[mt][0] * f[0];
-      base[(h0 + 1) * D + d] = o[mt][1] * f[1];
-      base[h0 * D + d + 8] = o[mt][2] * f[0];
-      base[(h0 + 1) * D + d + 8] = o[mt][3] * f[1];
-    }
+    if (tid == 0) p.arrivals[sc.seg_base + k] = 0;  // ready for the next call
+    __syncthreads();
   }
-  __syncthreads();
-  // Final values for G heads x D dims: 8 consecutive dims per thread step.
-  for (int e = threadIdx.x * 8; e < G * D; e += kWarps * 32 * 8) {
-    const int h = e / D, d = e % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w][h]);
-    float Lsum = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w)
-      Lsum += (wm[w][h] == -INFINITY) ? 0.f : wl[w][h] * fast_exp2(wm[w][h] - M);
-    float acc[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float4* src = reinterpret_cast<const float4*>(so + (w * 8 + h) * D + d);
-      const float4 u = src[0], v = src[1];
-      acc[0] += u.x; acc[1] += u.y; acc[2] += u.z; acc[3] += u.w;
-      acc[4] += v.x; acc[5] += v.y; acc[6] += v.z; acc[7] += v.w;
-    }
-    const float inv = 1.f / Lsum;
-    const int hq_idx = g * G + h;
-    if (nsplit == 1) {
-      uint4 pk;
-      pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-      pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-      pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-      pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-      *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(q0) * p.hq + hq_idx) * D + d) = pk;
-    } else {
-      const int64_t row = (static_cast<int64_t>(s) * p.max_splits + c) * p.hq + hq_idx;
-      float4* dst = reinterpret_cast<float4*>(p.part_o + row * D + d);
-      dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-      dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
-      if (d == 0) p.part_lse[row] = M + __log2f(Lsum);
-    }
-  }
-  if (nsplit == 1) return;
-
-  // Arrival: the last split of (sequence, KV head) to finish merges them all.
-  __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(p.arrivals + s * p.hkv + g, 1) == nsplit - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const int ns = min(nsplit, kMaxMergeSplits);
-  float* s_lse = reinterpret_cast<float*>(smem_raw);  // [ns][G], ring is free
-  const int64_t row0 = static_cast<int64_t>(s) * p.max_splits * p.hq + g * G;
-  for (int i = threadIdx.x; i < ns * G; i += kWarps * 32)
-    s_lse[i] = __ldcg(p.part_lse + row0 + static_cast<int64_t>(i / G) * p.hq + i % G);
-  __syncthreads();
-  for (int e = threadIdx.x * 4; e < G * D; e += kWarps * 32 * 4) {
-    const int h = e / D, d = e % D;
-    float M = -INFINITY;
-    for (int k = 0; k < ns; ++k) M = fmaxf(M, s_lse[k * G + h]);
-    float wsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < ns; ++k) {
-      const float w = fast_exp2(s_lse[k * G + h] - M);
-      const float4 u = __ldcg(reinterpret_cast<const float4*>(
-          p.part_o + (row0 + static_cast<int64_t>(k) * p.hq + h) * D + d));
-      wsum += w;
-      acc.x += w * u.x; acc.y += w * u.y; acc.z += w * u.z; acc.w += w * u.w;
-    }
-    const float inv = 1.f / wsum;
-    uint2 pk;
-    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(q0) * p.hq + g * G + h) * D + d) = pk;
-  }
-  if (threadIdx.x == 0) p.arrivals[s * p.hkv + g] = 0;  // ready for the next call
 }
 
-template <int D>
-constexpr size_t decode_smem() {
-  return static_cast<size_t>(kWarps) * stages_for(D) * 2 * kBlk * D * sizeof(__nv_bfloat16);
-}
-
-template <int D>
-int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
-  static_assert(decode_smem<D>() >= kWarps * 8 * D * sizeof(float), "merge buffer fits");
-  static_assert(decode_smem<D>() >= kMaxMergeSplits * 8 * sizeof(float), "lse buffer fits");
-  constexpr size_t smem = decode_smem<D>();
+template <int D, int NSEG>
+int launch_one(const Plan& plan, const DecodeParams& p, const Plan::DecodeLaunch& dl,
+               cudaStream_t stream) {
+  constexpr size_t smem = DecodeSmem<D>::kBytes;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, NSEG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return static_cast<int>(e);
     configured = true;
   }
+  static DecodeSched<NSEG> sc;  // host staging; copied into the launch parameters
+  const int n = dl.seg_end - dl.seg_begin;
+  sc.n_seg = n;
+  sc.bpc = dl.bpc;
+  sc.slot_base = dl.slot_base;
+  sc.seg_base = dl.seg_begin;
+  const int32_t base = plan.dseg_blk0[dl.seg_begin];
+  for (int i = 0; i < n; ++i) {
+    sc.seqhead[i] = plan.dseg_seqhead[dl.seg_begin + i];
+    sc.blk0[i] = plan.dseg_blk0[dl.seg_begin + i] - base;
+  }
+  sc.blk0[n] = plan.dseg_blk0[dl.seg_end] - base;
+  sc.n_blocks = sc.blk0[n];
+  decode_kernel<D, NSEG><<<dl.n_ctas, kWarps * 32, smem, stream>>>(p, sc);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return static_cast<int>(e);
+  trace_mark(RPA_KERNEL_DECODE_SPLIT, stream);
+  return 0;
+}
+
+template <int D>
+int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   DecodeParams p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.k = static_cast<const __nv_bfloat16*>(a.k_pages);
@@ -429,10 +568,9 @@ int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   p.window = a.window;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.ws = a.workspace;
-  p.part_o = plan.max_splits > 1 ? reinterpret_cast<float*>(a.workspace + plan.off_partial_o) : nullptr;
-  p.part_lse = plan.max_splits > 1 ? reinterpret_cast<float*>(a.workspace + plan.off_partial_lse) : nullptr;
-  p.arrivals = plan.max_splits > 1 ? reinterpret_cast<int32_t*>(a.workspace + plan.off_arrivals) : nullptr;
-  p.num_seqs = plan.num_seqs;
+  p.part_o = reinterpret_cast<float*>(a.workspace + plan.off_partial_o);
+  p.part_lse = reinterpret_cast<float*>(a.workspace + plan.off_partial_lse);
+  p.arrivals = reinterpret_cast<int32_t*>(a.workspace + plan.off_arrivals);
   p.hq = plan.hq;
   p.hkv = plan.hkv;
   p.group = plan.hq / plan.hkv;
@@ -441,14 +579,13 @@ int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   p.page_shift = shift;
   p.mpps = plan.mpps;
   p.num_pages = plan.num_pages;
-  p.kv_split = plan.kv_split;
-  p.max_splits = plan.max_splits;
   p.scale_log2 = a.sm_scale * 1.4426950408889634f;
-  dim3 grid(plan.num_seqs, plan.max_splits, plan.hkv);
-  decode_split_kernel<D><<<grid, kWarps * 32, smem, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return static_cast<int>(e);
-  trace_mark(RPA_KERNEL_DECODE_SPLIT, stream);
+  for (const Plan::DecodeLaunch& dl : plan.dlaunch) {
+    const int n = dl.seg_end - dl.seg_begin;
+    const int err = n <= kDecodeSegSmall ? launch_one<D, kDecodeSegSmall>(plan, p, dl, stream)
+                                         : launch_one<D, kDecodeSegLarge>(plan, p, dl, stream);
+    if (err) return err;
+  }
   return 0;
 }
 
@@ -489,13 +626,7 @@ bool decode_supported(int32_t head_dim, int32_t group) {
   return (head_dim == 64 || head_dim == 128 || head_dim == 256) && group >= 1 && group <= 8;
 }
 
-int decode_ctas_per_sm(int32_t head_dim) {
-  switch (head_dim) {
-    case 64: return static_cast<int>(220 * 1024 / decode_smem<64>());
-    case 128: return static_cast<int>(220 * 1024 / decode_smem<128>());
-    default: return static_cast<int>(220 * 1024 / decode_smem<256>());
-  }
-}
+int decode_ctas_per_sm(int32_t) { return 1; }
 
 int launch_decode(const Plan& plan, const Args& a, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);

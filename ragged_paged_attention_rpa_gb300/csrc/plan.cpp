@@ -27,7 +27,6 @@
 
 namespace rpa {
 
-int decode_ctas_per_sm(int32_t head_dim);   // decode.cu
 int prefill_ctas_per_sm(int32_t head_dim);  // prefill_tc.cu
 int prefill_tokens_per_block(int32_t head_dim, int32_t group);  // prefill_tc.cu
 
@@ -53,112 +52,80 @@ inline int64_t decode_visible(int32_t L, int32_t w) {
   return L - lo;
 }
 
-// Makespan, in token-equivalents per CTA slot, of greedy in-order dispatch of
-// `costs` onto `slots` identical slots (what the block scheduler does with a
-// one-CTA-per-slot grid).
-double list_schedule(const std::vector<double>& costs, int slots) {
-  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
-  for (int i = 0; i < slots; ++i) free_at.push(0.0);
-  double end = 0.0;
-  for (double c : costs) {
-    double t = free_at.top();
-    free_at.pop();
-    t += c;
-    end = std::max(end, t);
-    free_at.push(t);
-  }
-  return end;
-}
-
-// Fixed cost of one decode CTA (launch, prologue, merge) and of the combine
-// launch, in tokens streamed by one CTA slot in the same time.
-constexpr double kCtaOverheadTokens = 96.0;
-constexpr double kCombineLaunchTokens = 128.0;
-
+// Decode schedule: the visible keys of every (decode sequence, KV head) pair
+// form a segment of 16-key blocks; the blocks of all segments are laid end to
+// end and cut into equal contiguous ranges, one per CTA (one per SM: a single
+// balanced wave), so every CTA streams the same number of bytes whatever the
+// length mix.  Ranges shrink (more CTAs) only when one would touch more
+// segments or pages than the kernel's shared-memory tables hold.
 void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t* win,
-                 int32_t forced_split) {
-  std::vector<int64_t> vis;
-  std::vector<int32_t> seqs;
+                 int32_t forced_tokens) {
+  plan.dseg_seqhead.clear();
+  plan.dseg_blk0.assign(1, 0);
+  plan.dlaunch.clear();
+  std::vector<int32_t> seg_lo;  // first visible key of each segment
+  int32_t ndec = 0;
   for (int32_t s = 0; s < plan.num_seqs; ++s) {
     if (cu[s + 1] - cu[s] != 1) continue;
-    seqs.push_back(s);
-    vis.push_back(decode_visible(kv[s], win ? win[s] : 0));
-  }
-  plan.num_decode = static_cast<int32_t>(seqs.size());
-  if (seqs.empty()) return;
-  const int slots = plan.num_sms * decode_ctas_per_sm(plan.d);
-  const int32_t group = plan.hq / plan.hkv;
-  std::vector<int32_t> candidates;
-  // A split's page ids must fit the kernel's shared-memory table, and a
-  // sequence may have at most kMaxSplits splits.
-  const int64_t max_split_len = std::max<int64_t>(64, (kMaxSplitPages - 2) / 64 * 64 * plan.p);
-  int64_t max_vis0 = 1;
-  for (int64_t n : vis) max_vis0 = std::max(max_vis0, n);
-  const int64_t min_split_len = ceil_div(ceil_div(max_vis0, kMaxSplits), 64) * 64;
-  auto clamp_split = [&](int64_t x) {
-    x = std::max<int64_t>(x, min_split_len);
-    x = std::min<int64_t>(x, max_split_len);
-    return static_cast<int32_t>(std::max<int64_t>(64, x));
-  };
-  if (forced_split > 0) {
-    candidates.push_back(clamp_split(ceil_div(forced_split, 64) * 64));
-  } else {
-    for (int32_t c : {64, 128, 192, 256, 320, 384, 512, 640, 768, 1024, 1536, 2048, 3072, 4096})
-      candidates.push_back(clamp_split(c));
-  }
-  // Evaluate the candidate nearest to two waves first so that the lower bound
-  // below prunes most of the others without simulating them.
-  int64_t total_vis = 0, max_vis = 0;
-  for (int64_t n : vis) {
-    total_vis += n;
-    max_vis = std::max(max_vis, n);
-  }
-  const double two_waves = static_cast<double>(total_vis) * plan.hkv / (2.0 * slots);
-  std::stable_sort(candidates.begin(), candidates.end(), [&](int32_t a, int32_t b) {
-    return std::abs(a - two_waves) < std::abs(b - two_waves);
-  });
-  double best = -1.0;
-  int32_t best_split = candidates.front();
-  std::vector<double> costs;
-  for (int32_t split : candidates) {
-    // Lower bound: total work over the slots, or the longest CTA.
-    int64_t ctas = 0;
-    for (int64_t n : vis) ctas += ceil_div(n, split);
-    ctas *= plan.hkv;
-    const double lb = std::max(
-        (static_cast<double>(total_vis) * plan.hkv + kCtaOverheadTokens * ctas) / slots,
-        kCtaOverheadTokens + static_cast<double>(std::min<int64_t>(split, max_vis)));
-    if (best >= 0 && lb >= best) continue;
-    // Grid order: x = sequence (fastest), y = split, z = kv head.
-    int64_t max_n = 0;
-    for (int64_t n : vis) max_n = std::max(max_n, ceil_div(n, split));
-    costs.clear();
-    costs.reserve(static_cast<size_t>(ctas));
-    bool any_multi = false;
-    for (int32_t h = 0; h < plan.hkv; ++h)
-      for (int64_t c = 0; c < max_n; ++c)
-        for (size_t i = 0; i < vis.size(); ++i) {
-          int64_t n = ceil_div(vis[i], split);
-          if (c >= n) continue;
-          int64_t tok = std::min<int64_t>(split, vis[i] - c * split);
-          any_multi |= n > 1;
-          // A split writes and the combine reads G x D fp32 partials: 2G tokens.
-          costs.push_back(kCtaOverheadTokens + tok + (n > 1 ? 2.0 * group : 0.0));
-        }
-    double t = list_schedule(costs, slots) + (any_multi ? kCombineLaunchTokens : 0.0);
-    if (best < 0 || t < best - 1e-9 || (std::abs(t - best) <= 1e-9 && split > best_split)) {
-      best = t;
-      best_split = split;
+    ++ndec;
+    const int32_t w = win ? win[s] : 0;
+    const int32_t lo = (w > 0 && kv[s] - w > 0) ? kv[s] - w : 0;
+    const int32_t nb = static_cast<int32_t>(ceil_div(kv[s] - lo, 16));
+    for (int32_t g = 0; g < plan.hkv; ++g) {
+      plan.dseg_seqhead.push_back((s << 8) | g);
+      plan.dseg_blk0.push_back(plan.dseg_blk0.back() + nb);
+      seg_lo.push_back(lo);
     }
   }
-  plan.kv_split = best_split;
-  int64_t max_n = 0, ctas = 0;
-  for (int64_t n : vis) {
-    max_n = std::max(max_n, ceil_div(n, best_split));
-    ctas += ceil_div(n, best_split);
+  plan.num_decode = ndec;
+  const int32_t nseg = static_cast<int32_t>(plan.dseg_seqhead.size());
+  if (nseg == 0) return;
+  const std::vector<int32_t>& blk0 = plan.dseg_blk0;
+  const int32_t P = plan.p;
+  // Segments and pages touched by CTA range [b0, b1) of launch segments [sb, se).
+  auto fits = [&](int32_t sb, int32_t se, int32_t bpc) {
+    const int32_t base = blk0[sb], total = blk0[se] - base;
+    int32_t k = sb;
+    for (int32_t b0 = 0; b0 < total; b0 += bpc) {
+      const int32_t b1 = std::min(total, b0 + bpc);
+      while (blk0[k + 1] - base <= b0) ++k;
+      int32_t segs = 0, pages = 0;
+      for (int32_t kk = k; kk < se && blk0[kk] - base < b1; ++kk) {
+        ++segs;
+        const int32_t jb = std::max(b0, blk0[kk] - base) - (blk0[kk] - base);
+        const int32_t je = std::min(b1, blk0[kk + 1] - base) - (blk0[kk] - base);
+        const int64_t kb = seg_lo[kk] + 16 * static_cast<int64_t>(jb);
+        const int64_t ke = seg_lo[kk] + 16 * static_cast<int64_t>(je);  // upper bound
+        pages += static_cast<int32_t>((ke - 1) / P - kb / P + 1);
+      }
+      if (segs > kMaxCtaSegs || pages > kMaxCtaPages) return false;
+    }
+    return true;
+  };
+  int32_t slot_base = 0;
+  int64_t max_splits = 1, ctas = 0;
+  for (int32_t sb = 0; sb < nseg; sb += kDecodeSegLarge) {
+    const int32_t se = std::min(nseg, sb + kDecodeSegLarge);
+    const int32_t total = blk0[se] - blk0[sb];
+    int32_t bpc = forced_tokens > 0
+                      ? static_cast<int32_t>(ceil_div(forced_tokens, 16))
+                      : static_cast<int32_t>(ceil_div(total, static_cast<int64_t>(plan.num_sms)));
+    bpc = std::max<int32_t>(1, bpc);
+    while (bpc > 1 && !fits(sb, se, bpc)) bpc = std::max<int32_t>(1, bpc * 3 / 4);
+    const int32_t n_ctas = static_cast<int32_t>(ceil_div(total, bpc));
+    plan.dlaunch.push_back({sb, se, bpc, n_ctas, slot_base});
+    slot_base += 2 * n_ctas;
+    ctas += n_ctas;
+    for (int32_t k = sb; k < se; ++k) {
+      const int64_t ca = (blk0[k] - blk0[sb]) / bpc;
+      const int64_t cb = (blk0[k + 1] - 1 - blk0[sb]) / bpc;
+      max_splits = std::max<int64_t>(max_splits, cb - ca + 1);
+    }
   }
-  plan.max_splits = static_cast<int32_t>(std::max<int64_t>(max_n, 1));
-  plan.decode_ctas = ctas * plan.hkv;
+  plan.kv_split = plan.dlaunch.front().bpc * 16;
+  plan.max_splits = static_cast<int32_t>(max_splits);
+  plan.decode_ctas = ctas;
+  plan.dec_slots = slot_base;
 }
 
 void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t* win,
@@ -240,8 +207,11 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
                   : RPA_PATH_SIMT;
 
   plan.num_decode = ndec;
-  plan.kv_split = plan.max_splits = 0;
+  plan.kv_split = plan.max_splits = plan.dec_slots = 0;
   plan.decode_ctas = 0;
+  plan.dseg_seqhead.clear();
+  plan.dseg_blk0.clear();
+  plan.dlaunch.clear();
   if (tc_decode && ndec > 0) plan_decode(plan, cu, kv, win, opts.kv_split);
 
   plan.items.clear();
@@ -249,17 +219,19 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
   plan.prefill_ctas = 0;
   if (tc_prefill && plan.num_prefill > 0) plan_prefill(plan, cu, kv, win, opts.q_block);
 
-  // Workspace: header, then decode partials when some sequence splits.
+  // Workspace: header, then the decode partials (two slots per decode CTA,
+  // G x D fp32 each, plus G log2-sum-exps) and one arrival counter per
+  // decode segment.
   size_t off = kHeaderBytes;
-  plan.off_partial_o = plan.off_partial_lse = 0;
-  if (plan.max_splits > 1) {
-    const size_t rows = static_cast<size_t>(plan.num_seqs) * plan.max_splits * plan.hq;
+  plan.off_partial_o = plan.off_partial_lse = plan.off_arrivals = 0;
+  if (!plan.dlaunch.empty()) {
+    const size_t rows = static_cast<size_t>(plan.dec_slots) * group;
     plan.off_partial_o = off;
     off += (rows * plan.d * sizeof(float) + 255) / 256 * 256;
     plan.off_partial_lse = off;
     off += (rows * sizeof(float) + 255) / 256 * 256;
     plan.off_arrivals = off;
-    off += (static_cast<size_t>(plan.num_seqs) * plan.hkv * sizeof(int32_t) + 255) / 256 * 256;
+    off += (plan.dseg_seqhead.size() * sizeof(int32_t) + 255) / 256 * 256;
   }
   plan.ws_bytes = off;
   return RPA_OK;

@@ -21,11 +21,13 @@
 //              gathered page by page through the page table (2-stage ring);
 //   warp 1     MMA issuer: S = Q K^T (SMEM x SMEM -> TMEM), O += P V (P read
 //              from TMEM, V from SMEM), tcgen05.commit onto mbarriers;
-//   warps 2-5  softmax: one thread per row, reads S from TMEM, masks causal
-//              and window edges, keeps the running max / sum, writes P (bf16)
-//              to TMEM, rescales O in TMEM only when the max grew by more than
-//              2^8 (the result is the same; it bounds P by 256); epilogue
-//              O / l -> bf16 -> global.
+//   warps 2-9  softmax: two warps per 32-row quarter, each taking 32 of a
+//              tile's 64 keys; reads S from TMEM, masks causal and window edges
+//              (interior half-tiles skip the mask), exchanges row maxima with
+//              its partner through shared memory, keeps the running max / sum,
+//              writes P (bf16) to TMEM, rescales its half of O in TMEM only
+//              when the max grew by more than 2^8 (the result is the same; it
+//              bounds P by 256); epilogue O / l -> bf16 -> global.
 // Every wait is bounded; on a timeout the CTA records RPA_DEVERR_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -44,7 +46,7 @@ using namespace sm100;
 
 constexpr int kBM = 128;        // MMA rows per block
 constexpr int kBN = 64;         // keys per KV tile
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;   // producer, MMA, 8 softmax warps
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait, then give up
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
 
@@ -73,7 +75,7 @@ struct Layout {
   static constexpr int kKOff = kQOff + kQBytes;          // 2 stages
   static constexpr int kVOff = kKOff + 2 * kKVBytes;     // 2 stages
   static constexpr int kBarOff = kVOff + 2 * kKVBytes;
-  static constexpr int kUsed = kBarOff + 256 + 1024;    // barriers + alignment slack
+  static constexpr int kUsed = kBarOff + 4096 + 1024;   // barriers + exchange + alignment slack
   // Ask for more than half an SM's shared memory so that exactly one CTA
   // (which owns the SM's tensor memory) is resident per SM.
   static constexpr int kBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
@@ -92,6 +94,9 @@ struct Barriers {
   uint64_t fin;          // all MMAs of this CTA complete (teardown)
   uint32_t tmem_base;
   int abort;
+  uint64_t xbar[4];         // per row quarter: both softmax warps have posted their values
+  float xmax[2][2][4][32];  // row max of each half-tile, by tile parity / half / quarter / lane
+  float xl[2][4][32];       // row sums of each half, for the epilogue
 };
 
 struct Geom {
@@ -145,11 +150,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(&B.v_full[i], 1);
       mbar_init(&B.v_empty[i], 1);
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.p_full[i], 128);
+      mbar_init(&B.p_full[i], 256);
       mbar_init(&B.o_done[i], 1);
     }
-    mbar_init(&B.o_free, 128);
+    mbar_init(&B.o_free, 256);
     mbar_init(&B.fin, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&B.xbar[i], 64);
     B.abort = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_q);
@@ -310,10 +316,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int r = 32 * (warp & 3) + lane;               // TMEM lane = row
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    // Warps 2..9: quarter q = warp % 4 owns TMEM lanes (rows) 32q..32q+31;
+    // half hf owns key columns 32hf..32hf+31 of every 64-key tile and O
+    // columns [hf D/2, (hf+1) D/2).  The two warps of a quarter exchange row
+    // maxima (and, at the end, row sums) through shared memory.
+    const int q4 = warp & 3;
+    const int hf = (warp - 2) >> 2;
+    const int r = 32 * q4 + lane;                       // TMEM lane = row
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q4) << 16);
     const int tok = r / G, head = r % G;
+    const float c = p.scale_log2;
     uint32_t T = 0;
+    uint32_t xph = 0;   // phase of this quarter's exchange barrier
     bool alive = true;
     for (int it = blockIdx.x; it < items.n && alive; it += gridDim.x) {
       const Geom gm = item_geom(p, items.items[it]);
@@ -330,25 +344,42 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           break;
         }
         tc_fence_after();
-        uint32_t sr[2][32];
-        tmem_ld32(lane_addr + Lay::kSCol + st * kBN, sr[0]);
-        tmem_ld32(lane_addr + Lay::kSCol + st * kBN + 32, sr[1]);
+        uint32_t sr[32];
+        tmem_ld32(lane_addr + Lay::kSCol + st * kBN + hf * 32, sr);
         tmem_wait_ld();
-        const int32_t key0 = (gm.kt0 + j) * kBN;
-        float x[64];
+        const int32_t key0 = (gm.kt0 + j) * kBN + hf * 32;
+        // Interior half-tiles (every key visible to every row of the warp)
+        // skip the per-element mask; elsewhere masked scores become -inf.
+        const bool full = __all_sync(0xffffffffu, valid && key0 >= lo && key0 + 31 <= pos);
         float mx = -INFINITY;
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const int32_t key = key0 + c;
-          const bool vis = valid && key >= lo && key <= pos;
-          x[c] = vis ? __uint_as_float(sr[c >> 5][c & 31]) * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, x[c]);
+          for (int cc = 0; cc < 32; ++cc) mx = fmaxf(mx, __uint_as_float(sr[cc]));
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < 32; ++cc) {
+            const int32_t key = key0 + cc;
+            const bool vis = valid && key >= lo && key <= pos;
+            if (!vis) sr[cc] = __float_as_uint(-INFINITY);
+            mx = fmaxf(mx, __uint_as_float(sr[cc]));
+          }
         }
+        // Row max over both halves; scaling after the max keeps the order (c >= 0).
+        B.xmax[T & 1][hf][q4][lane] = mx;
+        mbar_arrive(&B.xbar[q4]);
+        if (!mbar_wait(&B.xbar[q4], xph, abort, kWaitNs)) {
+          alive = false;
+          break;
+        }
+        xph ^= 1;
+        mx = fmaxf(mx, B.xmax[T & 1][hf ^ 1][q4][lane]);
+        mx = (mx == -INFINITY) ? -INFINITY : mx * c;
         const float m_new = fmaxf(m_ref, mx);
         const bool grow = m_new > m_ref + 8.f;           // also true for the first visible key
-        const bool rescale_o = grow && l > 0.f;
+        const bool rescale_o = grow && m_ref != -INFINITY;
         if (__any_sync(0xffffffffu, rescale_o)) {
-          // O holds earlier tiles: wait for the last PV, then scale in TMEM.
+          // O holds earlier tiles: wait for the last PV, then scale this
+          // warp's half of the O columns in TMEM.
           const uint32_t Tp = T - 1;
           if (!mbar_wait(&B.o_done[Tp & 1], (Tp >> 1) & 1, abort, kWaitNs)) {
             alive = false;
@@ -357,12 +388,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           tc_fence_after();
           const float f = rescale_o ? fast_exp2(m_ref - m_new) : 1.f;
 #pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
             uint32_t o[32];
             tmem_ld32(lane_addr + Lay::kOCol + c0, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
+            for (int cc = 0; cc < 32; ++cc) o[cc] = __float_as_uint(__uint_as_float(o[cc]) * f);
             tmem_st32(lane_addr + Lay::kOCol + c0, o);
           }
           tmem_wait_st();
@@ -372,14 +403,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           m_ref = m_new;
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        uint32_t pk[32];
+        uint32_t pk[16];
         float ls = 0.f;
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = fast_exp2(x[2 * c] - m_use);
-          const float p1 = fast_exp2(x[2 * c + 1] - m_use);
-          ls += p0 + p1;
-          pk[c] = pack_bf16x2(p0, p1);
+          for (int cc = 0; cc < 16; ++cc) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * cc]), c, -m_use));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * cc + 1]), c, -m_use));
+            ls += p0 + p1;
+            pk[cc] = pack_bf16x2(p0, p1);
+          }
+        } else {
+          constexpr uint32_t kNegInf = 0xff800000u;
+#pragma unroll
+          for (int cc = 0; cc < 16; ++cc) {
+            const float p0 = sr[2 * cc] == kNegInf
+                                 ? 0.f : fast_exp2(fmaf(__uint_as_float(sr[2 * cc]), c, -m_use));
+            const float p1 = sr[2 * cc + 1] == kNegInf
+                                 ? 0.f : fast_exp2(fmaf(__uint_as_float(sr[2 * cc + 1]), c, -m_use));
+            ls += p0 + p1;
+            pk[cc] = pack_bf16x2(p0, p1);
+          }
         }
         l += ls;
         // The P buffer was last read by the PV two tiles back.
@@ -388,14 +432,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           break;
         }
         tc_fence_after();
-        tmem_st32(lane_addr + Lay::kPCol + st * (kBN / 2), pk);
+        tmem_st16(lane_addr + Lay::kPCol + st * (kBN / 2) + hf * 16, pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&B.p_full[st]);
       }
       if (!alive) break;
       if (gm.ntiles == 0) continue;
-      // Epilogue: wait for the last PV, then O / l -> bf16 -> out.
+      // Row sum over both halves.
+      B.xl[hf][q4][lane] = l;
+      mbar_arrive(&B.xbar[q4]);
+      if (!mbar_wait(&B.xbar[q4], xph, abort, kWaitNs)) {
+        alive = false;
+        break;
+      }
+      xph ^= 1;
+      l += B.xl[hf ^ 1][q4][lane];
+      // Epilogue: wait for the last PV, then O / l -> bf16 -> out (this
+      // warp's half of the columns).
       const uint32_t Tl = T - 1;
       if (!mbar_wait(&B.o_done[Tl & 1], (Tl >> 1) & 1, abort, kWaitNs)) {
         alive = false;
@@ -406,23 +460,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       __nv_bfloat16* orow =
           p.out + (static_cast<int64_t>(gm.t0 + tok) * p.hq + gm.g * G + head) * D;
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
         uint32_t o[32];
         tmem_ld32(lane_addr + Lay::kOCol + c0, o);
         tmem_wait_ld();
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int q = 0; q < 4; ++q) {
             uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv, __uint_as_float(o[8 * q4 + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
-            dst[q4] = v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+            dst[q] = v;
           }
         }
       }
+      // xl is rewritten for the next item only after both warps of the
+      // quarter have read it: they meet again at the next tile's exchange.
       tc_fence_before();
       mbar_arrive(&B.o_free);
     }

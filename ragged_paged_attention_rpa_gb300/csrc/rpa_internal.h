@@ -25,10 +25,13 @@ struct PrefillItem {
 // longer lists are split over several launches.
 constexpr int kMaxItemsPerLaunch = 3072;
 
-// Most pages one decode split may touch (its page ids sit in shared memory),
-// and most splits per sequence.
-constexpr int kMaxSplitPages = 1024;
-constexpr int kMaxSplits = 64;
+// Decode schedule limits: segments one decode launch carries in its
+// parameters (two sizes), and segments / pages one decode CTA's range may
+// touch (their tables sit in shared memory).
+constexpr int kDecodeSegSmall = 256;
+constexpr int kDecodeSegLarge = 2048;
+constexpr int kMaxCtaSegs = 64;
+constexpr int kMaxCtaPages = 512;
 
 struct Plan {
   // Problem description (checked against every rpa_forward call).
@@ -42,11 +45,23 @@ struct Plan {
   bool simt_prefill = false;         // prefill sequences handled by the SIMT kernel
   int32_t num_sms = 152;
 
-  // Decode (q_len == 1) on the split-KV kernel.
+  // Decode (q_len == 1) on the split-KV kernel.  Segments = (sequence, KV
+  // head) pairs in stream order; blocks are 16 keys; each launch cuts its
+  // segments' block stream into equal ranges, one per CTA.
+  struct DecodeLaunch {
+    int32_t seg_begin, seg_end;  // segments [seg_begin, seg_end)
+    int32_t bpc;                 // blocks per CTA
+    int32_t n_ctas;
+    int32_t slot_base;           // first partial slot (two per CTA)
+  };
   int32_t num_decode = 0;
-  int32_t kv_split = 0;   // tokens per split (multiple of 64)
-  int32_t max_splits = 0;
-  int64_t decode_ctas = 0;  // non-empty (seq, split, kv head) CTAs
+  int32_t kv_split = 0;   // tokens per CTA range (16 x blocks per CTA, first launch)
+  int32_t max_splits = 0; // most CTAs any segment is cut across
+  int64_t decode_ctas = 0;
+  std::vector<int32_t> dseg_seqhead;  // (sequence << 8) | kv head
+  std::vector<int32_t> dseg_blk0;     // block prefix, size segments + 1
+  std::vector<DecodeLaunch> dlaunch;
+  int32_t dec_slots = 0;              // partial slots over all launches
 
   // Prefill (q_len > 1).
   int32_t num_prefill = 0;

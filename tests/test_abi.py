@@ -56,53 +56,66 @@ def ceil_div(a, b):
     return -(-a // b)
 
 
-def test_decode_plan_covers_every_key():
+def decode_partition(b, num_sms=152, tokens_per_cta=0):
+    """Expected decode schedule, restated from its definition: 16-key blocks
+    of every (decode sequence, KV head) laid end to end, cut into equal
+    ranges (one per SM unless a block count per CTA is forced)."""
+    nb = []
+    for s in range(b.num_seqs):
+        if b.cu_q_lens[s + 1] - b.cu_q_lens[s] != 1:
+            continue
+        L = int(b.kv_lens[s])
+        w = 0 if b.window is None else int(b.window[s])
+        vis = min(L, w) if w > 0 else L
+        nb += [ceil_div(vis, 16)] * b.num_kv_heads
+    total = sum(nb)
+    bpc = ceil_div(tokens_per_cta, 16) if tokens_per_cta else ceil_div(total, num_sms)
+    n_ctas = ceil_div(total, bpc)
+    starts = np.concatenate([[0], np.cumsum(nb)])
+    spans = [(starts[i + 1] - 1) // bpc - starts[i] // bpc + 1 for i in range(len(nb))]
+    return dict(segments=len(nb), bpc=bpc, n_ctas=n_ctas, max_splits=max(spans))
+
+
+def test_decode_plan_is_one_balanced_wave():
     b = workloads.decode_batch(seed=1, meta_only=True)
     p = plan_of(b)
     info = p.info()
     assert info["num_decode_seqs"] == 128 and info["num_prefill_seqs"] == 0
     assert info["path"] == RPA_PATH_TC
-    split = info["kv_split"]
-    assert split % 64 == 0 and split > 0
-    nsplit = [ceil_div(int(L), split) for L in b.kv_lens]
-    assert info["max_splits"] == max(nsplit)
-    # Workspace: 256-byte header, fp32 partial O and LSE for every split slot,
-    # one int32 arrival counter per (sequence, KV head).
-    if info["max_splits"] > 1:
-        rows = b.num_seqs * info["max_splits"] * b.num_q_heads
-        want = (256 + ceil_div(rows * b.head_dim * 4, 256) * 256 + ceil_div(rows * 4, 256) * 256
-                + ceil_div(b.num_seqs * b.num_kv_heads * 4, 256) * 256)
-    else:
-        want = 256
-    assert info["workspace_bytes"] == p.workspace_bytes == want
+    want = decode_partition(b)
+    assert info["kv_split"] == 16 * want["bpc"]
+    assert info["max_splits"] == want["max_splits"]
+    assert want["n_ctas"] <= 152
+    # Workspace: 256-byte header, two fp32 partial slots (G x D, plus G
+    # log2-sum-exps) per decode CTA, one int32 arrival counter per segment.
+    G = b.num_q_heads // b.num_kv_heads
+    slots = 2 * want["n_ctas"]
+    want_ws = (256 + ceil_div(slots * G * b.head_dim * 4, 256) * 256
+               + ceil_div(slots * G * 4, 256) * 256 + ceil_div(want["segments"] * 4, 256) * 256)
+    assert info["workspace_bytes"] == p.workspace_bytes == want_ws
 
 
-def test_decode_split_respects_window():
+def test_decode_plan_respects_window_and_forced_range():
     b = workloads.mixed_batch(seed=4, meta_only=True)
     info = plan_of(b, kv_split=256).info()
+    want = decode_partition(b, tokens_per_cta=256)
     assert info["kv_split"] == 256
-    vis = []
-    for s in range(b.num_seqs):
-        if b.cu_q_lens[s + 1] - b.cu_q_lens[s] != 1:
-            continue
-        L, w = int(b.kv_lens[s]), int(b.window[s])
-        vis.append(min(L, w) if w > 0 else L)
-    assert info["max_splits"] == max(ceil_div(v, 256) for v in vis)
+    assert info["max_splits"] == want["max_splits"]
     assert info["num_decode_seqs"] == 512 and info["num_prefill_seqs"] == 4
 
 
-def test_forced_split_is_rounded_to_64():
+def test_forced_range_is_rounded_to_16():
     b = workloads.decode_batch(seed=1, meta_only=True)
-    assert plan_of(b, kv_split=100).info()["kv_split"] == 128
+    assert plan_of(b, kv_split=100).info()["kv_split"] == 112
 
 
-def test_split_count_is_capped():
-    # 64 splits at most per sequence: a 64-token split of a 100k-token context
-    # is raised to ceil(100000 / 64) rounded up to 64.
-    b = workloads.make_batch([1], [100000], num_q_heads=8, num_kv_heads=1, head_dim=256,
-                             page_size=128, meta_only=True)
-    info = plan_of(b, kv_split=64).info()
-    assert info["max_splits"] <= 64 and info["kv_split"] == 1600
+def test_cta_ranges_shrink_to_fit_the_page_table():
+    # Page size 1: a 4096-token range would touch 4096 pages, more than a CTA's
+    # shared-memory page table holds (512), so ranges shrink below 512 tokens.
+    b = workloads.make_batch([1] * 152, [4096] * 152, num_q_heads=8, num_kv_heads=1,
+                             head_dim=256, page_size=1, meta_only=True)
+    info = plan_of(b).info()
+    assert info["kv_split"] <= 512
 
 
 def test_f32_takes_the_simt_path():
