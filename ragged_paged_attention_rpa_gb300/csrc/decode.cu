@@ -151,7 +151,7 @@ struct DecodeSmem {
   static constexpr size_t kRing = size_t(kWarps) * S * 2 * TILE * 2;
   static constexpr size_t kQ = 2 * 8 * D * 2;                   // two Q tiles (G <= 8)
   static constexpr int kORow = D + 4;                           // padded row of the merge buffer
-  static constexpr size_t kO = 8 * kORow * 4;
+  static constexpr size_t kO = 2 * 8 * kORow * 4;            // two merge buffers
   static constexpr size_t kBytes = kRing + kQ + kO;
 };
 
@@ -247,7 +247,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc
       if (si.pg_off + i < kMaxCtaPages) s_pages[si.pg_off + i] = page;
     }
   }
-  // ---- Q of the first two segments; zero the merge buffer.
+  // ---- Q of the first two segments.
   for (int t = 0; t < 2 && t < nseg; ++t) {
     const SegInfo& si = s_seg[t];
     if (si.bad) continue;
@@ -256,7 +256,6 @@ decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc
     uint4* dst = reinterpret_cast<uint4*>(qs + t * 8 * D);
     for (int e = tid; e < G * D / 8; e += kWarps * 32) dst[e] = src[e];
   }
-  for (int e = tid; e < 8 * L::kORow; e += kWarps * 32) so[e] = 0.f;
   __syncthreads();
 
   const int32_t psize = 1 << p.page_shift;
@@ -415,6 +414,9 @@ decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc
         if (e < G * D / 8) qn[r] = reinterpret_cast<const uint4*>(qsrc)[e];
       }
     }
+    // Deterministic sum of the four scaled warp states: warps 0 and 1 store
+    // into buffers 0 and 1, then warps 2 and 3 add into them; the two
+    // buffers are summed in a fixed order below.
     {
       const int h0 = 2 * (lane & 3);
       float f[2];
@@ -425,18 +427,28 @@ decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w][h0 + jj]);
         f[jj] = (m[jj] == -INFINITY) ? 0.f : fast_exp2(m[jj] - M);
       }
-      const bool h0v = h0 < G && f[0] != 0.f, h1v = h0 + 1 < G && f[1] != 0.f;
+      float* buf = so + (warp & 1) * 8 * L::kORow;
+      for (int round = 0; round < 2; ++round) {
+        if ((warp >> 1) == round) {
 #pragma unroll
-      for (int mt = 0; mt < KT; ++mt) {
-        const int d = mt * 16 + (lane >> 2);
-        if (h0v) {
-          atomicAdd(so + h0 * L::kORow + d, o[mt][0] * f[0]);
-          atomicAdd(so + h0 * L::kORow + d + 8, o[mt][2] * f[0]);
+          for (int mt = 0; mt < KT; ++mt) {
+            const int d = mt * 16 + (lane >> 2);
+            float* r0 = buf + h0 * L::kORow + d;
+            float* r1 = buf + (h0 + 1) * L::kORow + d;
+            if (round == 0) {
+              r0[0] = o[mt][0] * f[0];
+              r0[8] = o[mt][2] * f[0];
+              r1[0] = o[mt][1] * f[1];
+              r1[8] = o[mt][3] * f[1];
+            } else {
+              r0[0] += o[mt][0] * f[0];
+              r0[8] += o[mt][2] * f[0];
+              r1[0] += o[mt][1] * f[1];
+              r1[8] += o[mt][3] * f[1];
+            }
+          }
         }
-        if (h1v) {
-          atomicAdd(so + (h0 + 1) * L::kORow + d, o[mt][1] * f[1]);
-          atomicAdd(so + (h0 + 1) * L::kORow + d + 8, o[mt][3] * f[1]);
-        }
+        if (round == 0) __syncthreads();
       }
     }
     if (load_q) {
@@ -460,9 +472,10 @@ decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc
       for (int w = 0; w < kWarps; ++w)
         Lsum += (wm[w][h] == -INFINITY) ? 0.f : wl[w][h] * fast_exp2(wm[w][h] - M);
       const float inv = 1.f / Lsum;
-      float* src = so + h * L::kORow + d;
-      const float4 u = make_float4(src[0] * inv, src[1] * inv, src[2] * inv, src[3] * inv);
-      src[0] = src[1] = src[2] = src[3] = 0.f;
+      const float* s0 = so + h * L::kORow + d;
+      const float* s1 = s0 + 8 * L::kORow;
+      const float4 u = make_float4((s0[0] + s1[0]) * inv, (s0[1] + s1[1]) * inv,
+                                   (s0[2] + s1[2]) * inv, (s0[3] + s1[3]) * inv);
       if (si.whole) {
         uint2 pk;
         pk.x = pack_bf16x2(u.x, u.y);
