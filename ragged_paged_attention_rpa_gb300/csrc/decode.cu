@@ -21,10 +21,13 @@
 // length mix.  A CTA's range may start or end inside a segment.
 //
 // CTA.  Four independent warps take the range's blocks round-robin (warp w:
-// blocks w, w+4, ... of each segment) and copy each block's K and V rows into
-// their own shared-memory ring with coalesced 16-byte cp.async loads through
-// the page table (the page ids of the whole range are read into shared memory
-// once, first).  Per block a warp runs
+// blocks w, w+4, ... of each segment).  Blocks sit on absolute 16-key
+// boundaries, so with pages of 16 tokens or more a block is 16 consecutive
+// rows of one page: one lane of the warp fetches it with TMA (a 3-D tensor map
+// over the pool, 128-byte swizzled boxes of 64 dims x 16 rows) into the
+// warp's own shared-memory ring, completion on an mbarrier.  The page ids of
+// the CTA's whole range are read into shared memory once, first.  Per block a
+// warp runs
 //     S^T[16 keys x 8 heads] = K . Q^T     (mma.m16n8k16, bf16 -> fp32)
 //     O^T[D x 8 heads]     += V^T . P^T   (P^T rebuilt in registers by a
 //                                          warp-level 8x8 transpose)
@@ -36,6 +39,7 @@
 // its partials: out = sum_c 2^(lse_c - M) O_c / sum_c 2^(lse_c - M).
 #include "common.cuh"
 #include "rpa_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace rpa {
 
@@ -74,7 +78,8 @@ struct DecodeSched {
 
 struct SegInfo {
   int32_t s, g, q0;      // sequence, kv head, its query token
-  int32_t kb, ke;        // keys [kb, ke) of this CTA's part
+  int32_t kb, ke;        // keys [kb, ke) of this CTA's part (kb on a 16-key boundary)
+  int32_t lo;            // first visible key of the sequence
   int32_t nb;            // 16-key blocks in this CTA's part
   int32_t slot0, pg_off; // first page-table slot; offset in the shared page list
   int32_t npg;           // pages of this part
@@ -85,19 +90,6 @@ struct SegInfo {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;  // 0: zero-fill, nothing read
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -126,11 +118,11 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Element offset of 16-byte chunk `chunk` of row `row` in a [rows][D] bf16
-// tile whose chunks are XOR-swizzled by row (conflict-free ldmatrix).
-template <int D>
+// Element offset of 16-byte chunk `chunk` of row `row` in a 16-row bf16 tile
+// as TMA writes it: D/64 boxes of [16 rows][64 dims], 128-byte swizzle (the
+// 16-byte chunk index XORed with the row's low three bits).
 __device__ __forceinline__ int swz(int row, int chunk) {
-  return row * D + ((chunk ^ (row & 7)) << 3);
+  return (chunk >> 3) * (16 * 64) + row * 64 + (((chunk & 7) ^ (row & 7)) << 3);
 }
 
 // Largest i in [0, n) with a[i] <= x (a sorted ascending, a[0] <= x).
@@ -152,19 +144,20 @@ struct DecodeSmem {
   static constexpr size_t kQ = 2 * 8 * D * 2;                   // two Q tiles (G <= 8)
   static constexpr int kORow = D + 4;                           // padded row of the merge buffer
   static constexpr size_t kO = 2 * 8 * kORow * 4;            // two merge buffers
-  static constexpr size_t kBytes = kRing + kQ + kO;
+  static constexpr size_t kBytes = kRing + kQ + kO + 1024;    // + 1024-byte alignment
 };
 
 template <int D, int NSEG>
 __global__ void __launch_bounds__(kWarps * 32, 1)
-decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc) {
+decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+              const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc) {
   using L = DecodeSmem<D>;
   constexpr int S = L::S;
   constexpr int KT = D / 16;        // k-steps of the score MMA, m-tiles of the PV MMA
-  constexpr int CPR = D / 8;        // 16-byte chunks per row
-  constexpr int RPI = 32 / CPR > 0 ? 32 / CPR : 1;  // rows per copy instruction
   constexpr int TILE = L::TILE;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
+  extern __shared__ __align__(128) unsigned char smem_dyn[];
+  unsigned char* smem_raw = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
   __nv_bfloat16* rings = reinterpret_cast<__nv_bfloat16*>(smem_raw);
   __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smem_raw + L::kRing);
   float* so = reinterpret_cast<float*>(smem_raw + L::kRing + L::kQ);
@@ -172,7 +165,8 @@ decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc
   __shared__ SegInfo s_seg[kMaxCtaSegs];
   __shared__ uint32_t valid_mask[kWarps][S];
   __shared__ float wm[kWarps][8], wl[kWarps][8];
-  __shared__ int s_nseg, s_last;
+  __shared__ int s_nseg, s_last, s_abort;
+  __shared__ __align__(8) uint64_t full_bar[kWarps][S];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int G = p.group;
@@ -188,6 +182,13 @@ decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc
     nseg = kMaxCtaSegs;
   }
 
+  if (tid == 0) {
+    for (int i = 0; i < kWarps * S; ++i) sm100::mbar_init(&full_bar[i / S][i % S], 1);
+    s_abort = 0;
+    sm100::fence_barrier_init();
+    sm100::prefetch_tmap(&tm_k);
+    sm100::prefetch_tmap(&tm_v);
+  }
   // ---- Segment table of this CTA's range.
   for (int t = tid; t < nseg; t += kWarps * 32) {
     const int k = kfirst + t;
@@ -201,13 +202,14 @@ decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc
     const int32_t W = p.window ? __ldg(p.window + si.s) : 0;
     const int32_t lo = (W > 0 && Lk - W > 0) ? Lk - W : 0;
     const int32_t nb_plan = sc.blk0[k + 1] - sc.blk0[k];
-    si.bad = (__ldg(p.cu_q_lens + si.s + 1) - si.q0 != 1 || (Lk - lo + kBlk - 1) / kBlk != nb_plan)
-                 ? 1 : 0;
+    si.bad = (__ldg(p.cu_q_lens + si.s + 1) - si.q0 != 1 ||
+              (Lk + kBlk - 1) / kBlk - lo / kBlk != nb_plan) ? 1 : 0;
     if (si.bad) report_error(p.ws, RPA_DEVERR_LENGTHS, si.s);
     const int32_t jb = max(cb0, sc.blk0[k]) - sc.blk0[k];
     const int32_t je = min(cb1, sc.blk0[k + 1]) - sc.blk0[k];
-    si.kb = lo + kBlk * jb;
-    si.ke = min(Lk, lo + kBlk * je);
+    si.lo = lo;
+    si.kb = (lo / kBlk + jb) * kBlk;
+    si.ke = min(Lk, (lo / kBlk + je) * kBlk);
     if (si.ke < si.kb) si.ke = si.kb;
     si.nb = si.bad ? 0 : je - jb;
     si.whole = (jb == 0 && je == nb_plan) ? 1 : 0;
@@ -258,47 +260,43 @@ decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc
   }
   __syncthreads();
 
-  const int32_t psize = 1 << p.page_shift;
   __nv_bfloat16* ring = rings + warp * S * 2 * TILE;
+  volatile int* abort = &s_abort;
   // Issue cursor over this warp's blocks: segment ist, local block isj.
   int ist = 0, isj = warp;
   while (ist < nseg && isj >= s_seg[ist].nb) { ++ist; isj = warp; }
+  int issued = 0;
   auto issue = [&](int st) {
-    if (ist < nseg) {
-      const SegInfo& si = s_seg[ist];
-      const int32_t key0 = si.kb + isj * kBlk;
-      int32_t page = 0;
-      bool ok = false;
-      if (lane < kBlk) {
-        const int32_t key = key0 + lane;
-        const int32_t idx = si.pg_off + (key >> p.page_shift) - si.slot0;
-        if (key < si.ke && idx < kMaxCtaPages) {
-          page = s_pages[idx];
-          ok = page >= 0;
-        }
-      }
-      const uint32_t vmask = __ballot_sync(0xffffffffu, ok);
-      if (lane == 0) valid_mask[warp][st] = vmask;
+    if (ist >= nseg) return;
+    const SegInfo& si = s_seg[ist];
+    const int32_t key0 = si.kb + isj * kBlk;
+    // Lanes 0..15: validity of one key each (visible and on a good page).
+    const int32_t idx = si.pg_off + (key0 >> p.page_shift) - si.slot0;
+    const int32_t page = idx < kMaxCtaPages ? s_pages[idx] : -1;
+    const int32_t key = key0 + lane;
+    const bool ok = lane < kBlk && page >= 0 && key >= si.lo && key < si.ke;
+    const uint32_t vmask = __ballot_sync(0xffffffffu, ok);
+    if (lane == 0) {
+      valid_mask[warp][st] = vmask;
+      // Rows of the block: page * P + (key0 % P); a bad page reads zeros.
+      const int32_t row = page >= 0 ? page * (1 << p.page_shift) + (key0 & ((1 << p.page_shift) - 1))
+                                    : -kBlk;
       __nv_bfloat16* kt = ring + st * 2 * TILE;
       __nv_bfloat16* vt = kt + TILE;
-      const int g = si.g;
+      // Earlier generic-proxy reads of this stage come before the async writes.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      sm100::mbar_arrive_expect_tx(&full_bar[warp][st], 2 * kBlk * D * 2);
 #pragma unroll
-      for (int r0 = 0; r0 < kBlk; r0 += RPI) {
-        const int r = r0 + lane / CPR;
-        const int ch = lane % CPR;
-        const int32_t pg = __shfl_sync(0xffffffffu, page, r & 31);
-        const bool v = (vmask >> r) & 1u;
-        const int32_t key = key0 + r;
-        const int64_t off =
-            ((static_cast<int64_t>(pg) * psize + (key & (psize - 1))) * p.hkv + g) * D + ch * 8;
-        cp_async16(smem_u32(kt + swz<D>(r, ch)), v ? p.k + off : p.k, v);
-        cp_async16(smem_u32(vt + swz<D>(r, ch)), v ? p.v + off : p.v, v);
+      for (int c = 0; c < D / 64; ++c) {
+        sm100::tma_load_3d(kt + c * kBlk * 64, &tm_k, &full_bar[warp][st], c * 64, si.g, row);
+        sm100::tma_load_3d(vt + c * kBlk * 64, &tm_v, &full_bar[warp][st], c * 64, si.g, row);
       }
-      isj += kWarps;
-      while (ist < nseg && isj >= s_seg[ist].nb) { ++ist; isj = warp; }
     }
-    cp_async_commit();
+    ++issued;
+    isj += kWarps;
+    while (ist < nseg && isj >= s_seg[ist].nb) { ++ist; isj = warp; }
   };
+  __syncwarp();
 #pragma unroll
   for (int i = 0; i < S - 1; ++i) issue(i);
 
@@ -326,9 +324,11 @@ decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc
 
     for (int j = warp; j < si.nb; j += kWarps, ++count) {
       issue((count + S - 1) % S);
-      cp_async_wait<S - 1>();
-      __syncwarp();
       const int st = count % S;
+      if (!sm100::mbar_wait(&full_bar[warp][st], (count / S) & 1, abort, 2000000000ull)) {
+        if (lane == 0) report_error(p.ws, RPA_DEVERR_TIMEOUT, c);
+        break;
+      }
       const __nv_bfloat16* kt = ring + st * 2 * TILE;
       const __nv_bfloat16* vt = kt + TILE;
       const uint32_t vmask = valid_mask[warp][st];
@@ -339,7 +339,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc
 #pragma unroll
         for (int kt2 = 0; kt2 < KT; ++kt2) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4(smem_u32(kt + swz<D>(row, 2 * kt2 + hi)), a0, a1, a2, a3);
+          ldsm_x4(smem_u32(kt + swz(row, 2 * kt2 + hi)), a0, a1, a2, a3);
           if (kt2 & 1) mma_bf16(sb, a0, a1, a2, a3, qf[kt2][0], qf[kt2][1]);
           else mma_bf16(sa, a0, a1, a2, a3, qf[kt2][0], qf[kt2][1]);
         }
@@ -381,7 +381,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc
 #pragma unroll
         for (int mt = 0; mt < KT; ++mt) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(smem_u32(vt + swz<D>(row, 2 * mt + hi)), a0, a1, a2, a3);
+          ldsm_x4_t(smem_u32(vt + swz(row, 2 * mt + hi)), a0, a1, a2, a3);
           mma_bf16(o[mt], a0, a1, a2, a3, b0, b1);
         }
       }
@@ -488,7 +488,14 @@ decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc
     }
     __syncthreads();
   }
-  cp_async_wait<0>();
+  if (*abort) {
+    // Let every copy this warp started land before the CTA exits.
+    for (int i = count; i < issued; ++i) {
+      int dummy = 0;
+      sm100::mbar_wait(&full_bar[warp][i % S], (i / S) & 1, &dummy, 200000000ull);
+    }
+    return;
+  }
 
   // ---- Arrivals for the cut segments (first and last of the range).
   for (int which = 0; which < 2; ++which) {
@@ -538,8 +545,8 @@ decode_kernel(const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc
 }
 
 template <int D, int NSEG>
-int launch_one(const Plan& plan, const DecodeParams& p, const Plan::DecodeLaunch& dl,
-               cudaStream_t stream) {
+int launch_one(const Plan& plan, const DecodeParams& p, const CUtensorMap& tk,
+               const CUtensorMap& tv, const Plan::DecodeLaunch& dl, cudaStream_t stream) {
   constexpr size_t smem = DecodeSmem<D>::kBytes;
   static bool configured = false;
   if (!configured) {
@@ -562,7 +569,7 @@ int launch_one(const Plan& plan, const DecodeParams& p, const Plan::DecodeLaunch
   }
   sc.blk0[n] = plan.dseg_blk0[dl.seg_end] - base;
   sc.n_blocks = sc.blk0[n];
-  decode_kernel<D, NSEG><<<dl.n_ctas, kWarps * 32, smem, stream>>>(p, sc);
+  decode_kernel<D, NSEG><<<dl.n_ctas, kWarps * 32, smem, stream>>>(tk, tv, p, sc);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return static_cast<int>(e);
   trace_mark(RPA_KERNEL_DECODE_SPLIT, stream);
@@ -593,10 +600,16 @@ int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   p.mpps = plan.mpps;
   p.num_pages = plan.num_pages;
   p.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  CUtensorMap tk, tv;
+  const uint64_t rows = static_cast<uint64_t>(plan.num_pages) * plan.p;
+  if (!make_tmap_3d(&tk, a.k_pages, D, plan.hkv, rows, 1, kBlk) ||
+      !make_tmap_3d(&tv, a.v_pages, D, plan.hkv, rows, 1, kBlk))
+    return static_cast<int>(cudaErrorInvalidValue);
   for (const Plan::DecodeLaunch& dl : plan.dlaunch) {
     const int n = dl.seg_end - dl.seg_begin;
-    const int err = n <= kDecodeSegSmall ? launch_one<D, kDecodeSegSmall>(plan, p, dl, stream)
-                                         : launch_one<D, kDecodeSegLarge>(plan, p, dl, stream);
+    const int err = n <= kDecodeSegSmall
+                        ? launch_one<D, kDecodeSegSmall>(plan, p, tk, tv, dl, stream)
+                        : launch_one<D, kDecodeSegLarge>(plan, p, tk, tv, dl, stream);
     if (err) return err;
   }
   return 0;
@@ -635,8 +648,9 @@ int noalloc_scratch(void** ptr) {
   return 0;
 }
 
-bool decode_supported(int32_t head_dim, int32_t group) {
-  return (head_dim == 64 || head_dim == 128 || head_dim == 256) && group >= 1 && group <= 8;
+bool decode_supported(int32_t head_dim, int32_t group, int32_t page_size) {
+  return (head_dim == 64 || head_dim == 128 || head_dim == 256) && group >= 1 && group <= 8 &&
+         page_size >= kBlk;
 }
 
 int decode_ctas_per_sm(int32_t) { return 1; }

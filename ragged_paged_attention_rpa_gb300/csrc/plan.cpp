@@ -70,11 +70,13 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
     ++ndec;
     const int32_t w = win ? win[s] : 0;
     const int32_t lo = (w > 0 && kv[s] - w > 0) ? kv[s] - w : 0;
-    const int32_t nb = static_cast<int32_t>(ceil_div(kv[s] - lo, 16));
+    // Blocks sit on absolute 16-key boundaries (keys before lo are masked),
+    // so with pages of 16 or more tokens a block never straddles two pages.
+    const int32_t nb = static_cast<int32_t>(ceil_div(kv[s], 16) - lo / 16);
     for (int32_t g = 0; g < plan.hkv; ++g) {
       plan.dseg_seqhead.push_back((s << 8) | g);
       plan.dseg_blk0.push_back(plan.dseg_blk0.back() + nb);
-      seg_lo.push_back(lo);
+      seg_lo.push_back(lo / 16 * 16);
     }
   }
   plan.num_decode = ndec;
@@ -185,7 +187,7 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
   if (want == RPA_PATH_TC && f32) return RPA_ERR_UNSUPPORTED;
   bool tc_decode = false, tc_prefill = false;
   if (want != RPA_PATH_SIMT && !f32) {
-    tc_decode = decode_supported(plan.d, group);
+    tc_decode = decode_supported(plan.d, group, plan.p);
     tc_prefill = prefill_tc_supported(plan.d, plan.p, group);
   }
   int32_t ndec = 0;

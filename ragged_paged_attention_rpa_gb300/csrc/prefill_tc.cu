@@ -17,21 +17,22 @@
 //
 // One CTA (persistent, one per SM) walks a longest-first list of work items
 // (sequence, query block, KV head).  Warp roles:
-//   warp 0     TMA producer: Q block once per item, then 64-key K and V tiles
-//              gathered page by page through the page table (2-stage ring);
-//   warp 1     MMA issuer: S = Q K^T (SMEM x SMEM -> TMEM), O += P V (P read
+//   warp 0     TMA producer of the Q block (once per item) and of 64-key K
+//              tiles gathered page by page through the page table (3-deep ring);
+//   warp 1     TMA producer of the V tiles (2-deep ring), so K runs ahead of V;
+//   warp 2     MMA issuer: S = Q K^T (SMEM x SMEM -> TMEM), O += P V (P read
 //              from TMEM, V from SMEM), tcgen05.commit onto mbarriers;
-//   warps 2-9  softmax: two warps per 32-row quarter, each taking 32 of a
-//              tile's 64 keys; reads S from TMEM, masks causal and window edges
-//              (interior half-tiles skip the mask), exchanges row maxima with
-//              its partner through shared memory, keeps the running max / sum,
-//              writes P (bf16) to TMEM, rescales its half of O in TMEM only
-//              when the max grew by more than 2^8 (the result is the same; it
-//              bounds P by 256); epilogue O / l -> bf16 -> global.
+//   warps 3-6  softmax: one thread per row (TMEM lane), 64 keys per tile;
+//              reads S from TMEM, masks causal and window edges (interior
+//              tiles skip the mask), keeps the running max / sum in fp32,
+//              exponentiates with the MUFU unit and, for one pair in four,
+//              with a polynomial on the FMA pipe (paired fp32 instructions),
+//              writes P (bf16) to TMEM, rescales O in TMEM only when the max
+//              grew by more than 2^8 (the result is the same; it bounds P by
+//              256); epilogue O / l -> bf16 -> global.
 // Every wait is bounded; on a timeout the CTA records RPA_DEVERR_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include <algorithm>
 
@@ -46,7 +47,10 @@ using namespace sm100;
 
 constexpr int kBM = 128;        // MMA rows per block
 constexpr int kBN = 64;         // keys per KV tile
-constexpr int kThreads = 320;   // producer, MMA, 8 softmax warps
+constexpr int kKS = 3;          // K ring depth
+constexpr int kVS = 2;          // V ring depth
+constexpr int kThreads = 224;   // K producer, V producer, MMA, 4 softmax warps
+constexpr int kPolyEvery = 4;   // one pair of exponentials in four on the FMA pipe
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait, then give up
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
 
@@ -72,10 +76,10 @@ struct Layout {
   static constexpr int kQBytes = kBM * D * 2;
   static constexpr int kKVBytes = kBN * D * 2;           // one K (or V) tile
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kQBytes;          // 2 stages
-  static constexpr int kVOff = kKOff + 2 * kKVBytes;     // 2 stages
-  static constexpr int kBarOff = kVOff + 2 * kKVBytes;
-  static constexpr int kUsed = kBarOff + 4096 + 1024;   // barriers + exchange + alignment slack
+  static constexpr int kKOff = kQOff + kQBytes;
+  static constexpr int kVOff = kKOff + kKS * kKVBytes;
+  static constexpr int kBarOff = kVOff + kVS * kKVBytes;
+  static constexpr int kUsed = kBarOff + 256 + 1024;    // barriers + alignment slack
   // Ask for more than half an SM's shared memory so that exactly one CTA
   // (which owns the SM's tensor memory) is resident per SM.
   static constexpr int kBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
@@ -88,15 +92,12 @@ struct Layout {
 
 struct Barriers {
   uint64_t q_full, q_empty;
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t k_full[kKS], k_empty[kKS], v_full[kVS], v_empty[kVS];
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t o_free;
   uint64_t fin;          // all MMAs of this CTA complete (teardown)
   uint32_t tmem_base;
   int abort;
-  uint64_t xbar[4];         // per row quarter: both softmax warps have posted their values
-  float xmax[2][2][4][32];  // row max of each half-tile, by tile parity / half / quarter / lane
-  float xl[2][4][32];       // row sums of each half, for the epilogue
 };
 
 struct Geom {
@@ -125,6 +126,21 @@ __device__ __forceinline__ Geom item_geom(const PrefillParams& p, const PrefillI
   return r;
 }
 
+// TMA source row of box `b` of KV tile j of an item (-box_rows: a box wholly
+// out of bounds, which the TMA fills with zeros).
+__device__ __forceinline__ int32_t box_row(const PrefillParams& p, const Geom& gm, int j, int b) {
+  const int32_t key = (gm.kt0 + j) * kBN + b * p.box_rows;
+  const int32_t pos_last = gm.pos_first + gm.ntok - 1;
+  if (key > pos_last) return -p.box_rows;
+  const int32_t page = __ldg(p.page_table + static_cast<int64_t>(gm.seq) * p.mpps +
+                             (key >> p.page_shift));
+  if (page < 0 || page >= p.num_pages) {
+    report_error(p.ws, RPA_DEVERR_PAGE_ID, gm.seq);
+    return -p.box_rows;
+  }
+  return page * p.page_size + (key & (p.page_size - 1));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -144,25 +160,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   if (threadIdx.x == 0) {
     mbar_init(&B.q_full, 1);
     mbar_init(&B.q_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kKS; ++i) {
       mbar_init(&B.k_full[i], 1);
       mbar_init(&B.k_empty[i], 1);
+    }
+    for (int i = 0; i < kVS; ++i) {
       mbar_init(&B.v_full[i], 1);
       mbar_init(&B.v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.p_full[i], 256);
+      mbar_init(&B.p_full[i], 128);
       mbar_init(&B.o_done[i], 1);
     }
-    mbar_init(&B.o_free, 256);
+    mbar_init(&B.o_free, 128);
     mbar_init(&B.fin, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&B.xbar[i], 64);
     B.abort = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
   }
-  if (warp == 1) {
+  if (warp == 2) {
     tmem_alloc(&B.tmem_base, Lay::kCols);
     tmem_relinquish();
   }
@@ -172,82 +191,64 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const uint32_t tmem = B.tmem_base;
   const int G = p.group;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    uint32_t T = 0, I = 0;
+  if (warp <= 1) {
+    // ------------------------------------------------------------ producers
+    // Warp 0 loads Q and K, warp 1 loads V; each keeps its own ring.
+    const bool is_k = warp == 0;
+    const int depth = is_k ? kKS : kVS;
+    uint64_t* full = is_k ? B.k_full : B.v_full;
+    uint64_t* empty = is_k ? B.k_empty : B.v_empty;
+    __nv_bfloat16* ring = is_k ? k_s : v_s;
+    const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+    uint32_t T = 0, I = 0, issued_q = 0;
     const int nbox = kBN / p.box_rows;
     const uint32_t q_box_bytes = static_cast<uint32_t>(G * p.qb_tokens) * 128u;
     bool alive = true;
     for (int it = blockIdx.x; it < items.n && alive; it += gridDim.x) {
       const Geom gm = item_geom(p, items.items[it]);
       if (!gm.ok) {
-        if (lane == 0) report_error(p.ws, RPA_DEVERR_LENGTHS, gm.seq);
+        if (lane == 0 && is_k) report_error(p.ws, RPA_DEVERR_LENGTHS, gm.seq);
         continue;
       }
       const uint32_t Icur = I++;
-      if (lane == 0) {
+      if (is_k && lane == 0) {
         alive = mbar_wait(&B.q_empty, (Icur & 1) ^ 1, abort, kWaitNs);
         if (alive) {
           mbar_arrive_expect_tx(&B.q_full, q_box_bytes * Lay::kChunks);
           for (int c = 0; c < Lay::kChunks; ++c)
             tma_load_3d(q_s + c * kBM * 64, &tm_q, &B.q_full, c * 64, gm.g * G, gm.t0);
+          ++issued_q;
         }
       }
       alive = __shfl_sync(0xffffffffu, alive, 0);
-      const int32_t* pt = p.page_table + static_cast<int64_t>(gm.seq) * p.mpps;
-      const int32_t pos_last = gm.pos_first + gm.ntok - 1;
       for (int j = 0; j < gm.ntiles && alive; ++j, ++T) {
-        const int st = T & 1;
-        const uint32_t ph = (T >> 1) & 1;
-        const int32_t key0 = (gm.kt0 + j) * kBN;
-        // Lane b < nbox resolves the page of box b (rows key0 + b * box_rows ...).
-        int32_t row = -p.box_rows;  // out of bounds: the TMA fills zeros
-        if (lane < nbox) {
-          const int32_t key = key0 + lane * p.box_rows;
-          const int32_t slot = key >> p.page_shift;
-          if (key <= pos_last) {
-            const int32_t page = __ldg(pt + slot);
-            if (page >= 0 && page < p.num_pages)
-              row = page * p.page_size + (key & (p.page_size - 1));
-            else
-              report_error(p.ws, RPA_DEVERR_PAGE_ID, gm.seq);
-          }
-        }
-        if (lane == 0) alive = mbar_wait(&B.k_empty[st], ph ^ 1, abort, kWaitNs);
+        const int st = T % depth;
+        const uint32_t ph = (T / depth) & 1;
+        const int32_t row = lane < nbox ? box_row(p, gm, j, lane) : 0;
+        if (lane == 0) alive = mbar_wait(&empty[st], ph ^ 1, abort, kWaitNs);
         alive = __shfl_sync(0xffffffffu, alive, 0);
         if (!alive) break;
-        if (lane == 0) mbar_arrive_expect_tx(&B.k_full[st], Lay::kKVBytes);
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], Lay::kKVBytes);
         __syncwarp();
         if (lane < nbox)
           for (int c = 0; c < Lay::kChunks; ++c)
-            tma_load_3d(k_s + st * kBN * D + c * kBN * 64 + lane * p.box_rows * 64, &tm_k,
-                        &B.k_full[st], c * 64, gm.g, row);
-        if (lane == 0) alive = mbar_wait(&B.v_empty[st], ph ^ 1, abort, kWaitNs);
-        alive = __shfl_sync(0xffffffffu, alive, 0);
-        if (!alive) break;
-        if (lane == 0) mbar_arrive_expect_tx(&B.v_full[st], Lay::kKVBytes);
-        __syncwarp();
-        if (lane < nbox)
-          for (int c = 0; c < Lay::kChunks; ++c)
-            tma_load_3d(v_s + st * kBN * D + c * kBN * 64 + lane * p.box_rows * 64, &tm_v,
-                        &B.v_full[st], c * 64, gm.g, row);
+            tma_load_3d(ring + st * kBN * D + c * kBN * 64 + lane * p.box_rows * 64, tm, &full[st],
+                        c * 64, gm.g, row);
       }
     }
     if (!alive && lane == 0) {
-      // Let every copy this CTA started land before its shared memory goes.
+      // Let every copy this warp started land before its shared memory goes.
       report_error(p.ws, RPA_DEVERR_TIMEOUT, blockIdx.x);
-      for (int i = 0; i < 2; ++i) {
-        for (uint32_t ph = 0; ph < 2; ++ph) {
-          int dummy = 0;
-          mbar_wait(&B.k_full[i], ph, &dummy, kDrainNs);
-          dummy = 0;
-          mbar_wait(&B.v_full[i], ph, &dummy, kDrainNs);
-        }
+      for (uint32_t t = (T > static_cast<uint32_t>(depth) ? T - depth : 0); t < T; ++t) {
+        int dummy = 0;
+        mbar_wait(&full[t % depth], (t / depth) & 1, &dummy, kDrainNs);
       }
-      int dummy = 0;
-      mbar_wait(&B.q_full, 0, &dummy, kDrainNs);
+      if (is_k && issued_q > 0) {
+        int dummy = 0;
+        mbar_wait(&B.q_full, (issued_q - 1) & 1, &dummy, kDrainNs);
+      }
     }
-  } else if (warp == 1) {
+  } else if (warp == 2) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(kBN, 0);
@@ -256,23 +257,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       uint32_t T = 0, I = 0;
       bool alive = true;
       auto issue_pv = [&](uint32_t Tp, int jp) -> bool {
-        const int st = Tp & 1;
-        const uint32_t ph = (Tp >> 1) & 1;
-        if (!mbar_wait(&B.p_full[st], ph, abort, kWaitNs)) return false;
-        if (!mbar_wait(&B.v_full[st], ph, abort, kWaitNs)) return false;
+        const int sb = Tp & 1;
+        const int vs = Tp % kVS;
+        if (!mbar_wait(&B.p_full[sb], (Tp >> 1) & 1, abort, kWaitNs)) return false;
+        if (!mbar_wait(&B.v_full[vs], (Tp / kVS) & 1, abort, kWaitNs)) return false;
         if (jp == 0 && !mbar_wait(&B.o_free, (I & 1) ^ 1, abort, kWaitNs)) return false;
         tc_fence_after();
-        const uint32_t vb = v_base + st * Lay::kKVBytes;
+        const uint32_t vb = v_base + vs * Lay::kKVBytes;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           // V as MN-major B: 8-key groups 1024 B apart (SBO), 64-dim chunks
           // one tile-chunk apart (LBO); 16 keys per MMA = 2048 B.
           const uint64_t bdesc = smem_desc(vb + kk * 2048, kBN * 128, 1024);
-          mma_ts(tmem + Lay::kOCol, tmem + Lay::kPCol + st * (kBN / 2) + kk * 8, bdesc, kIdPV,
+          mma_ts(tmem + Lay::kOCol, tmem + Lay::kPCol + sb * (kBN / 2) + kk * 8, bdesc, kIdPV,
                  (jp > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&B.o_done[st]);
-        mma_commit(&B.v_empty[st]);
+        mma_commit(&B.o_done[sb]);
+        mma_commit(&B.v_empty[vs]);
         return true;
       };
       for (int it = blockIdx.x; it < items.n && alive; it += gridDim.x) {
@@ -280,14 +281,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (!gm.ok) continue;
         alive = mbar_wait(&B.q_full, I & 1, abort, kWaitNs);
         for (int j = 0; j < gm.ntiles && alive; ++j, ++T) {
-          const int st = T & 1;
-          const uint32_t ph = (T >> 1) & 1;
-          if (!mbar_wait(&B.k_full[st], ph, abort, kWaitNs)) {
+          const int ks = T % kKS;
+          if (!mbar_wait(&B.k_full[ks], (T / kKS) & 1, abort, kWaitNs)) {
             alive = false;
             break;
           }
           tc_fence_after();
-          const uint32_t kb = k_base + st * Lay::kKVBytes;
+          const uint32_t kb = k_base + ks * Lay::kKVBytes;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             // K-major, 128-byte swizzle: 16 elements = 32 B inside a 64-wide
@@ -295,10 +295,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const uint32_t c = kk >> 2, w = (kk & 3) * 32;
             const uint64_t adesc = smem_desc(q_base + c * (kBM * 128) + w, 16, 1024);
             const uint64_t bdesc = smem_desc(kb + c * (kBN * 128) + w, 16, 1024);
-            mma_ss(tmem + Lay::kSCol + st * kBN, adesc, bdesc, kIdS, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + Lay::kSCol + (T & 1) * kBN, adesc, bdesc, kIdS, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&B.s_full[st]);
-          mma_commit(&B.k_empty[st]);
+          mma_commit(&B.s_full[T & 1]);
+          mma_commit(&B.k_empty[ks]);
           if (j >= 1 && !issue_pv(T - 1, j - 1)) {
             alive = false;
             break;
@@ -316,18 +316,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    // Warps 2..9: quarter q = warp % 4 owns TMEM lanes (rows) 32q..32q+31;
-    // half hf owns key columns 32hf..32hf+31 of every 64-key tile and O
-    // columns [hf D/2, (hf+1) D/2).  The two warps of a quarter exchange row
-    // maxima (and, at the end, row sums) through shared memory.
-    const int q4 = warp & 3;
-    const int hf = (warp - 2) >> 2;
+    const int q4 = warp & 3;                            // TMEM lane quarter of this warp
     const int r = 32 * q4 + lane;                       // TMEM lane = row
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q4) << 16);
     const int tok = r / G, head = r % G;
     const float c = p.scale_log2;
     uint32_t T = 0;
-    uint32_t xph = 0;   // phase of this quarter's exchange barrier
     bool alive = true;
     for (int it = blockIdx.x; it < items.n && alive; it += gridDim.x) {
       const Geom gm = item_geom(p, items.items[it]);
@@ -338,48 +332,52 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < gm.ntiles; ++j, ++T) {
         const int st = T & 1;
-        const uint32_t ph = (T >> 1) & 1;
-        if (!mbar_wait(&B.s_full[st], ph, abort, kWaitNs)) {
+        if (!mbar_wait(&B.s_full[st], (T >> 1) & 1, abort, kWaitNs)) {
           alive = false;
           break;
         }
         tc_fence_after();
-        uint32_t sr[32];
-        tmem_ld32(lane_addr + Lay::kSCol + st * kBN + hf * 32, sr);
+        uint32_t sr[64];
+        {
+          uint32_t (&lo32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+          uint32_t (&hi32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+          tmem_ld32(lane_addr + Lay::kSCol + st * kBN, lo32);
+          tmem_ld32(lane_addr + Lay::kSCol + st * kBN + 32, hi32);
+        }
         tmem_wait_ld();
-        const int32_t key0 = (gm.kt0 + j) * kBN + hf * 32;
-        // Interior half-tiles (every key visible to every row of the warp)
-        // skip the per-element mask; elsewhere masked scores become -inf.
-        const bool full = __all_sync(0xffffffffu, valid && key0 >= lo && key0 + 31 <= pos);
-        float mx = -INFINITY;
+        const int32_t key0 = (gm.kt0 + j) * kBN;
+        // Interior tiles (every key visible to every row of the warp) skip
+        // the per-element mask; elsewhere masked scores become -inf.
+        const bool full = __all_sync(0xffffffffu, valid && key0 >= lo && key0 + kBN - 1 <= pos);
+        float mx;
         if (full) {
+          float m3[22];
 #pragma unroll
-          for (int cc = 0; cc < 32; ++cc) mx = fmaxf(mx, __uint_as_float(sr[cc]));
+          for (int i = 0; i < 21; ++i)
+            m3[i] = fmax3(__uint_as_float(sr[3 * i]), __uint_as_float(sr[3 * i + 1]),
+                          __uint_as_float(sr[3 * i + 2]));
+          m3[21] = __uint_as_float(sr[63]);
+#pragma unroll
+          for (int i = 0; i < 7; ++i) m3[i] = fmax3(m3[3 * i], m3[3 * i + 1], m3[3 * i + 2]);
+          m3[7] = m3[21];
+          mx = fmax3(fmax3(m3[0], m3[1], m3[2]), fmax3(m3[3], m3[4], m3[5]), fmaxf(m3[6], m3[7]));
         } else {
+          mx = -INFINITY;
 #pragma unroll
-          for (int cc = 0; cc < 32; ++cc) {
+          for (int cc = 0; cc < 64; ++cc) {
             const int32_t key = key0 + cc;
             const bool vis = valid && key >= lo && key <= pos;
-            if (!vis) sr[cc] = __float_as_uint(-INFINITY);
+            if (!vis) sr[cc] = 0xff800000u;   // -inf
             mx = fmaxf(mx, __uint_as_float(sr[cc]));
           }
         }
-        // Row max over both halves; scaling after the max keeps the order (c >= 0).
-        B.xmax[T & 1][hf][q4][lane] = mx;
-        mbar_arrive(&B.xbar[q4]);
-        if (!mbar_wait(&B.xbar[q4], xph, abort, kWaitNs)) {
-          alive = false;
-          break;
-        }
-        xph ^= 1;
-        mx = fmaxf(mx, B.xmax[T & 1][hf ^ 1][q4][lane]);
+        // Scaling after the max keeps the order (c >= 0).
         mx = (mx == -INFINITY) ? -INFINITY : mx * c;
         const float m_new = fmaxf(m_ref, mx);
         const bool grow = m_new > m_ref + 8.f;           // also true for the first visible key
-        const bool rescale_o = grow && m_ref != -INFINITY;
+        const bool rescale_o = grow && l > 0.f;
         if (__any_sync(0xffffffffu, rescale_o)) {
-          // O holds earlier tiles: wait for the last PV, then scale this
-          // warp's half of the O columns in TMEM.
+          // O holds earlier tiles: wait for the last PV, then scale in TMEM.
           const uint32_t Tp = T - 1;
           if (!mbar_wait(&B.o_done[Tp & 1], (Tp >> 1) & 1, abort, kWaitNs)) {
             alive = false;
@@ -388,7 +386,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           tc_fence_after();
           const float f = rescale_o ? fast_exp2(m_ref - m_new) : 1.f;
 #pragma unroll 1
-          for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
+          for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
             tmem_ld32(lane_addr + Lay::kOCol + c0, o);
             tmem_wait_ld();
@@ -403,23 +401,40 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           m_ref = m_new;
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        uint32_t pk[16];
-        float ls = 0.f;
+        uint32_t pk[32];
+        float ls;
         if (full) {
+          // Paired fp32 arithmetic; one pair in kPolyEvery takes its 2^x on
+          // the FMA pipe instead of the MUFU unit.
+          const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_use, -m_use);
+          uint64_t acc = f2_pack(0.f, 0.f);
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * cc]), c, -m_use));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * cc + 1]), c, -m_use));
-            ls += p0 + p1;
+          for (int cc = 0; cc < 32; ++cc) {
+            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[2 * cc]),
+                                               __uint_as_float(sr[2 * cc + 1])), c2, nm2);
+            uint64_t p2;
+            if (cc % kPolyEvery == kPolyEvery - 1) {
+              p2 = exp2_poly2(x2);
+            } else {
+              float x0, x1;
+              f2_unpack(x2, x0, x1);
+              p2 = f2_pack(fast_exp2(x0), fast_exp2(x1));
+            }
+            acc = f2_add(acc, p2);
+            float p0, p1;
+            f2_unpack(p2, p0, p1);
             pk[cc] = pack_bf16x2(p0, p1);
           }
+          float a0, a1;
+          f2_unpack(acc, a0, a1);
+          ls = a0 + a1;
         } else {
-          constexpr uint32_t kNegInf = 0xff800000u;
+          ls = 0.f;
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc) {
-            const float p0 = sr[2 * cc] == kNegInf
+          for (int cc = 0; cc < 32; ++cc) {
+            const float p0 = sr[2 * cc] == 0xff800000u
                                  ? 0.f : fast_exp2(fmaf(__uint_as_float(sr[2 * cc]), c, -m_use));
-            const float p1 = sr[2 * cc + 1] == kNegInf
+            const float p1 = sr[2 * cc + 1] == 0xff800000u
                                  ? 0.f : fast_exp2(fmaf(__uint_as_float(sr[2 * cc + 1]), c, -m_use));
             ls += p0 + p1;
             pk[cc] = pack_bf16x2(p0, p1);
@@ -432,24 +447,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           break;
         }
         tc_fence_after();
-        tmem_st16(lane_addr + Lay::kPCol + st * (kBN / 2) + hf * 16, pk);
+        tmem_st32(lane_addr + Lay::kPCol + st * (kBN / 2), pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&B.p_full[st]);
       }
       if (!alive) break;
       if (gm.ntiles == 0) continue;
-      // Row sum over both halves.
-      B.xl[hf][q4][lane] = l;
-      mbar_arrive(&B.xbar[q4]);
-      if (!mbar_wait(&B.xbar[q4], xph, abort, kWaitNs)) {
-        alive = false;
-        break;
-      }
-      xph ^= 1;
-      l += B.xl[hf ^ 1][q4][lane];
-      // Epilogue: wait for the last PV, then O / l -> bf16 -> out (this
-      // warp's half of the columns).
+      // Epilogue: wait for the last PV, then O / l -> bf16 -> out.
       const uint32_t Tl = T - 1;
       if (!mbar_wait(&B.o_done[Tl & 1], (Tl >> 1) & 1, abort, kWaitNs)) {
         alive = false;
@@ -460,7 +465,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       __nv_bfloat16* orow =
           p.out + (static_cast<int64_t>(gm.t0 + tok) * p.hq + gm.g * G + head) * D;
 #pragma unroll 1
-      for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
+      for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
         tmem_ld32(lane_addr + Lay::kOCol + c0, o);
         tmem_wait_ld();
@@ -477,8 +482,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           }
         }
       }
-      // xl is rewritten for the next item only after both warps of the
-      // quarter have read it: they meet again at the next tile's exchange.
       tc_fence_before();
       mbar_arrive(&B.o_free);
     }
@@ -488,41 +491,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // Teardown: every MMA must be finished before TMEM is released.
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, Lay::kCols);
   }
-}
-
-using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
-
-EncodeFn encode_fn() {
-  static EncodeFn fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(ptr);
-  }
-  return fn;
-}
-
-// 3-D bf16 tensor map [outer][mid][D] with a 128-byte-swizzled box
-// (64, box_mid, box_outer).
-bool make_map(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid, uint64_t outer,
-              uint32_t box_mid, uint32_t box_outer) {
-  EncodeFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[3] = {d, mid, outer};
-  cuuint64_t strides[2] = {d * 2, d * mid * 2};
-  cuuint32_t box[3] = {64, box_mid, box_outer};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
 }
 
 template <int D>
@@ -540,11 +512,11 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   const int qb = plan.q_block;
   const int box_rows = plan.p < kBN ? plan.p : kBN;
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, a.q, D, plan.hq, static_cast<uint64_t>(plan.total_q), G, qb) ||
-      !make_map(&tk, a.k_pages, D, plan.hkv, static_cast<uint64_t>(plan.num_pages) * plan.p, 1,
-                box_rows) ||
-      !make_map(&tv, a.v_pages, D, plan.hkv, static_cast<uint64_t>(plan.num_pages) * plan.p, 1,
-                box_rows))
+  if (!make_tmap_3d(&tq, a.q, D, plan.hq, static_cast<uint64_t>(plan.total_q), G, qb) ||
+      !make_tmap_3d(&tk, a.k_pages, D, plan.hkv, static_cast<uint64_t>(plan.num_pages) * plan.p, 1,
+                    box_rows) ||
+      !make_tmap_3d(&tv, a.v_pages, D, plan.hkv, static_cast<uint64_t>(plan.num_pages) * plan.p, 1,
+                    box_rows))
     return static_cast<int>(cudaErrorInvalidValue);
   PrefillParams p;
   p.page_table = a.page_table;
@@ -583,7 +555,7 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
 
 bool prefill_tc_supported(int32_t head_dim, int32_t page_size, int32_t group) {
   return (head_dim == 64 || head_dim == 128 || head_dim == 256) && page_size >= 16 &&
-         group >= 1 && group <= kBM && encode_fn() != nullptr;
+         group >= 1 && group <= kBM;
 }
 
 int prefill_ctas_per_sm(int32_t) { return 1; }

@@ -2,6 +2,8 @@
 // launchers of librpa.  Not part of the public interface (include/rpa.h).
 #pragma once
 
+#include <cuda.h>
+
 #include <cstddef>
 #include <cstdint>
 #include <vector>
@@ -114,6 +116,12 @@ bool prefill_tc_supported(int32_t head_dim, int32_t page_size, int32_t group);
 int noalloc_scratch(void** ptr);
 
 // Whether the split-KV decode supports this shape (decode.cu).
-bool decode_supported(int32_t head_dim, int32_t group);
+bool decode_supported(int32_t head_dim, int32_t group, int32_t page_size);
+
+// TMA tensor maps (tmap.cpp): a 3-D bf16 tensor [outer][mid][d] with a
+// 128-byte-swizzled box of (64, box_mid, box_outer) elements.
+bool tmap_available();
+bool make_tmap_3d(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid, uint64_t outer,
+                  uint32_t box_mid, uint32_t box_outer);
 
 }  // namespace rpa

@@ -177,6 +177,59 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- paired fp32
+
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 2^x for a pair of arguments on the FMA pipe (no MUFU): Cody-Waite style
+// range reduction x = n + f with n = round(x) (the 1.5 * 2^23 shifter) and
+// f in [-0.5, 0.5], a degree-3 polynomial for 2^f whose coefficients are a
+// relative-error minimax fit computed for this library (max relative error
+// 7.5e-5, ample for P that is rounded to bf16), and 2^n added into the
+// exponent field.  Arguments below -125 are clamped (result ~2^-125).
+__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
+  float a, b;
+  f2_unpack(x2, a, b);
+  a = fmaxf(a, -125.f);
+  b = fmaxf(b, -125.f);
+  x2 = f2_pack(a, b);
+  const uint64_t shifter = f2_pack(12582912.f, 12582912.f);
+  const uint64_t t2 = f2_add(x2, shifter);
+  const uint64_t n2 = f2_add(t2, f2_pack(-12582912.f, -12582912.f));
+  const uint64_t fr = f2_fma(n2, f2_pack(-1.f, -1.f), x2);
+  uint64_t p = f2_fma(f2_pack(0.05517132f, 0.05517132f), fr, f2_pack(0.24261054f, 0.24261054f));
+  p = f2_fma(p, fr, f2_pack(0.69326097f, 0.69326097f));
+  p = f2_fma(p, fr, f2_pack(0.99992812f, 0.99992812f));
+  float pa, pb, ta, tb;
+  f2_unpack(p, pa, pb);
+  f2_unpack(t2, ta, tb);
+  pa = __int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23));
+  pb = __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23));
+  return f2_pack(pa, pb);
+}
+
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
 // stride byte offsets, fixed version bits 46-48 = 0b001, swizzle mode in
 // bits 61-63 (2 = 128-byte swizzle).

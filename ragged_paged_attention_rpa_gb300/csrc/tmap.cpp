@@ -1,0 +1,50 @@
+// TMA tensor maps for librpa's kernels (host side): cuTensorMapEncodeTiled,
+// reached through the runtime's driver entry point so that the library needs
+// no link against libcuda.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "rpa_internal.h"
+
+namespace rpa {
+namespace {
+
+using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(ptr);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+}  // namespace
+
+bool tmap_available() { return encode_fn() != nullptr; }
+
+bool make_tmap_3d(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid, uint64_t outer,
+                  uint32_t box_mid, uint32_t box_outer) {
+  EncodeFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {d, mid, outer};
+  cuuint64_t strides[2] = {d * 2, d * mid * 2};
+  cuuint32_t box[3] = {64, box_mid, box_outer};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace rpa

@@ -57,17 +57,18 @@ def ceil_div(a, b):
 
 
 def decode_partition(b, num_sms=152, tokens_per_cta=0):
-    """Expected decode schedule, restated from its definition: 16-key blocks
-    of every (decode sequence, KV head) laid end to end, cut into equal
-    ranges (one per SM unless a block count per CTA is forced)."""
+    """Expected decode schedule, restated from its definition: the 16-key
+    blocks (on absolute 16-key boundaries) covering the visible keys of every
+    (decode sequence, KV head), laid end to end and cut into equal ranges
+    (one per SM unless a block count per CTA is forced)."""
     nb = []
     for s in range(b.num_seqs):
         if b.cu_q_lens[s + 1] - b.cu_q_lens[s] != 1:
             continue
         L = int(b.kv_lens[s])
         w = 0 if b.window is None else int(b.window[s])
-        vis = min(L, w) if w > 0 else L
-        nb += [ceil_div(vis, 16)] * b.num_kv_heads
+        lo = max(0, L - w) if w > 0 else 0
+        nb += [ceil_div(L, 16) - lo // 16] * b.num_kv_heads
     total = sum(nb)
     bpc = ceil_div(tokens_per_cta, 16) if tokens_per_cta else ceil_div(total, num_sms)
     n_ctas = ceil_div(total, bpc)

@@ -87,6 +87,7 @@ SMALL = [
     ([1] * 6 + [20], [3, 64, 65, 200, 1000, 5, 40], 8, 2, 128, 32, [0, 16, 0, 100, 0, 2, 9]),
     ([1, 1, 1, 70], [2000, 37, 513, 90], 2, 2, 256, 16, [1000, 0, 64, 0]),
     ([1, 1, 64, 1], [129, 4097, 64, 1], 16, 2, 64, 64, None),
+    ([1, 3, 1], [40, 20, 7], 4, 1, 64, 8, [0, 0, 3]),          # 8-token pages: CUDA-core path
 ]
 
 
