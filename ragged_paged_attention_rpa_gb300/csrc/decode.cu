@@ -74,6 +74,9 @@ struct DecodeSched {
   int32_t n_seg, bpc, n_blocks, slot_base, seg_base;
   int32_t seqhead[NSEG];
   int32_t blk0[NSEG + 1];
+  // From the plan's host metadata (validated there): query token, first
+  // visible key and length of each segment's sequence.
+  int32_t q0[NSEG], lo[NSEG], len[NSEG];
 };
 
 struct SegInfo {
@@ -197,14 +200,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     si.s = sh >> 8;
     si.g = sh & 255;
     si.gseg = k;
-    si.q0 = __ldg(p.cu_q_lens + si.s);
-    const int32_t Lk = __ldg(p.kv_lens + si.s);
-    const int32_t W = p.window ? __ldg(p.window + si.s) : 0;
-    const int32_t lo = (W > 0 && Lk - W > 0) ? Lk - W : 0;
+    si.q0 = sc.q0[k];
+    const int32_t Lk = sc.len[k];
+    const int32_t lo = sc.lo[k];
     const int32_t nb_plan = sc.blk0[k + 1] - sc.blk0[k];
-    si.bad = (__ldg(p.cu_q_lens + si.s + 1) - si.q0 != 1 ||
-              (Lk + kBlk - 1) / kBlk - lo / kBlk != nb_plan) ? 1 : 0;
-    if (si.bad) report_error(p.ws, RPA_DEVERR_LENGTHS, si.s);
+    si.bad = 0;
     const int32_t jb = max(cb0, sc.blk0[k]) - sc.blk0[k];
     const int32_t je = min(cb1, sc.blk0[k + 1]) - sc.blk0[k];
     si.lo = lo;
@@ -249,15 +249,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       if (si.pg_off + i < kMaxCtaPages) s_pages[si.pg_off + i] = page;
     }
   }
-  // ---- Q of the first two segments.
-  for (int t = 0; t < 2 && t < nseg; ++t) {
-    const SegInfo& si = s_seg[t];
-    if (si.bad) continue;
-    const uint4* src = reinterpret_cast<const uint4*>(
-        p.q + (static_cast<int64_t>(si.q0) * p.hq + si.g * G) * D);
-    uint4* dst = reinterpret_cast<uint4*>(qs + t * 8 * D);
-    for (int e = tid; e < G * D / 8; e += kWarps * 32) dst[e] = src[e];
-  }
   __syncthreads();
 
   __nv_bfloat16* ring = rings + warp * S * 2 * TILE;
@@ -299,6 +290,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   __syncwarp();
 #pragma unroll
   for (int i = 0; i < S - 1; ++i) issue(i);
+  // Q of the first two segments, while the first copies are in flight.
+  for (int t = 0; t < 2 && t < nseg; ++t) {
+    const SegInfo& si = s_seg[t];
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.q + (static_cast<int64_t>(si.q0) * p.hq + si.g * G) * D);
+    uint4* dst = reinterpret_cast<uint4*>(qs + t * 8 * D);
+    for (int e = tid; e < G * D / 8; e += kWarps * 32) dst[e] = src[e];
+  }
+  __syncthreads();
 
   int count = 0;  // blocks consumed by this warp
   for (int t = 0; t < nseg; ++t) {
@@ -564,8 +564,12 @@ int launch_one(const Plan& plan, const DecodeParams& p, const CUtensorMap& tk,
   sc.seg_base = dl.seg_begin;
   const int32_t base = plan.dseg_blk0[dl.seg_begin];
   for (int i = 0; i < n; ++i) {
-    sc.seqhead[i] = plan.dseg_seqhead[dl.seg_begin + i];
-    sc.blk0[i] = plan.dseg_blk0[dl.seg_begin + i] - base;
+    const int k = dl.seg_begin + i;
+    sc.seqhead[i] = plan.dseg_seqhead[k];
+    sc.blk0[i] = plan.dseg_blk0[k] - base;
+    sc.q0[i] = plan.dseg_q0[k];
+    sc.lo[i] = plan.dseg_lo[k];
+    sc.len[i] = plan.dseg_len[k];
   }
   sc.blk0[n] = plan.dseg_blk0[dl.seg_end] - base;
   sc.n_blocks = sc.blk0[n];

@@ -62,8 +62,11 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
                  int32_t forced_tokens) {
   plan.dseg_seqhead.clear();
   plan.dseg_blk0.assign(1, 0);
+  plan.dseg_q0.clear();
+  plan.dseg_lo.clear();
+  plan.dseg_len.clear();
   plan.dlaunch.clear();
-  std::vector<int32_t> seg_lo;  // first visible key of each segment
+  std::vector<int32_t> seg_lo;  // first block's first key of each segment
   int32_t ndec = 0;
   for (int32_t s = 0; s < plan.num_seqs; ++s) {
     if (cu[s + 1] - cu[s] != 1) continue;
@@ -76,6 +79,9 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
     for (int32_t g = 0; g < plan.hkv; ++g) {
       plan.dseg_seqhead.push_back((s << 8) | g);
       plan.dseg_blk0.push_back(plan.dseg_blk0.back() + nb);
+      plan.dseg_q0.push_back(cu[s]);
+      plan.dseg_lo.push_back(lo);
+      plan.dseg_len.push_back(kv[s]);
       seg_lo.push_back(lo / 16 * 16);
     }
   }

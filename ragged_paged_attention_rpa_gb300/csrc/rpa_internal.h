@@ -31,7 +31,7 @@ constexpr int kMaxItemsPerLaunch = 3072;
 // parameters (two sizes), and segments / pages one decode CTA's range may
 // touch (their tables sit in shared memory).
 constexpr int kDecodeSegSmall = 256;
-constexpr int kDecodeSegLarge = 2048;
+constexpr int kDecodeSegLarge = 1024;
 constexpr int kMaxCtaSegs = 64;
 constexpr int kMaxCtaPages = 512;
 
@@ -62,6 +62,7 @@ struct Plan {
   int64_t decode_ctas = 0;
   std::vector<int32_t> dseg_seqhead;  // (sequence << 8) | kv head
   std::vector<int32_t> dseg_blk0;     // block prefix, size segments + 1
+  std::vector<int32_t> dseg_q0, dseg_lo, dseg_len;  // query token, first visible key, length
   std::vector<DecodeLaunch> dlaunch;
   int32_t dec_slots = 0;              // partial slots over all launches
 
