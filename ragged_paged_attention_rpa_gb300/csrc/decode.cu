@@ -168,7 +168,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   __shared__ SegInfo s_seg[kMaxCtaSegs];
   __shared__ uint32_t valid_mask[kWarps][S];
   __shared__ float wm[kWarps][8], wl[kWarps][8];
-  __shared__ int s_nseg, s_last, s_abort;
+  __shared__ int s_nseg, s_abort;
   __shared__ __align__(8) uint64_t full_bar[kWarps][S];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
@@ -497,39 +497,59 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     return;
   }
 
-  // ---- Arrivals for the cut segments (first and last of the range).
+  // ---- Arrivals for the cut segments (the first and last of the range):
+  // one fence, both counters bumped at once, and the CTA that completes a
+  // segment merges its partials.
+  __shared__ int s_cut_seg[2], s_merge[2];
+  if (tid < 2) {
+    const int t = tid == 0 ? 0 : nseg - 1;
+    const SegInfo& si = s_seg[t];
+    const bool cut = !(tid == 1 && nseg == 1) && !si.whole && !si.bad;
+    s_cut_seg[tid] = cut ? si.gseg : -1;
+  }
+  __syncthreads();
+  if (s_cut_seg[0] < 0 && s_cut_seg[1] < 0) return;
+  __threadfence();
+  __syncthreads();
+  if (tid < 2) {
+    const int k = s_cut_seg[tid];
+    bool last = false;
+    if (k >= 0) {
+      const int ca = sc.blk0[k] / sc.bpc;
+      const int cb = (sc.blk0[k + 1] - 1) / sc.bpc;
+      last = atomicAdd(p.arrivals + sc.seg_base + k, 1) == (cb - ca);
+    }
+    s_merge[tid] = last ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_merge[0] && !s_merge[1]) return;
+  __threadfence();
   for (int which = 0; which < 2; ++which) {
-    const int t = which == 0 ? 0 : nseg - 1;
-    if (which == 1 && nseg == 1) break;
-    const SegInfo si = s_seg[t];
-    if (si.whole || si.bad) continue;
+    if (!s_merge[which]) continue;
+    const SegInfo si = s_seg[which == 0 ? 0 : nseg - 1];
     const int k = si.gseg;
     const int ca = sc.blk0[k] / sc.bpc;
     const int cb = (sc.blk0[k + 1] - 1) / sc.bpc;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0)
-      s_last = atomicAdd(p.arrivals + sc.seg_base + k, 1) == (cb - ca);
-    __syncthreads();
-    if (!s_last) continue;
-    __threadfence();
     // Slots: the first CTA holds this segment in slot 0 if the segment starts
     // its range, else in slot 1; every later CTA holds it in slot 0.
     const int first_slot = (sc.blk0[k] != ca * sc.bpc) ? 1 : 0;
     for (int e = tid * 4; e < G * D; e += kWarps * 32 * 4) {
       const int h = e / D, d = e % D;
       float M = -INFINITY;
+#pragma unroll 4
       for (int cc = ca; cc <= cb; ++cc) {
         const int sl = sc.slot_base + 2 * cc + (cc == ca ? first_slot : 0);
         M = fmaxf(M, __ldcg(p.part_lse + static_cast<int64_t>(sl) * G + h));
       }
       float wsum = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
       for (int cc = ca; cc <= cb; ++cc) {
         const int sl = sc.slot_base + 2 * cc + (cc == ca ? first_slot : 0);
-        const float w = fast_exp2(__ldcg(p.part_lse + static_cast<int64_t>(sl) * G + h) - M);
+        const float lse = __ldcg(p.part_lse + static_cast<int64_t>(sl) * G + h);
         const float4 u = __ldcg(reinterpret_cast<const float4*>(
             p.part_o + (static_cast<int64_t>(sl) * G + h) * D + d));
+        const float w = fast_exp2(lse - M);
         wsum += w;
         acc.x += w * u.x; acc.y += w * u.y; acc.z += w * u.z; acc.w += w * u.w;
       }
@@ -540,7 +560,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(si.q0) * p.hq + si.g * G + h) * D + d) = pk;
     }
     if (tid == 0) p.arrivals[sc.seg_base + k] = 0;  // ready for the next call
-    __syncthreads();
   }
 }
 
