@@ -21,7 +21,10 @@
 //              tiles gathered page by page through the page table (3-deep ring);
 //   warp 1     TMA producer of the V tiles (2-deep ring), so K runs ahead of V;
 //   warp 2     MMA issuer: S = Q K^T (SMEM x SMEM -> TMEM), O += P V (P read
-//              from TMEM, V from SMEM), tcgen05.commit onto mbarriers;
+//              from TMEM, V from SMEM), tcgen05.commit onto mbarriers.  Score
+//              tiles run two ahead of the PV products (three S buffers in
+//              TMEM), so the tensor core works on S(j+1) and S(j+2) while the
+//              softmax of tile j is in flight;
 //   warps 3-6  softmax: one thread per row (TMEM lane), 64 keys per tile;
 //              reads S from TMEM, masks causal and window edges (interior
 //              tiles skip the mask), keeps the running max / sum in fp32,
@@ -85,15 +88,15 @@ struct Layout {
   static constexpr int kBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
   // TMEM columns.
   static constexpr int kOCol = 0;
-  static constexpr int kSCol = D;                        // 2 x 64
-  static constexpr int kPCol = D + 2 * kBN;              // 2 x 32
-  static constexpr int kCols = (D + 2 * kBN + kBN) <= 256 ? 256 : 512;
+  static constexpr int kSCol = D;                        // 3 x 64
+  static constexpr int kPCol = D + 3 * kBN;              // 2 x 32
+  static constexpr int kCols = 512;                      // D + 256 <= 512
 };
 
 struct Barriers {
   uint64_t q_full, q_empty;
   uint64_t k_full[kKS], k_empty[kKS], v_full[kVS], v_empty[kVS];
-  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t s_full[3], p_full[2], o_done[2];
   uint64_t o_free;
   uint64_t fin;          // all MMAs of this CTA complete (teardown)
   uint32_t tmem_base;
@@ -168,8 +171,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(&B.v_full[i], 1);
       mbar_init(&B.v_empty[i], 1);
     }
+    for (int i = 0; i < 3; ++i) mbar_init(&B.s_full[i], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&B.s_full[i], 1);
       mbar_init(&B.p_full[i], 128);
       mbar_init(&B.o_done[i], 1);
     }
@@ -276,36 +279,46 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         mma_commit(&B.v_empty[vs]);
         return true;
       };
+      // S(j) into S buffer (T % 3); K-major, 128-byte swizzle: 16 elements =
+      // 32 B inside a 64-wide chunk; chunks of Q are 16 KB apart, of K 8 KB.
+      auto issue_s = [&](uint32_t Ts) -> bool {
+        const int ks = Ts % kKS;
+        if (!mbar_wait(&B.k_full[ks], (Ts / kKS) & 1, abort, kWaitNs)) return false;
+        tc_fence_after();
+        const uint32_t kb = k_base + ks * Lay::kKVBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t c = kk >> 2, w = (kk & 3) * 32;
+          const uint64_t adesc = smem_desc(q_base + c * (kBM * 128) + w, 16, 1024);
+          const uint64_t bdesc = smem_desc(kb + c * (kBN * 128) + w, 16, 1024);
+          mma_ss(tmem + Lay::kSCol + (Ts % 3) * kBN, adesc, bdesc, kIdS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&B.s_full[Ts % 3]);
+        mma_commit(&B.k_empty[ks]);
+        return true;
+      };
       for (int it = blockIdx.x; it < items.n && alive; it += gridDim.x) {
         const Geom gm = item_geom(p, items.items[it]);
         if (!gm.ok) continue;
         alive = mbar_wait(&B.q_full, I & 1, abort, kWaitNs);
-        for (int j = 0; j < gm.ntiles && alive; ++j, ++T) {
-          const int ks = T % kKS;
-          if (!mbar_wait(&B.k_full[ks], (T / kKS) & 1, abort, kWaitNs)) {
-            alive = false;
-            break;
+        // Order: S(0), S(1), then for each j: S(j + 2), PV(j).  S(j + 2)
+        // reuses the buffer of S(j - 1), whose softmax finished before PV(j - 1)
+        // was issued.  Q is released as soon as the item's last S is issued.
+        const int n = gm.ntiles;
+        auto issue_s_item = [&](int j) -> bool {
+          const bool ok = issue_s(T + j);
+          if (ok && j == n - 1) mma_commit(&B.q_empty);
+          return ok;
+        };
+        for (int j = 0; j < 2 && j < n && alive; ++j) alive = issue_s_item(j);
+        for (int j = 0; j < n && alive; ++j) {
+          if (j + 2 < n) {
+            alive = issue_s_item(j + 2);
+            if (!alive) break;
           }
-          tc_fence_after();
-          const uint32_t kb = k_base + ks * Lay::kKVBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            // K-major, 128-byte swizzle: 16 elements = 32 B inside a 64-wide
-            // chunk; chunks of Q are 16 KB apart, chunks of K 8 KB apart.
-            const uint32_t c = kk >> 2, w = (kk & 3) * 32;
-            const uint64_t adesc = smem_desc(q_base + c * (kBM * 128) + w, 16, 1024);
-            const uint64_t bdesc = smem_desc(kb + c * (kBN * 128) + w, 16, 1024);
-            mma_ss(tmem + Lay::kSCol + (T & 1) * kBN, adesc, bdesc, kIdS, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&B.s_full[T & 1]);
-          mma_commit(&B.k_empty[ks]);
-          if (j >= 1 && !issue_pv(T - 1, j - 1)) {
-            alive = false;
-            break;
-          }
+          alive = issue_pv(T + j, j);
         }
-        if (alive && gm.ntiles > 0) alive = issue_pv(T - 1, gm.ntiles - 1);
-        mma_commit(&B.q_empty);
+        T += n;
         ++I;
       }
       // Every MMA issued must finish before TMEM is released.
@@ -331,8 +344,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const int32_t lo = first_visible(pos, gm.W);
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < gm.ntiles; ++j, ++T) {
-        const int st = T & 1;
-        if (!mbar_wait(&B.s_full[st], (T >> 1) & 1, abort, kWaitNs)) {
+        const int st = T & 1;          // P buffer
+        const int sb = T % 3;          // S buffer
+        if (!mbar_wait(&B.s_full[sb], (T / 3) & 1, abort, kWaitNs)) {
           alive = false;
           break;
         }
@@ -341,8 +355,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         {
           uint32_t (&lo32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
           uint32_t (&hi32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-          tmem_ld32(lane_addr + Lay::kSCol + st * kBN, lo32);
-          tmem_ld32(lane_addr + Lay::kSCol + st * kBN + 32, hi32);
+          tmem_ld32(lane_addr + Lay::kSCol + sb * kBN, lo32);
+          tmem_ld32(lane_addr + Lay::kSCol + sb * kBN + 32, hi32);
         }
         tmem_wait_ld();
         const int32_t key0 = (gm.kt0 + j) * kBN;
