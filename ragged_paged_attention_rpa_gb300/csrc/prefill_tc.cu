@@ -20,11 +20,13 @@
 //   warp 0     TMA producer of the Q block (once per item) and of 64-key K
 //              tiles gathered page by page through the page table (3-deep ring);
 //   warp 1     TMA producer of the V tiles (2-deep ring), so K runs ahead of V;
-//   warp 2     MMA issuer: S = Q K^T (SMEM x SMEM -> TMEM), O += P V (P read
-//              from TMEM, V from SMEM), tcgen05.commit onto mbarriers.  Score
-//              tiles run two ahead of the PV products (three S buffers in
-//              TMEM), so the tensor core works on S(j+1) and S(j+2) while the
-//              softmax of tile j is in flight;
+//   warp 2     MMA issuer: copies each item's Q block from shared memory into
+//              tensor memory once (tcgen05.cp), then S = Q K^T (Q from TMEM,
+//              K from SMEM: the score MMAs no longer re-read Q through shared
+//              memory, whose bandwidth bounded them) and O += P V (P from
+//              TMEM, V from SMEM); tcgen05.commit onto mbarriers.  The score
+//              tile runs one ahead of the PV product (two S buffers; P is
+//              written over its own S);
 //   warps 3-6  softmax: one thread per row (TMEM lane), 64 keys per tile;
 //              reads S from TMEM, masks causal and window edges (interior
 //              tiles skip the mask), keeps the running max / sum in fp32,
@@ -87,16 +89,18 @@ struct Layout {
   // (which owns the SM's tensor memory) is resident per SM.
   static constexpr int kBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
   // TMEM columns.
+  // O: D columns; Q: D/2 (bf16 pairs); two S buffers of 64, P (bf16 pairs)
+  // written over the first 32 columns of its own S buffer.
   static constexpr int kOCol = 0;
-  static constexpr int kSCol = D;                        // 3 x 64
-  static constexpr int kPCol = D + 3 * kBN;              // 2 x 32
-  static constexpr int kCols = 512;                      // D + 256 <= 512
+  static constexpr int kQCol = D;
+  static constexpr int kSCol = D + D / 2;
+  static constexpr int kCols = (D + D / 2 + 2 * kBN) <= 256 ? 256 : 512;
 };
 
 struct Barriers {
   uint64_t q_full, q_empty;
   uint64_t k_full[kKS], k_empty[kKS], v_full[kVS], v_empty[kVS];
-  uint64_t s_full[3], p_full[2], o_done[2];
+  uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t o_free;
   uint64_t fin;          // all MMAs of this CTA complete (teardown)
   uint32_t tmem_base;
@@ -171,8 +175,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(&B.v_full[i], 1);
       mbar_init(&B.v_empty[i], 1);
     }
-    for (int i = 0; i < 3; ++i) mbar_init(&B.s_full[i], 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&B.s_full[i], 1);
       mbar_init(&B.p_full[i], 128);
       mbar_init(&B.o_done[i], 1);
     }
@@ -270,17 +274,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           // V as MN-major B: 8-key groups 1024 B apart (SBO), 64-dim chunks
-          // one tile-chunk apart (LBO); 16 keys per MMA = 2048 B.
+          // one tile-chunk apart (LBO); 16 keys per MMA = 2048 B.  P (A) sits
+          // in the first 32 columns of its S buffer, 8 columns per 16 keys.
           const uint64_t bdesc = smem_desc(vb + kk * 2048, kBN * 128, 1024);
-          mma_ts(tmem + Lay::kOCol, tmem + Lay::kPCol + sb * (kBN / 2) + kk * 8, bdesc, kIdPV,
+          mma_ts(tmem + Lay::kOCol, tmem + Lay::kSCol + sb * kBN + kk * 8, bdesc, kIdPV,
                  (jp > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&B.o_done[sb]);
         mma_commit(&B.v_empty[vs]);
         return true;
       };
-      // S(j) into S buffer (T % 3); K-major, 128-byte swizzle: 16 elements =
-      // 32 B inside a 64-wide chunk; chunks of Q are 16 KB apart, of K 8 KB.
+      // S(j) into S buffer (T & 1): A = Q from TMEM (8 columns per 16 dims),
+      // B = K, K-major 128-byte swizzle (16 elements = 32 B inside a 64-wide
+      // chunk; chunks 8 KB apart).
       auto issue_s = [&](uint32_t Ts) -> bool {
         const int ks = Ts % kKS;
         if (!mbar_wait(&B.k_full[ks], (Ts / kKS) & 1, abort, kWaitNs)) return false;
@@ -289,11 +295,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t c = kk >> 2, w = (kk & 3) * 32;
-          const uint64_t adesc = smem_desc(q_base + c * (kBM * 128) + w, 16, 1024);
           const uint64_t bdesc = smem_desc(kb + c * (kBN * 128) + w, 16, 1024);
-          mma_ss(tmem + Lay::kSCol + (Ts % 3) * kBN, adesc, bdesc, kIdS, kk > 0 ? 1u : 0u);
+          mma_ts(tmem + Lay::kSCol + (Ts & 1) * kBN, tmem + Lay::kQCol + kk * 8, bdesc, kIdS,
+                 kk > 0 ? 1u : 0u);
         }
-        mma_commit(&B.s_full[Ts % 3]);
+        mma_commit(&B.s_full[Ts & 1]);
         mma_commit(&B.k_empty[ks]);
         return true;
       };
@@ -301,19 +307,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const Geom gm = item_geom(p, items.items[it]);
         if (!gm.ok) continue;
         alive = mbar_wait(&B.q_full, I & 1, abort, kWaitNs);
-        // Order: S(0), S(1), then for each j: S(j + 2), PV(j).  S(j + 2)
-        // reuses the buffer of S(j - 1), whose softmax finished before PV(j - 1)
-        // was issued.  Q is released as soon as the item's last S is issued.
+        if (!alive) break;
+        // Q: shared memory -> tensor memory, one 16-dim slice per copy (the
+        // same K-major swizzled slices an MMA would read).  In order with the
+        // MMAs, so it lands after the previous item's last score tile; the
+        // shared-memory buffer is free for the next item once the copies are
+        // done.
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t c = kk >> 2, w = (kk & 3) * 32;
+          tmem_cp_128x256b(tmem + Lay::kQCol + kk * 8,
+                           smem_desc(q_base + c * (kBM * 128) + w, 16, 1024));
+        }
+        mma_commit(&B.q_empty);
+        // Order: S(0), then for each j: S(j + 1), PV(j).  S(j + 1) overwrites
+        // the buffer holding P(j - 1), which PV(j - 1) (issued before it) read.
         const int n = gm.ntiles;
-        auto issue_s_item = [&](int j) -> bool {
-          const bool ok = issue_s(T + j);
-          if (ok && j == n - 1) mma_commit(&B.q_empty);
-          return ok;
-        };
-        for (int j = 0; j < 2 && j < n && alive; ++j) alive = issue_s_item(j);
+        if (n > 0) alive = issue_s(T);
         for (int j = 0; j < n && alive; ++j) {
-          if (j + 2 < n) {
-            alive = issue_s_item(j + 2);
+          if (j + 1 < n) {
+            alive = issue_s(T + j + 1);
             if (!alive) break;
           }
           alive = issue_pv(T + j, j);
@@ -344,9 +358,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const int32_t lo = first_visible(pos, gm.W);
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < gm.ntiles; ++j, ++T) {
-        const int st = T & 1;          // P buffer
-        const int sb = T % 3;          // S buffer
-        if (!mbar_wait(&B.s_full[sb], (T / 3) & 1, abort, kWaitNs)) {
+        const int sb = T & 1;          // S buffer (P is written over it)
+        if (!mbar_wait(&B.s_full[sb], (T >> 1) & 1, abort, kWaitNs)) {
           alive = false;
           break;
         }
@@ -455,16 +468,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           }
         }
         l += ls;
-        // The P buffer was last read by the PV two tiles back.
-        if (T >= 2 && !mbar_wait(&B.o_done[st], ((T - 2) >> 1) & 1, abort, kWaitNs)) {
-          alive = false;
-          break;
-        }
-        tc_fence_after();
-        tmem_st32(lane_addr + Lay::kPCol + st * (kBN / 2), pk);
+        // P over the first 32 columns of this tile's S buffer (already read).
+        tmem_st32(lane_addr + Lay::kSCol + sb * kBN, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&B.p_full[st]);
+        mbar_arrive(&B.p_full[sb]);
       }
       if (!alive) break;
       if (gm.ntiles == 0) continue;
