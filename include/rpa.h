@@ -80,7 +80,10 @@ enum {
   RPA_DEVERR_PAGE_ID = 1,    /* a page-table entry outside [0, num_pages)       */
   RPA_DEVERR_LENGTHS = 2,    /* device lengths disagree with the plan's copies  */
   RPA_DEVERR_PLAN = 3,       /* the work list in the workspace is not this plan */
-  RPA_DEVERR_TIMEOUT = 4     /* a bounded wait inside a kernel gave up          */
+  RPA_DEVERR_TIMEOUT = 4,    /* a bounded wait inside a kernel gave up          */
+  RPA_DEVERR_LAUNCH = 5      /* a kernel found its launch unusable (shared
+                                memory base not 1024-byte aligned) and did
+                                nothing                                        */
 };
 
 /* Kernel paths a plan may use. */

@@ -17,17 +17,20 @@
 //
 // One CTA (persistent, one per SM) walks a longest-first list of work items
 // (sequence, query block, KV head).  Warp roles:
-//   warp 0     TMA producer of the Q block (once per item) and of 64-key K
-//              tiles gathered page by page through the page table (3-deep ring);
-//   warp 1     TMA producer of the V tiles (2-deep ring), so K runs ahead of V;
-//   warp 2     MMA issuer: copies each item's Q block from shared memory into
-//              tensor memory once (tcgen05.cp), then S = Q K^T (Q from TMEM,
-//              K from SMEM: the score MMAs no longer re-read Q through shared
-//              memory, whose bandwidth bounded them) and O += P V (P from
-//              TMEM, V from SMEM); tcgen05.commit onto mbarriers.  The score
-//              tile runs one ahead of the PV product (two S buffers; P is
-//              written over its own S);
-//   warps 3-6  softmax: one thread per row (TMEM lane), 64 keys per tile;
+//   warp 0     TMA producer of the Q block (once per item) and of K, gathered
+//              page by page through the page table into a ring of 16 KB
+//              stages (one 64-dimension chunk of a 128-key tile each);
+//   warp 1     TMA producer of V into its own ring of 16 KB stages (8192 / D
+//              keys x all D dimensions each), so K runs ahead of V;
+//   warp 2     MMA issuer: S = Q K^T over 128-key tiles (SMEM x SMEM -> TMEM,
+//              N = 128: narrower score MMAs leave the tensor core partly
+//              idle) and O += P V (P from TMEM, V from SMEM), one ring stage
+//              at a time; tcgen05.commit onto mbarriers.  The score tile runs
+//              one ahead of the PV product (two S buffers; P is written over
+//              its own S);
+//   warps 3-10 softmax: two warps per 32 rows (a TMEM lane quarter), one
+//              thread per row and 64 of the tile's 128 keys each; the pair
+//              swaps row maxima through shared memory every tile;
 //              reads S from TMEM, masks causal and window edges (interior
 //              tiles skip the mask), keeps the running max / sum in fp32,
 //              exponentiates with the MUFU unit and, for one pair in four,
@@ -51,10 +54,11 @@ namespace {
 using namespace sm100;
 
 constexpr int kBM = 128;        // MMA rows per block
-constexpr int kBN = 64;         // keys per KV tile
-constexpr int kKS = 3;          // K ring depth
-constexpr int kVS = 2;          // V ring depth
-constexpr int kThreads = 224;   // K producer, V producer, MMA, 4 softmax warps
+constexpr int kBN = 128;        // keys per score tile (N of the score MMAs)
+constexpr int kStage = 16384;   // bytes per K or V ring stage
+constexpr int kKS = 5;          // K ring depth (stages)
+constexpr int kVS = 5;          // V ring depth (stages)
+constexpr int kThreads = 352;   // K producer, V producer, MMA, 8 softmax warps
 constexpr int kPolyEvery = 4;   // one pair of exponentials in four on the FMA pipe
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait, then give up
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
@@ -71,30 +75,34 @@ struct PrefillParams {
   const int32_t* window;
   __nv_bfloat16* out;
   unsigned char* ws;
-  int32_t hq, group, qb_tokens, page_size, page_shift, box_rows, mpps, num_pages;
+  int32_t hq, group, qb_tokens, page_size, page_shift, box_rows_k, box_rows_v, mpps, num_pages;
   float scale_log2;
 };
 
+// A score tile's K streams through the K ring one 64-dimension chunk at a
+// time (128 keys x 128 B = one stage); its V streams through the V ring
+// kVKeys keys at a time (all D dimensions, kVKeys x D x 2 B = one stage).
+// Either way a tile is D / 64 stages, and one stage feeds whole MMAs, so the
+// tensor core starts on a tile before all of it has landed.
 template <int D>
 struct Layout {
   static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms per row
+  static constexpr int kVKeys = 8192 / D;                // keys per V stage
   static constexpr int kQBytes = kBM * D * 2;
-  static constexpr int kKVBytes = kBN * D * 2;           // one K (or V) tile
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQBytes;
-  static constexpr int kVOff = kKOff + kKS * kKVBytes;
-  static constexpr int kBarOff = kVOff + kVS * kKVBytes;
-  static constexpr int kUsed = kBarOff + 256 + 1024;    // barriers + alignment slack
+  static constexpr int kVOff = kKOff + kKS * kStage;
+  static constexpr int kBarOff = kVOff + kVS * kStage;
+  static constexpr int kXchOff = kBarOff + 512;         // softmax pair exchange
+  static constexpr int kUsed = kXchOff + 2 * 2 * kBM * 4;
   // Ask for more than half an SM's shared memory so that exactly one CTA
   // (which owns the SM's tensor memory) is resident per SM.
   static constexpr int kBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
-  // TMEM columns.
-  // O: D columns; Q: D/2 (bf16 pairs); two S buffers of 64, P (bf16 pairs)
-  // written over the first 32 columns of its own S buffer.
+  // TMEM columns: O (D), then two S buffers of 128; P (bf16 pairs) is
+  // written over the first 64 columns of its own S buffer.
   static constexpr int kOCol = 0;
-  static constexpr int kQCol = D;
-  static constexpr int kSCol = D + D / 2;
-  static constexpr int kCols = (D + D / 2 + 2 * kBN) <= 256 ? 256 : 512;
+  static constexpr int kSCol = D;
+  static constexpr int kCols = 512;                      // D + 256 <= 512
 };
 
 struct Barriers {
@@ -103,9 +111,12 @@ struct Barriers {
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t o_free;
   uint64_t fin;          // all MMAs of this CTA complete (teardown)
+  uint64_t xbar[4];      // softmax pair exchange, one per TMEM lane quarter
   uint32_t tmem_base;
   int abort;
 };
+
+static_assert(sizeof(Barriers) <= 512, "barrier block");
 
 struct Geom {
   int32_t seq, g, t0, ntok, pos_first, kt0, ntiles, W;
@@ -133,17 +144,42 @@ __device__ __forceinline__ Geom item_geom(const PrefillParams& p, const PrefillI
   return r;
 }
 
-// TMA source row of box `b` of KV tile j of an item (-box_rows: a box wholly
-// out of bounds, which the TMA fills with zeros).
-__device__ __forceinline__ int32_t box_row(const PrefillParams& p, const Geom& gm, int j, int b) {
-  const int32_t key = (gm.kt0 + j) * kBN + b * p.box_rows;
+// Maximum of N floats (stored as bits) as a tree of three-input maxima.
+template <int N>
+__device__ __forceinline__ float max_tree(const uint32_t* v) {
+  if constexpr (N == 1) {
+    return __uint_as_float(v[0]);
+  } else if constexpr (N == 2) {
+    return fmaxf(__uint_as_float(v[0]), __uint_as_float(v[1]));
+  } else {
+    constexpr int M = (N + 2) / 3;
+    uint32_t t[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+      const float a = __uint_as_float(v[3 * i]);
+      float m = a;
+      if (3 * i + 2 < N)
+        m = fmax3(a, __uint_as_float(v[3 * i + 1]), __uint_as_float(v[3 * i + 2]));
+      else if (3 * i + 1 < N)
+        m = fmaxf(a, __uint_as_float(v[3 * i + 1]));
+      t[i] = __float_as_uint(m);
+    }
+    return max_tree<M>(t);
+  }
+}
+
+// TMA source row of the box of `rows` keys starting at `key` (a box never
+// crosses a page; -rows: a box wholly past the item's last query, which the
+// TMA fills with zeros).
+__device__ __forceinline__ int32_t box_row(const PrefillParams& p, const Geom& gm, int32_t key,
+                                           int32_t rows) {
   const int32_t pos_last = gm.pos_first + gm.ntok - 1;
-  if (key > pos_last) return -p.box_rows;
+  if (key > pos_last) return -rows;
   const int32_t page = __ldg(p.page_table + static_cast<int64_t>(gm.seq) * p.mpps +
                              (key >> p.page_shift));
   if (page < 0 || page >= p.num_pages) {
     report_error(p.ws, RPA_DEVERR_PAGE_ID, gm.seq);
-    return -p.box_rows;
+    return -rows;
   }
   return page * p.page_size + (key & (p.page_size - 1));
 }
@@ -154,9 +190,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams p,
                   const __grid_constant__ ItemList items) {
   using Lay = Layout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // The 128-byte swizzle needs 1024-byte aligned tiles; the layout fills
+  // the shared memory with no slack, so a misaligned base ends the launch.
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_addr(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) report_error(p.ws, RPA_DEVERR_LAUNCH, blockIdx.x);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   __nv_bfloat16* q_s = reinterpret_cast<__nv_bfloat16*>(smem + Lay::kQOff);
   __nv_bfloat16* k_s = reinterpret_cast<__nv_bfloat16*>(smem + Lay::kKOff);
   __nv_bfloat16* v_s = reinterpret_cast<__nv_bfloat16*>(smem + Lay::kVOff);
@@ -177,10 +218,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.p_full[i], 128);
+      mbar_init(&B.p_full[i], 256);
       mbar_init(&B.o_done[i], 1);
     }
-    mbar_init(&B.o_free, 128);
+    mbar_init(&B.o_free, 256);
+    for (int i = 0; i < 4; ++i) mbar_init(&B.xbar[i], 64);
     mbar_init(&B.fin, 1);
     B.abort = 0;
     fence_barrier_init();
@@ -200,15 +242,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   if (warp <= 1) {
     // ------------------------------------------------------------ producers
-    // Warp 0 loads Q and K, warp 1 loads V; each keeps its own ring.
+    // Warp 0 loads Q and K, warp 1 loads V; each keeps its own ring of
+    // 16 KB stages, counted by C across tiles and items.
     const bool is_k = warp == 0;
     const int depth = is_k ? kKS : kVS;
     uint64_t* full = is_k ? B.k_full : B.v_full;
     uint64_t* empty = is_k ? B.k_empty : B.v_empty;
-    __nv_bfloat16* ring = is_k ? k_s : v_s;
+    uint8_t* ring = smem + (is_k ? Lay::kKOff : Lay::kVOff);
     const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
-    uint32_t T = 0, I = 0, issued_q = 0;
-    const int nbox = kBN / p.box_rows;
+    const int rows = is_k ? p.box_rows_k : p.box_rows_v;
+    const int nbox = (is_k ? kBN : Lay::kVKeys) / rows;    // boxes per stage (<= 8)
+    uint32_t C = 0, I = 0, issued_q = 0;
     const uint32_t q_box_bytes = static_cast<uint32_t>(G * p.qb_tokens) * 128u;
     bool alive = true;
     for (int it = blockIdx.x; it < items.n && alive; it += gridDim.x) {
@@ -228,25 +272,37 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
       }
       alive = __shfl_sync(0xffffffffu, alive, 0);
-      for (int j = 0; j < gm.ntiles && alive; ++j, ++T) {
-        const int st = T % depth;
-        const uint32_t ph = (T / depth) & 1;
-        const int32_t row = lane < nbox ? box_row(p, gm, j, lane) : 0;
-        if (lane == 0) alive = mbar_wait(&empty[st], ph ^ 1, abort, kWaitNs);
-        alive = __shfl_sync(0xffffffffu, alive, 0);
-        if (!alive) break;
-        if (lane == 0) mbar_arrive_expect_tx(&full[st], Lay::kKVBytes);
-        __syncwarp();
-        if (lane < nbox)
-          for (int c = 0; c < Lay::kChunks; ++c)
-            tma_load_3d(ring + st * kBN * D + c * kBN * 64 + lane * p.box_rows * 64, tm, &full[st],
-                        c * 64, gm.g, row);
+      for (int j = 0; j < gm.ntiles && alive; ++j) {
+        const int32_t key0 = (gm.kt0 + j) * kBN;
+        // K: the same 128 keys for every chunk of the tile.
+        const int32_t krow = (is_k && lane < nbox) ? box_row(p, gm, key0 + lane * rows, rows) : 0;
+        for (int sgi = 0; sgi < Lay::kChunks; ++sgi, ++C) {
+          const int st = C % depth;
+          const uint32_t ph = (C / depth) & 1;
+          const int32_t row = is_k ? krow
+                              : (lane < nbox ? box_row(p, gm, key0 + sgi * Lay::kVKeys + lane * rows, rows)
+                                             : 0);
+          if (lane == 0) alive = mbar_wait(&empty[st], ph ^ 1, abort, kWaitNs);
+          alive = __shfl_sync(0xffffffffu, alive, 0);
+          if (!alive) break;
+          if (lane == 0) mbar_arrive_expect_tx(&full[st], kStage);
+          __syncwarp();
+          if (lane < nbox) {
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(ring + st * kStage) + lane * rows * 64;
+            if (is_k) {
+              tma_load_3d(dst, tm, &full[st], sgi * 64, gm.g, row);
+            } else {
+              for (int c = 0; c < Lay::kChunks; ++c)
+                tma_load_3d(dst + c * Lay::kVKeys * 64, tm, &full[st], c * 64, gm.g, row);
+            }
+          }
+        }
       }
     }
     if (!alive && lane == 0) {
       // Let every copy this warp started land before its shared memory goes.
       report_error(p.ws, RPA_DEVERR_TIMEOUT, blockIdx.x);
-      for (uint32_t t = (T > static_cast<uint32_t>(depth) ? T - depth : 0); t < T; ++t) {
+      for (uint32_t t = (C > static_cast<uint32_t>(depth) ? C - depth : 0); t < C; ++t) {
         int dummy = 0;
         mbar_wait(&full[t % depth], (t / depth) & 1, &dummy, kDrainNs);
       }
@@ -257,106 +313,128 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(kBN, 0);
-      constexpr uint32_t kIdPV = idesc_bf16(D, 1);
-      const uint32_t q_base = smem_addr(q_s), k_base = smem_addr(k_s), v_base = smem_addr(v_s);
-      uint32_t T = 0, I = 0;
-      bool alive = true;
-      auto issue_pv = [&](uint32_t Tp, int jp) -> bool {
-        const int sb = Tp & 1;
-        const int vs = Tp % kVS;
-        if (!mbar_wait(&B.p_full[sb], (Tp >> 1) & 1, abort, kWaitNs)) return false;
-        if (!mbar_wait(&B.v_full[vs], (Tp / kVS) & 1, abort, kWaitNs)) return false;
-        if (jp == 0 && !mbar_wait(&B.o_free, (I & 1) ^ 1, abort, kWaitNs)) return false;
+    // The whole warp walks the schedule and waits; one elected lane issues
+    // every MMA and commit (see mma_ss).
+    constexpr uint32_t kIdS = idesc_bf16(kBN, 0);
+    constexpr uint32_t kIdPV = idesc_bf16(D, 1);
+    const uint32_t q_base = smem_addr(q_s), k_base = smem_addr(k_s), v_base = smem_addr(v_s);
+    uint32_t T = 0, I = 0, CK = 0, CV = 0;   // tiles, items, K / V stages
+    bool alive = true;
+    // A wait the whole warp agrees on.
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      const bool ok = mbar_wait(bar, parity, abort, kWaitNs);
+      return __all_sync(0xffffffffu, ok);
+    };
+    // O += P(Tp) V(Tp): one V stage (kVKeys keys x D) at a time.  V is the
+    // MN-major B operand: 8-key groups 1024 B apart (SBO), 64-dimension
+    // chunks kVKeys x 128 B apart (LBO); 16 keys per MMA = 2048 B.  P (A)
+    // sits in the first 64 columns of its S buffer, 8 columns per 16 keys.
+    auto issue_pv = [&](uint32_t Tp, int jp) -> bool {
+      const int sb = Tp & 1;
+      if (!wait(&B.p_full[sb], (Tp >> 1) & 1)) return false;
+      if (jp == 0 && !wait(&B.o_free, (I & 1) ^ 1)) return false;
+      for (int sgi = 0; sgi < Lay::kChunks; ++sgi, ++CV) {
+        const int vs = CV % kVS;
+        if (!wait(&B.v_full[vs], (CV / kVS) & 1)) return false;
         tc_fence_after();
-        const uint32_t vb = v_base + vs * Lay::kKVBytes;
+        const uint32_t vb = v_base + vs * kStage;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // V as MN-major B: 8-key groups 1024 B apart (SBO), 64-dim chunks
-          // one tile-chunk apart (LBO); 16 keys per MMA = 2048 B.  P (A) sits
-          // in the first 32 columns of its S buffer, 8 columns per 16 keys.
-          const uint64_t bdesc = smem_desc(vb + kk * 2048, kBN * 128, 1024);
-          mma_ts(tmem + Lay::kOCol, tmem + Lay::kSCol + sb * kBN + kk * 8, bdesc, kIdPV,
-                 (jp > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < Lay::kVKeys / 16; ++kk) {
+          const int kg = sgi * (Lay::kVKeys / 16) + kk;     // 16-key group of the tile
+          const uint64_t bdesc = smem_desc(vb + kk * 2048, Lay::kVKeys * 128, 1024);
+          mma_ts(tmem + Lay::kOCol, tmem + Lay::kSCol + sb * kBN + kg * 8, bdesc, kIdPV,
+                 (jp > 0 || kg > 0) ? 1u : 0u);
         }
-        mma_commit(&B.o_done[sb]);
         mma_commit(&B.v_empty[vs]);
-        return true;
-      };
-      // S(j) into S buffer (T & 1): A = Q from TMEM (8 columns per 16 dims),
-      // B = K, K-major 128-byte swizzle (16 elements = 32 B inside a 64-wide
-      // chunk; chunks 8 KB apart).
-      auto issue_s = [&](uint32_t Ts) -> bool {
-        const int ks = Ts % kKS;
-        if (!mbar_wait(&B.k_full[ks], (Ts / kKS) & 1, abort, kWaitNs)) return false;
-        tc_fence_after();
-        const uint32_t kb = k_base + ks * Lay::kKVBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t c = kk >> 2, w = (kk & 3) * 32;
-          const uint64_t bdesc = smem_desc(kb + c * (kBN * 128) + w, 16, 1024);
-          mma_ts(tmem + Lay::kSCol + (Ts & 1) * kBN, tmem + Lay::kQCol + kk * 8, bdesc, kIdS,
-                 kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&B.s_full[Ts & 1]);
-        mma_commit(&B.k_empty[ks]);
-        return true;
-      };
-      for (int it = blockIdx.x; it < items.n && alive; it += gridDim.x) {
-        const Geom gm = item_geom(p, items.items[it]);
-        if (!gm.ok) continue;
-        alive = mbar_wait(&B.q_full, I & 1, abort, kWaitNs);
-        if (!alive) break;
-        // Q: shared memory -> tensor memory, one 16-dim slice per copy (the
-        // same K-major swizzled slices an MMA would read).  In order with the
-        // MMAs, so it lands after the previous item's last score tile; the
-        // shared-memory buffer is free for the next item once the copies are
-        // done.
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t c = kk >> 2, w = (kk & 3) * 32;
-          tmem_cp_128x256b(tmem + Lay::kQCol + kk * 8,
-                           smem_desc(q_base + c * (kBM * 128) + w, 16, 1024));
-        }
-        mma_commit(&B.q_empty);
-        // Order: S(0), then for each j: S(j + 1), PV(j).  S(j + 1) overwrites
-        // the buffer holding P(j - 1), which PV(j - 1) (issued before it) read.
-        const int n = gm.ntiles;
-        if (n > 0) alive = issue_s(T);
-        for (int j = 0; j < n && alive; ++j) {
-          if (j + 1 < n) {
-            alive = issue_s(T + j + 1);
-            if (!alive) break;
-          }
-          alive = issue_pv(T + j, j);
-        }
-        T += n;
-        ++I;
       }
-      // Every MMA issued must finish before TMEM is released.
-      mma_commit(&B.fin);
-      int dummy = 0;
-      mbar_wait(&B.fin, 0, &dummy, kDrainNs);
-      if (!alive) report_error(p.ws, RPA_DEVERR_TIMEOUT, blockIdx.x);
+      mma_commit(&B.o_done[sb]);
+      return true;
+    };
+    // S(Ts) into S buffer (Ts & 1): one K stage (a 64-dimension chunk of 128
+    // keys) at a time.  Q and K are K-major with the 128-byte swizzle: 16
+    // elements = 32 B inside a chunk; Q's chunks are 16 KB apart.
+    auto issue_s = [&](uint32_t Ts) -> bool {
+      const uint32_t sc = tmem + Lay::kSCol + (Ts & 1) * kBN;
+      for (int c = 0; c < Lay::kChunks; ++c, ++CK) {
+        const int ks = CK % kKS;
+        if (!wait(&B.k_full[ks], (CK / kKS) & 1)) return false;
+        tc_fence_after();
+        const uint32_t kb = k_base + ks * kStage;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint64_t adesc = smem_desc(q_base + c * (kBM * 128) + w * 32, 16, 1024);
+          const uint64_t bdesc = smem_desc(kb + w * 32, 16, 1024);
+          mma_ss(sc, adesc, bdesc, kIdS, (c > 0 || w > 0) ? 1u : 0u);
+        }
+        mma_commit(&B.k_empty[ks]);
+      }
+      mma_commit(&B.s_full[Ts & 1]);
+      return true;
+    };
+    for (int it = blockIdx.x; it < items.n && alive; it += gridDim.x) {
+      const Geom gm = item_geom(p, items.items[it]);
+      if (!gm.ok) continue;
+      alive = wait(&B.q_full, I & 1);
+      if (!alive) break;
+      // Order: S(0), then for each j: S(j + 1), PV(j).  S(j + 1) overwrites
+      // the buffer holding P(j - 1), which PV(j - 1) (issued before it) read.
+      // Q is released once the item's last score tile is issued.
+      const int n = gm.ntiles;
+      if (n > 0) alive = issue_s(T);
+      if (n <= 1) mma_commit(&B.q_empty);
+      for (int j = 0; j < n && alive; ++j) {
+        if (j + 1 < n) {
+          alive = issue_s(T + j + 1);
+          if (!alive) break;
+          if (j + 2 == n) mma_commit(&B.q_empty);
+        }
+        alive = issue_pv(T + j, j);
+      }
+      T += n;
+      ++I;
     }
+    // Every MMA issued must finish before TMEM is released.
+    mma_commit(&B.fin);
+    int dummy = 0;
+    mbar_wait(&B.fin, 0, &dummy, kDrainNs);
+    __syncwarp();
+    if (!alive && lane == 0) report_error(p.ws, RPA_DEVERR_TIMEOUT, blockIdx.x);
   } else {
     // ------------------------------------------------------------ softmax + epilogue
+    // Two warps per TMEM lane quarter (32 rows): half h takes keys
+    // [64h, 64h + 64) of every tile and columns [hD/2, (h+1)D/2) of O.  The
+    // pair swaps row maxima every tile (and row sums once per item) through
+    // shared memory, paced by the quarter's mbarrier; both then take the
+    // same decisions, so O and P stay consistent.
     const int q4 = warp & 3;                            // TMEM lane quarter of this warp
+    const int h = (warp - 3) >> 2;                      // key / column half
     const int r = 32 * q4 + lane;                       // TMEM lane = row
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q4) << 16);
     const int tok = r / G, head = r % G;
     const float c = p.scale_log2;
-    uint32_t T = 0;
+    float* xch = reinterpret_cast<float*>(smem + Lay::kXchOff);   // [2][2][kBM]
+    uint64_t* xbar = &B.xbar[q4];
+    uint32_t T = 0, X = 0;                              // tiles, exchanges
     bool alive = true;
+    // Publish v for this row, wait for the partner's, return it.
+    auto swap = [&](float v) -> float {
+      xch[((X & 1) * 2 + h) * kBM + r] = v;
+      tc_fence_before();                // this warp's TMEM reads come first
+      mbar_arrive(xbar);
+      const bool ok = mbar_wait(xbar, X & 1, abort, kWaitNs);
+      tc_fence_after();
+      const float o = xch[((X & 1) * 2 + (h ^ 1)) * kBM + r];
+      ++X;
+      if (!ok) alive = false;
+      return o;
+    };
     for (int it = blockIdx.x; it < items.n && alive; it += gridDim.x) {
       const Geom gm = item_geom(p, items.items[it]);
       if (!gm.ok) continue;
       const bool valid = tok < gm.ntok && r < G * p.qb_tokens;
       const int32_t pos = gm.pos_first + tok;
       const int32_t lo = first_visible(pos, gm.W);
-      float m_ref = -INFINITY, l = 0.f;
+      float m_ref = -INFINITY, l = 0.f;                 // l: this half's sum
       for (int j = 0; j < gm.ntiles; ++j, ++T) {
         const int sb = T & 1;          // S buffer (P is written over it)
         if (!mbar_wait(&B.s_full[sb], (T >> 1) & 1, abort, kWaitNs)) {
@@ -365,46 +443,34 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         tc_fence_after();
         uint32_t sr[64];
-        {
-          uint32_t (&lo32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-          uint32_t (&hi32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-          tmem_ld32(lane_addr + Lay::kSCol + sb * kBN, lo32);
-          tmem_ld32(lane_addr + Lay::kSCol + sb * kBN + 32, hi32);
-        }
+        tmem_ld32(lane_addr + Lay::kSCol + sb * kBN + 64 * h,
+                  *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(lane_addr + Lay::kSCol + sb * kBN + 64 * h + 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_wait_ld();
-        const int32_t key0 = (gm.kt0 + j) * kBN;
-        // Interior tiles (every key visible to every row of the warp) skip
+        const int32_t key0 = (gm.kt0 + j) * kBN + 64 * h;
+        // Interior halves (every key visible to every row of the warp) skip
         // the per-element mask; elsewhere masked scores become -inf.
-        const bool full = __all_sync(0xffffffffu, valid && key0 >= lo && key0 + kBN - 1 <= pos);
-        float mx;
-        if (full) {
-          float m3[22];
-#pragma unroll
-          for (int i = 0; i < 21; ++i)
-            m3[i] = fmax3(__uint_as_float(sr[3 * i]), __uint_as_float(sr[3 * i + 1]),
-                          __uint_as_float(sr[3 * i + 2]));
-          m3[21] = __uint_as_float(sr[63]);
-#pragma unroll
-          for (int i = 0; i < 7; ++i) m3[i] = fmax3(m3[3 * i], m3[3 * i + 1], m3[3 * i + 2]);
-          m3[7] = m3[21];
-          mx = fmax3(fmax3(m3[0], m3[1], m3[2]), fmax3(m3[3], m3[4], m3[5]), fmaxf(m3[6], m3[7]));
-        } else {
-          mx = -INFINITY;
+        const bool full = __all_sync(0xffffffffu, valid && key0 >= lo && key0 + 63 <= pos);
+        if (!full) {
 #pragma unroll
           for (int cc = 0; cc < 64; ++cc) {
             const int32_t key = key0 + cc;
             const bool vis = valid && key >= lo && key <= pos;
             if (!vis) sr[cc] = 0xff800000u;   // -inf
-            mx = fmaxf(mx, __uint_as_float(sr[cc]));
           }
         }
+        float mx = max_tree<64>(sr);
+        mx = fmaxf(mx, swap(mx));
+        if (!alive) break;
         // Scaling after the max keeps the order (c >= 0).
         mx = (mx == -INFINITY) ? -INFINITY : mx * c;
         const float m_new = fmaxf(m_ref, mx);
         const bool grow = m_new > m_ref + 8.f;           // also true for the first visible key
-        const bool rescale_o = grow && l > 0.f;
+        const bool rescale_o = grow && m_ref != -INFINITY;
         if (__any_sync(0xffffffffu, rescale_o)) {
-          // O holds earlier tiles: wait for the last PV, then scale in TMEM.
+          // O holds earlier tiles: wait for the last PV, then scale this
+          // half's columns in TMEM.
           const uint32_t Tp = T - 1;
           if (!mbar_wait(&B.o_done[Tp & 1], (Tp >> 1) & 1, abort, kWaitNs)) {
             alive = false;
@@ -413,7 +479,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           tc_fence_after();
           const float f = rescale_o ? fast_exp2(m_ref - m_new) : 1.f;
 #pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
             uint32_t o[32];
             tmem_ld32(lane_addr + Lay::kOCol + c0, o);
             tmem_wait_ld();
@@ -428,6 +494,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           m_ref = m_new;
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        // P for this half's 64 keys: 32 packed columns over the S buffer's
+        // columns [32h, 32h + 32), scores of half 0 that both halves have
+        // read before the exchange above.
         uint32_t pk[32];
         float ls;
         if (full) {
@@ -468,15 +537,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           }
         }
         l += ls;
-        // P over the first 32 columns of this tile's S buffer (already read).
-        tmem_st32(lane_addr + Lay::kSCol + sb * kBN, pk);
+        tmem_st32(lane_addr + Lay::kSCol + sb * kBN + 32 * h, pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&B.p_full[sb]);
       }
       if (!alive) break;
       if (gm.ntiles == 0) continue;
-      // Epilogue: wait for the last PV, then O / l -> bf16 -> out.
+      // Epilogue: the row sum over both halves, then wait for the last PV
+      // and write this half's columns: O / l -> bf16 -> out.
+      l += swap(l);
+      if (!alive) break;
       const uint32_t Tl = T - 1;
       if (!mbar_wait(&B.o_done[Tl & 1], (Tl >> 1) & 1, abort, kWaitNs)) {
         alive = false;
@@ -487,7 +558,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       __nv_bfloat16* orow =
           p.out + (static_cast<int64_t>(gm.t0 + tok) * p.hq + gm.g * G + head) * D;
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
         uint32_t o[32];
         tmem_ld32(lane_addr + Lay::kOCol + c0, o);
         tmem_wait_ld();
@@ -532,13 +603,14 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   }
   const int G = plan.hq / plan.hkv;
   const int qb = plan.q_block;
-  const int box_rows = plan.p < kBN ? plan.p : kBN;
+  const int box_rows_k = std::min(plan.p, kBN);
+  const int box_rows_v = std::min(plan.p, Lay::kVKeys);
   CUtensorMap tq, tk, tv;
   if (!make_tmap_3d(&tq, a.q, D, plan.hq, static_cast<uint64_t>(plan.total_q), G, qb) ||
       !make_tmap_3d(&tk, a.k_pages, D, plan.hkv, static_cast<uint64_t>(plan.num_pages) * plan.p, 1,
-                    box_rows) ||
+                    box_rows_k) ||
       !make_tmap_3d(&tv, a.v_pages, D, plan.hkv, static_cast<uint64_t>(plan.num_pages) * plan.p, 1,
-                    box_rows))
+                    box_rows_v))
     return static_cast<int>(cudaErrorInvalidValue);
   PrefillParams p;
   p.page_table = a.page_table;
@@ -554,7 +626,8 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   int shift = 0;
   while ((1 << shift) < plan.p) ++shift;
   p.page_shift = shift;
-  p.box_rows = box_rows;
+  p.box_rows_k = box_rows_k;
+  p.box_rows_v = box_rows_v;
   p.mpps = plan.mpps;
   p.num_pages = plan.num_pages;
   p.scale_log2 = a.sm_scale * 1.4426950408889634f;
