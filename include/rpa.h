@@ -171,8 +171,8 @@ rpa_status_t rpa_plan_get_info(const rpa_plan_t* plan, rpa_plan_info* info);
  *            NULL-ness and values must match the plan's window_host
  *   out      [total_q, num_q_heads, head_dim]            dtype, 16-B aligned
  *   workspace: at least the plan's workspace_bytes, 256-B aligned, and
- *            zero-filled before its first use (every call leaves it ready for
- *            the next one: its per-sequence arrival counters return to zero).
+ *            zero-filled before its first use (its error word must start at
+ *            zero; the rest is scratch the call overwrites).
  *            Scratch owned by the call while it runs; the error word lives at
  *            its start and is sticky until rpa_get_device_error clears it.
  *   Pages: the prefill kernel reads whole pages, so the slots of a sequence's
@@ -180,8 +180,10 @@ rpa_status_t rpa_plan_get_info(const rpa_plan_t* plan, rpa_plan_info* info);
  *            zero-initialised pool satisfies this).
  * The scalar arguments must equal the plan's, else RPA_ERR_PLAN_MISMATCH.
  * sm_scale multiplies q.k before the softmax (1/sqrt(head_dim) is usual).
- * Enqueues at most three kernels on `stream` (split-KV decode, tensor-core
- * prefill, CUDA-core path) and returns without waiting for them.
+ * Enqueues on `stream` the split-KV decode kernel and, where a sequence is
+ * cut across its CTAs, the log-sum-exp combine kernel (a programmatic
+ * dependent launch), then the tensor-core prefill and the CUDA-core path, as
+ * the batch needs, and returns without waiting for them.
  */
 rpa_status_t rpa_forward(const void* q, const void* k_pages, const void* v_pages,
                          const int32_t* page_table, const int32_t* cu_q_lens,
@@ -249,7 +251,8 @@ rpa_status_t rpa_forward_decode_noalloc(const void* q, const void* k_pages,
  *     recorded.
  */
 enum {
-  RPA_KERNEL_DECODE_SPLIT = 0,   /* split-KV decode (merges its splits) */
+  RPA_KERNEL_DECODE_SPLIT = 0,   /* split-KV decode                    */
+  RPA_KERNEL_DECODE_COMBINE = 1, /* log-sum-exp combine of cut sequences */
   RPA_KERNEL_PREFILL_TC = 2,     /* tensor-core prefill               */
   RPA_KERNEL_SIMT = 3            /* CUDA-core (fp32) path             */
 };

@@ -42,7 +42,7 @@ EXPORTS = ["rpa_plan", "rpa_plan_destroy", "rpa_plan_get_info", "rpa_forward",
            "rpa_get_device_error", "rpa_clear_device_error", "rpa_trace_begin",
            "rpa_trace_end", "rpa_status_string", "rpa_forward_decode_noalloc"]
 
-RPA_KERNEL_NAMES = {0: "decode_split", 2: "prefill_tc", 3: "simt"}
+RPA_KERNEL_NAMES = {0: "decode_split", 1: "decode_combine", 2: "prefill_tc", 3: "simt"}
 
 
 class RpaError(RuntimeError):

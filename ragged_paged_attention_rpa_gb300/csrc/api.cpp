@@ -185,12 +185,8 @@ rpa_status_t rpa_forward_decode_noalloc(const void* q, const void* k_pages,
   void* scratch = nullptr;
   if (rpa::noalloc_scratch(&scratch) != 0) return RPA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // The error word and the arrival counters must start at zero.
+  // The error word must start at zero.
   if (cudaMemsetAsync(scratch, 0, rpa::kHeaderBytes, s) != cudaSuccess) return RPA_ERR_CUDA;
-  if (!p.dseg_seqhead.empty() &&
-      cudaMemsetAsync(static_cast<unsigned char*>(scratch) + p.off_arrivals, 0,
-                      p.dseg_seqhead.size() * sizeof(int32_t), s) != cudaSuccess)
-    return RPA_ERR_CUDA;
   rpa::Args a{q, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window, sm_scale,
               out, static_cast<unsigned char*>(scratch)};
   rpa::trace_start(stream);

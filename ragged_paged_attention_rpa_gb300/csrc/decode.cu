@@ -16,9 +16,10 @@
 //
 // Schedule.  The visible keys of every (decode sequence, KV head) pair form a
 // "segment" of 16-key blocks; the segments are laid end to end and the block
-// stream is cut into equal contiguous ranges, one per CTA (one CTA per SM, a
-// single wave), so every CTA streams the same number of bytes whatever the
-// length mix.  A CTA's range may start or end inside a segment.
+// stream is cut into contiguous ranges of equal cost (blocks plus a fixed
+// charge per segment touched), one per CTA (one CTA per SM, a single wave),
+// so every CTA finishes at about the same time whatever the length mix.  A
+// CTA's range may start or end inside a segment.
 //
 // CTA.  Four independent warps take the range's blocks round-robin (warp w:
 // blocks w, w+4, ... of each segment).  Blocks sit on absolute 16-key
@@ -34,9 +35,9 @@
 // with an online softmax per head.  The copy pipeline runs on across segment
 // boundaries.  At the end of each segment the warps merge in shared memory; a
 // segment wholly inside the range writes the output, a cut one writes an fp32
-// partial (O / l and log2-sum-exp).  The CTA that finishes a cut segment last
-// (a per-segment arrival counter in the workspace, reset by that CTA) merges
-// its partials: out = sum_c 2^(lse_c - M) O_c / sum_c 2^(lse_c - M).
+// partial (O / l and log2-sum-exp).  A second kernel, launched as a
+// programmatic dependent, combines the partials of every cut segment:
+// out = sum_c 2^(lse_c - M) O_c / sum_c 2^(lse_c - M).
 #include "common.cuh"
 #include "rpa_internal.h"
 #include "sm100_ptx.cuh"
@@ -62,22 +63,41 @@ struct DecodeParams {
   unsigned char* ws;
   float* part_o;      // [2 * total CTAs][G][D]
   float* part_lse;    // [2 * total CTAs][G]
-  int32_t* arrivals;  // [segments], zero between calls
   int32_t hq, hkv, group, page_shift, mpps, num_pages;
   float scale_log2;   // sm_scale * log2(e)
 };
 
 // One launch's share of the block stream.  seqhead[i] = (sequence << 8) | kv
 // head of segment i; blk0[i] = first block of segment i (blk0[n_seg] = total).
+// CTA c takes blocks [c * bpc, (c + 1) * bpc) where bpc > 0, else
+// [cta0[c], cta0[c + 1]).
 template <int NSEG>
 struct DecodeSched {
-  int32_t n_seg, bpc, n_blocks, slot_base, seg_base;
+  int32_t n_seg, bpc, n_blocks, slot_base, seg_base, n_ctas;
+  int32_t cta0[kMaxDecodeCtas + 1];
   int32_t seqhead[NSEG];
   int32_t blk0[NSEG + 1];
   // From the plan's host metadata (validated there): query token, first
   // visible key and length of each segment's sequence.
   int32_t q0[NSEG], lo[NSEG], len[NSEG];
 };
+
+template <int NSEG>
+__device__ __forceinline__ int32_t range_start(const DecodeSched<NSEG>& sc, int c) {
+  return sc.bpc > 0 ? min(c * sc.bpc, sc.n_blocks) : sc.cta0[c];
+}
+
+// The CTA whose range holds block x.
+template <int NSEG>
+__device__ __forceinline__ int cta_of(const DecodeSched<NSEG>& sc, int32_t x) {
+  if (sc.bpc > 0) return x / sc.bpc;
+  int lo = 0, hi = sc.n_ctas - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sc.cta0[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
 
 struct SegInfo {
   int32_t s, g, q0;      // sequence, kv head, its query token
@@ -170,12 +190,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   __shared__ float wm[kWarps][8], wl[kWarps][8];
   __shared__ int s_nseg, s_abort;
   __shared__ __align__(8) uint64_t full_bar[kWarps][S];
+  __shared__ __align__(8) uint64_t q_bar[2];   // Q buffer t & 1 holds segment t's queries
 
+  // The combine kernel may be scheduled now; it waits for this grid's end.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int G = p.group;
   const int c = blockIdx.x;
-  const int32_t cb0 = c * sc.bpc;
-  const int32_t cb1 = min(cb0 + sc.bpc, sc.n_blocks);
+  const int32_t cb0 = range_start(sc, c);
+  const int32_t cb1 = range_start(sc, c + 1);
   if (cb0 >= cb1) return;
   const int kfirst = seg_of(sc, cb0);
   const int klast = seg_of(sc, cb1 - 1);
@@ -187,6 +210,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
   if (tid == 0) {
     for (int i = 0; i < kWarps * S; ++i) sm100::mbar_init(&full_bar[i / S][i % S], 1);
+    sm100::mbar_init(&q_bar[0], 1);
+    sm100::mbar_init(&q_bar[1], 1);
     s_abort = 0;
     sm100::fence_barrier_init();
     sm100::prefetch_tmap(&tm_k);
@@ -290,19 +315,27 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   __syncwarp();
 #pragma unroll
   for (int i = 0; i < S - 1; ++i) issue(i);
-  // Q of the first two segments, while the first copies are in flight.
-  for (int t = 0; t < 2 && t < nseg; ++t) {
+  // Q of segment t: G x D contiguous bf16 (the G heads of KV head g are
+  // adjacent), one bulk copy into buffer t & 1 on q_bar[t & 1].
+  int q_last0 = -1, q_last1 = -1;   // (thread 0) last segment copied into buffer 0 / 1
+  auto load_q = [&](int t) {
     const SegInfo& si = s_seg[t];
-    const uint4* src = reinterpret_cast<const uint4*>(
-        p.q + (static_cast<int64_t>(si.q0) * p.hq + si.g * G) * D);
-    uint4* dst = reinterpret_cast<uint4*>(qs + t * 8 * D);
-    for (int e = tid; e < G * D / 8; e += kWarps * 32) dst[e] = src[e];
-  }
+    if (t & 1) q_last1 = t; else q_last0 = t;
+    const __nv_bfloat16* src = p.q + (static_cast<int64_t>(si.q0) * p.hq + si.g * G) * D;
+    sm100::mbar_arrive_expect_tx(&q_bar[t & 1], G * D * 2);
+    sm100::bulk_load(qs + (t & 1) * 8 * D, src, G * D * 2, &q_bar[t & 1]);
+  };
+  if (tid == 0)
+    for (int t = 0; t < 2 && t < nseg; ++t) load_q(t);
   __syncthreads();
 
   int count = 0;  // blocks consumed by this warp
   for (int t = 0; t < nseg; ++t) {
     const SegInfo si = s_seg[t];
+    if (!sm100::mbar_wait(&q_bar[t & 1], (t >> 1) & 1, abort, 2000000000ull)) {
+      if (lane == 0) report_error(p.ws, RPA_DEVERR_TIMEOUT, c);
+      break;
+    }
     // Q^T as the B operand: lane holds head lane/4, dims 2(lane%4)+{0,1} (+8).
     uint32_t qf[KT][2];
     {
@@ -401,18 +434,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       wl[warp][2 * lane + 1] = l[1];
     }
     __syncthreads();
-    // Q of segment t + 2 goes into the buffer segment t used.
-    uint4 qn[2];
-    const bool load_q = t + 2 < nseg && !s_seg[t + 2].bad;
-    const __nv_bfloat16* qsrc = nullptr;
-    if (load_q) {
-      const SegInfo& sn = s_seg[t + 2];
-      qsrc = p.q + (static_cast<int64_t>(sn.q0) * p.hq + sn.g * G) * D;
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int e = tid + r * kWarps * 32;
-        if (e < G * D / 8) qn[r] = reinterpret_cast<const uint4*>(qsrc)[e];
-      }
+    // Every warp holds segment t's queries in registers now: buffer t & 1
+    // takes segment t + 2's (the async copy is ordered after those reads).
+    if (tid == 0 && t + 2 < nseg) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      load_q(t + 2);
     }
     // Deterministic sum of the four scaled warp states: warps 0 and 1 store
     // into buffers 0 and 1, then warps 2 and 3 add into them; the two
@@ -451,14 +477,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         if (round == 0) __syncthreads();
       }
     }
-    if (load_q) {
-      uint4* dst = reinterpret_cast<uint4*>(qs + (t & 1) * 8 * D);
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int e = tid + r * kWarps * 32;
-        if (e < G * D / 8) dst[e] = qn[r];
-      }
-    }
     __syncthreads();
     // Normalise; write the output (whole segment) or this CTA's partial.
     const int slot = sc.slot_base + 2 * c + (t == 0 ? 0 : 1);
@@ -494,73 +512,120 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       int dummy = 0;
       sm100::mbar_wait(&full_bar[warp][i % S], (i / S) & 1, &dummy, 200000000ull);
     }
+    if (tid == 0)
+      for (int b = 0; b < 2; ++b) {
+        const int last = b ? q_last1 : q_last0;
+        if (last >= 0) {
+          int dummy = 0;
+          sm100::mbar_wait(&q_bar[b], (last >> 1) & 1, &dummy, 200000000ull);
+        }
+      }
     return;
   }
+}
 
-  // ---- Arrivals for the cut segments (the first and last of the range):
-  // one fence, both counters bumped at once, and the CTA that completes a
-  // segment merges its partials.
-  __shared__ int s_cut_seg[2], s_merge[2];
-  if (tid < 2) {
-    const int t = tid == 0 ? 0 : nseg - 1;
-    const SegInfo& si = s_seg[t];
-    const bool cut = !(tid == 1 && nseg == 1) && !si.whole && !si.bad;
-    s_cut_seg[tid] = cut ? si.gseg : -1;
+// Combine of the segments cut across CTAs: one CTA per cut segment,
+//   out = sum_c 2^(lse_c - M) O_c / sum_c 2^(lse_c - M),  M = max_c lse_c,
+// over the fp32 partials (O_c = O / l of part c, lse_c its log2-sum-exp).
+// Launched as a programmatic dependent of the decode kernel: its CTAs start
+// early and wait for every decode CTA's partials to be visible, so the merge
+// runs against an idle memory system, in one round of loads.
+struct CombineList {
+  int32_t n, slot_base;
+  Plan::DecodeCut cut[kMaxDecodeCtas];
+};
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32)
+decode_combine_kernel(const DecodeParams p, const __grid_constant__ CombineList cl) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (static_cast<int>(blockIdx.x) >= cl.n) return;
+  const Plan::DecodeCut cut = cl.cut[blockIdx.x];
+  const int G = p.group, tid = threadIdx.x;
+  auto slot_of = [&](int i) { return cl.slot_base + 2 * (cut.ca + i) + (i == 0 ? cut.first : 0); };
+  // Each thread owns kPer groups of 4 output values (one head each) and reads
+  // every part's log2-sum-exp and partial for them in one round of loads
+  // (four parts at a time), rescaling its running sum as the maximum grows.
+  constexpr int kPer = (8 * D) / (kWarps * 32 * 4);          // float4 groups per thread (G <= 8)
+  float4 acc[kPer];
+  float M[kPer], wsum[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    M[u] = -INFINITY;
+    wsum[u] = 0.f;
   }
-  __syncthreads();
-  if (s_cut_seg[0] < 0 && s_cut_seg[1] < 0) return;
-  __threadfence();
-  __syncthreads();
-  if (tid < 2) {
-    const int k = s_cut_seg[tid];
-    bool last = false;
-    if (k >= 0) {
-      const int ca = sc.blk0[k] / sc.bpc;
-      const int cb = (sc.blk0[k + 1] - 1) / sc.bpc;
-      last = atomicAdd(p.arrivals + sc.seg_base + k, 1) == (cb - ca);
-    }
-    s_merge[tid] = last ? 1 : 0;
-  }
-  __syncthreads();
-  if (!s_merge[0] && !s_merge[1]) return;
-  __threadfence();
-  for (int which = 0; which < 2; ++which) {
-    if (!s_merge[which]) continue;
-    const SegInfo si = s_seg[which == 0 ? 0 : nseg - 1];
-    const int k = si.gseg;
-    const int ca = sc.blk0[k] / sc.bpc;
-    const int cb = (sc.blk0[k + 1] - 1) / sc.bpc;
-    // Slots: the first CTA holds this segment in slot 0 if the segment starts
-    // its range, else in slot 1; every later CTA holds it in slot 0.
-    const int first_slot = (sc.blk0[k] != ca * sc.bpc) ? 1 : 0;
-    for (int e = tid * 4; e < G * D; e += kWarps * 32 * 4) {
-      const int h = e / D, d = e % D;
-      float M = -INFINITY;
-#pragma unroll 4
-      for (int cc = ca; cc <= cb; ++cc) {
-        const int sl = sc.slot_base + 2 * cc + (cc == ca ? first_slot : 0);
-        M = fmaxf(M, __ldcg(p.part_lse + static_cast<int64_t>(sl) * G + h));
+  for (int i0 = 0; i0 < cut.nparts; i0 += 4) {
+    float4 v[4][kPer];
+    float lse[4][kPer];
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int e = tid * 4 + u * kWarps * 32 * 4;
+        const bool ok = i0 + ii < cut.nparts && e < G * D;
+        const int64_t sl = ok ? slot_of(i0 + ii) : 0;
+        v[ii][u] = ok ? __ldcg(reinterpret_cast<const float4*>(p.part_o + sl * G * D + e))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        lse[ii][u] = ok ? __ldcg(p.part_lse + sl * G + e / D) : -INFINITY;
       }
-      float wsum = 0.f;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-      for (int cc = ca; cc <= cb; ++cc) {
-        const int sl = sc.slot_base + 2 * cc + (cc == ca ? first_slot : 0);
-        const float lse = __ldcg(p.part_lse + static_cast<int64_t>(sl) * G + h);
-        const float4 u = __ldcg(reinterpret_cast<const float4*>(
-            p.part_o + (static_cast<int64_t>(sl) * G + h) * D + d));
-        const float w = fast_exp2(lse - M);
-        wsum += w;
-        acc.x += w * u.x; acc.y += w * u.y; acc.z += w * u.z; acc.w += w * u.w;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      float mn = M[u];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) mn = fmaxf(mn, lse[ii][u]);
+      if (mn == -INFINITY) continue;
+      const float f = fast_exp2(M[u] - mn);   // 0 while nothing is accumulated
+      acc[u].x *= f; acc[u].y *= f; acc[u].z *= f; acc[u].w *= f;
+      wsum[u] *= f;
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) {
+        const float wt = fast_exp2(lse[ii][u] - mn);
+        wsum[u] += wt;
+        acc[u].x += wt * v[ii][u].x;
+        acc[u].y += wt * v[ii][u].y;
+        acc[u].z += wt * v[ii][u].z;
+        acc[u].w += wt * v[ii][u].w;
       }
-      const float inv = 1.f / wsum;
-      uint2 pk;
-      pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-      pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-      *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(si.q0) * p.hq + si.g * G + h) * D + d) = pk;
+      M[u] = mn;
     }
-    if (tid == 0) p.arrivals[sc.seg_base + k] = 0;  // ready for the next call
   }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int e = tid * 4 + u * kWarps * 32 * 4;
+    if (e >= G * D) continue;
+    const int h = e / D, d = e % D;
+    const float inv = 1.f / wsum[u];
+    uint2 pk;
+    pk.x = pack_bf16x2(acc[u].x * inv, acc[u].y * inv);
+    pk.y = pack_bf16x2(acc[u].z * inv, acc[u].w * inv);
+    *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(cut.q0) * p.hq + cut.g * G + h) * D + d) = pk;
+  }
+}
+
+template <int D>
+int launch_combine(const Plan& plan, const DecodeParams& p, const Plan::DecodeLaunch& dl,
+                   cudaStream_t stream) {
+  static CombineList cl;  // host staging; copied into the launch parameters
+  for (int off = 0; off < dl.n_cut; off += kMaxDecodeCtas) {
+    cl.n = std::min(kMaxDecodeCtas, dl.n_cut - off);
+    cl.slot_base = dl.slot_base;
+    for (int i = 0; i < cl.n; ++i) cl.cut[i] = plan.dcut[dl.cut_begin + off + i];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cl.n);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, p, cl);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    trace_mark(RPA_KERNEL_DECODE_COMBINE, stream);
+  }
+  return 0;
 }
 
 template <int D, int NSEG>
@@ -579,6 +644,11 @@ int launch_one(const Plan& plan, const DecodeParams& p, const CUtensorMap& tk,
   const int n = dl.seg_end - dl.seg_begin;
   sc.n_seg = n;
   sc.bpc = dl.bpc;
+  sc.n_ctas = dl.n_ctas;
+  if (dl.bpc == 0) {
+    if (dl.n_ctas > kMaxDecodeCtas) return static_cast<int>(cudaErrorInvalidValue);
+    for (int i = 0; i <= dl.n_ctas; ++i) sc.cta0[i] = plan.dcta_blk0[dl.cta_begin + i];
+  }
   sc.slot_base = dl.slot_base;
   sc.seg_base = dl.seg_begin;
   const int32_t base = plan.dseg_blk0[dl.seg_begin];
@@ -613,7 +683,6 @@ int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   p.ws = a.workspace;
   p.part_o = reinterpret_cast<float*>(a.workspace + plan.off_partial_o);
   p.part_lse = reinterpret_cast<float*>(a.workspace + plan.off_partial_lse);
-  p.arrivals = reinterpret_cast<int32_t*>(a.workspace + plan.off_arrivals);
   p.hq = plan.hq;
   p.hkv = plan.hkv;
   p.group = plan.hq / plan.hkv;
@@ -630,9 +699,10 @@ int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
     return static_cast<int>(cudaErrorInvalidValue);
   for (const Plan::DecodeLaunch& dl : plan.dlaunch) {
     const int n = dl.seg_end - dl.seg_begin;
-    const int err = n <= kDecodeSegSmall
-                        ? launch_one<D, kDecodeSegSmall>(plan, p, tk, tv, dl, stream)
-                        : launch_one<D, kDecodeSegLarge>(plan, p, tk, tv, dl, stream);
+    int err = n <= kDecodeSegSmall
+                  ? launch_one<D, kDecodeSegSmall>(plan, p, tk, tv, dl, stream)
+                  : launch_one<D, kDecodeSegLarge>(plan, p, tk, tv, dl, stream);
+    if (!err) err = launch_combine<D>(plan, p, dl, stream);
     if (err) return err;
   }
   return 0;

@@ -54,10 +54,14 @@ inline int64_t decode_visible(int32_t L, int32_t w) {
 
 // Decode schedule: the visible keys of every (decode sequence, KV head) pair
 // form a segment of 16-key blocks; the blocks of all segments are laid end to
-// end and cut into equal contiguous ranges, one per CTA (one per SM: a single
-// balanced wave), so every CTA streams the same number of bytes whatever the
-// length mix.  Ranges shrink (more CTAs) only when one would touch more
-// segments or pages than the kernel's shared-memory tables hold.
+// end and cut into contiguous ranges, one per CTA (at most one per SM: a
+// single wave).  A range costs its blocks plus kDecodeSegCost for every
+// segment it touches (each segment ends in a merge of the CTA's warps and a
+// write); the cut makes the largest cost as small as the SM count allows, so
+// CTAs that touch many short sequences get fewer blocks.  A range also ends
+// where it would touch more segments or pages than the kernel's
+// shared-memory tables hold.  A forced range size (options) gives ranges of
+// equal block counts instead.
 void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t* win,
                  int32_t forced_tokens) {
   plan.dseg_seqhead.clear();
@@ -66,6 +70,8 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
   plan.dseg_lo.clear();
   plan.dseg_len.clear();
   plan.dlaunch.clear();
+  plan.dcta_blk0.clear();
+  plan.dcut.clear();
   std::vector<int32_t> seg_lo;  // first block's first key of each segment
   int32_t ndec = 0;
   for (int32_t s = 0; s < plan.num_seqs; ++s) {
@@ -90,6 +96,12 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
   if (nseg == 0) return;
   const std::vector<int32_t>& blk0 = plan.dseg_blk0;
   const int32_t P = plan.p;
+  // Pages holding local blocks [jb, jb + t) of segment k.
+  auto pages_of = [&](int32_t k, int32_t jb, int32_t t) {
+    const int64_t kb = seg_lo[k] + 16 * static_cast<int64_t>(jb);
+    const int64_t ke = seg_lo[k] + 16 * static_cast<int64_t>(jb + t);
+    return static_cast<int32_t>((ke - 1) / P - kb / P + 1);
+  };
   // Segments and pages touched by CTA range [b0, b1) of launch segments [sb, se).
   auto fits = [&](int32_t sb, int32_t se, int32_t bpc) {
     const int32_t base = blk0[sb], total = blk0[se] - base;
@@ -102,35 +114,115 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
         ++segs;
         const int32_t jb = std::max(b0, blk0[kk] - base) - (blk0[kk] - base);
         const int32_t je = std::min(b1, blk0[kk + 1] - base) - (blk0[kk] - base);
-        const int64_t kb = seg_lo[kk] + 16 * static_cast<int64_t>(jb);
-        const int64_t ke = seg_lo[kk] + 16 * static_cast<int64_t>(je);  // upper bound
-        pages += static_cast<int32_t>((ke - 1) / P - kb / P + 1);
+        pages += pages_of(kk, jb, je - jb);
       }
       if (segs > kMaxCtaSegs || pages > kMaxCtaPages) return false;
     }
     return true;
   };
+  // Greedy cut of launch segments [sb, se) into ranges of cost <= T (each
+  // range takes at least one block); returns the range starts (launch-relative,
+  // closing entry = total), or stops early once more than `cap` ranges.
+  auto cut = [&](int32_t sb, int32_t se, int64_t T, int32_t cap, std::vector<int32_t>& starts) {
+    const int32_t base = blk0[sb], total = blk0[se] - base;
+    starts.assign(1, 0);
+    int32_t b = 0, k = sb;
+    while (b < total) {
+      if (static_cast<int32_t>(starts.size()) > cap) return;
+      int64_t cost = 0;
+      int32_t segs = 0, pages = 0;
+      bool first = true;
+      while (b < total) {
+        while (blk0[k + 1] - base <= b) ++k;
+        const int32_t jb = b - (blk0[k] - base);
+        const int32_t rem = blk0[k + 1] - base - b;
+        if (segs == kMaxCtaSegs) break;
+        int64_t t = std::min<int64_t>(rem, T - cost - kDecodeSegCost);
+        if (t <= 0) {
+          if (!first) break;
+          t = 1;
+        }
+        // Largest t whose pages still fit.
+        const int32_t room = kMaxCtaPages - pages;
+        if (pages_of(k, jb, static_cast<int32_t>(t)) > room) {
+          const int64_t kb = seg_lo[k] + 16 * static_cast<int64_t>(jb);
+          const int64_t tmax = ((kb / P + room) * P - kb) / 16;
+          if (tmax <= 0 && !first) break;
+          t = std::max<int64_t>(1, std::min(t, tmax));
+        }
+        cost += kDecodeSegCost + t;
+        ++segs;
+        pages += pages_of(k, jb, static_cast<int32_t>(t));
+        b += static_cast<int32_t>(t);
+        first = false;
+        if (t < rem) break;  // the range ends inside this segment
+      }
+      starts.push_back(b);
+    }
+  };
   int32_t slot_base = 0;
   int64_t max_splits = 1, ctas = 0;
+  std::vector<int32_t> starts;
   for (int32_t sb = 0; sb < nseg; sb += kDecodeSegLarge) {
     const int32_t se = std::min(nseg, sb + kDecodeSegLarge);
     const int32_t total = blk0[se] - blk0[sb];
-    int32_t bpc = forced_tokens > 0
-                      ? static_cast<int32_t>(ceil_div(forced_tokens, 16))
-                      : static_cast<int32_t>(ceil_div(total, static_cast<int64_t>(plan.num_sms)));
-    bpc = std::max<int32_t>(1, bpc);
-    while (bpc > 1 && !fits(sb, se, bpc)) bpc = std::max<int32_t>(1, bpc * 3 / 4);
-    const int32_t n_ctas = static_cast<int32_t>(ceil_div(total, bpc));
-    plan.dlaunch.push_back({sb, se, bpc, n_ctas, slot_base});
-    slot_base += 2 * n_ctas;
-    ctas += n_ctas;
-    for (int32_t k = sb; k < se; ++k) {
-      const int64_t ca = (blk0[k] - blk0[sb]) / bpc;
-      const int64_t cb = (blk0[k + 1] - 1 - blk0[sb]) / bpc;
-      max_splits = std::max<int64_t>(max_splits, cb - ca + 1);
+    const int32_t base = blk0[sb];
+    Plan::DecodeLaunch dl{sb, se, 0, 0, slot_base, 0, 0, 0};
+    bool uniform = forced_tokens > 0;
+    if (!uniform) {
+      const int32_t cap = std::min<int32_t>(plan.num_sms, kMaxDecodeCtas);
+      int64_t lo = kDecodeSegCost + 1, hi = total + static_cast<int64_t>(kDecodeSegCost) * (se - sb + 1);
+      cut(sb, se, hi, cap, starts);
+      if (static_cast<int32_t>(starts.size()) - 1 > cap) {
+        uniform = true;  // the tables' limits alone need more CTAs than listed
+      } else {
+        while (lo < hi) {
+          const int64_t mid = (lo + hi) / 2;
+          cut(sb, se, mid, cap, starts);
+          if (static_cast<int32_t>(starts.size()) - 1 <= cap && starts.back() == total)
+            hi = mid;
+          else
+            lo = mid + 1;
+        }
+        cut(sb, se, lo, cap, starts);
+        dl.n_ctas = static_cast<int32_t>(starts.size()) - 1;
+        dl.cta_begin = static_cast<int32_t>(plan.dcta_blk0.size());
+        plan.dcta_blk0.insert(plan.dcta_blk0.end(), starts.begin(), starts.end());
+      }
     }
+    if (uniform) {
+      int32_t bpc = forced_tokens > 0
+                        ? static_cast<int32_t>(ceil_div(forced_tokens, 16))
+                        : static_cast<int32_t>(ceil_div(total, static_cast<int64_t>(plan.num_sms)));
+      bpc = std::max<int32_t>(1, bpc);
+      while (bpc > 1 && !fits(sb, se, bpc)) bpc = std::max<int32_t>(1, bpc * 3 / 4);
+      dl.bpc = bpc;
+      dl.n_ctas = static_cast<int32_t>(ceil_div(total, bpc));
+      starts.clear();
+      for (int32_t c = 0; c <= dl.n_ctas; ++c) starts.push_back(std::min(total, c * bpc));
+    }
+    slot_base += 2 * dl.n_ctas;
+    ctas += dl.n_ctas;
+    // Longest range, the segments cut across CTAs (merged by the combine
+    // kernel) and the most ranges any segment is cut across.
+    int32_t longest = 0;
+    for (int32_t c = 0; c < dl.n_ctas; ++c) longest = std::max(longest, starts[c + 1] - starts[c]);
+    if (sb == 0) plan.kv_split = longest * 16;
+    dl.cut_begin = static_cast<int32_t>(plan.dcut.size());
+    for (int32_t k = sb; k < se; ++k) {
+      const int32_t b0 = blk0[k] - base, b1 = blk0[k + 1] - base;
+      if (b1 == b0) continue;
+      const int64_t ca = std::upper_bound(starts.begin(), starts.end(), b0) - starts.begin() - 1;
+      const int64_t cb = std::upper_bound(starts.begin(), starts.end(), b1 - 1) - starts.begin() - 1;
+      max_splits = std::max<int64_t>(max_splits, cb - ca + 1);
+      if (cb > ca)
+        plan.dcut.push_back({static_cast<int32_t>(ca), starts[ca] != b0 ? 1 : 0,
+                             static_cast<int32_t>(cb - ca + 1), plan.dseg_q0[k],
+                             plan.dseg_seqhead[k] & 255});
+    }
+    dl.n_cut = static_cast<int32_t>(plan.dcut.size()) - dl.cut_begin;
+    plan.dlaunch.push_back(dl);
   }
-  plan.kv_split = plan.dlaunch.front().bpc * 16;
   plan.max_splits = static_cast<int32_t>(max_splits);
   plan.decode_ctas = ctas;
   plan.dec_slots = slot_base;
@@ -228,18 +320,15 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
   if (tc_prefill && plan.num_prefill > 0) plan_prefill(plan, cu, kv, win, opts.q_block);
 
   // Workspace: header, then the decode partials (two slots per decode CTA,
-  // G x D fp32 each, plus G log2-sum-exps) and one arrival counter per
-  // decode segment.
+  // G x D fp32 each, plus G log2-sum-exps).
   size_t off = kHeaderBytes;
-  plan.off_partial_o = plan.off_partial_lse = plan.off_arrivals = 0;
+  plan.off_partial_o = plan.off_partial_lse = 0;
   if (!plan.dlaunch.empty()) {
     const size_t rows = static_cast<size_t>(plan.dec_slots) * group;
     plan.off_partial_o = off;
     off += (rows * plan.d * sizeof(float) + 255) / 256 * 256;
     plan.off_partial_lse = off;
     off += (rows * sizeof(float) + 255) / 256 * 256;
-    plan.off_arrivals = off;
-    off += (plan.dseg_seqhead.size() * sizeof(int32_t) + 255) / 256 * 256;
   }
   plan.ws_bytes = off;
   return RPA_OK;

@@ -34,6 +34,11 @@ constexpr int kDecodeSegSmall = 256;
 constexpr int kDecodeSegLarge = 1024;
 constexpr int kMaxCtaSegs = 64;
 constexpr int kMaxCtaPages = 512;
+// Most CTAs a cost-balanced decode launch lists (their range starts travel in
+// the launch parameters), and the charge, in 16-key blocks, for each segment
+// a CTA's range touches (its in-CTA merge and output).
+constexpr int kMaxDecodeCtas = 1024;
+constexpr int kDecodeSegCost = 5;
 
 struct Plan {
   // Problem description (checked against every rpa_forward call).
@@ -49,21 +54,33 @@ struct Plan {
 
   // Decode (q_len == 1) on the split-KV kernel.  Segments = (sequence, KV
   // head) pairs in stream order; blocks are 16 keys; each launch cuts its
-  // segments' block stream into equal ranges, one per CTA.
+  // segments' block stream into contiguous ranges, one per CTA: ranges of
+  // equal cost (blocks plus a fixed charge per segment touched), listed in
+  // dcta_blk0, or, where bpc > 0, ranges of bpc blocks each.
   struct DecodeLaunch {
     int32_t seg_begin, seg_end;  // segments [seg_begin, seg_end)
-    int32_t bpc;                 // blocks per CTA
+    int32_t bpc;                 // > 0: blocks per CTA (uniform ranges)
     int32_t n_ctas;
     int32_t slot_base;           // first partial slot (two per CTA)
+    int32_t cta_begin;           // bpc == 0: ranges in dcta_blk0[cta_begin ...]
+    int32_t cut_begin, n_cut;    // segments cut across CTAs: dcut[cut_begin ...]
+  };
+  // A segment cut across CTAs ca .. ca + nparts - 1 of its launch: CTA ca
+  // holds its partial in slot 2 ca + first (first = 1 when the segment is
+  // not the first of ca's range), every later CTA c in slot 2 c.
+  struct DecodeCut {
+    int32_t ca, first, nparts, q0, g;
   };
   int32_t num_decode = 0;
-  int32_t kv_split = 0;   // tokens per CTA range (16 x blocks per CTA, first launch)
+  int32_t kv_split = 0;   // tokens of the longest CTA range of the first launch
   int32_t max_splits = 0; // most CTAs any segment is cut across
   int64_t decode_ctas = 0;
   std::vector<int32_t> dseg_seqhead;  // (sequence << 8) | kv head
   std::vector<int32_t> dseg_blk0;     // block prefix, size segments + 1
   std::vector<int32_t> dseg_q0, dseg_lo, dseg_len;  // query token, first visible key, length
   std::vector<DecodeLaunch> dlaunch;
+  std::vector<int32_t> dcta_blk0;     // per launch: n_ctas + 1 range starts (launch-relative)
+  std::vector<DecodeCut> dcut;
   int32_t dec_slots = 0;              // partial slots over all launches
 
   // Prefill (q_len > 1).
@@ -73,7 +90,7 @@ struct Plan {
   int32_t prefill_ctas = 0;
 
   // Workspace.
-  size_t off_partial_o = 0, off_partial_lse = 0, off_arrivals = 0, ws_bytes = kHeaderBytes;
+  size_t off_partial_o = 0, off_partial_lse = 0, ws_bytes = kHeaderBytes;
 };
 
 // Scheduler (plan.cpp): fills everything but the problem description, which

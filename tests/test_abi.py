@@ -56,11 +56,17 @@ def ceil_div(a, b):
     return -(-a // b)
 
 
+SEG_COST = 5  # blocks charged per segment a decode CTA's range touches
+
+
 def decode_partition(b, num_sms=152, tokens_per_cta=0):
     """Expected decode schedule, restated from its definition: the 16-key
     blocks (on absolute 16-key boundaries) covering the visible keys of every
-    (decode sequence, KV head), laid end to end and cut into equal ranges
-    (one per SM unless a block count per CTA is forced)."""
+    (decode sequence, KV head), laid end to end and cut into contiguous
+    ranges.  Forced: ranges of equal block counts.  Otherwise a range costs
+    its blocks plus SEG_COST per segment it touches, and the cut takes the
+    smallest cost cap T for which ranges grown as long as T allows number at
+    most one per SM."""
     nb = []
     for s in range(b.num_seqs):
         if b.cu_q_lens[s + 1] - b.cu_q_lens[s] != 1:
@@ -70,11 +76,48 @@ def decode_partition(b, num_sms=152, tokens_per_cta=0):
         lo = max(0, L - w) if w > 0 else 0
         nb += [ceil_div(L, 16) - lo // 16] * b.num_kv_heads
     total = sum(nb)
-    bpc = ceil_div(tokens_per_cta, 16) if tokens_per_cta else ceil_div(total, num_sms)
-    n_ctas = ceil_div(total, bpc)
-    starts = np.concatenate([[0], np.cumsum(nb)])
-    spans = [(starts[i + 1] - 1) // bpc - starts[i] // bpc + 1 for i in range(len(nb))]
-    return dict(segments=len(nb), bpc=bpc, n_ctas=n_ctas, max_splits=max(spans))
+    starts = np.concatenate([[0], np.cumsum(nb)]).astype(np.int64)
+
+    def ranges_for(T):
+        out, pos = [0], 0
+        while pos < total:
+            cost, end = 0, pos
+            while end < total:
+                k = int(np.searchsorted(starts, end, side="right")) - 1
+                room = T - cost - SEG_COST
+                if room <= 0 and end > pos:
+                    break
+                take = min(int(starts[k + 1]) - end, max(room, 1))
+                cost += SEG_COST + take
+                end += take
+                if end < starts[k + 1]:
+                    break
+            out.append(end)
+            pos = end
+        return out
+
+    if tokens_per_cta:
+        bpc = ceil_div(tokens_per_cta, 16)
+        bounds = list(range(0, total, bpc)) + [total]
+    else:
+        lo_T, hi_T = SEG_COST + 1, total + SEG_COST * (len(nb) + 1)
+        while lo_T < hi_T:
+            mid = (lo_T + hi_T) // 2
+            if len(ranges_for(mid)) - 1 <= num_sms:
+                hi_T = mid
+            else:
+                lo_T = mid + 1
+        bounds = ranges_for(lo_T)
+    n_ctas = len(bounds) - 1
+    longest = max(bounds[i + 1] - bounds[i] for i in range(n_ctas))
+    cta = lambda x: int(np.searchsorted(bounds, x, side="right")) - 1
+    spans = [cta(starts[i + 1] - 1) - cta(starts[i]) + 1 for i in range(len(nb)) if nb[i] > 0]
+    # The shared-memory table limits (64 segments, 512 pages per range) do
+    # not bind for the batches these tests use.
+    for i in range(n_ctas):
+        assert sum(1 for k in range(len(nb))
+                   if starts[k] < bounds[i + 1] and starts[k + 1] > bounds[i]) <= 64
+    return dict(segments=len(nb), longest=longest, n_ctas=n_ctas, max_splits=max(spans))
 
 
 def test_decode_plan_is_one_balanced_wave():
@@ -84,15 +127,15 @@ def test_decode_plan_is_one_balanced_wave():
     assert info["num_decode_seqs"] == 128 and info["num_prefill_seqs"] == 0
     assert info["path"] == RPA_PATH_TC
     want = decode_partition(b)
-    assert info["kv_split"] == 16 * want["bpc"]
+    assert info["kv_split"] == 16 * want["longest"]
     assert info["max_splits"] == want["max_splits"]
     assert want["n_ctas"] <= 152
     # Workspace: 256-byte header, two fp32 partial slots (G x D, plus G
-    # log2-sum-exps) per decode CTA, one int32 arrival counter per segment.
+    # log2-sum-exps) per decode CTA.
     G = b.num_q_heads // b.num_kv_heads
     slots = 2 * want["n_ctas"]
     want_ws = (256 + ceil_div(slots * G * b.head_dim * 4, 256) * 256
-               + ceil_div(slots * G * 4, 256) * 256 + ceil_div(want["segments"] * 4, 256) * 256)
+               + ceil_div(slots * G * 4, 256) * 256)
     assert info["workspace_bytes"] == p.workspace_bytes == want_ws
 
 
