@@ -60,8 +60,9 @@ FALLBACK_TFLOPS = 1900.0
 # ----------------------------------------------------------------- workload
 
 
-def algorithmic_counts(b):
-    """Visible (query, key) pairs, flops and bytes of one step.
+def algorithmic_counts(b, part=None):
+    """Visible (query, key) pairs, flops and bytes of one step (part =
+    "decode" or "prefill": only the sequences with one query, or with more).
 
     Pairs: for query i of sequence s at pos = L - q_len + i, keys
     max(0, pos - W + 1) .. pos.  FLOPs = 4 * D * Hq * pairs (QK^T and PV).
@@ -74,7 +75,7 @@ def algorithmic_counts(b):
     pairs = kv_tokens = pages = 0
     for s in range(b.num_seqs):
         ql = int(b.cu_q_lens[s + 1] - b.cu_q_lens[s])
-        if ql == 0:
+        if ql == 0 or (part == "decode" and ql != 1) or (part == "prefill" and ql == 1):
             continue
         L = int(b.kv_lens[s])
         w = 0 if b.window is None else int(b.window[s])
@@ -86,7 +87,9 @@ def algorithmic_counts(b):
         pages += (L - 1) // p - first // p + 1
     flops = 4.0 * d * hq * pairs
     meta = (2 * b.num_seqs + 1 + (b.num_seqs if b.window is not None else 0)) * 4
-    byts = (kv_tokens * hkv * d * 2 * esz + 2 * b.total_q * hq * d * esz + pages * 4 + meta)
+    nq = sum(int(b.cu_q_lens[s + 1] - b.cu_q_lens[s]) for s in range(b.num_seqs)
+             if part is None or (part == "decode") == (b.cu_q_lens[s + 1] - b.cu_q_lens[s] == 1))
+    byts = (kv_tokens * hkv * d * 2 * esz + 2 * nq * hq * d * esz + pages * 4 + meta)
     return dict(pairs=pairs, kv_tokens=kv_tokens, flops=flops, bytes=float(byts))
 
 
@@ -398,11 +401,18 @@ def main():
     tokens = b.total_q
     ms_per_step = total_ms / K
     value = world * tokens * K / (total_ms / 1e3)
-    decode_heavy = info["num_prefill_seqs"] == 0 or args.workload in ("decode", "mixed")
     dom = max(kernels, key=lambda k: kernels[k]["avg_us"] * kernels[k]["launches_per_step"])
     dom_us = kernels[dom]["avg_us"]
+    # The dominant kernel's own work: the decode sequences' bytes for the
+    # decode kernel, the prefill sequences' FLOPs for the prefill kernel.
+    if dom == "decode_split":
+        dom_counts, decode_heavy = algorithmic_counts(b, "decode"), True
+    elif dom == "prefill_tc":
+        dom_counts, decode_heavy = algorithmic_counts(b, "prefill"), False
+    else:
+        dom_counts, decode_heavy = counts, info["num_prefill_seqs"] == 0
     if decode_heavy:
-        achieved = counts["bytes"] / (dom_us * 1e-6) / 1e9
+        achieved = dom_counts["bytes"] / (dom_us * 1e-6) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak}
@@ -410,7 +420,7 @@ def main():
                "simt": "ragged_paged_attention_rpa_gb300/csrc/simt.cu"}.get(
                    dom, "ragged_paged_attention_rpa_gb300/csrc/decode.cu")
     else:
-        achieved = counts["flops"] / (dom_us * 1e-6) / 1e12
+        achieved = dom_counts["flops"] / (dom_us * 1e-6) / 1e12
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak}

@@ -55,6 +55,7 @@ using namespace sm100;
 
 constexpr int kBM = 128;        // MMA rows per block
 constexpr int kBN = 128;        // keys per score tile (N of the score MMAs)
+constexpr int kTileAlign = 64;  // score tiles start on multiples of this many keys
 constexpr int kStage = 16384;   // bytes per K or V ring stage
 constexpr int kKS = 5;          // K ring depth (stages)
 constexpr int kVS = 5;          // V ring depth (stages)
@@ -119,7 +120,7 @@ struct Barriers {
 static_assert(sizeof(Barriers) <= 512, "barrier block");
 
 struct Geom {
-  int32_t seq, g, t0, ntok, pos_first, kt0, ntiles, W;
+  int32_t seq, g, t0, ntok, pos_first, key_first, ntiles, W;
   bool ok;
 };
 
@@ -139,8 +140,10 @@ __device__ __forceinline__ Geom item_geom(const PrefillParams& p, const PrefillI
   r.ok = r.ntok > 0 && r.pos_first >= 0 && pos_last < L &&
          (pos_last >> p.page_shift) < p.mpps;
   const int32_t klo = first_visible(r.pos_first, r.W);
-  r.kt0 = klo / kBN;
-  r.ntiles = r.ok ? pos_last / kBN - r.kt0 + 1 : 0;
+  // Tiles start on a 64-key boundary at or below the first visible key (a
+  // 128-key boundary would mask up to 127 keys of a window's first tile).
+  r.key_first = klo / kTileAlign * kTileAlign;
+  r.ntiles = r.ok ? (pos_last - r.key_first) / kBN + 1 : 0;
   return r;
 }
 
@@ -273,7 +276,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       alive = __shfl_sync(0xffffffffu, alive, 0);
       for (int j = 0; j < gm.ntiles && alive; ++j) {
-        const int32_t key0 = (gm.kt0 + j) * kBN;
+        const int32_t key0 = gm.key_first + j * kBN;
         // K: the same 128 keys for every chunk of the tile.
         const int32_t krow = (is_k && lane < nbox) ? box_row(p, gm, key0 + lane * rows, rows) : 0;
         for (int sgi = 0; sgi < Lay::kChunks; ++sgi, ++C) {
@@ -448,7 +451,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tmem_ld32(lane_addr + Lay::kSCol + sb * kBN + 64 * h + 32,
                   *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_wait_ld();
-        const int32_t key0 = (gm.kt0 + j) * kBN + 64 * h;
+        const int32_t key0 = gm.key_first + j * kBN + 64 * h;
         // Interior halves (every key visible to every row of the warp) skip
         // the per-element mask; elsewhere masked scores become -inf.
         const bool full = __all_sync(0xffffffffu, valid && key0 >= lo && key0 + 63 <= pos);
@@ -603,8 +606,8 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   }
   const int G = plan.hq / plan.hkv;
   const int qb = plan.q_block;
-  const int box_rows_k = std::min(plan.p, kBN);
-  const int box_rows_v = std::min(plan.p, Lay::kVKeys);
+  const int box_rows_k = std::min(plan.p, kTileAlign);   // boxes never cross a page
+  const int box_rows_v = std::min(std::min(plan.p, Lay::kVKeys), kTileAlign);
   CUtensorMap tq, tk, tv;
   if (!make_tmap_3d(&tq, a.q, D, plan.hq, static_cast<uint64_t>(plan.total_q), G, qb) ||
       !make_tmap_3d(&tk, a.k_pages, D, plan.hkv, static_cast<uint64_t>(plan.num_pages) * plan.p, 1,
