@@ -151,6 +151,7 @@ PREFILL = [
     ([45, 80], [45, 300], 6, 2, 128, 64, [0, 33]),                         # G = 3
     ([40, 17], [100, 17], 16, 1, 64, 32, [0, 5]),                          # G = 16
     ([130, 65], [130, 2000], 2, 2, 256, 16, [0, 0]),                       # G = 1, P = 16
+    ([300, 150], [600, 150], 8, 2, 64, 128, [100, 70]),                    # D = 64, P = 128, windows
 ]
 
 
@@ -163,6 +164,21 @@ def test_prefill_tc_small(case):
     info = plan.info()
     assert err == 0 and info["path"] == RPA_PATH_TC and info["num_prefill_items"] > 0
     assert_bf16_close(got, oracle_rows(b), "prefill case %d" % case)
+
+
+def test_decode_many_short_sequences():
+    """Thousands of short decode sequences: several launches, many sequences
+    per CTA range, cut sequences merged by the combine kernel."""
+    rng = np.random.default_rng(5)
+    n = 2500
+    kv = rng.integers(1, 65, size=n).tolist()
+    b = workloads.make_batch([1] * n, kv, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                             page_size=16, windows=[0 if i % 3 else 9 for i in range(n)],
+                             seed=91)
+    got, err, plan = run_gpu(b)
+    assert err == 0 and plan.info()["path"] == RPA_PATH_TC
+    assert plan.info()["num_decode_seqs"] == n
+    assert_bf16_close(got, oracle_rows(b), "many short decode sequences")
 
 
 @pytest.mark.parametrize("q_block", [64, 32, 16, 8])
