@@ -100,6 +100,10 @@ typedef struct rpa_plan_options {
   int32_t q_block;          /* prefill query block, tokens (0: choose)          */
   int32_t kv_split;         /* decode split length, tokens (0: choose)          */
   int32_t num_sms;          /* SMs to plan for (0: ask the current device, else 152) */
+  int32_t prefill_pairs;    /* tensor-core prefill on SM pairs (one M = 256 MMA
+                               over two adjacent query blocks): 0 or 1 not
+                               used (single-SM kernel), 2 required (else
+                               RPA_ERR_UNSUPPORTED; head_dim 128 or 256)        */
 } rpa_plan_options;
 
 /* What a plan chose; filled by rpa_plan_get_info. */
@@ -113,6 +117,9 @@ typedef struct rpa_plan_info {
   int32_t num_prefill_items;/* (sequence, query block, kv head) work items      */
   int32_t prefill_ctas;     /* persistent prefill CTAs launched                 */
   int64_t workspace_bytes;  /* bytes rpa_forward needs                          */
+  int32_t prefill_pairs;    /* 1: prefill runs on SM pairs, items are pairs of
+                               query blocks                                     */
+  int32_t reserved;
 } rpa_plan_info;
 
 typedef struct rpa_plan rpa_plan_t;

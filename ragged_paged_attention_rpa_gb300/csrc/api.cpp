@@ -65,7 +65,9 @@ rpa_status_t rpa_plan(rpa_plan_t** plan, const int32_t* cu_q_lens_host,
       return RPA_ERR_INVALID_ARG;
     std::memcpy(&o, opts, static_cast<size_t>(opts->struct_size));
   }
-  if (o.q_block < 0 || o.kv_split < 0 || o.num_sms < 0) return RPA_ERR_INVALID_ARG;
+  if (o.q_block < 0 || o.kv_split < 0 || o.num_sms < 0 || o.prefill_pairs < 0 ||
+      o.prefill_pairs > 2)
+    return RPA_ERR_INVALID_ARG;
   rpa_status_t st = rpa::validate_metadata(cu_q_lens_host, kv_lens_host, num_seqs,
                                            page_size, max_pages_per_seq);
   if (st != RPA_OK) return st;
@@ -113,6 +115,8 @@ rpa_status_t rpa_plan_get_info(const rpa_plan_t* plan, rpa_plan_info* info) {
   info->num_prefill_items = static_cast<int32_t>(p.items.size());
   info->prefill_ctas = p.prefill_ctas;
   info->workspace_bytes = static_cast<int64_t>(p.ws_bytes);
+  info->prefill_pairs = p.prefill_pairs ? 1 : 0;
+  info->reserved = 0;
   return RPA_OK;
 }
 
@@ -148,7 +152,8 @@ rpa_status_t rpa_forward(const void* q, const void* k_pages, const void* v_pages
     if (err) return RPA_ERR_CUDA;
   }
   if (!p.items.empty()) {
-    err = rpa::launch_prefill_tc(p, a, stream);
+    err = p.prefill_pairs ? rpa::launch_prefill_pair(p, a, stream)
+                          : rpa::launch_prefill_tc(p, a, stream);
     if (err) return RPA_ERR_CUDA;
   }
   if (p.simt_decode || p.simt_prefill) {

@@ -228,6 +228,9 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
   plan.dec_slots = slot_base;
 }
 
+// Prefill work items, longest first for a persistent grid: (sequence, query
+// block, KV head), or with SM pairs (sequence, pair of adjacent query blocks,
+// KV head), costed by the keys the item streams.
 void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t* win,
                   int32_t forced_q_block) {
   const int32_t group = plan.hq / plan.hkv;
@@ -245,12 +248,13 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
     if (ql <= 1) continue;
     const int32_t L = kv[s];
     const int32_t w = win ? win[s] : 0;
-    const int64_t nb = ceil_div(ql, qb);
+    const int64_t span = plan.prefill_pairs ? 2 * qb : qb;   // query tokens per item
+    const int64_t nb = ceil_div(ql, span);
     for (int64_t b = 0; b < nb; ++b) {
-      // Keys streamed by this block: from the first visible key of its first
+      // Keys streamed by this item: from the first visible key of its first
       // query to its last query's own position.
-      int64_t pos0 = static_cast<int64_t>(L) - ql + b * qb;
-      int64_t pos1 = std::min<int64_t>(static_cast<int64_t>(L) - ql + (b + 1) * qb, L) - 1;
+      int64_t pos0 = static_cast<int64_t>(L) - ql + b * span;
+      int64_t pos1 = std::min<int64_t>(static_cast<int64_t>(L) - ql + (b + 1) * span, L) - 1;
       int64_t lo = (w > 0 && pos0 - (w - 1) > 0) ? pos0 - (w - 1) : 0;
       int64_t keys = pos1 - lo + 1;
       for (int32_t h = 0; h < plan.hkv; ++h)
@@ -264,8 +268,9 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
   plan.items.clear();
   for (const Cost& c : all) plan.items.push_back(c.item);
   const int64_t slots = static_cast<int64_t>(plan.num_sms) * prefill_ctas_per_sm(plan.d);
+  const int64_t per_item = plan.prefill_pairs ? 2 : 1;      // CTAs per item
   plan.prefill_ctas = static_cast<int32_t>(
-      std::min<int64_t>(static_cast<int64_t>(plan.items.size()), slots));
+      per_item * std::min<int64_t>(static_cast<int64_t>(plan.items.size()), slots / per_item));
 }
 
 }  // namespace
@@ -317,6 +322,11 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
   plan.items.clear();
   plan.q_block = 0;
   plan.prefill_ctas = 0;
+  const bool pairs_ok = tc_prefill && prefill_pair_supported(plan.d, plan.p, group);
+  if (opts.prefill_pairs == 2 && plan.num_prefill > 0 && !pairs_ok) return RPA_ERR_UNSUPPORTED;
+  // Chosen only on request: on GB300 the pair kernel's cross-SM barrier
+  // round trips cost more per tile than its halved copy traffic saves.
+  plan.prefill_pairs = pairs_ok && plan.num_prefill > 0 && opts.prefill_pairs == 2;
   if (tc_prefill && plan.num_prefill > 0) plan_prefill(plan, cu, kv, win, opts.q_block);
 
   // Workspace: header, then the decode partials (two slots per decode CTA,

@@ -86,6 +86,7 @@ struct Plan {
   // Prefill (q_len > 1).
   int32_t num_prefill = 0;
   int32_t q_block = 0;
+  bool prefill_pairs = false;      // items are pairs of query blocks (SM-pair kernel)
   std::vector<PrefillItem> items;  // longest first
   int32_t prefill_ctas = 0;
 
@@ -121,6 +122,7 @@ struct Args {
 int launch_simt(const Plan& plan, const Args& a, void* stream);
 int launch_decode(const Plan& plan, const Args& a, void* stream);
 int launch_prefill_tc(const Plan& plan, const Args& a, void* stream);
+int launch_prefill_pair(const Plan& plan, const Args& a, void* stream);
 
 // Tracing hooks (trace.cpp): trace_start before a call's first launch,
 // trace_mark after each launch (no-ops unless tracing is on).
@@ -129,6 +131,8 @@ void trace_mark(int kernel, void* stream);
 
 // Whether the tensor-core prefill supports this shape (prefill_tc.cu).
 bool prefill_tc_supported(int32_t head_dim, int32_t page_size, int32_t group);
+// Whether the SM-pair prefill supports this shape (prefill_pair.cu).
+bool prefill_pair_supported(int32_t head_dim, int32_t page_size, int32_t group);
 // Device address of the fixed no-allocation scratch array on the current
 // device (decode.cu); resolved on the first call per device.
 int noalloc_scratch(void** ptr);

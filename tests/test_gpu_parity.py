@@ -181,6 +181,19 @@ def test_decode_many_short_sequences():
     assert_bf16_close(got, oracle_rows(b), "many short decode sequences")
 
 
+@pytest.mark.parametrize("case", [0, 2, 3, 5, 7])
+def test_prefill_sm_pairs(case):
+    """The SM-pair prefill kernel (one M = 256 MMA over two query blocks)."""
+    ql, kv, hq, hkv, d, p, win = PREFILL[case]
+    b = workloads.make_batch(ql, kv, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                             page_size=p, windows=win, seed=600 + case)
+    got, err, plan = run_gpu(b, prefill_pairs=2)
+    info = plan.info()
+    assert err == 0 and info["prefill_pairs"] == 1
+    assert info["prefill_ctas"] % 2 == 0
+    assert_bf16_close(got, oracle_rows(b), "pair prefill case %d" % case)
+
+
 @pytest.mark.parametrize("q_block", [64, 32, 16, 8])
 def test_prefill_q_block_invariance(q_block):
     """The query block changes scheduling, not the result."""
