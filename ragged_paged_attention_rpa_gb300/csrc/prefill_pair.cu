@@ -49,7 +49,7 @@ constexpr int kKS = 10;         // K ring depth (stages)
 constexpr int kVS = 10;         // V ring depth (stages)
 constexpr int kThreads = 352;   // K producer, V producer, MMA, 8 softmax warps
 constexpr int kSoftmaxWarps = 8;
-constexpr int kPolyEvery = 4;
+constexpr int kPolyEvery = 32;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 

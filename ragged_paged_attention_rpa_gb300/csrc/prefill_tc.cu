@@ -33,7 +33,7 @@
 //              swaps row maxima through shared memory every tile;
 //              reads S from TMEM, masks causal and window edges (interior
 //              tiles skip the mask), keeps the running max / sum in fp32,
-//              exponentiates with the MUFU unit and, for one pair in four,
+//              exponentiates with the MUFU unit and, for one pair in 32,
 //              with a polynomial on the FMA pipe (paired fp32 instructions),
 //              writes P (bf16) to TMEM, rescales O in TMEM only when the max
 //              grew by more than 2^8 (the result is the same; it bounds P by
@@ -60,7 +60,7 @@ constexpr int kStage = 16384;   // bytes per K or V ring stage
 constexpr int kKS = 5;          // K ring depth (stages)
 constexpr int kVS = 5;          // V ring depth (stages)
 constexpr int kThreads = 352;   // K producer, V producer, MMA, 8 softmax warps
-constexpr int kPolyEvery = 4;   // one pair of exponentials in four on the FMA pipe
+constexpr int kPolyEvery = 32;  // one pair of exponentials in 32 on the FMA pipe
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait, then give up
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
 
