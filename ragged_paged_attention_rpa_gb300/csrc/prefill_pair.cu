@@ -492,9 +492,11 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
           m_ref = m_new;
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        // Paired fp32 arithmetic (masked scores are -inf: 2^-inf = +0).
+        // One pair in kPolyEvery takes its 2^x on the FMA pipe.
         uint32_t pk[32];
         float ls;
-        if (full) {
+        {
           const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_use, -m_use);
           uint64_t acc = f2_pack(0.f, 0.f);
 #pragma unroll
@@ -517,17 +519,6 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
           float a0, a1;
           f2_unpack(acc, a0, a1);
           ls = a0 + a1;
-        } else {
-          ls = 0.f;
-#pragma unroll
-          for (int cc = 0; cc < 32; ++cc) {
-            const float p0 = sr[2 * cc] == 0xff800000u
-                                 ? 0.f : fast_exp2(fmaf(__uint_as_float(sr[2 * cc]), c, -m_use));
-            const float p1 = sr[2 * cc + 1] == 0xff800000u
-                                 ? 0.f : fast_exp2(fmaf(__uint_as_float(sr[2 * cc + 1]), c, -m_use));
-            ls += p0 + p1;
-            pk[cc] = pack_bf16x2(p0, p1);
-          }
         }
         l += ls;
         tmem_st32(lane_addr + Lay::kSCol + sb * kBN + 32 * h, pk);

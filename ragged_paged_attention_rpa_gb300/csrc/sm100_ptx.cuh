@@ -227,12 +227,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // f in [-0.5, 0.5], a degree-3 polynomial for 2^f whose coefficients are a
 // relative-error minimax fit computed for this library (max relative error
 // 7.5e-5, ample for P that is rounded to bf16), and 2^n added into the
-// exponent field.  Arguments below -125 are clamped (result ~2^-125).
+// exponent field.  Arguments below -125 (including -inf, a masked score)
+// give exactly 0.
 __device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
-  float a, b;
-  f2_unpack(x2, a, b);
-  a = fmaxf(a, -125.f);
-  b = fmaxf(b, -125.f);
+  float a0, b0;
+  f2_unpack(x2, a0, b0);
+  const float a = fmaxf(a0, -125.f);
+  const float b = fmaxf(b0, -125.f);
   x2 = f2_pack(a, b);
   const uint64_t shifter = f2_pack(12582912.f, 12582912.f);
   const uint64_t t2 = f2_add(x2, shifter);
@@ -244,8 +245,8 @@ __device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
   float pa, pb, ta, tb;
   f2_unpack(p, pa, pb);
   f2_unpack(t2, ta, tb);
-  pa = __int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23));
-  pb = __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23));
+  pa = a0 < -125.f ? 0.f : __int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23));
+  pb = b0 < -125.f ? 0.f : __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23));
   return f2_pack(pa, pb);
 }
 

@@ -39,7 +39,8 @@ def coefficients():
 def emulate(x):
     f32 = np.float32
     c0, c1, c2, c3 = (f32(v) for v in coefficients())
-    x = np.maximum(x.astype(f32), f32(-125.0))
+    x0 = x.astype(f32)
+    x = np.maximum(x0, f32(-125.0))
     t = (x + f32(12582912.0)).astype(f32)
     n = (t - f32(12582912.0)).astype(f32)
     fr = (x - n).astype(f32)
@@ -47,7 +48,13 @@ def emulate(x):
     p = (p * fr + c1).astype(f32)
     p = (p * fr + c0).astype(f32)
     bits = p.view(np.int32) + (t.view(np.int32) << 23)
-    return bits.astype(np.int32).view(np.float32)
+    return np.where(x0 < f32(-125.0), f32(0.0), bits.astype(np.int32).view(np.float32))
+
+
+def test_masked_scores_give_exact_zero():
+    x = np.array([-np.inf, -1e30, -200.0, -125.5], dtype=np.float32)
+    assert (emulate(x) == 0.0).all()
+    assert emulate(np.array([-125.0], dtype=np.float32))[0] > 0.0
 
 
 def test_poly_exp2_matches_float64_on_the_softmax_range():
@@ -84,3 +91,10 @@ def test_poly_exp2_on_gpu_matches_exp2f(tmp_path):
     assert rc == 0
     rel = np.abs(poly.astype(np.float64) - ref) / ref
     assert rel.max() < BOUND, rel.max()
+    # Masked scores (-inf) and arguments below the clamp give exactly 0.
+    x = np.array([-np.inf, -1e30, -200.0, -125.5], dtype=np.float32)
+    poly = np.empty_like(x)
+    ref = np.empty_like(x)
+    rc = L.exp2_poly_check(x.ctypes.data_as(vp), poly.ctypes.data_as(vp),
+                           ref.ctypes.data_as(vp), ctypes.c_int(x.size))
+    assert rc == 0 and (poly == 0.0).all(), poly
