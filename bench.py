@@ -93,6 +93,24 @@ def algorithmic_counts(b, part=None):
     return dict(pairs=pairs, kv_tokens=kv_tokens, flops=flops, bytes=float(byts))
 
 
+def new_token_rows(b, db, torch):
+    """Device copies of the step's new K/V rows ([total_q, Hkv, D]): the rows
+    the pools already hold at the new tokens' positions, so writing them
+    back leaves the cache as it was."""
+    P = b.page_size
+    idx = np.zeros(b.total_q, dtype=np.int64)
+    for s in range(b.num_seqs):
+        ql = int(b.cu_q_lens[s + 1] - b.cu_q_lens[s])
+        L = int(b.kv_lens[s])
+        for i in range(ql):
+            pos = L - ql + i
+            idx[int(b.cu_q_lens[s]) + i] = int(b.page_table[s, pos // P]) * P + pos % P
+    ii = torch.from_numpy(idx).cuda()
+    flat_k = db.k_pages.reshape(-1, b.num_kv_heads, b.head_dim)
+    flat_v = db.v_pages.reshape(-1, b.num_kv_heads, b.head_dim)
+    return flat_k[ii].contiguous(), flat_v[ii].contiguous()
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -249,6 +267,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--q-block", type=int, default=0)
     ap.add_argument("--kv-split", type=int, default=0)
+    ap.add_argument("--kv-write", action="store_true",
+                    help="time rpa_forward_kv: write the step's new K/V rows into their "
+                         "pages, then attend")
     return ap.parse_args()
 
 
@@ -327,6 +348,11 @@ def main():
     info = plan.info()
     ws = binding.alloc_workspace(plan)
     fwd = db.call(plan, ws)
+    if args.kv_write:
+        k_new, v_new = new_token_rows(b, db, torch)
+        fwd = binding.ForwardKvCall(db.q, k_new, v_new, db.k_pages, db.v_pages, db.page_table,
+                                    db.cu_q_lens, db.kv_lens, db.window, b.sm_scale, db.out,
+                                    plan, ws)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     evict = torch.ones(32 << 20, dtype=torch.int64, device="cuda")   # 256 MiB
     stream = torch.cuda.current_stream()
@@ -452,6 +478,8 @@ def main():
         "config": {"workload": b.name, "seed": b.seed,
                    "l2": "flushed before every timed step (256 MiB write, then a 256 MiB read that evicts the dirty lines)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
+                   "step": "rpa_forward_kv (KV-cache write of the new tokens, then attention)"
+                           if args.kv_write else "rpa_forward",
                    "plan": info},
         "achieved_gbs": counts["bytes"] / step_s / 1e9,
         "achieved_tflops": counts["flops"] / step_s / 1e12,

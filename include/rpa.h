@@ -201,6 +201,46 @@ rpa_status_t rpa_forward(const void* q, const void* k_pages, const void* v_pages
                          size_t workspace_bytes);
 
 /*
+ * KV-cache write of a step's new tokens ("TPU Deep Dive" slides, chapter 8,
+ * "Continuous batching with static shapes": ragged paged attention writes
+ * the KV cache of the step's tokens itself).
+ *
+ * For every sequence s and each of its q_len = cu_q_lens[s+1] - cu_q_lens[s]
+ * new tokens t = cu_q_lens[s] + i, at position pos = kv_lens[s] - q_len + i
+ * (the query positions rpa_forward attends from), and every KV head g:
+ *   k_pages[page_table[s][pos / page_size]][pos % page_size][g][:] = k_new[t][g][:]
+ * and V alike.  Nothing else in the pool changes.
+ *
+ * Device pointers: k_new, v_new [total_q, num_kv_heads, head_dim] of `dtype`,
+ * 16-B aligned; k_pages, v_pages, page_table, cu_q_lens, kv_lens as for
+ * rpa_forward (kv_lens include the new tokens).  head_dim * element size must
+ * be a multiple of 16 bytes; page_size a power of two.  `workspace` may be
+ * NULL; otherwise its error word records a page id outside [0, num_pages)
+ * or a position outside the page table (that row is skipped, never trapped).
+ * Enqueues one kernel on `stream`; does not synchronise.
+ */
+rpa_status_t rpa_write_kv(const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                          const int32_t* page_table, const int32_t* cu_q_lens,
+                          const int32_t* kv_lens, int32_t num_seqs, int32_t total_q,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                          int32_t max_pages_per_seq, int32_t num_pages, int32_t dtype,
+                          void* workspace, rpa_stream_t stream);
+
+/*
+ * rpa_write_kv of k_new / v_new, then rpa_forward over the updated cache, in
+ * order on `stream`: the step's cache update and its attention in one call.
+ * Arguments as rpa_forward plus k_new, v_new (as rpa_write_kv); the pool
+ * size and page-table width are the plan's.
+ */
+rpa_status_t rpa_forward_kv(const void* q, const void* k_new, const void* v_new, void* k_pages,
+                            void* v_pages, const int32_t* page_table, const int32_t* cu_q_lens,
+                            const int32_t* kv_lens, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                            const int32_t* window, float sm_scale, void* out,
+                            rpa_stream_t stream, const rpa_plan_t* plan, void* workspace,
+                            size_t workspace_bytes);
+
+/*
  * Read the device error word at the start of `workspace` after everything
  * enqueued on `stream` so far (this call synchronises `stream`), store it in
  * *err (an RPA_DEVERR_* code) and reset it to RPA_DEVERR_NONE.
@@ -261,7 +301,8 @@ enum {
   RPA_KERNEL_DECODE_SPLIT = 0,   /* split-KV decode                    */
   RPA_KERNEL_DECODE_COMBINE = 1, /* log-sum-exp combine of cut sequences */
   RPA_KERNEL_PREFILL_TC = 2,     /* tensor-core prefill               */
-  RPA_KERNEL_SIMT = 3            /* CUDA-core (fp32) path             */
+  RPA_KERNEL_SIMT = 3,           /* CUDA-core (fp32) path             */
+  RPA_KERNEL_KV_WRITE = 4        /* KV-cache write of new tokens      */
 };
 typedef struct rpa_trace_record {
   int32_t kernel; /* RPA_KERNEL_* */

@@ -145,3 +145,29 @@ def round_bf16(x):
     out = np.empty(x.shape, dtype=np.uint16)
     lib.rpa_oracle_round_bf16(_ptr(x), _ptr(out), x.size)
     return out
+
+
+def write_kv(k_pages, v_pages, k_new, v_new, page_table, cu_q_lens, kv_lens):
+    """The KV-cache write of a step's new tokens ("TPU Deep Dive" slides,
+    chapter 8, "Continuous batching with static shapes": ragged paged
+    attention writes the step's KV itself), as a plain loop: token
+    t = cu_q_lens[s] + i of sequence s sits at position
+    pos = kv_lens[s] - q_len + i, and its row for KV head g is copied to
+    page page_table[s][pos // P], slot pos % P.  Returns new copies of the
+    pools (any dtype; the copy is exact).  Parity pinned by
+    tests/test_oracle_pins.py (pools rebuilt bitwise from their own rows)."""
+    kp = np.array(k_pages, copy=True)
+    vp = np.array(v_pages, copy=True)
+    pt, cu, kl, _ = _meta(page_table, cu_q_lens, kv_lens, None)
+    P = kp.shape[1]
+    hkv = kp.shape[2]
+    for s in range(kl.shape[0]):
+        ql = int(cu[s + 1] - cu[s])
+        for i in range(ql):
+            t = int(cu[s]) + i
+            pos = int(kl[s]) - ql + i
+            page = int(pt[s, pos // P])
+            for g in range(hkv):
+                kp[page, pos % P, g, :] = k_new[t, g, :]
+                vp[page, pos % P, g, :] = v_new[t, g, :]
+    return kp, vp

@@ -40,9 +40,11 @@ RPA_PATH_TC = 2
 
 EXPORTS = ["rpa_plan", "rpa_plan_destroy", "rpa_plan_get_info", "rpa_forward",
            "rpa_get_device_error", "rpa_clear_device_error", "rpa_trace_begin",
-           "rpa_trace_end", "rpa_status_string", "rpa_forward_decode_noalloc"]
+           "rpa_trace_end", "rpa_status_string", "rpa_forward_decode_noalloc",
+           "rpa_write_kv", "rpa_forward_kv"]
 
-RPA_KERNEL_NAMES = {0: "decode_split", 1: "decode_combine", 2: "prefill_tc", 3: "simt"}
+RPA_KERNEL_NAMES = {0: "decode_split", 1: "decode_combine", 2: "prefill_tc", 3: "simt",
+                    4: "kv_write"}
 
 
 class RpaError(RuntimeError):
@@ -99,6 +101,12 @@ def lib() -> ctypes.CDLL:
         L.rpa_forward_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                   i32, vp, ctypes.c_float, vp, vp, vp]
         L.rpa_forward_decode_noalloc.restype = i32
+        L.rpa_write_kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                   i32, vp, vp]
+        L.rpa_write_kv.restype = i32
+        L.rpa_forward_kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
+                                     ctypes.c_float, vp, vp, vp, vp, ctypes.c_size_t]
+        L.rpa_forward_kv.restype = i32
         L.rpa_get_device_error.argtypes = [vp, vp, ctypes.POINTER(i32)]
         L.rpa_get_device_error.restype = i32
         L.rpa_clear_device_error.argtypes = [vp, vp]
@@ -223,6 +231,43 @@ def rpa_forward(q, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window,
         workspace.numel() * workspace.element_size())
     if st != RPA_OK:
         raise RpaError(st, "rpa_forward")
+
+
+def rpa_write_kv(k_new, v_new, k_pages, v_pages, page_table, cu_q_lens, kv_lens,
+                 num_pages: int, workspace=None, stream=None) -> None:
+    """rpa_write_kv on torch CUDA tensors: scatter the new tokens' K/V rows
+    ([total_q, Hkv, D]) into their pages."""
+    import torch
+    dt = k_pages.dtype
+    dtype = RPA_DTYPE_BF16 if dt == torch.bfloat16 else RPA_DTYPE_F32
+    total_q, hkv, d = (int(x) for x in k_new.shape)
+    st = lib().rpa_write_kv(
+        _dptr(k_new, "k_new", dt), _dptr(v_new, "v_new", dt), _dptr(k_pages, "k_pages", dt),
+        _dptr(v_pages, "v_pages", dt), _dptr(page_table, "page_table", torch.int32),
+        _dptr(cu_q_lens, "cu_q_lens", torch.int32), _dptr(kv_lens, "kv_lens", torch.int32),
+        int(kv_lens.numel()), total_q, hkv, d, int(k_pages.shape[1]), int(page_table.shape[1]),
+        int(num_pages), dtype, _dptr(workspace, "workspace"), _stream_ptr(stream))
+    if st != RPA_OK:
+        raise RpaError(st, "rpa_write_kv")
+
+
+def rpa_forward_kv(q, k_new, v_new, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window,
+                   sm_scale: float, out, plan: Plan, workspace, stream=None) -> None:
+    """rpa_forward_kv: write the new tokens' K/V into their pages, then attend."""
+    import torch
+    m = plan.meta
+    dt = torch.bfloat16 if m["dtype"] == RPA_DTYPE_BF16 else torch.float32
+    st = lib().rpa_forward_kv(
+        _dptr(q, "q", dt), _dptr(k_new, "k_new", dt), _dptr(v_new, "v_new", dt),
+        _dptr(k_pages, "k_pages", dt), _dptr(v_pages, "v_pages", dt),
+        _dptr(page_table, "page_table", torch.int32), _dptr(cu_q_lens, "cu_q_lens", torch.int32),
+        _dptr(kv_lens, "kv_lens", torch.int32), m["num_seqs"], m["num_q_heads"],
+        m["num_kv_heads"], m["head_dim"], m["page_size"],
+        _dptr(window, "window", torch.int32), float(sm_scale), _dptr(out, "out", dt),
+        _stream_ptr(stream), plan.handle, _dptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size())
+    if st != RPA_OK:
+        raise RpaError(st, "rpa_forward_kv")
 
 
 def rpa_forward_decode_noalloc(q, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window,
@@ -360,3 +405,24 @@ class ForwardCall:
         st = self._fn(*self._args)
         if st != RPA_OK:
             raise RpaError(st, "rpa_forward")
+
+
+class ForwardKvCall(ForwardCall):
+    """rpa_forward_kv (write the new tokens' K/V, then attend) with its
+    arguments marshalled once."""
+
+    def __init__(self, q, k_new, v_new, k_pages, v_pages, page_table, cu_q_lens, kv_lens,
+                 window, sm_scale: float, out, plan: Plan, workspace, stream=None):
+        import torch
+        super().__init__(q, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window,
+                         sm_scale, out, plan, workspace, stream)
+        dt = torch.bfloat16 if plan.meta["dtype"] == RPA_DTYPE_BF16 else torch.float32
+        self._keep = self._keep + (k_new, v_new)
+        a = self._args
+        self._args = (a[0], _dptr(k_new, "k_new", dt), _dptr(v_new, "v_new", dt)) + a[1:]
+        self._fn = lib().rpa_forward_kv
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != RPA_OK:
+            raise RpaError(st, "rpa_forward_kv")

@@ -124,6 +124,20 @@ int launch_decode(const Plan& plan, const Args& a, void* stream);
 int launch_prefill_tc(const Plan& plan, const Args& a, void* stream);
 int launch_prefill_pair(const Plan& plan, const Args& a, void* stream);
 
+// KV-cache write of a step's new tokens (kv_write.cu).
+struct KvWriteArgs {
+  const void* k_new;
+  const void* v_new;
+  void* k_pages;
+  void* v_pages;
+  const int32_t* page_table;
+  const int32_t* cu_q_lens;
+  const int32_t* kv_lens;
+  unsigned char* workspace;  // error word, or null
+  int32_t num_seqs, total_q, hkv, head_dim, elem_bytes, page_size, mpps, num_pages;
+};
+int launch_kv_write(const KvWriteArgs& a, void* stream);
+
 // Tracing hooks (trace.cpp): trace_start before a call's first launch,
 // trace_mark after each launch (no-ops unless tracing is on).
 void trace_start(void* stream);
