@@ -71,6 +71,7 @@ def algorithmic_counts(b, part=None):
     per-sequence metadata.  Counted from the realised lengths.
     """
     esz = 2 if b.dtype == "bf16" else 4
+    kv_esz = 1 if getattr(b, "k_fp8", None) is not None else esz   # e4m3 pages: 1 byte
     hq, hkv, d, p = b.num_q_heads, b.num_kv_heads, b.head_dim, b.page_size
     pairs = kv_tokens = pages = 0
     for s in range(b.num_seqs):
@@ -89,7 +90,8 @@ def algorithmic_counts(b, part=None):
     meta = (2 * b.num_seqs + 1 + (b.num_seqs if b.window is not None else 0)) * 4
     nq = sum(int(b.cu_q_lens[s + 1] - b.cu_q_lens[s]) for s in range(b.num_seqs)
              if part is None or (part == "decode") == (b.cu_q_lens[s + 1] - b.cu_q_lens[s] == 1))
-    byts = (kv_tokens * hkv * d * 2 * esz + 2 * nq * hq * d * esz + pages * 4 + meta)
+    scales = 2 * hkv * 4 if kv_esz == 1 else 0
+    byts = (kv_tokens * hkv * d * 2 * kv_esz + 2 * nq * hq * d * esz + pages * 4 + meta + scales)
     return dict(pairs=pairs, kv_tokens=kv_tokens, flops=flops, bytes=float(byts))
 
 
@@ -260,7 +262,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["rpa", "reference"], default="rpa")
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "tiny_prefill", "swa_prefill", "causal_prefill", "mixed"])
+                    choices=["decode", "decode_fp8", "tiny_prefill", "swa_prefill",
+                             "causal_prefill", "mixed"])
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -344,10 +347,16 @@ def main():
     b = make_workload(args)
     counts = algorithmic_counts(b)
     db = binding.Batch(b)
-    plan = db.plan(q_block=args.q_block, kv_split=args.kv_split)
+    fp8 = b.k_fp8 is not None
+    plan = db.plan(q_block=args.q_block, kv_split=args.kv_split,
+                   kv_dtype=binding.RPA_DTYPE_FP8_E4M3 if fp8 else 0)
     info = plan.info()
     ws = binding.alloc_workspace(plan)
     fwd = db.call(plan, ws)
+    if fp8:
+        fp8_dev = [torch.from_numpy(x).cuda() for x in (b.k_fp8, b.v_fp8, b.k_scale, b.v_scale)]
+        fwd = binding.ForwardFp8Call(db.q, *fp8_dev, db.page_table, db.cu_q_lens, db.kv_lens,
+                                     db.window, b.sm_scale, db.out, plan, ws)
     if args.kv_write:
         k_new, v_new = new_token_rows(b, db, torch)
         fwd = binding.ForwardKvCall(db.q, k_new, v_new, db.k_pages, db.v_pages, db.page_table,
@@ -421,7 +430,8 @@ def main():
                for k, v in per_kernel.items()}
 
     # End to end through the public API with host buffers.
-    e2e = run_e2e(args, b, db, plan, flush_l2, binding, torch)
+    e2e = run_e2e(args, b, db, plan, flush_l2, binding, torch,
+                  fp8_dev if b.k_fp8 is not None else None)
 
     peaks = load_peaks()
     tokens = b.total_q
@@ -479,7 +489,10 @@ def main():
                    "l2": "flushed before every timed step (256 MiB write, then a 256 MiB read that evicts the dirty lines)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "step": "rpa_forward_kv (KV-cache write of the new tokens, then attention)"
-                           if args.kv_write else "rpa_forward",
+                           if args.kv_write else ("rpa_forward_fp8kv" if b.k_fp8 is not None
+                                                  else "rpa_forward"),
+                   "kv_pages": "e4m3 bytes + fp32 scale per KV head (f16 products, fp32 "
+                               "accumulation)" if b.k_fp8 is not None else "bf16",
                    "plan": info},
         "achieved_gbs": counts["bytes"] / step_s / 1e9,
         "achieved_tflops": counts["flops"] / step_s / 1e12,
@@ -500,7 +513,7 @@ def main():
         dist.destroy_process_group()
 
 
-def run_e2e(args, b, db, plan_dev, flush_l2, binding, torch):
+def run_e2e(args, b, db, plan_dev, flush_l2, binding, torch, fp8_dev=None):
     """Per step: pinned H2D of q + metadata, rpa_plan on host metadata,
     rpa_forward, D2H of out; timed with events around the whole sequence."""
     stream = torch.cuda.current_stream()
@@ -532,11 +545,16 @@ def run_e2e(args, b, db, plan_dev, flush_l2, binding, torch):
         plan = binding.rpa_plan(b.cu_q_lens, b.kv_lens, b.window, b.num_q_heads,
                                 b.num_kv_heads, b.head_dim, b.page_size,
                                 b.max_pages_per_seq, b.num_pages,
-                                dtype=db.dtype, q_block=args.q_block, kv_split=args.kv_split)
+                                dtype=db.dtype, q_block=args.q_block, kv_split=args.kv_split,
+                                kv_dtype=binding.RPA_DTYPE_FP8_E4M3 if fp8_dev else 0)
         if plan.workspace_bytes > ws.numel():
             raise RuntimeError("workspace too small for the per-step plan")
-        binding.rpa_forward(qv, db.k_pages, db.v_pages, dmeta[0], dmeta[1], dmeta[2], win_d,
-                            b.sm_scale, db.out, plan, ws)
+        if fp8_dev:
+            binding.rpa_forward_fp8kv(qv, *fp8_dev, dmeta[0], dmeta[1], dmeta[2], win_d,
+                                      b.sm_scale, db.out, plan, ws)
+        else:
+            binding.rpa_forward(qv, db.k_pages, db.v_pages, dmeta[0], dmeta[1], dmeta[2],
+                                win_d, b.sm_scale, db.out, plan, ws)
         hout.copy_(db.out, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()

@@ -72,7 +72,9 @@ enum {
 };
 
 /* Element types of q, k_pages, v_pages and out (all four share one). */
-enum { RPA_DTYPE_BF16 = 0, RPA_DTYPE_F32 = 1 };
+enum { RPA_DTYPE_BF16 = 0, RPA_DTYPE_F32 = 1,
+       RPA_DTYPE_FP8_E4M3 = 2 /* K/V pages only: OCP e4m3 bytes (bias 7, 3-bit
+                                 mantissa, max 448), a float scale per KV head */ };
 
 /* Codes written into the workspace error word by the kernels. */
 enum {
@@ -104,6 +106,10 @@ typedef struct rpa_plan_options {
                                over two adjacent query blocks): 0 or 1 not
                                used (single-SM kernel), 2 required (else
                                RPA_ERR_UNSUPPORTED; head_dim 128 or 256)        */
+  int32_t kv_dtype;         /* dtype of the K/V pages: 0 or `dtype` (the same),
+                               or RPA_DTYPE_FP8_E4M3 with dtype BF16: decode
+                               batches only (every q_len <= 1), head_dim 128 or
+                               256, run through rpa_forward_fp8kv               */
 } rpa_plan_options;
 
 /* What a plan chose; filled by rpa_plan_get_info. */
@@ -119,7 +125,7 @@ typedef struct rpa_plan_info {
   int64_t workspace_bytes;  /* bytes rpa_forward needs                          */
   int32_t prefill_pairs;    /* 1: prefill runs on SM pairs, items are pairs of
                                query blocks                                     */
-  int32_t reserved;
+  int32_t kv_dtype;         /* dtype of the K/V pages (RPA_DTYPE_*)              */
 } rpa_plan_info;
 
 typedef struct rpa_plan rpa_plan_t;
@@ -225,6 +231,27 @@ rpa_status_t rpa_write_kv(const void* k_new, const void* v_new, void* k_pages, v
                           int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                           int32_t max_pages_per_seq, int32_t num_pages, int32_t dtype,
                           void* workspace, rpa_stream_t stream);
+
+/*
+ * Decode over fp8 (e4m3) K/V pages with a float scale per KV head
+ * ("TPU Deep Dive" slides, chapter 8, "KV cache layout": 8-bit KV packs four
+ * per 32-bit word; halving the KV bytes halves decode's dominant traffic).
+ * The stored keys and values are k_pages[...][g][:] * k_scale[g] and
+ * v_pages[...][g][:] * v_scale[g]; otherwise exactly rpa_forward.  The plan
+ * must have kv_dtype RPA_DTYPE_FP8_E4M3 (decode batch, bf16 q and out).
+ * k_pages, v_pages: [num_pages, page_size, num_kv_heads, head_dim] bytes,
+ * 128-B aligned; k_scale, v_scale: [num_kv_heads] float32 on the device.
+ * The products run as f16 (e4m3 is exact in f16; q is converted bf16 -> f16
+ * once per sequence), accumulation and softmax in fp32.
+ */
+rpa_status_t rpa_forward_fp8kv(const void* q, const void* k_pages, const void* v_pages,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* page_table, const int32_t* cu_q_lens,
+                               const int32_t* kv_lens, int32_t num_seqs, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                               const int32_t* window, float sm_scale, void* out,
+                               rpa_stream_t stream, const rpa_plan_t* plan, void* workspace,
+                               size_t workspace_bytes);
 
 /*
  * rpa_write_kv of k_new / v_new, then rpa_forward over the updated cache, in

@@ -171,3 +171,29 @@ def write_kv(k_pages, v_pages, k_new, v_new, page_table, cu_q_lens, kv_lens):
                 kp[page, pos % P, g, :] = k_new[t, g, :]
                 vp[page, pos % P, g, :] = v_new[t, g, :]
     return kp, vp
+
+
+def decode_e4m3(codes) -> np.ndarray:
+    """OCP fp8 e4m3 codes -> float32, from the format's definition: sign bit,
+    4-bit exponent with bias 7, 3-bit mantissa; exponent field 0 is
+    subnormal (m/8 * 2^-6); S.1111.111 is NaN (no infinities)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = c & 7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
+    out = sign * mag
+    out = np.where((e == 15) & (m == 7), np.nan, out)
+    return out.astype(np.float32)
+
+
+def dequantize_kv(codes, scale) -> np.ndarray:
+    """fp8 pages [num_pages, P, Hkv, D] with a scale per KV head -> float32
+    values (decoded code * scale of its head)."""
+    vals = decode_e4m3(codes)
+    return (vals * np.asarray(scale, dtype=np.float32)[None, None, :, None]).astype(np.float32)
+
+
+def bf16_bits_to_f32(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float32 (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)

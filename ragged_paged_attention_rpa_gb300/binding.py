@@ -27,6 +27,7 @@ RPA_ERR_PLAN_MISMATCH = -6
 
 RPA_DTYPE_BF16 = 0
 RPA_DTYPE_F32 = 1
+RPA_DTYPE_FP8_E4M3 = 2
 
 RPA_DEVERR_NONE = 0
 RPA_DEVERR_PAGE_ID = 1
@@ -41,7 +42,7 @@ RPA_PATH_TC = 2
 EXPORTS = ["rpa_plan", "rpa_plan_destroy", "rpa_plan_get_info", "rpa_forward",
            "rpa_get_device_error", "rpa_clear_device_error", "rpa_trace_begin",
            "rpa_trace_end", "rpa_status_string", "rpa_forward_decode_noalloc",
-           "rpa_write_kv", "rpa_forward_kv"]
+           "rpa_write_kv", "rpa_forward_kv", "rpa_forward_fp8kv"]
 
 RPA_KERNEL_NAMES = {0: "decode_split", 1: "decode_combine", 2: "prefill_tc", 3: "simt",
                     4: "kv_write"}
@@ -56,7 +57,8 @@ class RpaError(RuntimeError):
 class _Options(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_int32), ("path", ctypes.c_int32),
                 ("q_block", ctypes.c_int32), ("kv_split", ctypes.c_int32),
-                ("num_sms", ctypes.c_int32), ("prefill_pairs", ctypes.c_int32)]
+                ("num_sms", ctypes.c_int32), ("prefill_pairs", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -65,7 +67,7 @@ class PlanInfo(ctypes.Structure):
                 ("kv_split", ctypes.c_int32), ("max_splits", ctypes.c_int32),
                 ("num_prefill_items", ctypes.c_int32), ("prefill_ctas", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("prefill_pairs", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("kv_dtype", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: int(getattr(self, name)) for name, _ in self._fields_}
@@ -107,6 +109,9 @@ def lib() -> ctypes.CDLL:
         L.rpa_forward_kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
                                      ctypes.c_float, vp, vp, vp, vp, ctypes.c_size_t]
         L.rpa_forward_kv.restype = i32
+        L.rpa_forward_fp8kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                        vp, ctypes.c_float, vp, vp, vp, vp, ctypes.c_size_t]
+        L.rpa_forward_fp8kv.restype = i32
         L.rpa_get_device_error.argtypes = [vp, vp, ctypes.POINTER(i32)]
         L.rpa_get_device_error.restype = i32
         L.rpa_clear_device_error.argtypes = [vp, vp]
@@ -170,7 +175,7 @@ def rpa_plan(cu_q_lens_host, kv_lens_host, window_host, num_q_heads: int,
              num_kv_heads: int, head_dim: int, page_size: int, max_pages_per_seq: int,
              num_pages: int, dtype: int = RPA_DTYPE_BF16, path: int = RPA_PATH_AUTO,
              q_block: int = 0, kv_split: int = 0, num_sms: int = 0,
-             prefill_pairs: int = 0) -> Plan:
+             prefill_pairs: int = 0, kv_dtype: int = 0) -> Plan:
     """rpa_plan from host (numpy) metadata; returns a Plan."""
     cu = _np_i32(cu_q_lens_host)
     kv = _np_i32(kv_lens_host)
@@ -180,7 +185,8 @@ def rpa_plan(cu_q_lens_host, kv_lens_host, window_host, num_q_heads: int,
         raise ValueError("cu_q_lens must have num_seqs + 1 entries")
     if win is not None and win.shape[0] != num_seqs:
         raise ValueError("window must have num_seqs entries")
-    opts = _Options(ctypes.sizeof(_Options), path, q_block, kv_split, num_sms, prefill_pairs)
+    opts = _Options(ctypes.sizeof(_Options), path, q_block, kv_split, num_sms, prefill_pairs,
+                    kv_dtype)
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     st = lib().rpa_plan(ctypes.byref(handle), _np_ptr(cu), _np_ptr(kv), _np_ptr(win),
@@ -249,6 +255,26 @@ def rpa_write_kv(k_new, v_new, k_pages, v_pages, page_table, cu_q_lens, kv_lens,
         int(num_pages), dtype, _dptr(workspace, "workspace"), _stream_ptr(stream))
     if st != RPA_OK:
         raise RpaError(st, "rpa_write_kv")
+
+
+def rpa_forward_fp8kv(q, k_pages, v_pages, k_scale, v_scale, page_table, cu_q_lens, kv_lens,
+                      window, sm_scale: float, out, plan: Plan, workspace, stream=None) -> None:
+    """rpa_forward_fp8kv: decode over e4m3 K/V pages (uint8 tensors) with
+    float32 per-KV-head scales."""
+    import torch
+    m = plan.meta
+    st = lib().rpa_forward_fp8kv(
+        _dptr(q, "q", torch.bfloat16), _dptr(k_pages, "k_pages", torch.uint8),
+        _dptr(v_pages, "v_pages", torch.uint8), _dptr(k_scale, "k_scale", torch.float32),
+        _dptr(v_scale, "v_scale", torch.float32),
+        _dptr(page_table, "page_table", torch.int32), _dptr(cu_q_lens, "cu_q_lens", torch.int32),
+        _dptr(kv_lens, "kv_lens", torch.int32), m["num_seqs"], m["num_q_heads"],
+        m["num_kv_heads"], m["head_dim"], m["page_size"],
+        _dptr(window, "window", torch.int32), float(sm_scale), _dptr(out, "out", torch.bfloat16),
+        _stream_ptr(stream), plan.handle, _dptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size())
+    if st != RPA_OK:
+        raise RpaError(st, "rpa_forward_fp8kv")
 
 
 def rpa_forward_kv(q, k_new, v_new, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window,
@@ -405,6 +431,35 @@ class ForwardCall:
         st = self._fn(*self._args)
         if st != RPA_OK:
             raise RpaError(st, "rpa_forward")
+
+
+class ForwardFp8Call(ForwardCall):
+    """rpa_forward_fp8kv (decode over e4m3 pages) with its arguments
+    marshalled once."""
+
+    def __init__(self, q, k_fp8, v_fp8, k_scale, v_scale, page_table, cu_q_lens, kv_lens,
+                 window, sm_scale: float, out, plan: Plan, workspace, stream=None):
+        import torch
+        m = plan.meta
+        self._keep = (q, k_fp8, v_fp8, k_scale, v_scale, page_table, cu_q_lens, kv_lens, window,
+                      out, plan, workspace)
+        self._args = (
+            _dptr(q, "q", torch.bfloat16), _dptr(k_fp8, "k_pages", torch.uint8),
+            _dptr(v_fp8, "v_pages", torch.uint8), _dptr(k_scale, "k_scale", torch.float32),
+            _dptr(v_scale, "v_scale", torch.float32),
+            _dptr(page_table, "page_table", torch.int32),
+            _dptr(cu_q_lens, "cu_q_lens", torch.int32),
+            _dptr(kv_lens, "kv_lens", torch.int32), m["num_seqs"], m["num_q_heads"],
+            m["num_kv_heads"], m["head_dim"], m["page_size"],
+            _dptr(window, "window", torch.int32), float(sm_scale),
+            _dptr(out, "out", torch.bfloat16), _stream_ptr(stream), plan.handle,
+            _dptr(workspace, "workspace"), workspace.numel() * workspace.element_size())
+        self._fn = lib().rpa_forward_fp8kv
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != RPA_OK:
+            raise RpaError(st, "rpa_forward_fp8kv")
 
 
 class ForwardKvCall(ForwardCall):

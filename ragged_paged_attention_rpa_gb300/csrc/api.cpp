@@ -66,7 +66,7 @@ rpa_status_t rpa_plan(rpa_plan_t** plan, const int32_t* cu_q_lens_host,
     std::memcpy(&o, opts, static_cast<size_t>(opts->struct_size));
   }
   if (o.q_block < 0 || o.kv_split < 0 || o.num_sms < 0 || o.prefill_pairs < 0 ||
-      o.prefill_pairs > 2)
+      o.prefill_pairs > 2 || o.kv_dtype < 0 || o.kv_dtype > RPA_DTYPE_FP8_E4M3)
     return RPA_ERR_INVALID_ARG;
   rpa_status_t st = rpa::validate_metadata(cu_q_lens_host, kv_lens_host, num_seqs,
                                            page_size, max_pages_per_seq);
@@ -116,7 +116,7 @@ rpa_status_t rpa_plan_get_info(const rpa_plan_t* plan, rpa_plan_info* info) {
   info->prefill_ctas = p.prefill_ctas;
   info->workspace_bytes = static_cast<int64_t>(p.ws_bytes);
   info->prefill_pairs = p.prefill_pairs ? 1 : 0;
-  info->reserved = 0;
+  info->kv_dtype = p.kv_fp8 ? RPA_DTYPE_FP8_E4M3 : p.dtype;
   return RPA_OK;
 }
 
@@ -157,7 +157,7 @@ rpa_status_t rpa_forward(const void* q, const void* k_pages, const void* v_pages
   if (plan == nullptr) return RPA_ERR_INVALID_ARG;
   const rpa::Plan& p = plan->p;
   if (num_seqs != p.num_seqs || num_q_heads != p.hq || num_kv_heads != p.hkv ||
-      head_dim != p.d || page_size != p.p || (window != nullptr) != p.has_window)
+      head_dim != p.d || page_size != p.p || (window != nullptr) != p.has_window || p.kv_fp8)
     return RPA_ERR_PLAN_MISMATCH;
   if (workspace == nullptr || !aligned(workspace, 256)) return RPA_ERR_INVALID_ARG;
   if (workspace_bytes < p.ws_bytes) return RPA_ERR_WORKSPACE_TOO_SMALL;
@@ -172,6 +172,36 @@ rpa_status_t rpa_forward(const void* q, const void* k_pages, const void* v_pages
 
   rpa::Args a{q, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window, sm_scale,
               out, static_cast<unsigned char*>(workspace)};
+  return forward_launch(p, a, nullptr, stream);
+}
+
+rpa_status_t rpa_forward_fp8kv(const void* q, const void* k_pages, const void* v_pages,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* page_table, const int32_t* cu_q_lens,
+                               const int32_t* kv_lens, int32_t num_seqs, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                               const int32_t* window, float sm_scale, void* out,
+                               rpa_stream_t stream, const rpa_plan_t* plan, void* workspace,
+                               size_t workspace_bytes) {
+  if (plan == nullptr) return RPA_ERR_INVALID_ARG;
+  const rpa::Plan& p = plan->p;
+  if (num_seqs != p.num_seqs || num_q_heads != p.hq || num_kv_heads != p.hkv ||
+      head_dim != p.d || page_size != p.p || (window != nullptr) != p.has_window || !p.kv_fp8)
+    return RPA_ERR_PLAN_MISMATCH;
+  if (workspace == nullptr || !aligned(workspace, 256)) return RPA_ERR_INVALID_ARG;
+  if (workspace_bytes < p.ws_bytes) return RPA_ERR_WORKSPACE_TOO_SMALL;
+  if (p.total_q == 0) return RPA_OK;
+  if (q == nullptr || k_pages == nullptr || v_pages == nullptr || k_scale == nullptr ||
+      v_scale == nullptr || page_table == nullptr || cu_q_lens == nullptr ||
+      kv_lens == nullptr || out == nullptr)
+    return RPA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_pages, 128) ||
+      !aligned(v_pages, 128) || !aligned(k_scale, 4) || !aligned(v_scale, 4) ||
+      !aligned(page_table, 4) || !aligned(cu_q_lens, 4) || !aligned(kv_lens, 4) ||
+      !aligned(window, 4))
+    return RPA_ERR_INVALID_ARG;
+  rpa::Args a{q, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window, sm_scale,
+              out, static_cast<unsigned char*>(workspace), k_scale, v_scale};
   return forward_launch(p, a, nullptr, stream);
 }
 
@@ -245,7 +275,7 @@ rpa_status_t rpa_forward_decode_noalloc(const void* q, const void* k_pages,
   if (plan == nullptr) return RPA_ERR_INVALID_ARG;
   const rpa::Plan& p = plan->p;
   if (num_seqs != p.num_seqs || num_q_heads != p.hq || num_kv_heads != p.hkv ||
-      head_dim != p.d || page_size != p.p || (window != nullptr) != p.has_window)
+      head_dim != p.d || page_size != p.p || (window != nullptr) != p.has_window || p.kv_fp8)
     return RPA_ERR_PLAN_MISMATCH;
   if (p.num_prefill > 0 || p.simt_decode || p.dtype != RPA_DTYPE_BF16)
     return RPA_ERR_UNSUPPORTED;

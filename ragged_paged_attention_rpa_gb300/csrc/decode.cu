@@ -65,6 +65,8 @@ struct DecodeParams {
   float* part_lse;    // [2 * total CTAs][G]
   int32_t hq, hkv, group, page_shift, mpps, num_pages;
   float scale_log2;   // sm_scale * log2(e)
+  const float* k_scale;  // fp8 pages: per-KV-head scales (else unused)
+  const float* v_scale;
 };
 
 // One launch's share of the block stream.  seqhead[i] = (sequence << 8) | kv
@@ -132,6 +134,26 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
   return y;
 }
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two e4m3 values (low byte first) -> f16x2 (exact: e4m3 is a subset of f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n"
+      : "=r"(r) : "r"(two));
+  return r;
+}
 __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -140,6 +162,18 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+template <bool FP8>
+__device__ __forceinline__ void mma_t(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                      uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (FP8) mma_f16(c, a0, a1, a2, a3, b0, b1);
+  else mma_bf16(c, a0, a1, a2, a3, b0, b1);
+}
+template <bool FP8>
+__device__ __forceinline__ uint32_t pack_t(float lo, float hi) {
+  if constexpr (FP8) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
+}
+
 
 // Element offset of 16-byte chunk `chunk` of row `row` in a 16-row bf16 tile
 // as TMA writes it: D/64 boxes of [16 rows][64 dims], 128-byte swizzle (the
@@ -159,31 +193,60 @@ __device__ __forceinline__ int seg_of(const DecodeSched<NSEG>& sc, int32_t x) {
   return lo;
 }
 
-template <int D>
+// Shared memory of a decode CTA: per warp a ring of S stages (one 16-key
+// block of K and of V each, as TMA writes them: 128-byte swizzled rows), for
+// fp8 pages a per-warp f16 copy of the block being consumed, two Q tiles and
+// the merge buffers.
+template <int D, bool FP8>
 struct DecodeSmem {
-  static constexpr int S = stages_for(D);
-  static constexpr int TILE = kBlk * D;                         // bf16 elements
-  static constexpr size_t kRing = size_t(kWarps) * S * 2 * TILE * 2;
+  static constexpr int S = FP8 ? 4 : stages_for(D);
+  static constexpr int TILE = kBlk * D;                         // elements of a K (or V) tile
+  static constexpr int ESZ = FP8 ? 1 : 2;                       // bytes per element as stored
+  static constexpr size_t kStageBytes = size_t(2) * TILE * ESZ;
+  static constexpr size_t kRing = size_t(kWarps) * S * kStageBytes;
+  static constexpr size_t kConv = FP8 ? size_t(kWarps) * 2 * TILE * 2 : 0;
   static constexpr size_t kQ = 2 * 8 * D * 2;                   // two Q tiles (G <= 8)
   static constexpr int kORow = D + 4;                           // padded row of the merge buffer
-  static constexpr size_t kO = 2 * 8 * kORow * 4;            // two merge buffers
-  static constexpr size_t kBytes = kRing + kQ + kO + 1024;    // + 1024-byte alignment
+  static constexpr size_t kO = 2 * 8 * kORow * 4;               // two merge buffers
+  static constexpr size_t kBytes = kRing + kConv + kQ + kO + 1024;  // + 1024-byte alignment
 };
 
-template <int D, int NSEG>
+// An fp8 block (16 rows x D bytes, 128-byte swizzled rows of 128 bytes as TMA
+// writes them) -> f16 in the layout swz() reads (16-byte chunks of 8).
+template <int D>
+__device__ __forceinline__ void fp8_tile_to_f16(const unsigned char* src, __nv_bfloat16* dst,
+                                                int lane) {
+  constexpr int kGroups = D / 8;   // 8-element groups per row
+#pragma unroll
+  for (int k = 0; k < (kBlk * kGroups) / 32; ++k) {
+    const int gi = lane + 32 * k;
+    const int r = gi / kGroups, d0 = (gi % kGroups) * 8;
+    const int b = d0 & 127;
+    const uint2 w = *reinterpret_cast<const uint2*>(
+        src + (d0 >> 7) * (kBlk * 128) + r * 128 + ((((b >> 4) ^ (r & 7)) << 4) | (b & 15)));
+    uint4 o;
+    o.x = e4m3x2_to_f16x2(w.x & 0xffffu);
+    o.y = e4m3x2_to_f16x2(w.x >> 16);
+    o.z = e4m3x2_to_f16x2(w.y & 0xffffu);
+    o.w = e4m3x2_to_f16x2(w.y >> 16);
+    *reinterpret_cast<uint4*>(dst + swz(r, d0 >> 3)) = o;
+  }
+}
+
+template <int D, int NSEG, bool FP8>
 __global__ void __launch_bounds__(kWarps * 32, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc) {
-  using L = DecodeSmem<D>;
+  using L = DecodeSmem<D, FP8>;
   constexpr int S = L::S;
   constexpr int KT = D / 16;        // k-steps of the score MMA, m-tiles of the PV MMA
   constexpr int TILE = L::TILE;
   extern __shared__ __align__(128) unsigned char smem_dyn[];
   unsigned char* smem_raw = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
-  __nv_bfloat16* rings = reinterpret_cast<__nv_bfloat16*>(smem_raw);
-  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smem_raw + L::kRing);
-  float* so = reinterpret_cast<float*>(smem_raw + L::kRing + L::kQ);
+  __nv_bfloat16* conv = reinterpret_cast<__nv_bfloat16*>(smem_raw + L::kRing);
+  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smem_raw + L::kRing + L::kConv);
+  float* so = reinterpret_cast<float*>(smem_raw + L::kRing + L::kConv + L::kQ);
   __shared__ int32_t s_pages[kMaxCtaPages];
   __shared__ SegInfo s_seg[kMaxCtaSegs];
   __shared__ uint32_t valid_mask[kWarps][S];
@@ -276,7 +339,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   }
   __syncthreads();
 
-  __nv_bfloat16* ring = rings + warp * S * 2 * TILE;
+  unsigned char* ring = smem_raw + warp * S * L::kStageBytes;
   volatile int* abort = &s_abort;
   // Issue cursor over this warp's blocks: segment ist, local block isj.
   int ist = 0, isj = warp;
@@ -297,15 +360,17 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       // Rows of the block: page * P + (key0 % P); a bad page reads zeros.
       const int32_t row = page >= 0 ? page * (1 << p.page_shift) + (key0 & ((1 << p.page_shift) - 1))
                                     : -kBlk;
-      __nv_bfloat16* kt = ring + st * 2 * TILE;
-      __nv_bfloat16* vt = kt + TILE;
+      unsigned char* kt = ring + st * L::kStageBytes;
+      unsigned char* vt = kt + TILE * L::ESZ;
       // Earlier generic-proxy reads of this stage come before the async writes.
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      sm100::mbar_arrive_expect_tx(&full_bar[warp][st], 2 * kBlk * D * 2);
+      sm100::mbar_arrive_expect_tx(&full_bar[warp][st], static_cast<uint32_t>(L::kStageBytes));
+      // Boxes of 128-byte rows: 64 bf16 or 128 fp8 elements.
+      constexpr int kBoxElems = 128 / L::ESZ;
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        sm100::tma_load_3d(kt + c * kBlk * 64, &tm_k, &full_bar[warp][st], c * 64, si.g, row);
-        sm100::tma_load_3d(vt + c * kBlk * 64, &tm_v, &full_bar[warp][st], c * 64, si.g, row);
+      for (int c = 0; c < D / kBoxElems; ++c) {
+        sm100::tma_load_3d(kt + c * kBlk * 128, &tm_k, &full_bar[warp][st], c * kBoxElems, si.g, row);
+        sm100::tma_load_3d(vt + c * kBlk * 128, &tm_v, &full_bar[warp][st], c * kBoxElems, si.g, row);
       }
     }
     ++issued;
@@ -347,8 +412,18 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         const int d0 = kt * 16 + 2 * (lane & 3);
         qf[kt][0] = hv ? *reinterpret_cast<const uint32_t*>(qr + d0) : 0u;
         qf[kt][1] = hv ? *reinterpret_cast<const uint32_t*>(qr + d0 + 8) : 0u;
+        if constexpr (FP8) {
+          // bf16 pairs -> f16 pairs for the f16 products with the fp8 pages.
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            qf[kt][i] = pack_f16x2(__uint_as_float(qf[kt][i] << 16),
+                                   __uint_as_float(qf[kt][i] & 0xffff0000u));
+        }
       }
     }
+    // fp8 pages: the K scale joins the logit scale, the V scale the output.
+    const float sl2 = FP8 ? p.scale_log2 * __ldg(p.k_scale + si.g) : p.scale_log2;
+    const float vsc = FP8 ? __ldg(p.v_scale + si.g) : 1.f;
     float m[2] = {-INFINITY, -INFINITY};  // running max (log2 domain), heads 2(lane%4)+j
     float l[2] = {0.f, 0.f};              // this lane's share of the running sum
     float o[KT][4];
@@ -362,8 +437,20 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         if (lane == 0) report_error(p.ws, RPA_DEVERR_TIMEOUT, c);
         break;
       }
-      const __nv_bfloat16* kt = ring + st * 2 * TILE;
-      const __nv_bfloat16* vt = kt + TILE;
+      const __nv_bfloat16* kt;
+      const __nv_bfloat16* vt;
+      if constexpr (FP8) {
+        // The block as f16 in this warp's copy (the stage is then free).
+        __nv_bfloat16* ck = conv + warp * 2 * TILE;
+        fp8_tile_to_f16<D>(ring + st * L::kStageBytes, ck, lane);
+        fp8_tile_to_f16<D>(ring + st * L::kStageBytes + TILE, ck + TILE, lane);
+        __syncwarp();
+        kt = ck;
+        vt = ck + TILE;
+      } else {
+        kt = reinterpret_cast<const __nv_bfloat16*>(ring + st * L::kStageBytes);
+        vt = kt + TILE;
+      }
       const uint32_t vmask = valid_mask[warp][st];
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
       {
@@ -373,17 +460,17 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         for (int kt2 = 0; kt2 < KT; ++kt2) {
           uint32_t a0, a1, a2, a3;
           ldsm_x4(smem_u32(kt + swz(row, 2 * kt2 + hi)), a0, a1, a2, a3);
-          if (kt2 & 1) mma_bf16(sb, a0, a1, a2, a3, qf[kt2][0], qf[kt2][1]);
-          else mma_bf16(sa, a0, a1, a2, a3, qf[kt2][0], qf[kt2][1]);
+          if (kt2 & 1) mma_t<FP8>(sb, a0, a1, a2, a3, qf[kt2][0], qf[kt2][1]);
+          else mma_t<FP8>(sa, a0, a1, a2, a3, qf[kt2][0], qf[kt2][1]);
         }
       }
       const int r_top = lane >> 2, r_bot = r_top + 8;
       const bool v_top = (vmask >> r_top) & 1u, v_bot = (vmask >> r_bot) & 1u;
       float x[4];
-      x[0] = v_top ? (sa[0] + sb[0]) * p.scale_log2 : -INFINITY;
-      x[1] = v_top ? (sa[1] + sb[1]) * p.scale_log2 : -INFINITY;
-      x[2] = v_bot ? (sa[2] + sb[2]) * p.scale_log2 : -INFINITY;
-      x[3] = v_bot ? (sa[3] + sb[3]) * p.scale_log2 : -INFINITY;
+      x[0] = v_top ? (sa[0] + sb[0]) * sl2 : -INFINITY;
+      x[1] = v_top ? (sa[1] + sb[1]) * sl2 : -INFINITY;
+      x[2] = v_bot ? (sa[2] + sb[2]) * sl2 : -INFINITY;
+      x[3] = v_bot ? (sa[3] + sb[3]) * sl2 : -INFINITY;
       float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
@@ -406,8 +493,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         o[mt][2] *= al0;
         o[mt][3] *= al1;
       }
-      const uint32_t b0 = transpose8x8(pack_bf16x2(p0, p1));
-      const uint32_t b1 = transpose8x8(pack_bf16x2(p2, p3));
+      const uint32_t b0 = transpose8x8(pack_t<FP8>(p0, p1));
+      const uint32_t b1 = transpose8x8(pack_t<FP8>(p2, p3));
       {
         const int row = (lane & 7) + ((lane >> 4) << 3);
         const int hi = (lane >> 3) & 1;
@@ -415,7 +502,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         for (int mt = 0; mt < KT; ++mt) {
           uint32_t a0, a1, a2, a3;
           ldsm_x4_t(smem_u32(vt + swz(row, 2 * mt + hi)), a0, a1, a2, a3);
-          mma_bf16(o[mt], a0, a1, a2, a3, b0, b1);
+          mma_t<FP8>(o[mt], a0, a1, a2, a3, b0, b1);
         }
       }
       __syncwarp();
@@ -489,7 +576,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
       for (int w = 0; w < kWarps; ++w)
         Lsum += (wm[w][h] == -INFINITY) ? 0.f : wl[w][h] * fast_exp2(wm[w][h] - M);
-      const float inv = 1.f / Lsum;
+      const float inv = vsc / Lsum;
       const float* s0 = so + h * L::kORow + d;
       const float* s1 = s0 + 8 * L::kORow;
       const float4 u = make_float4((s0[0] + s1[0]) * inv, (s0[1] + s1[1]) * inv,
@@ -628,13 +715,13 @@ int launch_combine(const Plan& plan, const DecodeParams& p, const Plan::DecodeLa
   return 0;
 }
 
-template <int D, int NSEG>
+template <int D, int NSEG, bool FP8>
 int launch_one(const Plan& plan, const DecodeParams& p, const CUtensorMap& tk,
                const CUtensorMap& tv, const Plan::DecodeLaunch& dl, cudaStream_t stream) {
-  constexpr size_t smem = DecodeSmem<D>::kBytes;
+  constexpr size_t smem = DecodeSmem<D, FP8>::kBytes;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, NSEG>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, NSEG, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return static_cast<int>(e);
@@ -662,7 +749,7 @@ int launch_one(const Plan& plan, const DecodeParams& p, const CUtensorMap& tk,
   }
   sc.blk0[n] = plan.dseg_blk0[dl.seg_end] - base;
   sc.n_blocks = sc.blk0[n];
-  decode_kernel<D, NSEG><<<dl.n_ctas, kWarps * 32, smem, stream>>>(tk, tv, p, sc);
+  decode_kernel<D, NSEG, FP8><<<dl.n_ctas, kWarps * 32, smem, stream>>>(tk, tv, p, sc);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return static_cast<int>(e);
   trace_mark(RPA_KERNEL_DECODE_SPLIT, stream);
@@ -692,16 +779,27 @@ int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   p.mpps = plan.mpps;
   p.num_pages = plan.num_pages;
   p.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
   CUtensorMap tk, tv;
   const uint64_t rows = static_cast<uint64_t>(plan.num_pages) * plan.p;
-  if (!make_tmap_3d(&tk, a.k_pages, D, plan.hkv, rows, 1, kBlk) ||
-      !make_tmap_3d(&tv, a.v_pages, D, plan.hkv, rows, 1, kBlk))
+  const bool fp8 = plan.kv_fp8;
+  if (fp8 ? (!make_tmap_3d_u8(&tk, a.k_pages, D, plan.hkv, rows, 1, kBlk) ||
+             !make_tmap_3d_u8(&tv, a.v_pages, D, plan.hkv, rows, 1, kBlk))
+          : (!make_tmap_3d(&tk, a.k_pages, D, plan.hkv, rows, 1, kBlk) ||
+             !make_tmap_3d(&tv, a.v_pages, D, plan.hkv, rows, 1, kBlk)))
     return static_cast<int>(cudaErrorInvalidValue);
   for (const Plan::DecodeLaunch& dl : plan.dlaunch) {
     const int n = dl.seg_end - dl.seg_begin;
-    int err = n <= kDecodeSegSmall
-                  ? launch_one<D, kDecodeSegSmall>(plan, p, tk, tv, dl, stream)
-                  : launch_one<D, kDecodeSegLarge>(plan, p, tk, tv, dl, stream);
+    int err;
+    if (fp8)
+      err = n <= kDecodeSegSmall
+                ? launch_one<D, kDecodeSegSmall, true>(plan, p, tk, tv, dl, stream)
+                : launch_one<D, kDecodeSegLarge, true>(plan, p, tk, tv, dl, stream);
+    else
+      err = n <= kDecodeSegSmall
+                ? launch_one<D, kDecodeSegSmall, false>(plan, p, tk, tv, dl, stream)
+                : launch_one<D, kDecodeSegLarge, false>(plan, p, tk, tv, dl, stream);
     if (!err) err = launch_combine<D>(plan, p, dl, stream);
     if (err) return err;
   }

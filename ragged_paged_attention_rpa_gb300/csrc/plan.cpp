@@ -295,6 +295,15 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
   }
   int32_t ndec = 0;
   for (int32_t s = 0; s < plan.num_seqs; ++s) ndec += (cu[s + 1] - cu[s] == 1);
+  // fp8 (e4m3) K/V pages: the split-KV decode kernel only.
+  if (opts.kv_dtype != 0 && opts.kv_dtype != plan.dtype) {
+    if (opts.kv_dtype != RPA_DTYPE_FP8_E4M3) return RPA_ERR_INVALID_ARG;
+    // fp8 rows are fetched in 128-byte boxes: head_dim a multiple of 128.
+    if (plan.dtype != RPA_DTYPE_BF16 || want == RPA_PATH_SIMT || plan.num_prefill > 0 ||
+        !tc_decode || plan.d % 128 != 0)
+      return RPA_ERR_UNSUPPORTED;
+  }
+  plan.kv_fp8 = opts.kv_dtype == RPA_DTYPE_FP8_E4M3;
   if (want == RPA_PATH_TC) {
     if ((ndec > 0 && !tc_decode) || (plan.num_prefill > 0 && !tc_prefill))
       return RPA_ERR_UNSUPPORTED;

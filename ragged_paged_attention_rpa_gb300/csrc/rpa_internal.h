@@ -44,6 +44,7 @@ struct Plan {
   // Problem description (checked against every rpa_forward call).
   int32_t num_seqs = 0, hq = 0, hkv = 0, d = 0, p = 0, mpps = 0, num_pages = 0;
   int32_t dtype = RPA_DTYPE_BF16;
+  bool kv_fp8 = false;               // K/V pages are e4m3 bytes (decode only)
   bool has_window = false;
   int64_t total_q = 0;
 
@@ -116,6 +117,8 @@ struct Args {
   float sm_scale;
   void* out;
   unsigned char* workspace;
+  const float* k_scale = nullptr;  // fp8 pages: per-KV-head scales of K and V
+  const float* v_scale = nullptr;
 };
 
 // Kernel launchers; each returns cudaError_t as int (0 = success).
@@ -159,5 +162,8 @@ bool decode_supported(int32_t head_dim, int32_t group, int32_t page_size);
 bool tmap_available();
 bool make_tmap_3d(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid, uint64_t outer,
                   uint32_t box_mid, uint32_t box_outer);
+// The same over a byte tensor (fp8 pages), box (128, box_mid, box_outer).
+bool make_tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid, uint64_t outer,
+                     uint32_t box_mid, uint32_t box_outer);
 
 }  // namespace rpa

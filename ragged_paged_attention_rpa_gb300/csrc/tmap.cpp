@@ -47,4 +47,18 @@ bool make_tmap_3d(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid, ui
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid, uint64_t outer,
+                     uint32_t box_mid, uint32_t box_outer) {
+  EncodeFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {d, mid, outer};
+  cuuint64_t strides[2] = {d, d * mid};
+  cuuint32_t box[3] = {128, box_mid, box_outer};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace rpa

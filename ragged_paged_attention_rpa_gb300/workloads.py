@@ -36,6 +36,12 @@ class Batch:
     window: Optional[np.ndarray]  # [num_seqs] int32 (<= 0: full causal) or None
     sm_scale: float
     seed: int
+    # fp8 (e4m3) copies of the pools and their per-KV-head scales, when the
+    # batch is meant for the fp8 decode path (see with_fp8_kv).
+    k_fp8: Optional[np.ndarray] = None    # [num_pages, P, Hkv, D] uint8
+    v_fp8: Optional[np.ndarray] = None
+    k_scale: Optional[np.ndarray] = None  # [Hkv] float32
+    v_scale: Optional[np.ndarray] = None
 
     @property
     def num_seqs(self) -> int:
@@ -204,3 +210,44 @@ WORKLOADS = {
     "causal_prefill": lambda seed=3, **kw: prefill_8k(seed=seed, window=0, **kw),
     "mixed": mixed_batch,
 }
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """float -> OCP fp8 e4m3 codes (uint8): round to nearest even, saturating
+    at +-448 (exponent bias 7, 3 mantissa bits, subnormals 2^-9 apart)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    e = np.clip(np.floor(np.log2(np.maximum(a, 2.0 ** -10))), -6, 8)
+    q = np.minimum(np.round(a / 2.0 ** (e - 3)) * 2.0 ** (e - 3), 448.0)
+    sub = q < 2.0 ** -6
+    E = np.floor(np.log2(np.maximum(q, 2.0 ** -6)))
+    m_norm = np.round(q / 2.0 ** E * 8.0 - 8.0)
+    e_field = np.where(sub, 0, E + 7)
+    m_field = np.where(sub, np.round(q / 2.0 ** -9), m_norm)
+    code = (e_field.astype(np.uint8) << 3) | m_field.astype(np.uint8)
+    return code | (np.signbit(x).astype(np.uint8) << 7)
+
+
+def with_fp8_kv(b: Batch) -> Batch:
+    """The batch with e4m3 copies of its K/V pools: per KV head, scale =
+    max |value| / 448 over the pool, code = e4m3(value / scale)."""
+    def quant(pool):
+        if pool.dtype == np.uint16:                      # bf16 bits -> float32
+            vals = (pool.astype(np.uint32) << 16).view(np.float32)
+        else:
+            vals = pool.astype(np.float32)
+        hkv = pool.shape[2]
+        scale = np.empty(hkv, dtype=np.float32)
+        codes = np.empty(pool.shape, dtype=np.uint8)
+        for g in range(hkv):
+            m = float(np.abs(vals[:, :, g, :]).max())
+            scale[g] = np.float32(m / 448.0 if m > 0 else 1.0)
+            codes[:, :, g, :] = e4m3_encode(vals[:, :, g, :] / scale[g])
+        return codes, scale
+    kf, ks = quant(b.k_pages)
+    vf, vs = quant(b.v_pages)
+    return dataclasses.replace(b, name=b.name + "_fp8kv", k_fp8=kf, v_fp8=vf, k_scale=ks,
+                               v_scale=vs)
+
+
+WORKLOADS["decode_fp8"] = lambda seed=1, **kw: with_fp8_kv(decode_batch(seed=seed, **kw))

@@ -26,7 +26,7 @@ def built():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(rpa_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(rpa_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_binding_exports():
@@ -230,3 +230,21 @@ def test_forward_checks_before_any_launch():
     bad = list(args)
     bad[1] = ctypes.c_void_p((1 << 20) + 64)              # k_pages not 128-B aligned
     assert L.rpa_forward(*bad) == binding.RPA_ERR_INVALID_ARG
+
+
+def test_fp8_kv_plans_are_decode_only():
+    b = workloads.make_batch([1, 1, 1], [40, 900, 7], num_q_heads=8, num_kv_heads=1,
+                             head_dim=256, page_size=128, meta_only=True)
+    info = plan_of(b, kv_dtype=binding.RPA_DTYPE_FP8_E4M3).info()
+    assert info["kv_dtype"] == binding.RPA_DTYPE_FP8_E4M3 and info["path"] == RPA_PATH_TC
+    assert plan_of(b).info()["kv_dtype"] == binding.RPA_DTYPE_BF16
+    mixed = workloads.make_batch([1, 5], [40, 9], num_q_heads=8, num_kv_heads=1,
+                                 head_dim=256, page_size=128, meta_only=True)
+    with pytest.raises(RpaError) as e:
+        plan_of(mixed, kv_dtype=binding.RPA_DTYPE_FP8_E4M3)
+    assert e.value.status == binding.RPA_ERR_UNSUPPORTED
+    d64 = workloads.make_batch([1, 1], [40, 9], num_q_heads=8, num_kv_heads=1, head_dim=64,
+                               page_size=16, meta_only=True)
+    with pytest.raises(RpaError) as e:
+        plan_of(d64, kv_dtype=binding.RPA_DTYPE_FP8_E4M3)
+    assert e.value.status == binding.RPA_ERR_UNSUPPORTED
