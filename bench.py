@@ -8,12 +8,20 @@ A step is one rpa_forward over one seeded synthetic batch (every kernel of the
 hot path for that batch: split-KV decode + log-sum-exp combine for decode
 sequences, prefill for the rest), with q, the KV pages and the metadata
 resident in HBM and the plan built once for the batch, as a serving step
-reuses one plan for every layer.  L2 is flushed before every timed step (a
-256 MiB write, then a 256 MiB read so that the written lines' write-back to HBM
-falls outside the step); each step is bracketed by CUDA events on the
-launching stream.
-The host enqueues the timed loop behind a GPU sleep so that launch latency does
-not leak into the device timing.
+reuses one plan for every layer.  For inputs smaller than L2, L2 is flushed
+before every timed step (a 256 MiB write, then a 256 MiB read so that the
+written lines' write-back to HBM falls outside the step) and each step is
+bracketed by CUDA events on the launching stream.
+When one step's inputs exceed L2 (the decode batch reads 150 MB, the 8k
+prefills more) the timed steps rotate over R disjoint copies of the inputs
+instead: no step finds its data in L2, no flush is needed, and one event pair
+brackets the K steps (an event record costs about 2-3 us of device time on
+these machines, a large share of a 35 us step).  `flushed_step_ms` reports the
+flush-and-event-pair-per-step time beside it; `--flush` makes it the headline.
+The K timed steps are captured into one CUDA graph and replayed once, as a
+serving loop replays its decode step (kernel-to-kernel gaps of about 0.5-0.9
+us instead of about 2-3 us for stream launches); `--no-graph` enqueues the
+same loop from Python behind a GPU sleep instead.
 
 The default workload is the decode batch: 128 sequences with one query each,
 KV lengths uniform in [128, 2048], 8 query heads sharing one KV head of
@@ -38,6 +46,7 @@ import csv
 import hashlib
 import io
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -270,6 +279,12 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--q-block", type=int, default=0)
     ap.add_argument("--kv-split", type=int, default=0)
+    ap.add_argument("--flush", action="store_true",
+                    help="flush L2 before every step and time each step with its own "
+                         "event pair, even when a step's inputs exceed L2")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="enqueue the timed steps from Python instead of replaying them "
+                         "from a CUDA graph")
     ap.add_argument("--kv-write", action="store_true",
                     help="time rpa_forward_kv: write the step's new K/V rows into their "
                          "pages, then attend")
@@ -352,20 +367,57 @@ def main():
                    kv_dtype=binding.RPA_DTYPE_FP8_E4M3 if fp8 else 0)
     info = plan.info()
     ws = binding.alloc_workspace(plan)
-    fwd = db.call(plan, ws)
-    if fp8:
-        fp8_dev = [torch.from_numpy(x).cuda() for x in (b.k_fp8, b.v_fp8, b.k_scale, b.v_scale)]
-        fwd = binding.ForwardFp8Call(db.q, *fp8_dev, db.page_table, db.cu_q_lens, db.kv_lens,
-                                     db.window, b.sm_scale, db.out, plan, ws)
-    if args.kv_write:
-        k_new, v_new = new_token_rows(b, db, torch)
-        fwd = binding.ForwardKvCall(db.q, k_new, v_new, db.k_pages, db.v_pages, db.page_table,
-                                    db.cu_q_lens, db.kv_lens, db.window, b.sm_scale, db.out,
-                                    plan, ws)
+    fp8_dev = ([torch.from_numpy(x).cuda() for x in (b.k_fp8, b.v_fp8, b.k_scale, b.v_scale)]
+               if fp8 else None)
+    kv_new = None if not args.kv_write else new_token_rows(b, db, torch)
+
+    # Step inputs.  When one step's inputs exceed L2, the timed steps rotate
+    # over R disjoint copies of them (KV pools stacked R times with the page
+    # table shifted by r * num_pages, q and out per copy): the data a step
+    # reads were last touched R - 1 steps (more than 3 x L2 bytes) earlier,
+    # so no L2 flush is needed and one event pair brackets all K steps.
+    # Otherwise (or with --flush) there is one copy and L2 is flushed before
+    # every step, each step bracketed by its own event pair.
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 0)) \
+        or (126 << 20)
+    R = 0 if (args.flush or counts["bytes"] < l2_bytes) else \
+        max(2, math.ceil(3 * l2_bytes / counts["bytes"]))
+    N = b.num_pages
+    if R:
+        rplan = binding.rpa_plan(b.cu_q_lens, b.kv_lens, b.window, b.num_q_heads,
+                                 b.num_kv_heads, b.head_dim, b.page_size,
+                                 b.max_pages_per_seq, R * N, dtype=db.dtype,
+                                 q_block=args.q_block, kv_split=args.kv_split,
+                                 kv_dtype=binding.RPA_DTYPE_FP8_E4M3 if fp8 else 0)
+        pools = [torch.cat([x] * R) for x in
+                 ((fp8_dev[0], fp8_dev[1]) if fp8 else (db.k_pages, db.v_pages))]
+        copies = [dict(q=db.q if r == 0 else db.q.clone(),
+                       out=db.out if r == 0 else torch.empty_like(db.out),
+                       pt=torch.where(db.page_table >= 0, db.page_table + r * N,
+                                      db.page_table).contiguous())
+                  for r in range(R)]
+    else:
+        rplan, pools = plan, ((fp8_dev[0], fp8_dev[1]) if fp8 else (db.k_pages, db.v_pages))
+        copies = [dict(q=db.q, out=db.out, pt=db.page_table)]
+
+    def make_call(r=0):
+        # Copy r's call object, bound to the current stream (inside a graph
+        # capture: the capture stream).
+        c = copies[r]
+        if kv_new is not None:
+            return binding.ForwardKvCall(c["q"], kv_new[0], kv_new[1], pools[0], pools[1],
+                                         c["pt"], db.cu_q_lens, db.kv_lens, db.window,
+                                         b.sm_scale, c["out"], rplan, ws)
+        if fp8:
+            return binding.ForwardFp8Call(c["q"], pools[0], pools[1], fp8_dev[2], fp8_dev[3],
+                                          c["pt"], db.cu_q_lens, db.kv_lens, db.window,
+                                          b.sm_scale, c["out"], rplan, ws)
+        return binding.ForwardCall(c["q"], pools[0], pools[1], c["pt"], db.cu_q_lens,
+                                   db.kv_lens, db.window, b.sm_scale, c["out"], rplan, ws)
+
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     evict = torch.ones(32 << 20, dtype=torch.int64, device="cuda")   # 256 MiB
     stream = torch.cuda.current_stream()
-
     flushes = [0]
 
     def flush_l2():
@@ -376,50 +428,129 @@ def main():
         flush.fill_(flushes[0] & 0x7F)
         evict.sum()
 
-    # Warm-up (untimed).
-    for _ in range(max(3, args.warmup)):
-        flush_l2()
-        fwd()
+    def capture(n, events=None, flushed=False):
+        # A CUDA graph of n steps (copies in rotation; with `flushed`, an L2
+        # flush before each; with `events`, event pair k around step k).
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            calls = [make_call(r) for r in range(len(copies))]
+            for k in range(n):
+                if flushed:
+                    flush_l2()
+                if events is not None:
+                    events[k][0].record()
+                calls[k % len(calls)]()
+                if events is not None:
+                    events[k][1].record()
+        return g
+
+    # Warm-up (untimed): eager, then from a graph.
+    calls = [make_call(r) for r in range(len(copies))]
+    for k in range(max(3, args.warmup)):
+        if not R:
+            flush_l2()
+        calls[k % len(calls)]()
     torch.cuda.synchronize()
     if binding.rpa_get_device_error(ws) != 0:
         raise SystemExit("device error word set during warm-up")
 
-    # Timed region: K steps, each bracketed by events; enqueued behind a sleep.
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
+    use_graph = not args.no_graph
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+
+    def timed_per_step_events(n, flushed):
+        # n steps, each bracketed by its own event pair (graph or stream).
+        evs = [(torch.cuda.Event(enable_timing=True, external=use_graph),
+                torch.cuda.Event(enable_timing=True, external=use_graph)) for _ in range(n)]
+        g = capture(n, evs, flushed) if use_graph else None
+        if g is not None:
+            capture(max(3, args.warmup), None, flushed).replay()
+        torch.cuda.synchronize()
+        return evs, g
+
+    if R:
+        graph = capture(K) if use_graph else None
+        if graph is not None:
+            capture(max(3, args.warmup)).replay()
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_stop = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+    else:
+        ev, graph = timed_per_step_events(K, flushed=True)
     with ClockSampler(gpu_index) as clocks:
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
-        torch.cuda._sleep(int(2e6))
-        for k in range(K):
-            flush_l2()
-            ev[k][0].record(stream)
-            fwd()
-            ev[k][1].record(stream)
+        if R:
+            if graph is None:
+                torch.cuda._sleep(int(2e6))
+            e_start.record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                for k in range(K):
+                    calls[k % R]()
+            e_stop.record(stream)
+        elif graph is not None:
+            graph.replay()
+        else:
+            torch.cuda._sleep(int(2e6))
+            for k in range(K):
+                flush_l2()
+                ev[k][0].record(stream)
+                calls[0]()
+                ev[k][1].record(stream)
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
-    step_ms = [a.elapsed_time(e) for a, e in ev]
-    total_ms = float(sum(step_ms))
+    if R:
+        total_ms = e_start.elapsed_time(e_stop)
+        step_ms = None
+    else:
+        step_ms = [a.elapsed_time(e) for a, e in ev]
+        total_ms = float(sum(step_ms))
     if dist is not None:
         t = torch.tensor([total_ms], dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     if binding.rpa_get_device_error(ws) != 0:
         raise SystemExit("device error word set during the timed region")
+    if R:
+        for c in copies[1:]:
+            if not torch.equal(c["out"].view(torch.int16), copies[0]["out"].view(torch.int16)):
+                raise SystemExit("input copies gave different outputs")
+
+    # For comparison (not the headline): L2 flushed and an event pair around
+    # every step.
+    flushed_ms = None
+    if R and rank == 0:
+        nf = min(K, 300)
+        evf, gf = timed_per_step_events(nf, flushed=True)
+        torch.cuda.synchronize()
+        if gf is not None:
+            gf.replay()
+        else:
+            for k in range(nf):
+                flush_l2()
+                evf[k][0].record(stream)
+                calls[k % R]()
+                evf[k][1].record(stream)
+        torch.cuda.synchronize()
+        flushed_ms = statistics.mean(a.elapsed_time(e) for a, e in evf)
 
     # Kernel durations from the library's trace events (a separate pass of the
     # same loop, so the events do not touch the headline timing).
     n_trace = min(K, 500)
     binding.rpa_trace_begin(8 * n_trace)
-    torch.cuda._sleep(int(2e6))
-    for _ in range(n_trace):
-        flush_l2()
-        fwd()
+    if use_graph:
+        capture(n_trace, None, flushed=not R).replay()
+    else:
+        torch.cuda._sleep(int(2e6))
+        for k in range(n_trace):
+            if not R:
+                flush_l2()
+            calls[k % len(calls)]()
     torch.cuda.synchronize()
     recs = binding.rpa_trace_end(8 * n_trace)
     per_kernel = {}
@@ -486,8 +617,16 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if b.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": b.name, "seed": b.seed,
-                   "l2": "flushed before every timed step (256 MiB write, then a 256 MiB read that evicts the dirty lines)",
+                   "l2": ("no flush: one step reads %.0f MB (> %.0f MB of L2) and the steps rotate "
+                          "over %d disjoint copies of the inputs (KV pools, page tables, q, out), "
+                          "so a step's data were last touched %.0f MB earlier; one event pair "
+                          "around the K steps" % (counts["bytes"] / 1e6, l2_bytes / 1e6, R,
+                                                  (R - 1) * counts["bytes"] / 1e6)) if R else
+                         "flushed before every timed step (256 MiB write, then a 256 MiB read "
+                         "that evicts the dirty lines); an event pair around every step",
                    "parallelism": "replicas" if world > 1 else "single GPU",
+                   "launch": "stream (Python loop behind a GPU sleep)" if args.no_graph else
+                             "CUDA graph of the K timed steps, replayed once",
                    "step": "rpa_forward_kv (KV-cache write of the new tokens, then attention)"
                            if args.kv_write else ("rpa_forward_fp8kv" if b.k_fp8 is not None
                                                   else "rpa_forward"),
@@ -504,8 +643,9 @@ def main():
         "e2e": e2e,
         "gpu_launches": int(round(launches_per_step * K)),
         "clocks": clocks.summary(),
-        "step_ms_p50": statistics.median(step_ms),
-        "step_ms_min": min(step_ms),
+        "step_ms_p50": statistics.median(step_ms) if step_ms else None,
+        "step_ms_min": min(step_ms) if step_ms else None,
+        "flushed_step_ms": flushed_ms,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -197,6 +197,11 @@ rpa_status_t rpa_plan_get_info(const rpa_plan_t* plan, rpa_plan_info* info);
  * cut across its CTAs, the log-sum-exp combine kernel (a programmatic
  * dependent launch), then the tensor-core prefill and the CUDA-core path, as
  * the batch needs, and returns without waiting for them.
+ * CUDA graphs: the call only enqueues kernel launches (no allocation, copy
+ * or synchronisation), so it may be captured into a CUDA graph on `stream`;
+ * every replay reruns the attention on the same buffers with the schedule
+ * the plan held at capture (kernel parameters are baked into the graph), so
+ * a new plan needs a new capture.
  */
 rpa_status_t rpa_forward(const void* q, const void* k_pages, const void* v_pages,
                          const int32_t* page_table, const int32_t* cu_q_lens,
@@ -316,7 +321,9 @@ rpa_status_t rpa_forward_decode_noalloc(const void* q, const void* k_pages,
  * every rpa_forward call records a CUDA event on its stream before its first
  * kernel and after each kernel it launches, so that the device time of each
  * launch can be read back.  Tracing state is process-wide and not thread-safe;
- * tracing adds one event record per launch to the stream.
+ * tracing adds one event record per launch to the stream.  A call captured
+ * into a CUDA graph while tracing records its marks as event-record nodes of
+ * the graph; rpa_trace_end then reads the times of the last replay.
  *
  * rpa_trace_begin: start recording up to `capacity` launches (1..65536).
  * rpa_trace_end: synchronise on the recorded events, write up to *count

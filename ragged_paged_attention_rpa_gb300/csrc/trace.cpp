@@ -1,5 +1,6 @@
 // Kernel tracing for rpa_forward (rpa_trace_begin / rpa_trace_end): CUDA
-// events recorded around each launch on the caller's stream.
+// events recorded around each launch on the caller's stream, or event-record
+// nodes when the stream is being captured into a CUDA graph.
 #include <cuda_runtime.h>
 
 #include <vector>
@@ -33,7 +34,13 @@ cudaEvent_t take_event() {
 void record(int kernel, void* stream) {
   cudaEvent_t e = take_event();
   if (e == nullptr) return;
-  if (cudaEventRecord(e, static_cast<cudaStream_t>(stream)) != cudaSuccess) return;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Under stream capture the mark becomes an event-record node of the graph
+  // (recorded on every replay); otherwise a plain record.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return;
+  const unsigned flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0u;
+  if (cudaEventRecordWithFlags(e, s, flags) != cudaSuccess) return;
   g_marks.push_back({kernel, e});
 }
 
