@@ -38,6 +38,8 @@
 // partial (O / l and log2-sum-exp).  A second kernel, launched as a
 // programmatic dependent, combines the partials of every cut segment:
 // out = sum_c 2^(lse_c - M) O_c / sum_c 2^(lse_c - M).
+#include <algorithm>
+
 #include "common.cuh"
 #include "rpa_internal.h"
 #include "sm100_ptx.cuh"
@@ -76,7 +78,8 @@ struct DecodeParams {
 template <int NSEG>
 struct DecodeSched {
   int32_t n_seg, bpc, n_blocks, slot_base, seg_base, n_ctas;
-  int32_t cta0[kMaxDecodeCtas + 1];
+  int32_t cta0[kMaxDecodeGrid + 1];
+  int32_t cta_seg[kMaxDecodeGrid];   // first segment | last segment << 16
   int32_t seqhead[NSEG];
   int32_t blk0[NSEG + 1];
   // From the plan's host metadata (validated there): query token, first
@@ -110,7 +113,6 @@ struct SegInfo {
   int32_t npg;           // pages of this part
   int32_t whole;         // the segment lies entirely in this CTA's range
   int32_t gseg;          // segment index in the launch
-  int32_t bad;           // device metadata disagree with the plan: skipped
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -251,7 +253,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   __shared__ SegInfo s_seg[kMaxCtaSegs];
   __shared__ uint32_t valid_mask[kWarps][S];
   __shared__ float wm[kWarps][8], wl[kWarps][8];
-  __shared__ int s_nseg, s_abort;
+  __shared__ int s_npages, s_abort;
   __shared__ __align__(8) uint64_t full_bar[kWarps][S];
   __shared__ __align__(8) uint64_t q_bar[2];   // Q buffer t & 1 holds segment t's queries
 
@@ -263,8 +265,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   const int32_t cb0 = range_start(sc, c);
   const int32_t cb1 = range_start(sc, c + 1);
   if (cb0 >= cb1) return;
-  const int kfirst = seg_of(sc, cb0);
-  const int klast = seg_of(sc, cb1 - 1);
+  // First and last segment of the range: from the plan's per-CTA table, or
+  // by search for ranges of a fixed block count.
+  const int kfirst = sc.bpc > 0 ? seg_of(sc, cb0) : (sc.cta_seg[c] & 0xffff);
+  const int klast = sc.bpc > 0 ? seg_of(sc, cb1 - 1) : (sc.cta_seg[c] >> 16);
   int nseg = klast - kfirst + 1;
   if (nseg > kMaxCtaSegs) {
     if (tid == 0) report_error(p.ws, RPA_DEVERR_LENGTHS, c);
@@ -280,8 +284,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     sm100::prefetch_tmap(&tm_k);
     sm100::prefetch_tmap(&tm_v);
   }
-  // ---- Segment table of this CTA's range.
-  for (int t = tid; t < nseg; t += kWarps * 32) {
+  // ---- Segment table of this CTA's range.  Segment t's entry (and, from
+  // the page counts of the segments before it, its offset in the page list)
+  // comes from the launch parameters alone, so one barrier publishes it.
+  auto seg_info = [&](int t) {
     const int k = kfirst + t;
     const int32_t sh = sc.seqhead[k];
     SegInfo si;
@@ -292,55 +298,66 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int32_t Lk = sc.len[k];
     const int32_t lo = sc.lo[k];
     const int32_t nb_plan = sc.blk0[k + 1] - sc.blk0[k];
-    si.bad = 0;
     const int32_t jb = max(cb0, sc.blk0[k]) - sc.blk0[k];
     const int32_t je = min(cb1, sc.blk0[k + 1]) - sc.blk0[k];
     si.lo = lo;
     si.kb = (lo / kBlk + jb) * kBlk;
     si.ke = min(Lk, (lo / kBlk + je) * kBlk);
     if (si.ke < si.kb) si.ke = si.kb;
-    si.nb = si.bad ? 0 : je - jb;
+    si.nb = je - jb;
     si.whole = (jb == 0 && je == nb_plan) ? 1 : 0;
     si.slot0 = si.kb >> p.page_shift;
     si.npg = (si.ke > si.kb) ? ((si.ke - 1) >> p.page_shift) - si.slot0 + 1 : 0;
     si.pg_off = 0;
-    s_seg[t] = si;
-  }
-  __syncthreads();
-  if (tid == 0) {
+    return si;
+  };
+  for (int t = tid; t <= nseg; t += kWarps * 32) {
     int off = 0;
-    for (int t = 0; t < nseg; ++t) {
-      s_seg[t].pg_off = off;
-      off += s_seg[t].npg;
+    for (int u = 0; u < t; ++u) off += seg_info(u).npg;
+    if (t < nseg) {
+      SegInfo si = seg_info(t);
+      si.pg_off = off;
+      s_seg[t] = si;
+    } else {
+      // One past the last segment: the length of the page list.
+      s_npages = min(off, kMaxCtaPages);
+      if (off > kMaxCtaPages) report_error(p.ws, RPA_DEVERR_LENGTHS, c);
     }
-    if (off > kMaxCtaPages) report_error(p.ws, RPA_DEVERR_LENGTHS, c);
-    s_nseg = nseg;
   }
   __syncthreads();
-  // ---- Page ids of the range, read once.
-  for (int t = 0; t < nseg; ++t) {
+  // ---- Page ids of the range, read once (all loads in one round).
+  for (int i = tid; i < s_npages; i += kWarps * 32) {
+    int t = 0;
+    while (t + 1 < nseg && s_seg[t + 1].pg_off <= i) ++t;
     const SegInfo& si = s_seg[t];
-    const int n = si.npg;
-    const int32_t* pt = p.page_table + static_cast<int64_t>(si.s) * p.mpps;
-    for (int i = tid; i < n; i += kWarps * 32) {
-      const int32_t slot = si.slot0 + i;
-      int32_t page = -1;
-      if (slot >= p.mpps) {
-        report_error(p.ws, RPA_DEVERR_LENGTHS, si.s);
-      } else {
-        page = __ldg(pt + slot);
-        if (page < 0 || page >= p.num_pages) {
-          report_error(p.ws, RPA_DEVERR_PAGE_ID, si.s);
-          page = -1;
-        }
+    const int32_t slot = si.slot0 + (i - si.pg_off);
+    int32_t page = -1;
+    if (slot >= p.mpps) {
+      report_error(p.ws, RPA_DEVERR_LENGTHS, si.s);
+    } else {
+      page = __ldg(p.page_table + static_cast<int64_t>(si.s) * p.mpps + slot);
+      if (page < 0 || page >= p.num_pages) {
+        report_error(p.ws, RPA_DEVERR_PAGE_ID, si.s);
+        page = -1;
       }
-      if (si.pg_off + i < kMaxCtaPages) s_pages[si.pg_off + i] = page;
     }
+    s_pages[i] = page;
   }
   __syncthreads();
 
   unsigned char* ring = smem_raw + warp * S * L::kStageBytes;
   volatile int* abort = &s_abort;
+  // A warp's blocks in order: segment t, local blocks warp, warp + 4, ...
+  auto advance = [&](int& st_, int& j_) {
+    j_ += kWarps;
+    while (st_ < nseg && j_ >= s_seg[st_].nb) { ++st_; j_ = warp; }
+  };
+  auto page_of = [&](const SegInfo& si, int32_t key0) {
+    const int32_t idx = si.pg_off + (key0 >> p.page_shift) - si.slot0;
+    return idx < kMaxCtaPages ? s_pages[idx] : -1;
+  };
+  // Boxes of 128-byte rows: 64 bf16 or 128 fp8 elements.
+  constexpr int kBoxElems = 128 / L::ESZ;
   // Issue cursor over this warp's blocks: segment ist, local block isj.
   int ist = 0, isj = warp;
   while (ist < nseg && isj >= s_seg[ist].nb) { ++ist; isj = warp; }
@@ -350,8 +367,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const SegInfo& si = s_seg[ist];
     const int32_t key0 = si.kb + isj * kBlk;
     // Lanes 0..15: validity of one key each (visible and on a good page).
-    const int32_t idx = si.pg_off + (key0 >> p.page_shift) - si.slot0;
-    const int32_t page = idx < kMaxCtaPages ? s_pages[idx] : -1;
+    const int32_t page = page_of(si, key0);
     const int32_t key = key0 + lane;
     const bool ok = lane < kBlk && page >= 0 && key >= si.lo && key < si.ke;
     const uint32_t vmask = __ballot_sync(0xffffffffu, ok);
@@ -365,8 +381,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       // Earlier generic-proxy reads of this stage come before the async writes.
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       sm100::mbar_arrive_expect_tx(&full_bar[warp][st], static_cast<uint32_t>(L::kStageBytes));
-      // Boxes of 128-byte rows: 64 bf16 or 128 fp8 elements.
-      constexpr int kBoxElems = 128 / L::ESZ;
 #pragma unroll
       for (int c = 0; c < D / kBoxElems; ++c) {
         sm100::tma_load_3d(kt + c * kBlk * 128, &tm_k, &full_bar[warp][st], c * kBoxElems, si.g, row);
@@ -374,8 +388,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       }
     }
     ++issued;
-    isj += kWarps;
-    while (ist < nseg && isj >= s_seg[ist].nb) { ++ist; isj = warp; }
+    advance(ist, isj);
   };
   __syncwarp();
 #pragma unroll
@@ -527,9 +540,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       load_q(t + 2);
     }
-    // Deterministic sum of the four scaled warp states: warps 0 and 1 store
-    // into buffers 0 and 1, then warps 2 and 3 add into them; the two
-    // buffers are summed in a fixed order below.
+    // Each warp scales its state by its share of the normalised result,
+    // 2^(m_w - M) / L (times the V scale), with M the segment's max and L
+    // = sum_w l_w 2^(m_w - M) its sum; the scaled states are then summed in a
+    // fixed order: warps 0 and 1 store into buffers 0 and 1, warps 2 and 3
+    // add into them, and the two buffers are added while storing.
+    const int slot = sc.slot_base + 2 * c + (t == 0 ? 0 : 1);
     {
       const int h0 = 2 * (lane & 3);
       float f[2];
@@ -538,7 +554,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w][h0 + jj]);
-        f[jj] = (m[jj] == -INFINITY) ? 0.f : fast_exp2(m[jj] - M);
+        float Lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+          Lsum += (wm[w][h0 + jj] == -INFINITY) ? 0.f
+                                                 : wl[w][h0 + jj] * fast_exp2(wm[w][h0 + jj] - M);
+        f[jj] = (m[jj] == -INFINITY) ? 0.f : fast_exp2(m[jj] - M) * (vsc / Lsum);
+        // A cut segment's partial carries its log2-sum-exp.
+        if (!si.whole && warp == 0 && lane < 4 && h0 + jj < G)
+          p.part_lse[static_cast<int64_t>(slot) * G + h0 + jj] = M + __log2f(Lsum);
       }
       float* buf = so + (warp & 1) * 8 * L::kORow;
       for (int round = 0; round < 2; ++round) {
@@ -565,22 +589,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       }
     }
     __syncthreads();
-    // Normalise; write the output (whole segment) or this CTA's partial.
-    const int slot = sc.slot_base + 2 * c + (t == 0 ? 0 : 1);
-    for (int e = tid * 4; e < (si.bad ? 0 : G * D); e += kWarps * 32 * 4) {
+    // Write the output (whole segment) or this CTA's partial (O / L).
+    for (int e = tid * 4; e < G * D; e += kWarps * 32 * 4) {
       const int h = e / D, d = e % D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w][h]);
-      float Lsum = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w)
-        Lsum += (wm[w][h] == -INFINITY) ? 0.f : wl[w][h] * fast_exp2(wm[w][h] - M);
-      const float inv = vsc / Lsum;
       const float* s0 = so + h * L::kORow + d;
       const float* s1 = s0 + 8 * L::kORow;
-      const float4 u = make_float4((s0[0] + s1[0]) * inv, (s0[1] + s1[1]) * inv,
-                                   (s0[2] + s1[2]) * inv, (s0[3] + s1[3]) * inv);
+      const float4 u = make_float4(s0[0] + s1[0], s0[1] + s1[1], s0[2] + s1[2], s0[3] + s1[3]);
       if (si.whole) {
         uint2 pk;
         pk.x = pack_bf16x2(u.x, u.y);
@@ -588,7 +602,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(si.q0) * p.hq + si.g * G + h) * D + d) = pk;
       } else {
         *reinterpret_cast<float4*>(p.part_o + (static_cast<int64_t>(slot) * G + h) * D + d) = u;
-        if (d == 0) p.part_lse[static_cast<int64_t>(slot) * G + h] = M + __log2f(Lsum);
       }
     }
     __syncthreads();
@@ -733,7 +746,7 @@ int launch_one(const Plan& plan, const DecodeParams& p, const CUtensorMap& tk,
   sc.bpc = dl.bpc;
   sc.n_ctas = dl.n_ctas;
   if (dl.bpc == 0) {
-    if (dl.n_ctas > kMaxDecodeCtas) return static_cast<int>(cudaErrorInvalidValue);
+    if (dl.n_ctas > kMaxDecodeGrid) return static_cast<int>(cudaErrorInvalidValue);
     for (int i = 0; i <= dl.n_ctas; ++i) sc.cta0[i] = plan.dcta_blk0[dl.cta_begin + i];
   }
   sc.slot_base = dl.slot_base;
@@ -749,6 +762,16 @@ int launch_one(const Plan& plan, const DecodeParams& p, const CUtensorMap& tk,
   }
   sc.blk0[n] = plan.dseg_blk0[dl.seg_end] - base;
   sc.n_blocks = sc.blk0[n];
+  if (dl.bpc == 0) {
+    // Segment of a block: last k with blk0[k] <= x (segments may be empty).
+    auto seg_at = [&](int32_t x) {
+      return static_cast<int32_t>(std::upper_bound(sc.blk0, sc.blk0 + n, x) - sc.blk0) - 1;
+    };
+    for (int i = 0; i < dl.n_ctas; ++i) {
+      const int32_t b0 = sc.cta0[i], b1 = sc.cta0[i + 1];
+      sc.cta_seg[i] = b0 < b1 ? (seg_at(b0) | (seg_at(b1 - 1) << 16)) : 0;
+    }
+  }
   decode_kernel<D, NSEG, FP8><<<dl.n_ctas, kWarps * 32, smem, stream>>>(tk, tv, p, sc);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return static_cast<int>(e);

@@ -170,7 +170,7 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
     Plan::DecodeLaunch dl{sb, se, 0, 0, slot_base, 0, 0, 0};
     bool uniform = forced_tokens > 0;
     if (!uniform) {
-      const int32_t cap = std::min<int32_t>(plan.num_sms, kMaxDecodeCtas);
+      const int32_t cap = std::min<int32_t>(plan.num_sms, kMaxDecodeGrid);
       int64_t lo = kDecodeSegCost + 1, hi = total + static_cast<int64_t>(kDecodeSegCost) * (se - sb + 1);
       cut(sb, se, hi, cap, starts);
       if (static_cast<int32_t>(starts.size()) - 1 > cap) {

@@ -38,7 +38,10 @@ constexpr int kMaxCtaPages = 512;
 // the launch parameters), and the charge, in 16-key blocks, for each segment
 // a CTA's range touches (its in-CTA merge and output).
 constexpr int kMaxDecodeCtas = 1024;
-constexpr int kDecodeSegCost = 5;
+// Largest decode grid the plan's per-CTA range table describes (one wave:
+// at most one CTA per SM).
+constexpr int kMaxDecodeGrid = 512;
+constexpr int kDecodeSegCost = 7;
 
 struct Plan {
   // Problem description (checked against every rpa_forward call).

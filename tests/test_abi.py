@@ -56,7 +56,7 @@ def ceil_div(a, b):
     return -(-a // b)
 
 
-SEG_COST = 5  # blocks charged per segment a decode CTA's range touches
+SEG_COST = 7  # blocks charged per segment a decode CTA's range touches
 
 
 def decode_partition(b, num_sms=152, tokens_per_cta=0):
