@@ -272,7 +272,7 @@ def parse():
     ap.add_argument("--impl", choices=["rpa", "reference"], default="rpa")
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "decode_fp8", "tiny_prefill", "swa_prefill",
-                             "causal_prefill", "mixed"])
+                             "causal_prefill", "mixed", "spec_decode"])
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -197,3 +197,69 @@ def dequantize_kv(codes, scale) -> np.ndarray:
 def bf16_bits_to_f32(bits) -> np.ndarray:
     """bf16 bit patterns (uint16) -> float32 (exact)."""
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def rms_norm(x, weight, eps):
+    """RMS normalisation over the last axis, in float64: x / sqrt(mean(x^2) +
+    eps) * weight ("Chasing speed of light on TPU v6e", section "The Long
+    Tail": the q/k/v RMS norms run right before attention).  weight None =
+    no scaling."""
+    x = np.asarray(x, dtype=np.float64)
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + float(eps))
+    y = x * r
+    if weight is not None:
+        y = y * np.asarray(weight, dtype=np.float64)
+    return y
+
+
+def rope_angles(pos, head_dim, theta):
+    """Rotation angles [len(pos), D/2] in float64: pos * theta^(-2i/D)."""
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    inv_freq = np.power(float(theta), -2.0 * i / head_dim)
+    return np.asarray(pos, dtype=np.float64)[:, None] * inv_freq[None, :]
+
+
+def rope(y, pos, theta):
+    """Rotary position embedding of rows y [n, ..., D] at positions pos [n],
+    float64, halves convention: dimension i < D/2 pairs with i + D/2 and the
+    pair turns by the angle pos * theta^(-2i/D):
+        out_i       = y_i cos a - y_{i+D/2} sin a
+        out_{i+D/2} = y_{i+D/2} cos a + y_i sin a.
+    theta <= 0: no rotation."""
+    y = np.asarray(y, dtype=np.float64)
+    if theta <= 0:
+        return y.copy()
+    D = y.shape[-1]
+    a = rope_angles(pos, D, theta)
+    shape = (a.shape[0],) + (1,) * (y.ndim - 2) + (D // 2,)
+    c, s = np.cos(a).reshape(shape), np.sin(a).reshape(shape)
+    lo, hi = y[..., : D // 2], y[..., D // 2:]
+    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
+
+
+def token_positions(cu_q_lens, kv_lens):
+    """Position of every query token: kv_lens[s] - q_len_s + i."""
+    cu = np.asarray(cu_q_lens, dtype=np.int64)
+    kl = np.asarray(kv_lens, dtype=np.int64)
+    pos = np.empty(int(cu[-1]), dtype=np.int64)
+    for s in range(kl.shape[0]):
+        ql = int(cu[s + 1] - cu[s])
+        pos[cu[s]:cu[s + 1]] = kl[s] - ql + np.arange(ql)
+    return pos
+
+
+def qkv_prologue(q, k, v, q_weight, k_weight, v_weight, eps, theta, cu_q_lens, kv_lens):
+    """The step before attention, as plain float64 math: q and k rows RMS-
+    normalised (their weights; None = no norm) then rotated at their token's
+    position; v rows RMS-normalised when v_weight is given, never rotated.
+    q [T, Hq, D], k and v [T, Hkv, D] (any float dtype).  Returns float64
+    (q_out, k_out, v_out); the caller rounds and writes k/v into pages."""
+    pos = token_positions(cu_q_lens, kv_lens)
+
+    def norm(x, w):
+        return np.asarray(x, dtype=np.float64) if w is None else rms_norm(x, w, eps)
+
+    q_out = rope(norm(q, q_weight), pos, theta)
+    k_out = rope(norm(k, k_weight), pos, theta)
+    v_out = norm(v, v_weight)
+    return q_out, k_out, v_out

@@ -168,6 +168,20 @@ def decode_batch(seed: int = 1, num_seqs: int = 128, lo: int = 128, hi: int = 20
                       name="decode_b%d_l%d-%d_h8kv1_d256_p128" % (num_seqs, lo, hi))
 
 
+def spec_decode_batch(seed: int = 6, num_seqs: int = 128, spec: int = 8, lo: int = 128,
+                      hi: int = 2048, pool_pages: int = 4096, meta_only: bool = False) -> Batch:
+    """Multi-token (speculative) decode: the decode batch's shape with `spec`
+    new tokens per sequence (the drafted tokens verified in one step), KV
+    length uniform in [lo, hi] including them; 8 q / 1 kv heads, so one KV
+    head serves spec x 8 = 64 query rows; D 256, 128-token pages."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 106]))
+    kv = rng.integers(max(lo, spec), hi + 1, size=num_seqs)
+    return make_batch(np.full(num_seqs, spec, dtype=np.int64), kv, num_q_heads=8,
+                      num_kv_heads=1, head_dim=256, page_size=128, pool_pages=pool_pages,
+                      seed=seed, meta_only=meta_only,
+                      name="spec_decode_b%d_q%d_l%d-%d_h8kv1_d256_p128" % (num_seqs, spec, lo, hi))
+
+
 def prefill_8k(seed: int = 2, window: int = 1024, tokens: int = 8192,
                num_q_heads: int = 32, num_kv_heads: int = 16, meta_only: bool = False) -> Batch:
     """One 8192-token sequence attending causally to itself; 32 q / 16 kv heads,
@@ -209,6 +223,7 @@ WORKLOADS = {
     "swa_prefill": lambda seed=2, **kw: prefill_8k(seed=seed, window=1024, **kw),
     "causal_prefill": lambda seed=3, **kw: prefill_8k(seed=seed, window=0, **kw),
     "mixed": mixed_batch,
+    "spec_decode": spec_decode_batch,
 }
 
 

@@ -294,3 +294,40 @@ def test_mixed_workload_sampled():
     assert err == 0
     rows = sample_rows(b, n_random=64)
     assert_bf16_close(got[rows], oracle_rows(b, rows), "mixed")
+
+
+# ---------------------------------------------------------------- multi-token decode
+
+SPEC = [
+    # (spec tokens, Hq, Hkv, D, P): spec x G query rows per KV head
+    (8, 8, 1, 256, 128),     # 64 rows, the decode batch's heads
+    (4, 16, 2, 128, 64),     # 32 rows
+    (2, 8, 1, 64, 16),       # 16 rows
+    (16, 8, 1, 256, 128),    # 128 rows: one full tile
+]
+
+
+@pytest.mark.parametrize("case", range(len(SPEC)))
+def test_multi_token_decode(case):
+    """Speculative decode: every sequence verifies `spec` drafted tokens in one
+    step (causal among themselves, after the cached prefix); the tensor-core
+    kernel packs spec x G rows of one KV head into its M dimension."""
+    spec, hq, hkv, d, p = SPEC[case]
+    rng = np.random.default_rng(800 + case)
+    n = 24
+    kv = rng.integers(spec, 1500, size=n).tolist()
+    win = [0 if i % 3 else 300 for i in range(n)]
+    b = workloads.make_batch([spec] * n, kv, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                             page_size=p, windows=win, seed=810 + case)
+    got, err, plan = run_gpu(b)
+    info = plan.info()
+    assert err == 0 and info["path"] == RPA_PATH_TC and info["num_prefill_seqs"] == n
+    assert_bf16_close(got, oracle_rows(b), "multi-token decode case %d" % case)
+
+
+def test_spec_decode_workload_sampled():
+    b = workloads.WORKLOADS["spec_decode"]()
+    got, err, _ = run_gpu(b)
+    assert err == 0
+    rows = sample_rows(b, n_random=8)
+    assert_bf16_close(got[rows], oracle_rows(b, rows), "spec_decode")
