@@ -285,6 +285,9 @@ def parse():
     ap.add_argument("--no-graph", action="store_true",
                     help="enqueue the timed steps from Python instead of replaying them "
                          "from a CUDA graph")
+    ap.add_argument("--qkv-prologue", action="store_true",
+                    help="time rpa_forward_qkv: q/k RMS norm + rotary embedding, v norm and "
+                         "the KV write of the new tokens, then attention")
     ap.add_argument("--kv-write", action="store_true",
                     help="time rpa_forward_kv: write the step's new K/V rows into their "
                          "pages, then attend")
@@ -370,6 +373,19 @@ def main():
     fp8_dev = ([torch.from_numpy(x).cuda() for x in (b.k_fp8, b.v_fp8, b.k_scale, b.v_scale)]
                if fp8 else None)
     kv_new = None if not args.kv_write else new_token_rows(b, db, torch)
+    qkv = None
+    if args.qkv_prologue:
+        # The projection's q, k, v rows of the step (seeded N(0, 1)), norm
+        # weights near 1 and a rotary base of 10^4: the step runs the q/k/v
+        # prologue (norms, rotary embedding, KV write) before attention.
+        g = torch.Generator(device="cpu").manual_seed(1234)
+        D = b.head_dim
+        raw0 = tuple(torch.randn(b.total_q, h, D, generator=g).to(torch.bfloat16).cuda()
+                     for h in (b.num_q_heads, b.num_kv_heads, b.num_kv_heads))
+        qkv = dict(
+            raw=[raw0] + [tuple(x.clone() for x in raw0) for _ in range(2)],
+            w=[(0.5 + torch.rand(D, generator=g)).cuda() for _ in range(3)])
+        qkv["norm"] = binding.qkv_norm(*qkv["w"], eps=1e-6, rope_theta=10000.0)
 
     # Step inputs.  When one step's inputs exceed L2, the timed steps rotate
     # over R disjoint copies of them (KV pools stacked R times with the page
@@ -404,6 +420,11 @@ def main():
         # Copy r's call object, bound to the current stream (inside a graph
         # capture: the capture stream).
         c = copies[r]
+        if qkv is not None:
+            qr, kr, vr = qkv["raw"][r % 3]
+            return binding.ForwardQkvCall(qr, kr, vr, qkv["norm"], c["q"], pools[0], pools[1],
+                                          c["pt"], db.cu_q_lens, db.kv_lens, db.window,
+                                          b.sm_scale, c["out"], rplan, ws)
         if kv_new is not None:
             return binding.ForwardKvCall(c["q"], kv_new[0], kv_new[1], pools[0], pools[1],
                                          c["pt"], db.cu_q_lens, db.kv_lens, db.window,
@@ -578,6 +599,12 @@ def main():
         dom_counts, decode_heavy = algorithmic_counts(b, "prefill"), False
     else:
         dom_counts, decode_heavy = counts, info["num_prefill_seqs"] == 0
+    # The bound follows the kernel's arithmetic intensity against the ridge
+    # point of the peaks (multi-token decode runs on the tensor-core kernel
+    # but stays HBM-bound).
+    if not decode_heavy and dom_counts["bytes"] > 0:
+        ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+        decode_heavy = dom_counts["flops"] / dom_counts["bytes"] < ridge
     if decode_heavy:
         achieved = dom_counts["bytes"] / (dom_us * 1e-6) / 1e9
         peak = peaks["hbm_gbs"]
@@ -627,7 +654,9 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "launch": "stream (Python loop behind a GPU sleep)" if args.no_graph else
                              "CUDA graph of the K timed steps, replayed once",
-                   "step": "rpa_forward_kv (KV-cache write of the new tokens, then attention)"
+                   "step": "rpa_forward_qkv (q/k RMS norm + rotary embedding, v norm, KV "
+                           "write of the new tokens, then attention)" if args.qkv_prologue else
+                           "rpa_forward_kv (KV-cache write of the new tokens, then attention)"
                            if args.kv_write else ("rpa_forward_fp8kv" if b.k_fp8 is not None
                                                   else "rpa_forward"),
                    "kv_pages": "e4m3 bytes + fp32 scale per KV head (f16 products, fp32 "

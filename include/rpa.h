@@ -238,6 +238,66 @@ rpa_status_t rpa_write_kv(const void* k_new, const void* v_new, void* k_pages, v
                           void* workspace, rpa_stream_t stream);
 
 /*
+ * q/k/v prologue: the step right before attention ("Chasing speed of light on
+ * TPU v6e", section "The Long Tail": the q/k/v RMS norms and the rotary
+ * embedding run in the kernel before attention, which takes q, k and v as
+ * three arrays), fused with the KV-cache write.
+ *
+ * For every new token t = cu_q_lens[s] + i of sequence s, at position
+ * pos = kv_lens[s] - q_len_s + i, and page = page_table[s][pos / page_size]:
+ *   q_out[t][h][:]                        = rope(norm(q[t][h][:], q_weight), pos)
+ *   k_pages[page][pos % page_size][g][:]  = rope(norm(k[t][g][:], k_weight), pos)
+ *   v_pages[page][pos % page_size][g][:]  = norm(v[t][g][:], v_weight)
+ * norm(x, w)_d = x_d / sqrt(mean_d(x_d^2) + eps) * w_d, or x itself when w is
+ * NULL (a model whose norm scales by 1 + w passes 1 + w).
+ * rope (halves convention): for i < D/2, with a = pos * rope_theta^(-2i/D),
+ *   out_i = y_i cos a - y_{i+D/2} sin a,  out_{i+D/2} = y_{i+D/2} cos a + y_i sin a;
+ * rope_theta <= 0: no rotation.  fp32 arithmetic; the angle is reduced
+ * modulo 2 pi in extended precision (accurate for pos * frequency < 2^21).
+ *
+ * Device pointers: q, q_out [total_q, num_q_heads, head_dim]; k, v
+ * [total_q, num_kv_heads, head_dim]; all of `dtype` (BF16 or F32), 16-B
+ * aligned; q_out may equal q.  Weights: [head_dim] float32.  Pages, page
+ * table and lengths as for rpa_write_kv (kv_lens include the new tokens).
+ * head_dim in {64, 128, 256} (else RPA_ERR_UNSUPPORTED); page_size a power
+ * of two.  `workspace` may be NULL; otherwise its error word records a page
+ * id or position outside the table (that row is skipped, never trapped).
+ * Enqueues one kernel on `stream`; does not synchronise.
+ */
+typedef struct rpa_qkv_norm {
+  const float* q_weight; /* [head_dim] or NULL: q not normalised */
+  const float* k_weight; /* [head_dim] or NULL: k not normalised */
+  const float* v_weight; /* [head_dim] or NULL: v stored as given */
+  float eps;             /* added to the mean square */
+  float rope_theta;      /* rotary base (> 0), or <= 0 for none */
+} rpa_qkv_norm;
+
+rpa_status_t rpa_qkv_prologue(const void* q, const void* k, const void* v,
+                              const rpa_qkv_norm* norm, void* q_out, void* k_pages,
+                              void* v_pages, const int32_t* page_table,
+                              const int32_t* cu_q_lens, const int32_t* kv_lens,
+                              int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                              int32_t max_pages_per_seq, int32_t num_pages, int32_t dtype,
+                              void* workspace, rpa_stream_t stream);
+
+/*
+ * The prologue, then the attention on its output, on one stream: the step
+ * from the projection's q, k, v to the attention output.  q_buf receives
+ * the normalised, rotated q (rpa_qkv_prologue's q_out) and is the attention's
+ * query; the other arguments as rpa_qkv_prologue and rpa_forward (pool size
+ * and page-table width are the plan's).
+ */
+rpa_status_t rpa_forward_qkv(const void* q, const void* k, const void* v,
+                             const rpa_qkv_norm* norm, void* q_buf, void* k_pages,
+                             void* v_pages, const int32_t* page_table,
+                             const int32_t* cu_q_lens, const int32_t* kv_lens,
+                             int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t page_size, const int32_t* window,
+                             float sm_scale, void* out, rpa_stream_t stream,
+                             const rpa_plan_t* plan, void* workspace, size_t workspace_bytes);
+
+/*
  * Decode over fp8 (e4m3) K/V pages with a float scale per KV head
  * ("TPU Deep Dive" slides, chapter 8, "KV cache layout": 8-bit KV packs four
  * per 32-bit word; halving the KV bytes halves decode's dominant traffic).
@@ -336,7 +396,8 @@ enum {
   RPA_KERNEL_DECODE_COMBINE = 1, /* log-sum-exp combine of cut sequences */
   RPA_KERNEL_PREFILL_TC = 2,     /* tensor-core prefill               */
   RPA_KERNEL_SIMT = 3,           /* CUDA-core (fp32) path             */
-  RPA_KERNEL_KV_WRITE = 4        /* KV-cache write of new tokens      */
+  RPA_KERNEL_KV_WRITE = 4,       /* KV-cache write of new tokens      */
+  RPA_KERNEL_PROLOGUE = 5        /* q/k/v norm + rotary + KV write    */
 };
 typedef struct rpa_trace_record {
   int32_t kernel; /* RPA_KERNEL_* */

@@ -42,10 +42,19 @@ RPA_PATH_TC = 2
 EXPORTS = ["rpa_plan", "rpa_plan_destroy", "rpa_plan_get_info", "rpa_forward",
            "rpa_get_device_error", "rpa_clear_device_error", "rpa_trace_begin",
            "rpa_trace_end", "rpa_status_string", "rpa_forward_decode_noalloc",
-           "rpa_write_kv", "rpa_forward_kv", "rpa_forward_fp8kv"]
+           "rpa_write_kv", "rpa_forward_kv", "rpa_forward_fp8kv", "rpa_qkv_prologue",
+           "rpa_forward_qkv"]
 
 RPA_KERNEL_NAMES = {0: "decode_split", 1: "decode_combine", 2: "prefill_tc", 3: "simt",
-                    4: "kv_write"}
+                    4: "kv_write", 5: "prologue"}
+
+
+class QkvNorm(ctypes.Structure):
+    """rpa_qkv_norm: norm weights (device float32 [head_dim] or None), eps and
+    the rotary base (<= 0: no rotation)."""
+    _fields_ = [("q_weight", ctypes.c_void_p), ("k_weight", ctypes.c_void_p),
+                ("v_weight", ctypes.c_void_p), ("eps", ctypes.c_float),
+                ("rope_theta", ctypes.c_float)]
 
 
 class RpaError(RuntimeError):
@@ -112,6 +121,13 @@ def lib() -> ctypes.CDLL:
         L.rpa_forward_fp8kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                         vp, ctypes.c_float, vp, vp, vp, vp, ctypes.c_size_t]
         L.rpa_forward_fp8kv.restype = i32
+        L.rpa_qkv_prologue.argtypes = [vp, vp, vp, ctypes.POINTER(QkvNorm), vp, vp, vp, vp, vp,
+                                       vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp]
+        L.rpa_qkv_prologue.restype = i32
+        L.rpa_forward_qkv.argtypes = [vp, vp, vp, ctypes.POINTER(QkvNorm), vp, vp, vp, vp, vp,
+                                      vp, i32, i32, i32, i32, i32, vp, ctypes.c_float, vp, vp,
+                                      vp, vp, ctypes.c_size_t]
+        L.rpa_forward_qkv.restype = i32
         L.rpa_get_device_error.argtypes = [vp, vp, ctypes.POINTER(i32)]
         L.rpa_get_device_error.restype = i32
         L.rpa_clear_device_error.argtypes = [vp, vp]
@@ -255,6 +271,45 @@ def rpa_write_kv(k_new, v_new, k_pages, v_pages, page_table, cu_q_lens, kv_lens,
         int(num_pages), dtype, _dptr(workspace, "workspace"), _stream_ptr(stream))
     if st != RPA_OK:
         raise RpaError(st, "rpa_write_kv")
+
+
+def qkv_norm(q_weight=None, k_weight=None, v_weight=None, eps: float = 1e-6,
+             rope_theta: float = 10000.0) -> QkvNorm:
+    """An rpa_qkv_norm over device float32 weight tensors (kept alive by the
+    caller)."""
+    import torch
+    return QkvNorm(_dptr(q_weight, "q_weight", torch.float32),
+                   _dptr(k_weight, "k_weight", torch.float32),
+                   _dptr(v_weight, "v_weight", torch.float32), float(eps), float(rope_theta))
+
+
+def rpa_qkv_prologue(q, k, v, norm: QkvNorm, q_out, k_pages, v_pages, page_table, cu_q_lens,
+                     kv_lens, num_pages: int, workspace=None, stream=None) -> None:
+    """rpa_qkv_prologue on torch CUDA tensors: q/k RMS norm + rotary embedding,
+    v norm; q to q_out, k and v rows into their pages."""
+    import torch
+    dt = q.dtype
+    dtype = RPA_DTYPE_BF16 if dt == torch.bfloat16 else RPA_DTYPE_F32
+    total_q, hq, d = (int(x) for x in q.shape)
+    hkv = int(k.shape[1])
+    st = lib().rpa_qkv_prologue(
+        _dptr(q, "q", dt), _dptr(k, "k", dt), _dptr(v, "v", dt), ctypes.byref(norm),
+        _dptr(q_out, "q_out", dt), _dptr(k_pages, "k_pages", dt), _dptr(v_pages, "v_pages", dt),
+        _dptr(page_table, "page_table", torch.int32),
+        _dptr(cu_q_lens, "cu_q_lens", torch.int32), _dptr(kv_lens, "kv_lens", torch.int32),
+        int(kv_lens.numel()), total_q, hq, hkv, d, int(k_pages.shape[1]),
+        int(page_table.shape[1]), int(num_pages), dtype, _dptr(workspace, "workspace"),
+        _stream_ptr(stream))
+    if st != RPA_OK:
+        raise RpaError(st, "rpa_qkv_prologue")
+
+
+def rpa_forward_qkv(q, k, v, norm: QkvNorm, q_buf, k_pages, v_pages, page_table, cu_q_lens,
+                    kv_lens, window, sm_scale: float, out, plan: "Plan", workspace,
+                    stream=None) -> None:
+    """rpa_forward_qkv: the prologue into q_buf and the pages, then attention."""
+    ForwardQkvCall(q, k, v, norm, q_buf, k_pages, v_pages, page_table, cu_q_lens, kv_lens,
+                   window, sm_scale, out, plan, workspace, stream)()
 
 
 def rpa_forward_fp8kv(q, k_pages, v_pages, k_scale, v_scale, page_table, cu_q_lens, kv_lens,
@@ -481,3 +536,33 @@ class ForwardKvCall(ForwardCall):
         st = self._fn(*self._args)
         if st != RPA_OK:
             raise RpaError(st, "rpa_forward_kv")
+
+
+class ForwardQkvCall(ForwardCall):
+    """rpa_forward_qkv (q/k/v prologue, then attention) with its arguments
+    marshalled once."""
+
+    def __init__(self, q, k, v, norm: QkvNorm, q_buf, k_pages, v_pages, page_table, cu_q_lens,
+                 kv_lens, window, sm_scale: float, out, plan: "Plan", workspace, stream=None):
+        import torch
+        m = plan.meta
+        dt = torch.bfloat16 if m["dtype"] == RPA_DTYPE_BF16 else torch.float32
+        self._norm = norm
+        self._keep = (q, k, v, q_buf, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window,
+                      out, plan, workspace)
+        self._args = (
+            _dptr(q, "q", dt), _dptr(k, "k", dt), _dptr(v, "v", dt), ctypes.byref(norm),
+            _dptr(q_buf, "q_buf", dt), _dptr(k_pages, "k_pages", dt),
+            _dptr(v_pages, "v_pages", dt), _dptr(page_table, "page_table", torch.int32),
+            _dptr(cu_q_lens, "cu_q_lens", torch.int32),
+            _dptr(kv_lens, "kv_lens", torch.int32), m["num_seqs"], m["num_q_heads"],
+            m["num_kv_heads"], m["head_dim"], m["page_size"],
+            _dptr(window, "window", torch.int32), float(sm_scale), _dptr(out, "out", dt),
+            _stream_ptr(stream), plan.handle, _dptr(workspace, "workspace"),
+            workspace.numel() * workspace.element_size())
+        self._fn = lib().rpa_forward_qkv
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != RPA_OK:
+            raise RpaError(st, "rpa_forward_qkv")

@@ -125,10 +125,12 @@ namespace {
 // Launches the attention kernels of a validated call (after the optional
 // KV-cache write).
 rpa_status_t forward_launch(const rpa::Plan& p, const rpa::Args& a,
-                            const rpa::KvWriteArgs* kvw, rpa_stream_t stream) {
+                            const rpa::KvWriteArgs* kvw, rpa_stream_t stream,
+                            const rpa::PrologueArgs* pro = nullptr) {
   int err = 0;
   rpa::trace_start(stream);
   if (kvw != nullptr && rpa::launch_kv_write(*kvw, stream) != 0) return RPA_ERR_CUDA;
+  if (pro != nullptr && rpa::launch_prologue(*pro, stream) != 0) return RPA_ERR_CUDA;
   if (p.num_decode > 0 && !p.simt_decode) {
     err = rpa::launch_decode(p, a, stream);
     if (err) return RPA_ERR_CUDA;
@@ -262,6 +264,77 @@ rpa_status_t rpa_write_kv(const void* k_new, const void* v_new, void* k_pages, v
                       head_dim, esz, page_size, max_pages_per_seq, num_pages};
   rpa::trace_start(stream);
   return rpa::launch_kv_write(kw, stream) == 0 ? RPA_OK : RPA_ERR_CUDA;
+}
+
+rpa_status_t rpa_qkv_prologue(const void* q, const void* k, const void* v,
+                              const rpa_qkv_norm* norm, void* q_out, void* k_pages,
+                              void* v_pages, const int32_t* page_table,
+                              const int32_t* cu_q_lens, const int32_t* kv_lens,
+                              int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                              int32_t max_pages_per_seq, int32_t num_pages, int32_t dtype,
+                              void* workspace, rpa_stream_t stream) {
+  if (norm == nullptr || num_seqs < 1 || total_q < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
+      head_dim < 1 || page_size < 1 || (page_size & (page_size - 1)) != 0 ||
+      max_pages_per_seq < 1 || num_pages < 1 || !(norm->eps >= 0.f))
+    return RPA_ERR_INVALID_ARG;
+  if (dtype != RPA_DTYPE_BF16 && dtype != RPA_DTYPE_F32) return RPA_ERR_INVALID_ARG;
+  if (!rpa::prologue_supported(head_dim)) return RPA_ERR_UNSUPPORTED;
+  if (total_q == 0) return RPA_OK;
+  if (q == nullptr || k == nullptr || v == nullptr || q_out == nullptr || k_pages == nullptr ||
+      v_pages == nullptr || page_table == nullptr || cu_q_lens == nullptr || kv_lens == nullptr)
+    return RPA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q_out, 16) ||
+      !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(page_table, 4) ||
+      !aligned(cu_q_lens, 4) || !aligned(kv_lens, 4) || !aligned(norm->q_weight, 4) ||
+      !aligned(norm->k_weight, 4) || !aligned(norm->v_weight, 4) ||
+      (workspace != nullptr && !aligned(workspace, 256)))
+    return RPA_ERR_INVALID_ARG;
+  rpa::PrologueArgs pa{q, k, v, norm->q_weight, norm->k_weight, norm->v_weight, norm->eps,
+                       norm->rope_theta, q_out, k_pages, v_pages, page_table, cu_q_lens,
+                       kv_lens, static_cast<unsigned char*>(workspace), num_seqs, total_q,
+                       num_q_heads, num_kv_heads, head_dim,
+                       dtype == RPA_DTYPE_F32 ? 4 : 2, page_size, max_pages_per_seq,
+                       num_pages};
+  rpa::trace_start(stream);
+  return rpa::launch_prologue(pa, stream) == 0 ? RPA_OK : RPA_ERR_CUDA;
+}
+
+rpa_status_t rpa_forward_qkv(const void* q, const void* k, const void* v,
+                             const rpa_qkv_norm* norm, void* q_buf, void* k_pages,
+                             void* v_pages, const int32_t* page_table,
+                             const int32_t* cu_q_lens, const int32_t* kv_lens,
+                             int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t page_size, const int32_t* window,
+                             float sm_scale, void* out, rpa_stream_t stream,
+                             const rpa_plan_t* plan, void* workspace, size_t workspace_bytes) {
+  if (plan == nullptr || norm == nullptr || !(norm->eps >= 0.f)) return RPA_ERR_INVALID_ARG;
+  const rpa::Plan& p = plan->p;
+  if (num_seqs != p.num_seqs || num_q_heads != p.hq || num_kv_heads != p.hkv ||
+      head_dim != p.d || page_size != p.p || (window != nullptr) != p.has_window || p.kv_fp8)
+    return RPA_ERR_PLAN_MISMATCH;
+  if (!rpa::prologue_supported(head_dim)) return RPA_ERR_UNSUPPORTED;
+  if (workspace == nullptr || !aligned(workspace, 256)) return RPA_ERR_INVALID_ARG;
+  if (workspace_bytes < p.ws_bytes) return RPA_ERR_WORKSPACE_TOO_SMALL;
+  if (p.total_q == 0) return RPA_OK;
+  if (q == nullptr || k == nullptr || v == nullptr || q_buf == nullptr || k_pages == nullptr ||
+      v_pages == nullptr || page_table == nullptr || cu_q_lens == nullptr ||
+      kv_lens == nullptr || out == nullptr)
+    return RPA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q_buf, 16) ||
+      !aligned(out, 16) || !aligned(k_pages, 128) || !aligned(v_pages, 128) ||
+      !aligned(page_table, 4) || !aligned(cu_q_lens, 4) || !aligned(kv_lens, 4) ||
+      !aligned(window, 4) || !aligned(norm->q_weight, 4) || !aligned(norm->k_weight, 4) ||
+      !aligned(norm->v_weight, 4))
+    return RPA_ERR_INVALID_ARG;
+  rpa::PrologueArgs pa{q, k, v, norm->q_weight, norm->k_weight, norm->v_weight, norm->eps,
+                       norm->rope_theta, q_buf, k_pages, v_pages, page_table, cu_q_lens,
+                       kv_lens, static_cast<unsigned char*>(workspace), p.num_seqs, p.total_q,
+                       p.hq, p.hkv, p.d, p.dtype == RPA_DTYPE_F32 ? 4 : 2, p.p, p.mpps,
+                       p.num_pages};
+  rpa::Args a{q_buf, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window, sm_scale,
+              out, static_cast<unsigned char*>(workspace)};
+  return forward_launch(p, a, nullptr, stream, &pa);
 }
 
 rpa_status_t rpa_forward_decode_noalloc(const void* q, const void* k_pages,

@@ -56,4 +56,42 @@ __device__ __forceinline__ int32_t find_seq(const int32_t* cu, int32_t num_seqs,
   return lo;
 }
 
+// Per-sequence metadata of the new-token kernels (KV write, prologue): the
+// CTA copies cu_q_lens [num_seqs + 1] and kv_lens [num_seqs] into shared
+// memory in one round of loads when they fit (kMaxStagedSeqs), so that each
+// row's sequence search costs shared-memory reads instead of a chain of
+// dependent global loads.
+constexpr int kMaxStagedSeqs = 4096;
+
+__host__ __device__ constexpr size_t staged_meta_bytes(int32_t num_seqs) {
+  return num_seqs <= kMaxStagedSeqs ? static_cast<size_t>(2 * num_seqs + 1) * 4 : 0;
+}
+
+struct SeqMeta {
+  const int32_t* cu;   // shared or global
+  const int32_t* kl;
+  int32_t n;
+
+  // Sequence s of token t, its first token and its q_len.
+  __device__ __forceinline__ int32_t seq(int32_t t) const {
+    int32_t lo = 0, hi = n - 1;
+    while (lo < hi) {
+      const int32_t mid = (lo + hi + 1) >> 1;
+      if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  }
+};
+
+// Stage the metadata (all threads of the CTA take part; ends with a barrier
+// when staged).  `smem` holds staged_meta_bytes(num_seqs) bytes.
+__device__ __forceinline__ SeqMeta stage_seq_meta(int32_t* smem, const int32_t* cu,
+                                                 const int32_t* kl, int32_t num_seqs) {
+  if (num_seqs > kMaxStagedSeqs) return SeqMeta{cu, kl, num_seqs};
+  for (int i = threadIdx.x; i < 2 * num_seqs + 1; i += blockDim.x)
+    smem[i] = i <= num_seqs ? __ldg(cu + i) : __ldg(kl + (i - num_seqs - 1));
+  __syncthreads();
+  return SeqMeta{smem, smem + num_seqs + 1, num_seqs};
+}
+
 }  // namespace rpa

@@ -7,7 +7,8 @@
 // its row for KV head g goes to page page_table[s][pos / P], slot pos % P:
 //   k_pages[page][pos % P][g][:] = k_new[t][g][:]   (and V alike).
 // One warp per (token, KV head) row, 16-byte vector copies; a data-movement
-// kernel bound by HBM (each new row read once and written once).
+// kernel bound by HBM (each new row read once and written once).  The
+// sequence lookups read cu_q_lens and kv_lens staged in shared memory.
 #include <algorithm>
 
 #include "common.cuh"
@@ -29,6 +30,8 @@ struct KvWriteParams {
 };
 
 __global__ void __launch_bounds__(256) kv_write_kernel(const KvWriteParams p) {
+  extern __shared__ int32_t s_meta[];
+  const SeqMeta meta = stage_seq_meta(s_meta, p.cu_q_lens, p.kv_lens, p.num_seqs);
   const int lane = threadIdx.x & 31;
   const int64_t rows = static_cast<int64_t>(p.total_q) * p.hkv;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -36,16 +39,19 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const KvWriteParams p) {
        row < rows; row += warps) {
     const int32_t t = static_cast<int32_t>(row / p.hkv);
     const int32_t g = static_cast<int32_t>(row % p.hkv);
-    // Sequence of token t: the last s with cu_q_lens[s] <= t.
-    int lo = 0, hi = p.num_seqs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(p.cu_q_lens + mid) <= t) lo = mid; else hi = mid - 1;
+    const int64_t src = row * p.vec_per_row;
+    // Rows of up to 32 vectors (D * element size <= 512 B): load them before
+    // the lookups, which they do not depend on.
+    const bool one = p.vec_per_row <= 32;
+    uint4 kk = make_uint4(0, 0, 0, 0), vv = kk;
+    if (one && lane < p.vec_per_row) {
+      kk = __ldg(p.k_new + src + lane);
+      vv = __ldg(p.v_new + src + lane);
     }
-    const int32_t s = lo;
-    const int32_t q0 = __ldg(p.cu_q_lens + s);
-    const int32_t ql = __ldg(p.cu_q_lens + s + 1) - q0;
-    const int32_t pos = __ldg(p.kv_lens + s) - ql + (t - q0);
+    const int32_t s = meta.seq(t);
+    const int32_t q0 = meta.cu[s];
+    const int32_t ql = meta.cu[s + 1] - q0;
+    const int32_t pos = meta.kl[s] - ql + (t - q0);
     if (pos < 0 || t - q0 >= ql) {
       if (lane == 0 && p.ws) report_error(p.ws, RPA_DEVERR_LENGTHS, s);
       continue;
@@ -62,7 +68,13 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const KvWriteParams p) {
     }
     const int64_t dst = ((static_cast<int64_t>(page) * p.page_size + (pos & (p.page_size - 1))) *
                              p.hkv + g) * p.vec_per_row;
-    const int64_t src = row * p.vec_per_row;
+    if (one) {
+      if (lane < p.vec_per_row) {
+        p.k_pages[dst + lane] = kk;
+        p.v_pages[dst + lane] = vv;
+      }
+      continue;
+    }
     for (int v = lane; v < p.vec_per_row; v += 32) {
       p.k_pages[dst + v] = __ldg(p.k_new + src + v);
       p.v_pages[dst + v] = __ldg(p.v_new + src + v);
@@ -94,9 +106,9 @@ int launch_kv_write(const KvWriteArgs& a, void* stream) {
   p.mpps = a.mpps;
   p.num_pages = a.num_pages;
   const int64_t rows = static_cast<int64_t>(a.total_q) * a.hkv;
-  const int64_t blocks = std::min<int64_t>((rows + 7) / 8, 152 * 16);
+  const int64_t blocks = std::min<int64_t>((rows + 7) / 8, 152 * 8);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  kv_write_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(p);
+  kv_write_kernel<<<static_cast<int>(blocks), 256, staged_meta_bytes(p.num_seqs), s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return static_cast<int>(e);
   trace_mark(RPA_KERNEL_KV_WRITE, stream);

@@ -144,6 +144,28 @@ struct KvWriteArgs {
 };
 int launch_kv_write(const KvWriteArgs& a, void* stream);
 
+// The q/k/v prologue (prologue.cu): q/k RMS norm + rotary embedding, v norm,
+// q to q_out and k/v into their pages.
+struct PrologueArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* q_weight;  // null: no norm
+  const float* k_weight;
+  const float* v_weight;
+  float eps, rope_theta;  // rope_theta <= 0: no rotation
+  void* q_out;
+  void* k_pages;
+  void* v_pages;
+  const int32_t* page_table;
+  const int32_t* cu_q_lens;
+  const int32_t* kv_lens;
+  unsigned char* workspace;  // error word, or null
+  int32_t num_seqs, total_q, hq, hkv, head_dim, elem_bytes, page_size, mpps, num_pages;
+};
+bool prologue_supported(int32_t head_dim);
+int launch_prologue(const PrologueArgs& a, void* stream);
+
 // Tracing hooks (trace.cpp): trace_start before a call's first launch,
 // trace_mark after each launch (no-ops unless tracing is on).
 void trace_start(void* stream);
