@@ -279,6 +279,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--q-block", type=int, default=0)
     ap.add_argument("--kv-split", type=int, default=0)
+    ap.add_argument("--prefill-split", type=int, default=0,
+                    help="plan option: 0 choose, -1 never split prefill items, n > 0 parts "
+                         "of at most n key tiles")
     ap.add_argument("--flush", action="store_true",
                     help="flush L2 before every step and time each step with its own "
                          "event pair, even when a step's inputs exceed L2")
@@ -367,7 +370,8 @@ def main():
     db = binding.Batch(b)
     fp8 = b.k_fp8 is not None
     plan = db.plan(q_block=args.q_block, kv_split=args.kv_split,
-                   kv_dtype=binding.RPA_DTYPE_FP8_E4M3 if fp8 else 0)
+                   kv_dtype=binding.RPA_DTYPE_FP8_E4M3 if fp8 else 0,
+                   prefill_split=args.prefill_split)
     info = plan.info()
     ws = binding.alloc_workspace(plan)
     fp8_dev = ([torch.from_numpy(x).cuda() for x in (b.k_fp8, b.v_fp8, b.k_scale, b.v_scale)]
@@ -404,7 +408,8 @@ def main():
                                  b.num_kv_heads, b.head_dim, b.page_size,
                                  b.max_pages_per_seq, R * N, dtype=db.dtype,
                                  q_block=args.q_block, kv_split=args.kv_split,
-                                 kv_dtype=binding.RPA_DTYPE_FP8_E4M3 if fp8 else 0)
+                                 kv_dtype=binding.RPA_DTYPE_FP8_E4M3 if fp8 else 0,
+                                 prefill_split=args.prefill_split)
         pools = [torch.cat([x] * R) for x in
                  ((fp8_dev[0], fp8_dev[1]) if fp8 else (db.k_pages, db.v_pages))]
         copies = [dict(q=db.q if r == 0 else db.q.clone(),
@@ -715,7 +720,8 @@ def run_e2e(args, b, db, plan_dev, flush_l2, binding, torch, fp8_dev=None):
                                 b.num_kv_heads, b.head_dim, b.page_size,
                                 b.max_pages_per_seq, b.num_pages,
                                 dtype=db.dtype, q_block=args.q_block, kv_split=args.kv_split,
-                                kv_dtype=binding.RPA_DTYPE_FP8_E4M3 if fp8_dev else 0)
+                                kv_dtype=binding.RPA_DTYPE_FP8_E4M3 if fp8_dev else 0,
+                                prefill_split=args.prefill_split)
         if plan.workspace_bytes > ws.numel():
             raise RuntimeError("workspace too small for the per-step plan")
         if fp8_dev:

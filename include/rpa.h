@@ -110,6 +110,12 @@ typedef struct rpa_plan_options {
                                or RPA_DTYPE_FP8_E4M3 with dtype BF16: decode
                                batches only (every q_len <= 1), head_dim 128 or
                                256, run through rpa_forward_fp8kv               */
+  int32_t prefill_split;    /* 0 or -1: whole prefill work items; n > 0: lay
+                               the items' key tiles (128 keys each) end to end
+                               and cut them into ranges of n tiles, one per
+                               CTA; items crossing a range boundary run as
+                               parts whose fp32 partials a combine kernel
+                               merges                                           */
 } rpa_plan_options;
 
 /* What a plan chose; filled by rpa_plan_get_info. */
@@ -126,6 +132,8 @@ typedef struct rpa_plan_info {
   int32_t prefill_pairs;    /* 1: prefill runs on SM pairs, items are pairs of
                                query blocks                                     */
   int32_t kv_dtype;         /* dtype of the K/V pages (RPA_DTYPE_*)              */
+  int32_t prefill_split_items; /* prefill items split across CTAs              */
+  int32_t prefill_split_parts; /* parts those items became                     */
 } rpa_plan_info;
 
 typedef struct rpa_plan rpa_plan_t;
@@ -397,7 +405,8 @@ enum {
   RPA_KERNEL_PREFILL_TC = 2,     /* tensor-core prefill               */
   RPA_KERNEL_SIMT = 3,           /* CUDA-core (fp32) path             */
   RPA_KERNEL_KV_WRITE = 4,       /* KV-cache write of new tokens      */
-  RPA_KERNEL_PROLOGUE = 5        /* q/k/v norm + rotary + KV write    */
+  RPA_KERNEL_PROLOGUE = 5,       /* q/k/v norm + rotary + KV write    */
+  RPA_KERNEL_PREFILL_COMBINE = 6 /* combine of split prefill items    */
 };
 typedef struct rpa_trace_record {
   int32_t kernel; /* RPA_KERNEL_* */

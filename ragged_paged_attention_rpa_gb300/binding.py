@@ -46,7 +46,7 @@ EXPORTS = ["rpa_plan", "rpa_plan_destroy", "rpa_plan_get_info", "rpa_forward",
            "rpa_forward_qkv"]
 
 RPA_KERNEL_NAMES = {0: "decode_split", 1: "decode_combine", 2: "prefill_tc", 3: "simt",
-                    4: "kv_write", 5: "prologue"}
+                    4: "kv_write", 5: "prologue", 6: "prefill_combine"}
 
 
 class QkvNorm(ctypes.Structure):
@@ -67,7 +67,7 @@ class _Options(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_int32), ("path", ctypes.c_int32),
                 ("q_block", ctypes.c_int32), ("kv_split", ctypes.c_int32),
                 ("num_sms", ctypes.c_int32), ("prefill_pairs", ctypes.c_int32),
-                ("kv_dtype", ctypes.c_int32)]
+                ("kv_dtype", ctypes.c_int32), ("prefill_split", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -76,7 +76,8 @@ class PlanInfo(ctypes.Structure):
                 ("kv_split", ctypes.c_int32), ("max_splits", ctypes.c_int32),
                 ("num_prefill_items", ctypes.c_int32), ("prefill_ctas", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("prefill_pairs", ctypes.c_int32),
-                ("kv_dtype", ctypes.c_int32)]
+                ("kv_dtype", ctypes.c_int32), ("prefill_split_items", ctypes.c_int32),
+                ("prefill_split_parts", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: int(getattr(self, name)) for name, _ in self._fields_}
@@ -191,7 +192,7 @@ def rpa_plan(cu_q_lens_host, kv_lens_host, window_host, num_q_heads: int,
              num_kv_heads: int, head_dim: int, page_size: int, max_pages_per_seq: int,
              num_pages: int, dtype: int = RPA_DTYPE_BF16, path: int = RPA_PATH_AUTO,
              q_block: int = 0, kv_split: int = 0, num_sms: int = 0,
-             prefill_pairs: int = 0, kv_dtype: int = 0) -> Plan:
+             prefill_pairs: int = 0, kv_dtype: int = 0, prefill_split: int = 0) -> Plan:
     """rpa_plan from host (numpy) metadata; returns a Plan."""
     cu = _np_i32(cu_q_lens_host)
     kv = _np_i32(kv_lens_host)
@@ -202,7 +203,7 @@ def rpa_plan(cu_q_lens_host, kv_lens_host, window_host, num_q_heads: int,
     if win is not None and win.shape[0] != num_seqs:
         raise ValueError("window must have num_seqs entries")
     opts = _Options(ctypes.sizeof(_Options), path, q_block, kv_split, num_sms, prefill_pairs,
-                    kv_dtype)
+                    kv_dtype, prefill_split)
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     st = lib().rpa_plan(ctypes.byref(handle), _np_ptr(cu), _np_ptr(kv), _np_ptr(win),

@@ -66,7 +66,8 @@ rpa_status_t rpa_plan(rpa_plan_t** plan, const int32_t* cu_q_lens_host,
     std::memcpy(&o, opts, static_cast<size_t>(opts->struct_size));
   }
   if (o.q_block < 0 || o.kv_split < 0 || o.num_sms < 0 || o.prefill_pairs < 0 ||
-      o.prefill_pairs > 2 || o.kv_dtype < 0 || o.kv_dtype > RPA_DTYPE_FP8_E4M3)
+      o.prefill_pairs > 2 || o.kv_dtype < 0 || o.kv_dtype > RPA_DTYPE_FP8_E4M3 ||
+      o.prefill_split < -1 || o.prefill_split > 65535)
     return RPA_ERR_INVALID_ARG;
   rpa_status_t st = rpa::validate_metadata(cu_q_lens_host, kv_lens_host, num_seqs,
                                            page_size, max_pages_per_seq);
@@ -117,6 +118,8 @@ rpa_status_t rpa_plan_get_info(const rpa_plan_t* plan, rpa_plan_info* info) {
   info->workspace_bytes = static_cast<int64_t>(p.ws_bytes);
   info->prefill_pairs = p.prefill_pairs ? 1 : 0;
   info->kv_dtype = p.kv_fp8 ? RPA_DTYPE_FP8_E4M3 : p.dtype;
+  info->prefill_split_items = static_cast<int32_t>(p.psplit.size());
+  info->prefill_split_parts = p.n_split_items;
   return RPA_OK;
 }
 

@@ -232,7 +232,7 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
 // block, KV head), or with SM pairs (sequence, pair of adjacent query blocks,
 // KV head), costed by the keys the item streams.
 void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t* win,
-                  int32_t forced_q_block) {
+                  int32_t forced_q_block, int32_t forced_split) {
   const int32_t group = plan.hq / plan.hkv;
   const int32_t max_qb = prefill_tokens_per_block(plan.d, group);
   int32_t qb = max_qb;
@@ -240,6 +240,7 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
   plan.q_block = qb;
   struct Cost {
     int64_t cost;
+    int64_t tiles;
     PrefillItem item;
   };
   std::vector<Cost> all;
@@ -257,8 +258,12 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
       int64_t pos1 = std::min<int64_t>(static_cast<int64_t>(L) - ql + (b + 1) * span, L) - 1;
       int64_t lo = (w > 0 && pos0 - (w - 1) > 0) ? pos0 - (w - 1) : 0;
       int64_t keys = pos1 - lo + 1;
+      // Key tiles the kernel streams: from the 64-aligned tile start at or
+      // below the first visible key to the last query's position.
+      const int64_t key_first = lo / kPrefillTileAlign * kPrefillTileAlign;
+      const int64_t tiles = (pos1 - key_first) / kPrefillTileKeys + 1;
       for (int32_t h = 0; h < plan.hkv; ++h)
-        all.push_back({keys, PrefillItem{s, static_cast<int32_t>((b << 8) | h)}});
+        all.push_back({keys, tiles, PrefillItem{s, static_cast<int32_t>((b << 8) | h), 0}});
     }
   }
   // Longest first; ties keep (sequence, block, head) order, which keeps the
@@ -266,8 +271,83 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
   std::stable_sort(all.begin(), all.end(),
                    [](const Cost& a, const Cost& b) { return a.cost > b.cost; });
   plan.items.clear();
-  for (const Cost& c : all) plan.items.push_back(c.item);
+  plan.psplit.clear();
+  plan.n_split_items = 0;
   const int64_t slots = static_cast<int64_t>(plan.num_sms) * prefill_ctas_per_sm(plan.d);
+  // A persistent grid takes the items round-robin, longest first; its time
+  // is set by the CTA with the most tiles.  On request (prefill_split = n),
+  // lay every item's key tiles end to end and cut them into ranges of n
+  // tiles, one per CTA, as decode does: an item crossing a range boundary is
+  // split into parts, each leaving an fp32 partial that a combine merges.
+  // Not chosen automatically: on multi-token decode (one short item per
+  // sequence, the longest setting the step) GB300 measured 48.3 us split
+  // against 46.7 us whole, the kernel streaming each K tile in four column
+  // chunks, not the item balance, being the limit there.
+  const int64_t per = forced_split;
+  bool split = !plan.prefill_pairs && forced_split > 0 && !all.empty();
+  std::vector<std::vector<PrefillItem>> per_cta;
+  if (split) {
+    // Sequence order keeps an item's parts (and a sequence's items) adjacent.
+    std::vector<Cost> order = all;
+    std::stable_sort(order.begin(), order.end(), [](const Cost& a, const Cost& b) {
+      return a.item.seq != b.item.seq ? a.item.seq < b.item.seq
+                                      : a.item.qb_head < b.item.qb_head;
+    });
+    int64_t cta = 0, room = per, slot = 0;
+    per_cta.assign(1, {});
+    for (const Cost& c : order) {
+      int64_t j0 = 0;
+      PrefillSplit g{c.item.seq, c.item.qb_head, static_cast<int32_t>(slot), 0};
+      std::vector<std::pair<int64_t, int64_t>> parts;   // (cta, j0 << 32 | n)
+      while (j0 < c.tiles) {
+        if (room == 0) {
+          ++cta;
+          room = per;
+          per_cta.emplace_back();
+        }
+        const int64_t n = std::min(room, c.tiles - j0);
+        parts.push_back({cta, (j0 << 32) | n});
+        j0 += n;
+        room -= n;
+      }
+      if (parts.size() == 1) {
+        per_cta[static_cast<size_t>(parts[0].first)].push_back(c.item);
+        continue;
+      }
+      for (const auto& pr : parts) {
+        const int64_t pj0 = pr.second >> 32, pn = pr.second & 0xffffffff;
+        if (slot >= kSplitMaxSlots || pj0 >= kSplitMaxFirst || pn > kSplitMaxTiles) {
+          split = false;
+          break;
+        }
+        per_cta[static_cast<size_t>(pr.first)].push_back(
+            PrefillItem{c.item.seq, c.item.qb_head,
+                        split_code(static_cast<int32_t>(slot), static_cast<int32_t>(pj0),
+                                   static_cast<int32_t>(pn))});
+        ++slot;
+        ++g.nparts;
+      }
+      if (!split) break;
+      plan.psplit.push_back(g);
+    }
+    // CTA c runs items c, c + grid, ...: interleave the ranges, padding with
+    // skipped items (seq -1); all in one launch.
+    size_t rounds = 0;
+    for (const auto& v : per_cta) rounds = std::max(rounds, v.size());
+    const size_t grid = per_cta.size();
+    if (split && rounds * grid <= static_cast<size_t>(kMaxItemsPerLaunch)) {
+      for (size_t k = 0; k < rounds; ++k)
+        for (size_t c2 = 0; c2 < grid; ++c2)
+          plan.items.push_back(k < per_cta[c2].size() ? per_cta[c2][k]
+                                                      : PrefillItem{-1, 0, 0});
+      plan.n_split_items = static_cast<int32_t>(slot);
+      plan.prefill_ctas = static_cast<int32_t>(grid);
+      return;
+    }
+    plan.items.clear();
+    plan.psplit.clear();
+  }
+  for (const Cost& c : all) plan.items.push_back(c.item);
   const int64_t per_item = plan.prefill_pairs ? 2 : 1;      // CTAs per item
   plan.prefill_ctas = static_cast<int32_t>(
       per_item * std::min<int64_t>(static_cast<int64_t>(plan.items.size()), slots / per_item));
@@ -336,7 +416,8 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
   // Chosen only on request: on GB300 the pair kernel's cross-SM barrier
   // round trips cost more per tile than its halved copy traffic saves.
   plan.prefill_pairs = pairs_ok && plan.num_prefill > 0 && opts.prefill_pairs == 2;
-  if (tc_prefill && plan.num_prefill > 0) plan_prefill(plan, cu, kv, win, opts.q_block);
+  if (tc_prefill && plan.num_prefill > 0)
+    plan_prefill(plan, cu, kv, win, opts.q_block, opts.prefill_split);
 
   // Workspace: header, then the decode partials (two slots per decode CTA,
   // G x D fp32 each, plus G log2-sum-exps).
@@ -347,6 +428,15 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
     plan.off_partial_o = off;
     off += (rows * plan.d * sizeof(float) + 255) / 256 * 256;
     plan.off_partial_lse = off;
+    off += (rows * sizeof(float) + 255) / 256 * 256;
+  }
+  plan.off_ppart_o = plan.off_ppart_lse = 0;
+  if (plan.n_split_items > 0) {
+    // Prefill parts: one 128-row fp32 partial and its log2-sum-exps each.
+    const size_t rows = static_cast<size_t>(plan.n_split_items) * 128;
+    plan.off_ppart_o = off;
+    off += (rows * plan.d * sizeof(float) + 255) / 256 * 256;
+    plan.off_ppart_lse = off;
     off += (rows * sizeof(float) + 255) / 256 * 256;
   }
   plan.ws_bytes = off;

@@ -78,6 +78,10 @@ struct PrefillParams {
   unsigned char* ws;
   int32_t hq, group, qb_tokens, page_size, page_shift, box_rows_k, box_rows_v, mpps, num_pages;
   float scale_log2;
+  // Parts of split items (PrefillItem::split != 0): partial O / l and
+  // log2-sum-exp per row, in the part's slot.
+  float* ppart_o;      // [slot][kBM][D]
+  float* ppart_lse;    // [slot][kBM]
 };
 
 // A score tile's K streams through the K ring one 64-dimension chunk at a
@@ -126,6 +130,11 @@ struct Geom {
 
 __device__ __forceinline__ Geom item_geom(const PrefillParams& p, const PrefillItem& it) {
   Geom r;
+  if (it.seq < 0) {   // padding of an interleaved range list
+    r.ok = false;
+    r.ntiles = 0;
+    return r;
+  }
   r.seq = it.seq;
   r.g = it.qb_head & 255;
   const int32_t qb = it.qb_head >> 8;
@@ -144,6 +153,12 @@ __device__ __forceinline__ Geom item_geom(const PrefillParams& p, const PrefillI
   // 128-key boundary would mask up to 127 keys of a window's first tile).
   r.key_first = klo / kTileAlign * kTileAlign;
   r.ntiles = r.ok ? (pos_last - r.key_first) / kBN + 1 : 0;
+  if (it.split != 0) {
+    // One part of a split item: tiles [j0, j0 + n) of the item's range.
+    const int32_t j0 = split_first(it.split), n = split_tiles(it.split);
+    r.key_first += j0 * kBN;
+    r.ntiles = max(0, min(n, r.ntiles - j0));
+  }
   return r;
 }
 
@@ -200,6 +215,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (threadIdx.x == 0) report_error(p.ws, RPA_DEVERR_LAUNCH, blockIdx.x);
     return;
   }
+  // A combine of split items may be scheduled now; it waits for this grid.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   uint8_t* smem = smem_raw;
   __nv_bfloat16* q_s = reinterpret_cast<__nv_bfloat16*>(smem + Lay::kQOff);
   __nv_bfloat16* k_s = reinterpret_cast<__nv_bfloat16*>(smem + Lay::kKOff);
@@ -261,7 +278,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int it = blockIdx.x; it < items.n && alive; it += gridDim.x) {
       const Geom gm = item_geom(p, items.items[it]);
       if (!gm.ok) {
-        if (lane == 0 && is_k) report_error(p.ws, RPA_DEVERR_LENGTHS, gm.seq);
+        if (lane == 0 && is_k && items.items[it].seq >= 0)
+          report_error(p.ws, RPA_DEVERR_LENGTHS, gm.seq);
         continue;
       }
       const uint32_t Icur = I++;
@@ -535,7 +553,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         mbar_arrive(&B.p_full[sb]);
       }
       if (!alive) break;
-      if (gm.ntiles == 0) continue;
+      if (gm.ntiles == 0) {
+        // An empty part still tells the combine that it holds nothing.
+        if (items.items[it].split != 0 && h == 0 && valid)
+          p.ppart_lse[static_cast<int64_t>(split_slot(items.items[it].split)) * kBM + r] = -INFINITY;
+        continue;
+      }
       // Epilogue: the row sum over both halves, then wait for the last PV
       // and write this half's columns: O / l -> bf16 -> out.
       l += swap(l);
@@ -549,6 +572,31 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
       __nv_bfloat16* orow =
           p.out + (static_cast<int64_t>(gm.t0 + tok) * p.hq + gm.g * G + head) * D;
+      if (items.items[it].split != 0) {
+        // A part of a split item: fp32 O / l and the row's log2-sum-exp (a
+        // row with no visible key here: zeros and -inf).
+        const int64_t slot = split_slot(items.items[it].split);
+        float* prow = p.ppart_o + (slot * kBM + r) * D;
+        if (h == 0 && valid)
+          p.ppart_lse[slot * kBM + r] = (l > 0.f) ? m_ref + __log2f(l) : -INFINITY;
+#pragma unroll 1
+        for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + Lay::kOCol + c0, o);
+          tmem_wait_ld();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(prow + c0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
+                                   __uint_as_float(o[4 * q + 2]) * inv,
+                                   __uint_as_float(o[4 * q + 3]) * inv);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&B.o_free);
+        continue;
+      }
 #pragma unroll 1
       for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
         uint32_t o[32];
@@ -580,6 +628,91 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc_fence_after();
     tmem_dealloc(tmem, Lay::kCols);
   }
+}
+
+struct SplitList {
+  int32_t n;
+  PrefillSplit g[kMaxSplitGroupsPerLaunch];
+};
+
+// Merge the parts of each split item: for every row of the item's query
+// block, out = sum_k 2^(lse_k - M) O_k / sum_k 2^(lse_k - M) with M the
+// largest lse_k, rounded to bf16.  Grid (items, rows / 8), one warp per row:
+// the lanes read the parts' log2-sum-exps together, then every part's row
+// loads are issued before they are summed.
+template <int D>
+__global__ void __launch_bounds__(256)
+prefill_combine_kernel(const PrefillParams p, const __grid_constant__ SplitList gl) {
+  constexpr int E = D / 32;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (static_cast<int>(blockIdx.x) >= gl.n) return;
+  const PrefillSplit g = gl.g[blockIdx.x];
+  const int G = p.group;
+  const int32_t kvh = g.qb_head & 255, qb = g.qb_head >> 8;
+  const int32_t q0 = __ldg(p.cu_q_lens + g.seq);
+  const int32_t ql = __ldg(p.cu_q_lens + g.seq + 1) - q0;
+  const int32_t ntok = min(p.qb_tokens, ql - qb * p.qb_tokens);
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= ntok * G) return;
+  // Largest log2-sum-exp over the parts (lane k reads parts k, k + 32, ...).
+  float M = -INFINITY;
+  for (int k = lane; k < g.nparts; k += 32)
+    M = fmaxf(M, p.ppart_lse[static_cast<int64_t>(g.slot0 + k) * kBM + r]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float acc[E], wsum = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int k0 = 0; k0 < g.nparts; k0 += 32) {
+    const int nk = min(32, g.nparts - k0);
+    const float lse_l = lane < nk ? p.ppart_lse[static_cast<int64_t>(g.slot0 + k0 + lane) * kBM + r]
+                                  : -INFINITY;
+    const float w_l = lse_l == -INFINITY ? 0.f : fast_exp2(lse_l - M);
+    for (int k = 0; k < nk; ++k) {
+      const float w = __shfl_sync(0xffffffffu, w_l, k);
+      wsum += w;
+      const float* src = p.ppart_o + (static_cast<int64_t>(g.slot0 + k0 + k) * kBM + r) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; e += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src + e);
+        acc[e] = fmaf(w, v.x, acc[e]);
+        acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+        acc[e + 2] = fmaf(w, v.z, acc[e + 2]);
+        acc[e + 3] = fmaf(w, v.w, acc[e + 3]);
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const int tok = r / G, head = r % G;
+  __nv_bfloat16* dst = p.out +
+      (static_cast<int64_t>(q0 + qb * p.qb_tokens + tok) * p.hq + kvh * G + head) * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e += 2)
+    *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+}
+
+template <int D>
+int launch_prefill_combine(const Plan& plan, const PrefillParams& p, cudaStream_t stream) {
+  static SplitList gl;  // host staging; copied into the launch parameters
+  const int n = static_cast<int>(plan.psplit.size());
+  for (int off = 0; off < n; off += kMaxSplitGroupsPerLaunch) {
+    gl.n = std::min(kMaxSplitGroupsPerLaunch, n - off);
+    for (int i = 0; i < gl.n; ++i) gl.g[i] = plan.psplit[off + i];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gl.n, kBM / 8);   // 8 rows (warps) per CTA
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_combine_kernel<D>, p, gl);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    trace_mark(RPA_KERNEL_PREFILL_COMBINE, stream);
+  }
+  return 0;
 }
 
 template <int D>
@@ -623,6 +756,8 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   p.mpps = plan.mpps;
   p.num_pages = plan.num_pages;
   p.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  p.ppart_o = reinterpret_cast<float*>(a.workspace + plan.off_ppart_o);
+  p.ppart_lse = reinterpret_cast<float*>(a.workspace + plan.off_ppart_lse);
   static ItemList list;  // host staging; copied into the launch parameters
   const size_t n = plan.items.size();
   for (size_t off = 0; off < n; off += kMaxItemsPerLaunch) {
@@ -635,6 +770,7 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
     if (e != cudaSuccess) return static_cast<int>(e);
     trace_mark(RPA_KERNEL_PREFILL_TC, stream);
   }
+  if (!plan.psplit.empty()) return launch_prefill_combine<D>(plan, p, stream);
   return 0;
 }
 

@@ -10,6 +10,12 @@
 
 #include "rpa.h"
 
+#ifdef __CUDACC__
+#define RPA_HD __host__ __device__
+#else
+#define RPA_HD
+#endif
+
 namespace rpa {
 
 // Workspace layout: a 256-byte header (error word first), then the decode
@@ -21,11 +27,41 @@ constexpr size_t kHeaderBytes = 256;
 struct PrefillItem {
   int32_t seq;
   int32_t qb_head;  // (query block index << 8) | kv head
+  // 0: every key tile of the item.  Else one part of an item whose key
+  // tiles the plan split across CTAs: (slot << 21) | (first tile << 10) |
+  // tile count, as unsigned bits; the part leaves an fp32 partial in `slot`
+  // and a combine merges the parts.  seq < 0: padding, skipped.
+  int32_t split;
 };
+constexpr int kSplitMaxSlots = 2048, kSplitMaxFirst = 2048, kSplitMaxTiles = 1023;
+RPA_HD constexpr int32_t split_code(int32_t slot, int32_t j0, int32_t n) {
+  return static_cast<int32_t>((static_cast<uint32_t>(slot) << 21) |
+                              (static_cast<uint32_t>(j0) << 10) | static_cast<uint32_t>(n));
+}
+RPA_HD constexpr int32_t split_slot(int32_t c) {
+  return static_cast<int32_t>(static_cast<uint32_t>(c) >> 21);
+}
+RPA_HD constexpr int32_t split_first(int32_t c) {
+  return static_cast<int32_t>((static_cast<uint32_t>(c) >> 10) & 2047u);
+}
+RPA_HD constexpr int32_t split_tiles(int32_t c) {
+  return static_cast<int32_t>(static_cast<uint32_t>(c) & 1023u);
+}
 
 // Most work items one tensor-core prefill launch carries in its parameters;
 // longer lists are split over several launches.
-constexpr int kMaxItemsPerLaunch = 3072;
+constexpr int kMaxItemsPerLaunch = 2048;
+
+// Score tiles of the tensor-core prefill: 128 keys, starting on multiples of
+// 64 keys at or below the first visible key.
+constexpr int kPrefillTileKeys = 128;
+constexpr int kPrefillTileAlign = 64;
+
+// An item split into parts: its partial slots are [slot0, slot0 + nparts).
+struct PrefillSplit {
+  int32_t seq, qb_head, slot0, nparts;
+};
+constexpr int kMaxSplitGroupsPerLaunch = 1024;
 
 // Decode schedule limits: segments one decode launch carries in its
 // parameters (two sizes), and segments / pages one decode CTA's range may
@@ -91,11 +127,14 @@ struct Plan {
   int32_t num_prefill = 0;
   int32_t q_block = 0;
   bool prefill_pairs = false;      // items are pairs of query blocks (SM-pair kernel)
-  std::vector<PrefillItem> items;  // longest first
+  std::vector<PrefillItem> items;  // longest first, or CTA ranges interleaved
+  std::vector<PrefillSplit> psplit; // items split across CTAs (combined afterwards)
+  int32_t n_split_items = 0;        // partial slots (parts of split items)
   int32_t prefill_ctas = 0;
 
   // Workspace.
   size_t off_partial_o = 0, off_partial_lse = 0, ws_bytes = kHeaderBytes;
+  size_t off_ppart_o = 0, off_ppart_lse = 0;   // prefill parts: [slot][128 rows][D], [slot][128]
 };
 
 // Scheduler (plan.cpp): fills everything but the problem description, which

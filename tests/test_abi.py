@@ -248,3 +248,61 @@ def test_fp8_kv_plans_are_decode_only():
     with pytest.raises(RpaError) as e:
         plan_of(d64, kv_dtype=binding.RPA_DTYPE_FP8_E4M3)
     assert e.value.status == binding.RPA_ERR_UNSUPPORTED
+
+
+def prefill_tiles(b, q_block):
+    """Key tiles (128 keys, starting on a multiple of 64 at or below the first
+    visible key) of every prefill work item (sequence, query block), restated
+    from the attention's visibility rule."""
+    tiles = []
+    for s in range(b.num_seqs):
+        ql = int(b.cu_q_lens[s + 1] - b.cu_q_lens[s])
+        if ql <= 1:
+            continue
+        L = int(b.kv_lens[s])
+        w = 0 if b.window is None else int(b.window[s])
+        for blk in range(-(-ql // q_block)):
+            pos0 = L - ql + blk * q_block
+            pos1 = min(L - ql + (blk + 1) * q_block, L) - 1
+            lo = pos0 - (w - 1) if (w > 0 and pos0 - (w - 1) > 0) else 0
+            tiles.append((pos1 - lo // 64 * 64) // 128 + 1)
+    return tiles
+
+
+def range_parts(tiles, per):
+    """Items' tiles laid end to end and cut into ranges of `per` tiles: the
+    ranges, and the parts of items that cross a range boundary."""
+    ranges, parts, pos = 0, 0, 0
+    for t in tiles:
+        first, last = pos // per, (pos + t - 1) // per
+        if last > first:
+            parts += last - first + 1
+        pos += t
+    return -(-pos // per), parts
+
+
+def test_prefill_items_split_on_request():
+    """prefill_split = n lays the items' key tiles end to end (sequence order)
+    and cuts them into one range of n tiles per CTA; items crossing a range
+    boundary become parts.  Without the option nothing is split."""
+    b = workloads.WORKLOADS["spec_decode"](meta_only=True)
+    assert plan_of(b).info()["prefill_split_items"] == 0
+    per = 8
+    info = plan_of(b, prefill_split=per).info()
+    tiles = prefill_tiles(b, info["q_block"])           # sequence order
+    grid, parts = range_parts(tiles, per)
+    assert info["prefill_ctas"] == grid
+    assert info["prefill_split_parts"] == parts > 0
+    assert info["num_prefill_items"] % grid == 0        # interleaved rounds, padded
+    # Workspace: one 128-row fp32 partial (and log2-sum-exps) per part.
+    assert info["workspace_bytes"] >= parts * 128 * (256 + 1) * 4
+    assert plan_of(b, prefill_split=-1).info()["prefill_split_items"] == 0
+
+
+def test_prefill_split_forced():
+    b = workloads.make_batch([300, 20], [4000, 900], num_q_heads=8, num_kv_heads=2,
+                             head_dim=128, page_size=64, meta_only=True)
+    info = plan_of(b, prefill_split=3).info()
+    tiles = [t for t in prefill_tiles(b, info["q_block"]) for _ in range(2)]   # 2 KV heads
+    grid, parts = range_parts(tiles, 3)
+    assert info["prefill_split_parts"] == parts and info["prefill_ctas"] == grid

@@ -331,3 +331,16 @@ def test_spec_decode_workload_sampled():
     assert err == 0
     rows = sample_rows(b, n_random=8)
     assert_bf16_close(got[rows], oracle_rows(b, rows), "spec_decode")
+
+
+@pytest.mark.parametrize("case,tiles", [(0, 2), (1, 2), (2, 1), (3, 1), (5, 1), (7, 2), (8, 1)])
+def test_prefill_split_parts(case, tiles):
+    """Prefill items cut into parts of one or two key tiles (forced), each
+    part's fp32 partial merged by the combine kernel, against the oracle."""
+    ql, kv, hq, hkv, d, p, win = PREFILL[case]
+    b = workloads.make_batch(ql, kv, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                             page_size=p, windows=win, seed=1000 + case)
+    got, err, plan = run_gpu(b, prefill_split=tiles)
+    info = plan.info()
+    assert err == 0 and info["prefill_split_items"] > 0
+    assert_bf16_close(got, oracle_rows(b), "split prefill case %d" % case)
