@@ -171,11 +171,30 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
     bool uniform = forced_tokens > 0;
     if (!uniform) {
       const int32_t cap = std::min<int32_t>(plan.num_sms, kMaxDecodeGrid);
-      int64_t lo = kDecodeSegCost + 1, hi = total + static_cast<int64_t>(kDecodeSegCost) * (se - sb + 1);
+      const int64_t segs = se - sb;
+      // Bounds on the smallest feasible cap T: every segment costs at least
+      // once, so cap ranges need T >= (blocks + cost x segments) / cap; and a
+      // range the greedy cut closes costs at least T - cost, while the ranges
+      // together cost at most blocks + cost x (segments + cap), so T at that
+      // sum / (cap - 1) + cost + 1 needs no more than cap ranges (the table
+      // limits aside, which the check below covers).
+      int64_t lo = std::max<int64_t>(kDecodeSegCost + 1,
+                                     ceil_div(total + kDecodeSegCost * segs, static_cast<int64_t>(cap)));
+      int64_t hi = total + static_cast<int64_t>(kDecodeSegCost) * (segs + 1);
       cut(sb, se, hi, cap, starts);
       if (static_cast<int32_t>(starts.size()) - 1 > cap) {
         uniform = true;  // the tables' limits alone need more CTAs than listed
       } else {
+        if (cap > 1) {
+          const int64_t hi2 =
+              ceil_div(total + kDecodeSegCost * (segs + cap), static_cast<int64_t>(cap) - 1) +
+              kDecodeSegCost + 1;
+          if (hi2 < hi) {
+            cut(sb, se, hi2, cap, starts);
+            if (static_cast<int32_t>(starts.size()) - 1 <= cap && starts.back() == total) hi = hi2;
+          }
+        }
+        lo = std::min(lo, hi);
         while (lo < hi) {
           const int64_t mid = (lo + hi) / 2;
           cut(sb, se, mid, cap, starts);
