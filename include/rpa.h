@@ -134,6 +134,7 @@ typedef struct rpa_plan_info {
   int32_t kv_dtype;         /* dtype of the K/V pages (RPA_DTYPE_*)              */
   int32_t prefill_split_items; /* prefill items split across CTAs              */
   int32_t prefill_split_parts; /* parts those items became                     */
+  int32_t prefill_max_tiles;   /* key tiles of the busiest prefill CTA        */
 } rpa_plan_info;
 
 typedef struct rpa_plan rpa_plan_t;

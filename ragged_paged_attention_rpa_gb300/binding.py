@@ -77,7 +77,7 @@ class PlanInfo(ctypes.Structure):
                 ("num_prefill_items", ctypes.c_int32), ("prefill_ctas", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("prefill_pairs", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("prefill_split_items", ctypes.c_int32),
-                ("prefill_split_parts", ctypes.c_int32)]
+                ("prefill_split_parts", ctypes.c_int32), ("prefill_max_tiles", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: int(getattr(self, name)) for name, _ in self._fields_}

@@ -120,6 +120,7 @@ rpa_status_t rpa_plan_get_info(const rpa_plan_t* plan, rpa_plan_info* info) {
   info->kv_dtype = p.kv_fp8 ? RPA_DTYPE_FP8_E4M3 : p.dtype;
   info->prefill_split_items = static_cast<int32_t>(p.psplit.size());
   info->prefill_split_parts = p.n_split_items;
+  info->prefill_max_tiles = p.prefill_max_tiles;
   return RPA_OK;
 }
 

@@ -291,7 +291,9 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
                    [](const Cost& a, const Cost& b) { return a.cost > b.cost; });
   plan.items.clear();
   plan.psplit.clear();
+  plan.pcta0.clear();
   plan.n_split_items = 0;
+  plan.prefill_max_tiles = 0;
   const int64_t slots = static_cast<int64_t>(plan.num_sms) * prefill_ctas_per_sm(plan.d);
   // A persistent grid takes the items round-robin, longest first; its time
   // is set by the CTA with the most tiles.  On request (prefill_split = n),
@@ -349,16 +351,18 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
       if (!split) break;
       plan.psplit.push_back(g);
     }
-    // CTA c runs items c, c + grid, ...: interleave the ranges, padding with
-    // skipped items (seq -1); all in one launch.
-    size_t rounds = 0;
-    for (const auto& v : per_cta) rounds = std::max(rounds, v.size());
+    // CTA c runs its range's parts in order (per-CTA lists, one launch).
+    size_t count = 0;
+    for (const auto& v : per_cta) count += v.size();
     const size_t grid = per_cta.size();
-    if (split && rounds * grid <= static_cast<size_t>(kMaxItemsPerLaunch)) {
-      for (size_t k = 0; k < rounds; ++k)
-        for (size_t c2 = 0; c2 < grid; ++c2)
-          plan.items.push_back(k < per_cta[c2].size() ? per_cta[c2][k]
-                                                      : PrefillItem{-1, 0, 0});
+    if (split && count <= static_cast<size_t>(kMaxItemsPerLaunch) &&
+        grid <= static_cast<size_t>(kMaxPrefillGrid)) {
+      plan.prefill_max_tiles = static_cast<int32_t>(per);
+      plan.pcta0.assign(1, 0);
+      for (const auto& v : per_cta) {
+        plan.items.insert(plan.items.end(), v.begin(), v.end());
+        plan.pcta0.push_back(static_cast<int32_t>(plan.items.size()));
+      }
       plan.n_split_items = static_cast<int32_t>(slot);
       plan.prefill_ctas = static_cast<int32_t>(grid);
       return;
@@ -366,7 +370,46 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
     plan.items.clear();
     plan.psplit.clear();
   }
+  // Longest processing time first: each item, longest first, goes to the CTA
+  // with the fewest tiles so far; CTA c then runs its list in that order.
+  // (Striding over the longest-first list instead gives CTA 0 the largest
+  // item of every round: +7% tiles on the busiest CTA for a causal 8k
+  // prefill, +38% on the mixed batch's prefill part.)
+  const int64_t grid = std::min<int64_t>(static_cast<int64_t>(all.size()), slots);
+  if (!plan.prefill_pairs && static_cast<int64_t>(all.size()) <= kMaxItemsPerLaunch &&
+      grid <= kMaxPrefillGrid && grid > 0) {
+    using Load = std::pair<int64_t, int32_t>;   // (tiles so far, CTA)
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int32_t c = 0; c < grid; ++c) heap.push({0, c});
+    std::vector<std::vector<PrefillItem>> lists(static_cast<size_t>(grid));
+    for (const Cost& c : all) {
+      Load l = heap.top();
+      heap.pop();
+      lists[static_cast<size_t>(l.second)].push_back(c.item);
+      heap.push({l.first + c.tiles, l.second});
+    }
+    plan.pcta0.assign(1, 0);
+    for (const auto& v : lists) {
+      plan.items.insert(plan.items.end(), v.begin(), v.end());
+      plan.pcta0.push_back(static_cast<int32_t>(plan.items.size()));
+    }
+    plan.prefill_ctas = static_cast<int32_t>(grid);
+    int64_t busiest = 0;
+    while (!heap.empty()) {
+      busiest = std::max(busiest, heap.top().first);
+      heap.pop();
+    }
+    plan.prefill_max_tiles = static_cast<int32_t>(busiest);
+    return;
+  }
   for (const Cost& c : all) plan.items.push_back(c.item);
+  {
+    const int64_t g = std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(all.size()),
+                                                             slots / (plan.prefill_pairs ? 2 : 1)));
+    std::vector<int64_t> load(static_cast<size_t>(g), 0);
+    for (size_t i = 0; i < all.size(); ++i) load[i % static_cast<size_t>(g)] += all[i].tiles;
+    plan.prefill_max_tiles = static_cast<int32_t>(*std::max_element(load.begin(), load.end()));
+  }
   const int64_t per_item = plan.prefill_pairs ? 2 : 1;      // CTAs per item
   plan.prefill_ctas = static_cast<int32_t>(
       per_item * std::min<int64_t>(static_cast<int64_t>(plan.items.size()), slots / per_item));

@@ -64,10 +64,24 @@ constexpr int kPolyEvery = 32;  // one pair of exponentials in 32 on the FMA pip
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait, then give up
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
 
+// The launch's items.  n_ctas > 0: CTA c runs items [cta0[c], cta0[c + 1])
+// in order (the plan's per-CTA lists); else CTA c runs c, c + grid, ...
 struct ItemList {
   int32_t n;
+  int32_t n_ctas;
+  int32_t cta0[kMaxPrefillGrid + 1];
   PrefillItem items[kMaxItemsPerLaunch];
 };
+
+struct ItemRange {
+  int32_t begin, end, step;
+};
+
+__device__ __forceinline__ ItemRange my_items(const ItemList& items) {
+  if (items.n_ctas > 0)
+    return ItemRange{items.cta0[blockIdx.x], items.cta0[blockIdx.x + 1], 1};
+  return ItemRange{static_cast<int32_t>(blockIdx.x), items.n, static_cast<int32_t>(gridDim.x)};
+}
 
 struct PrefillParams {
   const int32_t* page_table;
@@ -218,6 +232,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // A combine of split items may be scheduled now; it waits for this grid.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   uint8_t* smem = smem_raw;
+  const ItemRange mine = my_items(items);
   __nv_bfloat16* q_s = reinterpret_cast<__nv_bfloat16*>(smem + Lay::kQOff);
   __nv_bfloat16* k_s = reinterpret_cast<__nv_bfloat16*>(smem + Lay::kKOff);
   __nv_bfloat16* v_s = reinterpret_cast<__nv_bfloat16*>(smem + Lay::kVOff);
@@ -275,7 +290,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint32_t C = 0, I = 0, issued_q = 0;
     const uint32_t q_box_bytes = static_cast<uint32_t>(G * p.qb_tokens) * 128u;
     bool alive = true;
-    for (int it = blockIdx.x; it < items.n && alive; it += gridDim.x) {
+    for (int it = mine.begin; it < mine.end && alive; it += mine.step) {
       const Geom gm = item_geom(p, items.items[it]);
       if (!gm.ok) {
         if (lane == 0 && is_k && items.items[it].seq >= 0)
@@ -392,7 +407,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mma_commit(&B.s_full[Ts & 1]);
       return true;
     };
-    for (int it = blockIdx.x; it < items.n && alive; it += gridDim.x) {
+    for (int it = mine.begin; it < mine.end && alive; it += mine.step) {
       const Geom gm = item_geom(p, items.items[it]);
       if (!gm.ok) continue;
       alive = wait(&B.q_full, I & 1);
@@ -449,7 +464,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (!ok) alive = false;
       return o;
     };
-    for (int it = blockIdx.x; it < items.n && alive; it += gridDim.x) {
+    for (int it = mine.begin; it < mine.end && alive; it += mine.step) {
       const Geom gm = item_geom(p, items.items[it]);
       if (!gm.ok) continue;
       const bool valid = tok < gm.ntok && r < G * p.qb_tokens;
@@ -764,7 +779,17 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
     const int cnt = static_cast<int>(std::min<size_t>(kMaxItemsPerLaunch, n - off));
     list.n = cnt;
     for (int i = 0; i < cnt; ++i) list.items[i] = plan.items[off + i];
-    const int grid = std::min(cnt, plan.prefill_ctas);
+    int grid = std::min(cnt, plan.prefill_ctas);
+    list.n_ctas = 0;
+    if (!plan.pcta0.empty()) {
+      // Per-CTA lists (the plan keeps them to one launch).
+      if (off != 0 || plan.pcta0.back() != cnt ||
+          static_cast<int>(plan.pcta0.size()) - 1 > kMaxPrefillGrid)
+        return static_cast<int>(cudaErrorInvalidValue);
+      grid = static_cast<int>(plan.pcta0.size()) - 1;
+      list.n_ctas = grid;
+      for (int c = 0; c <= grid; ++c) list.cta0[c] = plan.pcta0[c];
+    }
     prefill_tc_kernel<D><<<grid, kThreads, Lay::kBytes, stream>>>(tq, tk, tv, p, list);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return static_cast<int>(e);

@@ -62,6 +62,9 @@ struct PrefillSplit {
   int32_t seq, qb_head, slot0, nparts;
 };
 constexpr int kMaxSplitGroupsPerLaunch = 1024;
+// Largest persistent prefill grid whose per-CTA item lists the launch
+// parameters carry.
+constexpr int kMaxPrefillGrid = 256;
 
 // Decode schedule limits: segments one decode launch carries in its
 // parameters (two sizes), and segments / pages one decode CTA's range may
@@ -127,7 +130,11 @@ struct Plan {
   int32_t num_prefill = 0;
   int32_t q_block = 0;
   bool prefill_pairs = false;      // items are pairs of query blocks (SM-pair kernel)
-  std::vector<PrefillItem> items;  // longest first, or CTA ranges interleaved
+  std::vector<PrefillItem> items;  // longest first, or per-CTA lists (pcta0)
+  // Per-CTA item lists: CTA c runs items [pcta0[c], pcta0[c + 1]) in order;
+  // empty: CTA c runs items c, c + grid, ... (a list too long for one launch).
+  std::vector<int32_t> pcta0;
+  int32_t prefill_max_tiles = 0;    // key tiles of the busiest CTA
   std::vector<PrefillSplit> psplit; // items split across CTAs (combined afterwards)
   int32_t n_split_items = 0;        // partial slots (parts of split items)
   int32_t prefill_ctas = 0;

@@ -271,14 +271,17 @@ def prefill_tiles(b, q_block):
 
 def range_parts(tiles, per):
     """Items' tiles laid end to end and cut into ranges of `per` tiles: the
-    ranges, and the parts of items that cross a range boundary."""
-    ranges, parts, pos = 0, 0, 0
+    ranges, and the parts of items that cross a range boundary (and the items
+    that do not)."""
+    parts, whole, pos = 0, 0, 0
     for t in tiles:
         first, last = pos // per, (pos + t - 1) // per
         if last > first:
             parts += last - first + 1
+        else:
+            whole += 1
         pos += t
-    return -(-pos // per), parts
+    return -(-pos // per), parts, whole
 
 
 def test_prefill_items_split_on_request():
@@ -290,10 +293,10 @@ def test_prefill_items_split_on_request():
     per = 8
     info = plan_of(b, prefill_split=per).info()
     tiles = prefill_tiles(b, info["q_block"])           # sequence order
-    grid, parts = range_parts(tiles, per)
+    grid, parts, whole = range_parts(tiles, per)
     assert info["prefill_ctas"] == grid
     assert info["prefill_split_parts"] == parts > 0
-    assert info["num_prefill_items"] % grid == 0        # interleaved rounds, padded
+    assert info["num_prefill_items"] == parts + whole   # per-CTA lists, no padding
     # Workspace: one 128-row fp32 partial (and log2-sum-exps) per part.
     assert info["workspace_bytes"] >= parts * 128 * (256 + 1) * 4
     assert plan_of(b, prefill_split=-1).info()["prefill_split_items"] == 0
@@ -304,5 +307,29 @@ def test_prefill_split_forced():
                              head_dim=128, page_size=64, meta_only=True)
     info = plan_of(b, prefill_split=3).info()
     tiles = [t for t in prefill_tiles(b, info["q_block"]) for _ in range(2)]   # 2 KV heads
-    grid, parts = range_parts(tiles, 3)
+    grid, parts, _ = range_parts(tiles, 3)
     assert info["prefill_split_parts"] == parts and info["prefill_ctas"] == grid
+
+
+def lpt_busiest(tiles, n):
+    """Longest processing time first: each item, longest first, to the CTA
+    with the fewest tiles so far (ties: lowest index); the busiest CTA."""
+    import heapq
+    heap = [(0, c) for c in range(n)]
+    for t in sorted(tiles, reverse=True):
+        load, c = heapq.heappop(heap)
+        heapq.heappush(heap, (load + t, c))
+    return max(load for load, _ in heap)
+
+
+@pytest.mark.parametrize("name", ["causal_prefill", "swa_prefill", "mixed"])
+def test_prefill_items_scheduled_longest_first_to_least_loaded(name):
+    b = workloads.WORKLOADS[name](meta_only=True)
+    info = plan_of(b).info()
+    tiles = [t for t in prefill_tiles(b, info["q_block"]) for _ in range(b.num_kv_heads)]
+    n = min(len(tiles), 152)
+    assert info["prefill_ctas"] == n
+    assert info["prefill_max_tiles"] == lpt_busiest(tiles, n)
+    # Striding the longest-first list would load the busiest CTA more.
+    by_len = sorted(tiles, reverse=True)
+    assert max(sum(by_len[c::n]) for c in range(n)) >= info["prefill_max_tiles"]
