@@ -315,6 +315,22 @@ def dist_setup():
     return world, rank, local, pg
 
 
+def max_over_ranks(x: float, dist) -> float:
+    """The largest value of x over the ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, tokens: int, steps: int, total_ms: float) -> float:
+    """Whole-job query tokens/s: every rank processes `tokens` per step, the
+    job takes the slowest rank's time."""
+    return world * tokens * steps / (total_ms / 1e3)
+
+
 def run_reference(args, world, rank):
     """The reference arm: the CPU oracle, as it stands, on this host's cores."""
     if rank != 0:
@@ -536,10 +552,7 @@ def main():
     else:
         step_ms = [a.elapsed_time(e) for a, e in ev]
         total_ms = float(sum(step_ms))
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist)
     if binding.rpa_get_device_error(ws) != 0:
         raise SystemExit("device error word set during the timed region")
     if R:
@@ -593,7 +606,7 @@ def main():
     peaks = load_peaks()
     tokens = b.total_q
     ms_per_step = total_ms / K
-    value = world * tokens * K / (total_ms / 1e3)
+    value = job_value(world, tokens, K, total_ms)
     dom = max(kernels, key=lambda k: kernels[k]["avg_us"] * kernels[k]["launches_per_step"])
     dom_us = kernels[dom]["avg_us"]
     # The dominant kernel's own work: the decode sequences' bytes for the
