@@ -96,7 +96,16 @@ struct PrefillParams {
   // log2-sum-exp per row, in the part's slot.
   float* ppart_o;      // [slot][kBM][D]
   float* ppart_lse;    // [slot][kBM]
+  int32_t out_v8;      // `out` is 32-byte aligned: the epilogue stores 32 bytes at once
 };
+
+// One 32-byte store (eight 32-bit words) to a 32-byte aligned address.
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst),
+               "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+               "r"(w[7])
+               : "memory");
+}
 
 // A score tile's K streams through the K ring one 64-dimension chunk at a
 // time (128 keys x 128 B = one stage); its V streams through the V ring
@@ -464,8 +473,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (!ok) alive = false;
       return o;
     };
+    // The next item's geometry is read while this one runs (its loads
+    // would otherwise sit between this item's epilogue and the next tile).
+    Geom gm_next;
+    gm_next.ok = false;
+    if (mine.begin < mine.end) gm_next = item_geom(p, items.items[mine.begin]);
     for (int it = mine.begin; it < mine.end && alive; it += mine.step) {
-      const Geom gm = item_geom(p, items.items[it]);
+      const Geom gm = gm_next;
+      if (it + mine.step < mine.end) gm_next = item_geom(p, items.items[it + mine.step]);
       if (!gm.ok) continue;
       const bool valid = tok < gm.ntok && r < G * p.qb_tokens;
       const int32_t pos = gm.pos_first + tok;
@@ -618,15 +633,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tmem_ld32(lane_addr + Lay::kOCol + c0, o);
         tmem_wait_ld();
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+          // Each thread writes 64 bytes of its own row: two 32-byte stores
+          // when `out` is 32-byte aligned (half the store transactions of a
+          // warp that touches 32 rows at once), else four 16-byte ones.
+          uint32_t w[16];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-            dst[q] = v;
+          for (int q = 0; q < 16; ++q)
+            w[q] = pack_bf16x2(__uint_as_float(o[2 * q]) * inv, __uint_as_float(o[2 * q + 1]) * inv);
+          if (p.out_v8) {
+            st_global_v8(orow + c0, w);
+            st_global_v8(orow + c0 + 16, w + 8);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
           }
         }
       }
@@ -771,6 +791,7 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   p.mpps = plan.mpps;
   p.num_pages = plan.num_pages;
   p.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0 ? 1 : 0;
   p.ppart_o = reinterpret_cast<float*>(a.workspace + plan.off_ppart_o);
   p.ppart_lse = reinterpret_cast<float*>(a.workspace + plan.off_ppart_lse);
   static ItemList list;  // host staging; copied into the launch parameters
