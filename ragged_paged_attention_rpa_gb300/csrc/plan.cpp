@@ -96,11 +96,13 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
   if (nseg == 0) return;
   const std::vector<int32_t>& blk0 = plan.dseg_blk0;
   const int32_t P = plan.p;
+  int32_t pshift = 0;                      // page sizes are powers of two
+  while ((1 << pshift) < P) ++pshift;
   // Pages holding local blocks [jb, jb + t) of segment k.
   auto pages_of = [&](int32_t k, int32_t jb, int32_t t) {
     const int64_t kb = seg_lo[k] + 16 * static_cast<int64_t>(jb);
     const int64_t ke = seg_lo[k] + 16 * static_cast<int64_t>(jb + t);
-    return static_cast<int32_t>((ke - 1) / P - kb / P + 1);
+    return static_cast<int32_t>(((ke - 1) >> pshift) - (kb >> pshift) + 1);
   };
   // Segments and pages touched by CTA range [b0, b1) of launch segments [sb, se).
   auto fits = [&](int32_t sb, int32_t se, int32_t bpc) {
@@ -146,7 +148,7 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
         const int32_t room = kMaxCtaPages - pages;
         if (pages_of(k, jb, static_cast<int32_t>(t)) > room) {
           const int64_t kb = seg_lo[k] + 16 * static_cast<int64_t>(jb);
-          const int64_t tmax = ((kb / P + room) * P - kb) / 16;
+          const int64_t tmax = ((((kb >> pshift) + room) << pshift) - kb) / 16;
           if (tmax <= 0 && !first) break;
           t = std::max<int64_t>(1, std::min(t, tmax));
         }
@@ -181,29 +183,36 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
       int64_t lo = std::max<int64_t>(kDecodeSegCost + 1,
                                      ceil_div(total + kDecodeSegCost * segs, static_cast<int64_t>(cap)));
       int64_t hi = total + static_cast<int64_t>(kDecodeSegCost) * (segs + 1);
-      cut(sb, se, hi, cap, starts);
-      if (static_cast<int32_t>(starts.size()) - 1 > cap) {
+      auto feasible = [&](int64_t T, std::vector<int32_t>& st) {
+        cut(sb, se, T, cap, st);
+        return static_cast<int32_t>(st.size()) - 1 <= cap && st.back() == total;
+      };
+      std::vector<int32_t> best;                 // the cut of the smallest feasible cap so far
+      bool ok = false;
+      if (cap > 1) {
+        const int64_t hi2 =
+            ceil_div(total + kDecodeSegCost * (segs + cap), static_cast<int64_t>(cap) - 1) +
+            kDecodeSegCost + 1;
+        if (hi2 < hi && feasible(hi2, best)) {
+          hi = hi2;
+          ok = true;
+        }
+      }
+      if (!ok) ok = feasible(hi, best);
+      if (!ok) {
         uniform = true;  // the tables' limits alone need more CTAs than listed
       } else {
-        if (cap > 1) {
-          const int64_t hi2 =
-              ceil_div(total + kDecodeSegCost * (segs + cap), static_cast<int64_t>(cap) - 1) +
-              kDecodeSegCost + 1;
-          if (hi2 < hi) {
-            cut(sb, se, hi2, cap, starts);
-            if (static_cast<int32_t>(starts.size()) - 1 <= cap && starts.back() == total) hi = hi2;
-          }
-        }
         lo = std::min(lo, hi);
         while (lo < hi) {
           const int64_t mid = (lo + hi) / 2;
-          cut(sb, se, mid, cap, starts);
-          if (static_cast<int32_t>(starts.size()) - 1 <= cap && starts.back() == total)
+          if (feasible(mid, starts)) {
             hi = mid;
-          else
+            best.swap(starts);
+          } else {
             lo = mid + 1;
+          }
         }
-        cut(sb, se, lo, cap, starts);
+        starts.swap(best);
         dl.n_ctas = static_cast<int32_t>(starts.size()) - 1;
         dl.cta_begin = static_cast<int32_t>(plan.dcta_blk0.size());
         plan.dcta_blk0.insert(plan.dcta_blk0.end(), starts.begin(), starts.end());
