@@ -270,6 +270,7 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
     int64_t cost;
     int64_t tiles;
     PrefillItem item;
+    int32_t idx;   // position in (sequence, block, head) order
   };
   std::vector<Cost> all;
   for (int32_t s = 0; s < plan.num_seqs; ++s) {
@@ -291,13 +292,15 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
       const int64_t key_first = lo / kPrefillTileAlign * kPrefillTileAlign;
       const int64_t tiles = (pos1 - key_first) / kPrefillTileKeys + 1;
       for (int32_t h = 0; h < plan.hkv; ++h)
-        all.push_back({keys, tiles, PrefillItem{s, static_cast<int32_t>((b << 8) | h), 0}});
+        all.push_back({keys, tiles, PrefillItem{s, static_cast<int32_t>((b << 8) | h), 0},
+                       static_cast<int32_t>(all.size())});
     }
   }
   // Longest first; ties keep (sequence, block, head) order, which keeps the
   // CTAs that share a KV head's pages close together in time.
-  std::stable_sort(all.begin(), all.end(),
-                   [](const Cost& a, const Cost& b) { return a.cost > b.cost; });
+  std::sort(all.begin(), all.end(), [](const Cost& a, const Cost& b) {
+    return a.cost != b.cost ? a.cost > b.cost : a.idx < b.idx;
+  });
   plan.items.clear();
   plan.psplit.clear();
   plan.pcta0.clear();
@@ -319,10 +322,8 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
   if (split) {
     // Sequence order keeps an item's parts (and a sequence's items) adjacent.
     std::vector<Cost> order = all;
-    std::stable_sort(order.begin(), order.end(), [](const Cost& a, const Cost& b) {
-      return a.item.seq != b.item.seq ? a.item.seq < b.item.seq
-                                      : a.item.qb_head < b.item.qb_head;
-    });
+    std::sort(order.begin(), order.end(),
+              [](const Cost& a, const Cost& b) { return a.idx < b.idx; });
     int64_t cta = 0, room = per, slot = 0;
     per_cta.assign(1, {});
     for (const Cost& c : order) {
@@ -387,27 +388,38 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
   const int64_t grid = std::min<int64_t>(static_cast<int64_t>(all.size()), slots);
   if (!plan.prefill_pairs && static_cast<int64_t>(all.size()) <= kMaxItemsPerLaunch &&
       grid <= kMaxPrefillGrid && grid > 0) {
-    using Load = std::pair<int64_t, int32_t>;   // (tiles so far, CTA)
-    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-    for (int32_t c = 0; c < grid; ++c) heap.push({0, c});
-    std::vector<std::vector<PrefillItem>> lists(static_cast<size_t>(grid));
-    for (const Cost& c : all) {
-      Load l = heap.top();
-      heap.pop();
-      lists[static_cast<size_t>(l.second)].push_back(c.item);
-      heap.push({l.first + c.tiles, l.second});
+    // Min-heap of (tiles so far << 16 | CTA): ties go to the lowest CTA.
+    std::vector<uint64_t> heap(static_cast<size_t>(grid));
+    for (int32_t c = 0; c < grid; ++c) heap[static_cast<size_t>(c)] = static_cast<uint64_t>(c);
+    std::vector<int32_t> owner(all.size());
+    plan.pcta0.assign(static_cast<size_t>(grid) + 1, 0);
+    for (size_t i = 0; i < all.size(); ++i) {
+      const uint64_t top = heap[0];
+      const int32_t c = static_cast<int32_t>(top & 0xffff);
+      owner[i] = c;
+      ++plan.pcta0[static_cast<size_t>(c) + 1];
+      // Replace the root with its new load and sift it down.
+      const uint64_t v = top + (static_cast<uint64_t>(all[i].tiles) << 16);
+      size_t j = 0;
+      const size_t n = heap.size();
+      for (;;) {
+        size_t k = 2 * j + 1;
+        if (k >= n) break;
+        if (k + 1 < n && heap[k + 1] < heap[k]) ++k;
+        if (heap[k] >= v) break;
+        heap[j] = heap[k];
+        j = k;
+      }
+      heap[j] = v;
     }
-    plan.pcta0.assign(1, 0);
-    for (const auto& v : lists) {
-      plan.items.insert(plan.items.end(), v.begin(), v.end());
-      plan.pcta0.push_back(static_cast<int32_t>(plan.items.size()));
-    }
+    // CTA-major placement, each CTA's items in assignment (longest-first) order.
+    for (size_t c = 0; c < static_cast<size_t>(grid); ++c) plan.pcta0[c + 1] += plan.pcta0[c];
+    plan.items.resize(all.size());
+    std::vector<int32_t> fill(plan.pcta0.begin(), plan.pcta0.end() - 1);
+    for (size_t i = 0; i < all.size(); ++i) plan.items[static_cast<size_t>(fill[owner[i]]++)] = all[i].item;
     plan.prefill_ctas = static_cast<int32_t>(grid);
-    int64_t busiest = 0;
-    while (!heap.empty()) {
-      busiest = std::max(busiest, heap.top().first);
-      heap.pop();
-    }
+    uint64_t busiest = 0;
+    for (const uint64_t v : heap) busiest = std::max(busiest, v >> 16);
     plan.prefill_max_tiles = static_cast<int32_t>(busiest);
     return;
   }
