@@ -333,3 +333,57 @@ def test_prefill_items_scheduled_longest_first_to_least_loaded(name):
     # Striding the longest-first list would load the busiest CTA more.
     by_len = sorted(tiles, reverse=True)
     assert max(sum(by_len[c::n]) for c in range(n)) >= info["prefill_max_tiles"]
+
+
+def test_new_token_entry_points_check_before_any_launch():
+    """rpa_write_kv, rpa_qkv_prologue and rpa_forward_qkv reject bad arguments
+    on the host, before anything is enqueued (no GPU)."""
+    b = workloads.decode_batch(seed=1, num_seqs=4, meta_only=True)
+    p = plan_of(b)
+    L = binding.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    ws = ctypes.c_void_p(1 << 21)
+    w = ctypes.c_void_p(1 << 22)
+    norm = binding.QkvNorm(w.value, w.value, None, 1e-6, 10000.0)
+    # rpa_write_kv: page_size not a power of two; head_dim * 2 B not a multiple of 16 B.
+    kv_args = [fake] * 7 + [4, 4, 1, 256, 128, 16, 4096, binding.RPA_DTYPE_BF16, None, None]
+    bad = list(kv_args)
+    bad[11] = 96
+    assert L.rpa_write_kv(*bad) == binding.RPA_ERR_INVALID_ARG
+    bad = list(kv_args)
+    bad[10] = 4
+    assert L.rpa_write_kv(*bad) == binding.RPA_ERR_UNSUPPORTED
+    # rpa_qkv_prologue: unsupported head_dim, misaligned q, negative eps, null norm.
+    pro = [fake, fake, fake, ctypes.byref(norm), fake, fake, fake, fake, fake, fake,
+           4, 4, 8, 1, 256, 128, 16, 4096, binding.RPA_DTYPE_BF16, None, None]
+    bad = list(pro)
+    bad[14] = 96
+    assert L.rpa_qkv_prologue(*bad) == binding.RPA_ERR_UNSUPPORTED
+    bad = list(pro)
+    bad[0] = ctypes.c_void_p((1 << 20) + 8)
+    assert L.rpa_qkv_prologue(*bad) == binding.RPA_ERR_INVALID_ARG
+    neg = binding.QkvNorm(w.value, w.value, None, -1.0, 10000.0)
+    bad = list(pro)
+    bad[3] = ctypes.byref(neg)
+    assert L.rpa_qkv_prologue(*bad) == binding.RPA_ERR_INVALID_ARG
+    bad = list(pro)
+    bad[3] = None
+    assert L.rpa_qkv_prologue(*bad) == binding.RPA_ERR_INVALID_ARG
+    # rpa_forward_qkv: the plan's scalars must match; workspace size and alignment.
+    fq = [fake, fake, fake, ctypes.byref(norm), fake, fake, fake, fake, fake, fake,
+          b.num_seqs, 8, 1, 256, 128, None, 0.0625, fake, None, p.handle, ws, p.workspace_bytes]
+    bad = list(fq)
+    bad[11] = 16
+    assert L.rpa_forward_qkv(*bad) == binding.RPA_ERR_PLAN_MISMATCH
+    bad = list(fq)
+    bad[20] = ctypes.c_void_p((1 << 21) + 8)
+    assert L.rpa_forward_qkv(*bad) == binding.RPA_ERR_INVALID_ARG
+    bad = list(fq)
+    bad[4] = None                                         # null q_buf
+    assert L.rpa_forward_qkv(*bad) == binding.RPA_ERR_INVALID_ARG
+
+
+def test_plan_rejects_bad_split_option():
+    b = workloads.decode_batch(seed=1, num_seqs=4, meta_only=True)
+    with pytest.raises(binding.RpaError):
+        plan_of(b, prefill_split=-2)
