@@ -27,13 +27,15 @@
 // rows of one page: one lane of the warp fetches it with TMA (a 3-D tensor map
 // over the pool, 128-byte swizzled boxes of 64 dims x 16 rows) into the
 // warp's own shared-memory ring, completion on an mbarrier.  The page ids of
-// the CTA's whole range are read into shared memory once, first.  Per block a
+// the CTA's whole range are read into shared memory once, first, in one round
+// of loads (the range's first and last segment come from the plan).  Per block a
 // warp runs
 //     S^T[16 keys x 8 heads] = K . Q^T     (mma.m16n8k16, bf16 -> fp32)
 //     O^T[D x 8 heads]     += V^T . P^T   (P^T rebuilt in registers by a
 //                                          warp-level 8x8 transpose)
 // with an online softmax per head.  The copy pipeline runs on across segment
-// boundaries.  At the end of each segment the warps merge in shared memory; a
+// boundaries.  At the end of each segment the warps merge in shared memory,
+// each scaling its state by its share of the normalised result first; a
 // segment wholly inside the range writes the output, a cut one writes an fp32
 // partial (O / l and log2-sum-exp).  A second kernel, launched as a
 // programmatic dependent, combines the partials of every cut segment:

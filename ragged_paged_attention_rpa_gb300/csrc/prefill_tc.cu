@@ -15,8 +15,11 @@
 //    by the W queries that follow it, so whole KV tiles outside a block's
 //    causal window are never loaded.
 //
-// One CTA (persistent, one per SM) walks a longest-first list of work items
-// (sequence, query block, KV head).  Warp roles:
+// One CTA (persistent, one per SM) walks its own list of work items
+// (sequence, query block, KV head), given by the plan: items, longest first,
+// go to the CTA with the fewest key tiles so far.  On request an item's key
+// tiles are split across CTAs; each part writes an fp32 partial (O / l and
+// the log2-sum-exp per row) that prefill_combine_kernel merges.  Warp roles:
 //   warp 0     TMA producer of the Q block (once per item) and of K, gathered
 //              page by page through the page table into a ring of 16 KB
 //              stages (one 64-dimension chunk of a 128-key tile each);
@@ -37,7 +40,8 @@
 //              with a polynomial on the FMA pipe (paired fp32 instructions),
 //              writes P (bf16) to TMEM, rescales O in TMEM only when the max
 //              grew by more than 2^8 (the result is the same; it bounds P by
-//              256); epilogue O / l -> bf16 -> global.
+//              256); epilogue O / l -> bf16 -> global (32-byte stores),
+//              the next item's geometry read during the current item.
 // Every wait is bounded; on a timeout the CTA records RPA_DEVERR_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
