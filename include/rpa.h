@@ -206,6 +206,11 @@ rpa_status_t rpa_plan_get_info(const rpa_plan_t* plan, rpa_plan_info* info);
  * cut across its CTAs, the log-sum-exp combine kernel (a programmatic
  * dependent launch), then the tensor-core prefill and the CUDA-core path, as
  * the batch needs, and returns without waiting for them.
+ * Threads: calls from several host threads may run at once (launch
+ * parameters are staged per thread); each calling thread must have the
+ * stream's device current (cudaSetDevice, torch.cuda.set_device), else the
+ * call fails with RPA_ERR_CUDA (rpa_last_cuda_error gives the cudaError_t),
+ * and calls that share a workspace must be ordered on the GPU.
  * CUDA graphs: the call only enqueues kernel launches (no allocation, copy
  * or synchronisation), so it may be captured into a CUDA graph on `stream`;
  * every replay reruns the attention on the same buffers with the schedule
@@ -419,6 +424,10 @@ rpa_status_t rpa_trace_end(rpa_trace_record* records, int32_t* count);
 
 /* A static, human-readable name for a status code. */
 const char* rpa_status_string(rpa_status_t status);
+
+/* The cudaError_t behind the calling thread's last RPA_ERR_CUDA returned by a
+ * forward call (0 if none): for diagnostics. */
+int32_t rpa_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

@@ -43,7 +43,7 @@ EXPORTS = ["rpa_plan", "rpa_plan_destroy", "rpa_plan_get_info", "rpa_forward",
            "rpa_get_device_error", "rpa_clear_device_error", "rpa_trace_begin",
            "rpa_trace_end", "rpa_status_string", "rpa_forward_decode_noalloc",
            "rpa_write_kv", "rpa_forward_kv", "rpa_forward_fp8kv", "rpa_qkv_prologue",
-           "rpa_forward_qkv"]
+           "rpa_forward_qkv", "rpa_last_cuda_error"]
 
 RPA_KERNEL_NAMES = {0: "decode_split", 1: "decode_combine", 2: "prefill_tc", 3: "simt",
                     4: "kv_write", 5: "prologue", 6: "prefill_combine"}
@@ -60,7 +60,15 @@ class QkvNorm(ctypes.Structure):
 class RpaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__("%s: %s" % (where, status_string(status)))
+        self.cuda_error = 0
+        msg = "%s: %s" % (where, status_string(status))
+        if status == RPA_ERR_CUDA:
+            try:
+                self.cuda_error = int(lib().rpa_last_cuda_error())
+                msg += " (cudaError %d)" % self.cuda_error
+            except Exception:  # noqa: BLE001 - diagnostics only
+                pass
+        super().__init__(msg)
 
 
 class _Options(ctypes.Structure):
@@ -137,6 +145,8 @@ def lib() -> ctypes.CDLL:
         L.rpa_trace_begin.restype = i32
         L.rpa_trace_end.argtypes = [ctypes.POINTER(_TraceRecord), ctypes.POINTER(i32)]
         L.rpa_trace_end.restype = i32
+        L.rpa_last_cuda_error.argtypes = []
+        L.rpa_last_cuda_error.restype = i32
         L.rpa_status_string.argtypes = [i32]
         L.rpa_status_string.restype = ctypes.c_char_p
         _lib = L

@@ -10,6 +10,10 @@
 #include "rpa.h"
 #include "rpa_internal.h"
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 struct rpa_plan {
   rpa::Plan p;
 };
@@ -128,25 +132,33 @@ namespace {
 
 // Launches the attention kernels of a validated call (after the optional
 // KV-cache write).
+// The CUDA error behind this thread's last RPA_ERR_CUDA from a launch.
+thread_local int32_t g_last_cuda_error = 0;
+
+rpa_status_t cuda_failed(int err) {
+  g_last_cuda_error = err;
+  return RPA_ERR_CUDA;
+}
+
 rpa_status_t forward_launch(const rpa::Plan& p, const rpa::Args& a,
                             const rpa::KvWriteArgs* kvw, rpa_stream_t stream,
                             const rpa::PrologueArgs* pro = nullptr) {
   int err = 0;
   rpa::trace_start(stream);
-  if (kvw != nullptr && rpa::launch_kv_write(*kvw, stream) != 0) return RPA_ERR_CUDA;
-  if (pro != nullptr && rpa::launch_prologue(*pro, stream) != 0) return RPA_ERR_CUDA;
+  if (kvw != nullptr && (err = rpa::launch_kv_write(*kvw, stream)) != 0) return cuda_failed(err);
+  if (pro != nullptr && (err = rpa::launch_prologue(*pro, stream)) != 0) return cuda_failed(err);
   if (p.num_decode > 0 && !p.simt_decode) {
     err = rpa::launch_decode(p, a, stream);
-    if (err) return RPA_ERR_CUDA;
+    if (err) return cuda_failed(err);
   }
   if (!p.items.empty()) {
     err = p.prefill_pairs ? rpa::launch_prefill_pair(p, a, stream)
                           : rpa::launch_prefill_tc(p, a, stream);
-    if (err) return RPA_ERR_CUDA;
+    if (err) return cuda_failed(err);
   }
   if (p.simt_decode || p.simt_prefill) {
     err = rpa::launch_simt(p, a, stream);
-    if (err) return RPA_ERR_CUDA;
+    if (err) return cuda_failed(err);
   }
   return RPA_OK;
 }
@@ -377,6 +389,8 @@ rpa_status_t rpa_forward_decode_noalloc(const void* q, const void* k_pages,
   return RPA_OK;
 }
 
+int32_t rpa_last_cuda_error(void) { return g_last_cuda_error; }
+
 rpa_status_t rpa_get_device_error(void* workspace, rpa_stream_t stream, int32_t* err) {
   if (workspace == nullptr || err == nullptr) return RPA_ERR_INVALID_ARG;
   int32_t v = 0;
@@ -412,3 +426,21 @@ const char* rpa_status_string(rpa_status_t status) {
 }
 
 }  // extern "C"
+
+namespace rpa {
+
+int ensure_dynamic_smem(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({kernel, dev})) return 0;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  done.insert({kernel, dev});
+  return 0;
+}
+
+}  // namespace rpa

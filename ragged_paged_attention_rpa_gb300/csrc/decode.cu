@@ -708,7 +708,7 @@ decode_combine_kernel(const DecodeParams p, const __grid_constant__ CombineList 
 template <int D>
 int launch_combine(const Plan& plan, const DecodeParams& p, const Plan::DecodeLaunch& dl,
                    cudaStream_t stream) {
-  static CombineList cl;  // host staging; copied into the launch parameters
+  CombineList& cl = thread_staging<CombineList>();  // copied into the launch parameters
   for (int off = 0; off < dl.n_cut; off += kMaxDecodeCtas) {
     cl.n = std::min(kMaxDecodeCtas, dl.n_cut - off);
     cl.slot_base = dl.slot_base;
@@ -734,15 +734,11 @@ template <int D, int NSEG, bool FP8>
 int launch_one(const Plan& plan, const DecodeParams& p, const CUtensorMap& tk,
                const CUtensorMap& tv, const Plan::DecodeLaunch& dl, cudaStream_t stream) {
   constexpr size_t smem = DecodeSmem<D, FP8>::kBytes;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, NSEG, FP8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return static_cast<int>(e);
-    configured = true;
-  }
-  static DecodeSched<NSEG> sc;  // host staging; copied into the launch parameters
+  if (int e = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_kernel<D, NSEG, FP8>),
+                                  static_cast<int>(smem)))
+    return e;
+  // Host staging, copied into the launch parameters.
+  DecodeSched<NSEG>& sc = thread_staging<DecodeSched<NSEG>>();
   const int n = dl.seg_end - dl.seg_begin;
   sc.n_seg = n;
   sc.bpc = dl.bpc;

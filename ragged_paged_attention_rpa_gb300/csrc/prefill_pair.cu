@@ -577,12 +577,12 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
 template <int D>
 int launch_pair_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   using Lay = Layout<D>;
-  static bool configured = false;
-  static int max_pairs = 0;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
-    if (e != cudaSuccess) return static_cast<int>(e);
+  if (int e = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_pair_kernel<D>), Lay::kBytes))
+    return e;
+  // Clusters of two that fit at once (per thread: the query is cheap and its
+  // answer does not change for a device).
+  static thread_local int max_pairs = 0;
+  if (max_pairs == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * plan.num_sms / 2);
     cfg.blockDim = dim3(kThreads);
@@ -595,10 +595,9 @@ int launch_pair_t(const Plan& plan, const Args& a, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, prefill_pair_kernel<D>, &cfg);
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, prefill_pair_kernel<D>, &cfg);
     if (e != cudaSuccess || n <= 0) return static_cast<int>(e != cudaSuccess ? e : cudaErrorInvalidConfiguration);
     max_pairs = n;
-    configured = true;
   }
   const int G = plan.hq / plan.hkv;
   const int qb = plan.q_block;
@@ -630,7 +629,7 @@ int launch_pair_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   p.mpps = plan.mpps;
   p.num_pages = plan.num_pages;
   p.scale_log2 = a.sm_scale * 1.4426950408889634f;
-  static ItemList list;
+  ItemList& list = thread_staging<ItemList>();  // copied into the launch parameters
   const size_t n = plan.items.size();
   for (size_t off = 0; off < n; off += kMaxItemsPerLaunch) {
     const int cnt = static_cast<int>(std::min<size_t>(kMaxItemsPerLaunch, n - off));

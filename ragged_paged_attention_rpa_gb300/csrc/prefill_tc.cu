@@ -733,7 +733,7 @@ prefill_combine_kernel(const PrefillParams p, const __grid_constant__ SplitList 
 
 template <int D>
 int launch_prefill_combine(const Plan& plan, const PrefillParams& p, cudaStream_t stream) {
-  static SplitList gl;  // host staging; copied into the launch parameters
+  SplitList& gl = thread_staging<SplitList>();  // copied into the launch parameters
   const int n = static_cast<int>(plan.psplit.size());
   for (int off = 0; off < n; off += kMaxSplitGroupsPerLaunch) {
     gl.n = std::min(kMaxSplitGroupsPerLaunch, n - off);
@@ -757,14 +757,8 @@ int launch_prefill_combine(const Plan& plan, const PrefillParams& p, cudaStream_
 template <int D>
 int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   using Lay = Layout<D>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Lay::kBytes);
-    if (e != cudaSuccess) return static_cast<int>(e);
-    configured = true;
-  }
+  if (int e = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_tc_kernel<D>), Lay::kBytes))
+    return e;
   const int G = plan.hq / plan.hkv;
   const int qb = plan.q_block;
   const int box_rows_k = std::min(plan.p, kTileAlign);   // boxes never cross a page
@@ -798,7 +792,7 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0 ? 1 : 0;
   p.ppart_o = reinterpret_cast<float*>(a.workspace + plan.off_ppart_o);
   p.ppart_lse = reinterpret_cast<float*>(a.workspace + plan.off_ppart_lse);
-  static ItemList list;  // host staging; copied into the launch parameters
+  ItemList& list = thread_staging<ItemList>();  // copied into the launch parameters
   const size_t n = plan.items.size();
   for (size_t off = 0; off < n; off += kMaxItemsPerLaunch) {
     const int cnt = static_cast<int>(std::min<size_t>(kMaxItemsPerLaunch, n - off));

@@ -212,6 +212,19 @@ struct PrologueArgs {
 bool prologue_supported(int32_t head_dim);
 int launch_prologue(const PrologueArgs& a, void* stream);
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device); thread-safe.  Returns a cudaError_t.
+int ensure_dynamic_smem(const void* kernel, int bytes);
+
+// Per-thread host staging for a launch's parameter block (large structs that
+// are filled, then copied into the launch): one heap copy per thread.
+template <typename T>
+T& thread_staging() {
+  static thread_local T* buf = nullptr;
+  if (buf == nullptr) buf = new T();
+  return *buf;
+}
+
 // Tracing hooks (trace.cpp): trace_start before a call's first launch,
 // trace_mark after each launch (no-ops unless tracing is on).
 void trace_start(void* stream);

@@ -163,14 +163,9 @@ simt_attention_kernel(Args a, SimtParams p) {
 template <typename T, int D>
 int launch_simt_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   const size_t smem = (kRows * D + 2 * kKeys * (D + 1)) * sizeof(float);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(simt_attention_kernel<T, D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return static_cast<int>(e);
-    configured = true;
-  }
+  if (int e = ensure_dynamic_smem(reinterpret_cast<const void*>(simt_attention_kernel<T, D>),
+                                  static_cast<int>(smem)))
+    return e;
   SimtParams p;
   p.num_seqs = plan.num_seqs;
   p.hq = plan.hq;

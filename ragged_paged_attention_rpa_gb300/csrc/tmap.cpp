@@ -12,20 +12,19 @@ namespace {
 
 using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
 
+EncodeFn lookup_encode_fn() {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<EncodeFn>(ptr);
+  cudaGetLastError();
+  return nullptr;
+}
+
 EncodeFn encode_fn() {
-  static EncodeFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(ptr);
-    else
-      cudaGetLastError();
-  }
+  static const EncodeFn fn = lookup_encode_fn();   // looked up once, thread-safe
   return fn;
 }
 
