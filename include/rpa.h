@@ -24,8 +24,10 @@
  *
  * For sequence s with q_len = cu_q_lens[s+1] - cu_q_lens[s] and L = kv_lens[s],
  * query i (token t = cu_q_lens[s] + i) sits at position pos = L - q_len + i: the
- * new tokens are the last q_len entries of the cache, already written there by
- * the caller.  Key j is visible iff j <= pos and, when window[s] > 0,
+ * new tokens are the last q_len entries of the cache, already written there
+ * (by the caller, or first by rpa_forward_kv / rpa_forward_qkv, the fused KV
+ * write of "TPU Deep Dive" chapter 8).  Key j is visible iff j <= pos and,
+ * when window[s] > 0,
  * pos - j < window[s].  For every query head h:
  *     out[t][h] = sum_j softmax_j(sm_scale * q[t][h] . k_j) v_j
  * accumulated in fp32 and stored in the output dtype (bf16: round to nearest
@@ -37,7 +39,9 @@
  * A plan is a host object owned by the library between rpa_plan and
  * rpa_plan_destroy; it is read-only after creation, so one plan may serve many
  * rpa_forward calls (for instance every layer of a model step).  Two calls
- * that share a workspace must not overlap on the GPU.
+ * that share a workspace must not overlap on the GPU.  Several host threads
+ * may call at once, each with the stream's device current (see rpa_forward).
+ * The calls enqueue kernels only, so they can be captured into CUDA graphs.
  *
  * Errors.  Every entry point returns an rpa_status_t.  Shapes, dtypes,
  * pointer alignment and the plan/argument match are checked on the host before
