@@ -6,6 +6,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <memory>
 #include <vector>
 
 #include "rpa.h"
@@ -217,11 +218,12 @@ int launch_prologue(const PrologueArgs& a, void* stream);
 int ensure_dynamic_smem(const void* kernel, int bytes);
 
 // Per-thread host staging for a launch's parameter block (large structs that
-// are filled, then copied into the launch): one heap copy per thread.
+// are filled, then copied into the launch): one heap copy per thread, freed
+// when the thread exits.
 template <typename T>
 T& thread_staging() {
-  static thread_local T* buf = nullptr;
-  if (buf == nullptr) buf = new T();
+  static thread_local std::unique_ptr<T> buf;
+  if (!buf) buf.reset(new T());
   return *buf;
 }
 
