@@ -387,3 +387,28 @@ def test_plan_rejects_bad_split_option():
     b = workloads.decode_batch(seed=1, num_seqs=4, meta_only=True)
     with pytest.raises(binding.RpaError):
         plan_of(b, prefill_split=-2)
+
+
+def test_prefill_lists_fall_back_to_striding_beyond_one_launch():
+    """More items than one launch carries (sliding-window 8k with 16-token
+    query blocks: 8192 items): the items stay longest first and CTA c takes
+    c, c + 152, ...; the busiest CTA's tiles follow that striding."""
+    b = workloads.WORKLOADS["swa_prefill"](meta_only=True)
+    info = plan_of(b, q_block=16).info()
+    tiles = sorted((t for t in prefill_tiles(b, 16) for _ in range(b.num_kv_heads)), reverse=True)
+    assert info["num_prefill_items"] == len(tiles) == 8192
+    assert info["prefill_max_tiles"] == max(sum(tiles[c::152]) for c in range(152))
+
+
+def test_decode_plan_splits_into_launches_by_segment_count():
+    """Thousands of decode sequences exceed one launch's segment table: the
+    plan issues several launches, every block still covered exactly once."""
+    rng = np.random.default_rng(5)
+    n = 2500
+    kv = rng.integers(1, 65, size=n).tolist()
+    b = workloads.make_batch([1] * n, kv, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                             page_size=16, meta_only=True)
+    info = plan_of(b).info()
+    assert info["num_decode_seqs"] == n and info["path"] == binding.RPA_PATH_TC
+    # Workspace holds two partial slots per decode CTA of every launch.
+    assert info["workspace_bytes"] > 256
