@@ -6,6 +6,7 @@ from __future__ import annotations
 import ctypes
 import os
 import re
+import subprocess
 
 import numpy as np
 import pytest
@@ -412,3 +413,15 @@ def test_decode_plan_splits_into_launches_by_segment_count():
     assert info["num_decode_seqs"] == n and info["path"] == binding.RPA_PATH_TC
     # Workspace holds two partial slots per decode CTA of every launch.
     assert info["workspace_bytes"] > 256
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/rpa.h compiles as C11 and librpa links and plans from C."""
+    exe = str(tmp_path / "abi_c_check")
+    src = os.path.join(os.path.dirname(__file__), "csrc", "abi_c_check.c")
+    lib_dir = os.path.dirname(binding.LIB_PATH)
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I" + build.INCLUDE, src, "-o", exe,
+                    "-L" + lib_dir, "-lrpa", "-Wl,-rpath," + lib_dir], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.startswith("c abi ok")
