@@ -425,3 +425,46 @@ def test_header_is_plain_c(tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
     assert r.stdout.startswith("c abi ok")
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_decode_plan_matches_restatement_on_random_batches(seed):
+    """Random decode batches (sequence counts, lengths, windows, KV heads,
+    page sizes): the plan's longest range, most-split sequence and CTA count
+    (through the workspace size) equal the restated cost-balanced cut."""
+    rng = np.random.default_rng(4000 + seed)
+    hkv = int(rng.choice([1, 2, 4]))
+    n = int(rng.integers(1, 1024 // hkv + 1))    # one launch: at most 1024 segments
+    P = int(rng.choice([16, 32, 64, 128]))
+    # Lengths whose ranges stay within the kernel's page table (512 pages per
+    # range), which the restatement does not model.
+    kv = rng.integers(1, int(rng.choice([64, 600] if P < 64 else [64, 600, 4000])) + 1,
+                      size=n).tolist()
+    win = [int(w) if rng.random() < 0.4 else 0 for w in rng.integers(1, 2000, size=n)]
+    b = workloads.make_batch([1] * n, kv, num_q_heads=8 * hkv, num_kv_heads=hkv, head_dim=128,
+                             page_size=P, windows=win, meta_only=True)
+    info = plan_of(b).info()
+    want = decode_partition(b)
+    assert info["kv_split"] == 16 * want["longest"]
+    assert info["max_splits"] == want["max_splits"]
+    G = b.num_q_heads // b.num_kv_heads
+    slots = 2 * want["n_ctas"]
+    assert info["workspace_bytes"] == (256 + ceil_div(slots * G * 128 * 4, 256) * 256
+                                       + ceil_div(slots * G * 4, 256) * 256)
+
+
+def test_decode_plan_falls_back_to_fixed_ranges_when_tables_bind():
+    """1000 sequences of 4000 keys on 16-token pages: one range per SM would
+    touch ~1650 pages, more than a CTA's page table holds (512), so no cut
+    into 152 ranges is feasible; the plan takes fixed ranges small enough for
+    the table, in several waves, covering every block."""
+    b = workloads.make_batch([1] * 1000, [4000] * 1000, num_q_heads=8, num_kv_heads=1,
+                             head_dim=128, page_size=16, meta_only=True)
+    info = plan_of(b).info()
+    bpc = info["kv_split"] // 16
+    total = 1000 * ceil_div(4000, 16)
+    n_ctas = ceil_div(total, bpc)
+    assert n_ctas > 152 and bpc <= 512
+    slots = 2 * n_ctas
+    assert info["workspace_bytes"] == (256 + ceil_div(slots * 8 * 128 * 4, 256) * 256
+                                       + ceil_div(slots * 8 * 4, 256) * 256)
