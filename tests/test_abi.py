@@ -251,6 +251,26 @@ def test_fp8_kv_plans_are_decode_only():
     assert e.value.status == binding.RPA_ERR_UNSUPPORTED
 
 
+def prefill_items(b, q_block):
+    """(keys streamed, key tiles) of every prefill work item (sequence, query
+    block): the keys from the first visible key of its first query to its last
+    query's position; the 128-key tiles starting on a multiple of 64 at or
+    below that first key.  Restated from the attention's visibility rule."""
+    items = []
+    for s in range(b.num_seqs):
+        ql = int(b.cu_q_lens[s + 1] - b.cu_q_lens[s])
+        if ql <= 1:
+            continue
+        L = int(b.kv_lens[s])
+        w = 0 if b.window is None else int(b.window[s])
+        for blk in range(-(-ql // q_block)):
+            pos0 = L - ql + blk * q_block
+            pos1 = min(L - ql + (blk + 1) * q_block, L) - 1
+            lo = pos0 - (w - 1) if (w > 0 and pos0 - (w - 1) > 0) else 0
+            items.append((pos1 - lo + 1, (pos1 - lo // 64 * 64) // 128 + 1))
+    return items
+
+
 def prefill_tiles(b, q_block):
     """Key tiles (128 keys, starting on a multiple of 64 at or below the first
     visible key) of every prefill work item (sequence, query block), restated
@@ -312,14 +332,20 @@ def test_prefill_split_forced():
     assert info["prefill_split_parts"] == parts and info["prefill_ctas"] == grid
 
 
-def lpt_busiest(tiles, n):
-    """Longest processing time first: each item, longest first, to the CTA
-    with the fewest tiles so far (ties: lowest index); the busiest CTA."""
+def lpt_busiest(tiles, n, keys=None):
+    """Longest processing time first: each item, longest first (by keys
+    streamed when given, ties in list order), to the CTA with the fewest tiles
+    so far (ties: lowest index); the busiest CTA's tiles."""
     import heapq
+    order = range(len(tiles))
+    if keys is not None:
+        order = sorted(order, key=lambda i: (-keys[i], i))
+    else:
+        order = sorted(order, key=lambda i: (-tiles[i], i))
     heap = [(0, c) for c in range(n)]
-    for t in sorted(tiles, reverse=True):
+    for i in order:
         load, c = heapq.heappop(heap)
-        heapq.heappush(heap, (load + t, c))
+        heapq.heappush(heap, (load + tiles[i], c))
     return max(load for load, _ in heap)
 
 
@@ -327,10 +353,11 @@ def lpt_busiest(tiles, n):
 def test_prefill_items_scheduled_longest_first_to_least_loaded(name):
     b = workloads.WORKLOADS[name](meta_only=True)
     info = plan_of(b).info()
-    tiles = [t for t in prefill_tiles(b, info["q_block"]) for _ in range(b.num_kv_heads)]
+    items = [it for it in prefill_items(b, info["q_block"]) for _ in range(b.num_kv_heads)]
+    tiles = [t for _, t in items]
     n = min(len(tiles), 152)
     assert info["prefill_ctas"] == n
-    assert info["prefill_max_tiles"] == lpt_busiest(tiles, n)
+    assert info["prefill_max_tiles"] == lpt_busiest(tiles, n, keys=[k for k, _ in items])
     # Striding the longest-first list would load the busiest CTA more.
     by_len = sorted(tiles, reverse=True)
     assert max(sum(by_len[c::n]) for c in range(n)) >= info["prefill_max_tiles"]
@@ -468,3 +495,24 @@ def test_decode_plan_falls_back_to_fixed_ranges_when_tables_bind():
     slots = 2 * n_ctas
     assert info["workspace_bytes"] == (256 + ceil_div(slots * 8 * 128 * 4, 256) * 256
                                        + ceil_div(slots * 8 * 4, 256) * 256)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_prefill_schedule_matches_restatement_on_random_batches(seed):
+    rng = np.random.default_rng(5000 + seed)
+    n = int(rng.integers(1, 12))
+    hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 4, 8]))
+    ql = rng.integers(2, 1500, size=n)
+    kv = (ql + rng.integers(0, 3000, size=n)).tolist()
+    win = [int(w) if rng.random() < 0.5 else 0 for w in rng.integers(1, 2000, size=n)]
+    b = workloads.make_batch(ql.tolist(), kv, num_q_heads=G * hkv, num_kv_heads=hkv,
+                             head_dim=128, page_size=64, windows=win, meta_only=True)
+    info = plan_of(b).info()
+    items = [it for it in prefill_items(b, info["q_block"]) for _ in range(hkv)]
+    if len(items) > 2048:      # beyond one launch: striding (tested separately)
+        pytest.skip("more items than one launch carries")
+    n_ctas = min(len(items), 152)
+    assert info["prefill_ctas"] == n_ctas
+    assert info["prefill_max_tiles"] == lpt_busiest([t for _, t in items], n_ctas,
+                                                    keys=[k for k, _ in items])
