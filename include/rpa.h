@@ -168,6 +168,8 @@ typedef struct rpa_plan rpa_plan_t;
  *       (may be NULL) the device workspace rpa_forward needs.
  * Returns RPA_OK, RPA_ERR_INVALID_ARG or RPA_ERR_UNSUPPORTED; on error *plan
  * is set to NULL.
+ * RPA_LOG=1 in the environment makes every rpa_plan print one line about
+ * the plan it built (paths, CTAs, ranges, items, workspace) to stderr.
  */
 rpa_status_t rpa_plan(rpa_plan_t** plan, const int32_t* cu_q_lens_host,
                       const int32_t* kv_lens_host, const int32_t* window_host,

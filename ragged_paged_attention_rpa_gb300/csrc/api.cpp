@@ -3,16 +3,16 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
+#include <set>
+#include <utility>
 
 #include "rpa.h"
 #include "rpa_internal.h"
-
-#include <mutex>
-#include <set>
-#include <utility>
 
 struct rpa_plan {
   rpa::Plan p;
@@ -21,6 +21,29 @@ struct rpa_plan {
 namespace {
 
 bool is_pow2(int32_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// RPA_LOG=1 in the environment: every rpa_plan prints one line to stderr.
+bool log_plans() {
+  static const bool on = [] {
+    const char* v = std::getenv("RPA_LOG");
+    return v != nullptr && v[0] == '1';
+  }();
+  return on;
+}
+
+void log_plan(const rpa::Plan& p) {
+  int64_t cuts = static_cast<int64_t>(p.dcut.size());
+  std::fprintf(stderr,
+               "librpa plan: %d seqs (%d decode, %d prefill), %s path; decode: %d launch(es), "
+               "%lld CTAs, longest range %d tokens, %lld cut sequences; prefill: %zu items on "
+               "%d CTAs, q_block %d, busiest CTA %d key tiles, %d split parts; workspace %zu "
+               "bytes\n",
+               p.num_seqs, p.num_decode, p.num_prefill,
+               p.path == RPA_PATH_TC ? "tensor-core" : "CUDA-core",
+               static_cast<int>(p.dlaunch.size()), static_cast<long long>(p.decode_ctas),
+               p.kv_split, static_cast<long long>(cuts), p.items.size(), p.prefill_ctas,
+               p.q_block, p.prefill_max_tiles, p.n_split_items, p.ws_bytes);
+}
 
 bool aligned(const void* ptr, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0;
@@ -100,6 +123,7 @@ rpa_status_t rpa_plan(rpa_plan_t** plan, const int32_t* cu_q_lens_host,
   }
   *plan = pl;
   if (workspace_bytes) *workspace_bytes = p.ws_bytes;
+  if (log_plans()) log_plan(p);
   return RPA_OK;
 }
 

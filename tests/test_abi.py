@@ -516,3 +516,20 @@ def test_prefill_schedule_matches_restatement_on_random_batches(seed):
     assert info["prefill_ctas"] == n_ctas
     assert info["prefill_max_tiles"] == lpt_busiest([t for _, t in items], n_ctas,
                                                     keys=[k for k, _ in items])
+
+
+def test_plan_log_line_when_asked():
+    """RPA_LOG=1: every rpa_plan prints one line about the plan to stderr."""
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "from ragged_paged_attention_rpa_gb300 import binding, workloads\n"
+            "b = workloads.decode_batch(seed=1, meta_only=True)\n"
+            "binding.rpa_plan(b.cu_q_lens, b.kv_lens, b.window, 8, 1, 256, 128,\n"
+            "                 b.max_pages_per_seq, b.num_pages, num_sms=152)\n" % build.ROOT)
+    import sys as _sys
+    on = subprocess.run([_sys.executable, "-c", code], capture_output=True, text=True,
+                        env=dict(os.environ, RPA_LOG="1"), timeout=120)
+    off = subprocess.run([_sys.executable, "-c", code], capture_output=True, text=True,
+                         env={k: v for k, v in os.environ.items() if k != "RPA_LOG"}, timeout=120)
+    assert on.returncode == 0 and off.returncode == 0, on.stderr + off.stderr
+    assert on.stderr.count("librpa plan: 128 seqs (128 decode, 0 prefill)") == 1, on.stderr
+    assert "librpa plan" not in off.stderr
