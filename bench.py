@@ -277,8 +277,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--q-block", type=int, default=0)
-    ap.add_argument("--kv-split", type=int, default=0)
+    ap.add_argument("--q-block", type=int, default=int(os.environ.get("RPA_QBLOCK", "0")),
+                    help="prefill query block in tokens (default: $RPA_QBLOCK, else chosen)")
+    ap.add_argument("--kv-split", type=int, default=int(os.environ.get("RPA_KV_SPLIT", "0")),
+                    help="decode range length in tokens (default: $RPA_KV_SPLIT, else chosen)")
     ap.add_argument("--prefill-split", type=int, default=0,
                     help="plan option: 0 choose, -1 never split prefill items, n > 0 parts "
                          "of at most n key tiles")
