@@ -382,6 +382,12 @@ def main():
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
     torch.cuda.set_device(local)
+    # Rank 0 builds (a no-op when librpa.so is current); the other ranks wait,
+    # so concurrent compilers never write the same object files.
+    if rank == 0:
+        build.build()
+    if dist is not None:
+        dist.barrier()
     build.build()
     b = make_workload(args)
     counts = algorithmic_counts(b)
