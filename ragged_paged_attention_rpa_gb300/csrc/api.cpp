@@ -272,8 +272,9 @@ rpa_status_t rpa_forward_kv(const void* q, const void* k_new, const void* v_new,
     return RPA_ERR_INVALID_ARG;
   const int32_t esz = p.dtype == RPA_DTYPE_F32 ? 4 : 2;
   rpa::KvWriteArgs kw{k_new, v_new, k_pages, v_pages, page_table, cu_q_lens, kv_lens,
-                      static_cast<unsigned char*>(workspace), p.num_seqs, p.total_q, p.hkv,
-                      p.d, esz, p.p, p.mpps, p.num_pages};
+                      static_cast<unsigned char*>(workspace), p.num_seqs,
+                      static_cast<int32_t>(p.total_q), p.hkv, p.d, esz, p.p, p.mpps,
+                      p.num_pages};
   rpa::Args a{q, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window, sm_scale,
               out, static_cast<unsigned char*>(workspace)};
   return forward_launch(p, a, &kw, stream);
@@ -369,9 +370,9 @@ rpa_status_t rpa_forward_qkv(const void* q, const void* k, const void* v,
     return RPA_ERR_INVALID_ARG;
   rpa::PrologueArgs pa{q, k, v, norm->q_weight, norm->k_weight, norm->v_weight, norm->eps,
                        norm->rope_theta, q_buf, k_pages, v_pages, page_table, cu_q_lens,
-                       kv_lens, static_cast<unsigned char*>(workspace), p.num_seqs, p.total_q,
-                       p.hq, p.hkv, p.d, p.dtype == RPA_DTYPE_F32 ? 4 : 2, p.p, p.mpps,
-                       p.num_pages};
+                       kv_lens, static_cast<unsigned char*>(workspace), p.num_seqs,
+                       static_cast<int32_t>(p.total_q), p.hq, p.hkv, p.d,
+                       p.dtype == RPA_DTYPE_F32 ? 4 : 2, p.p, p.mpps, p.num_pages};
   rpa::Args a{q_buf, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window, sm_scale,
               out, static_cast<unsigned char*>(workspace)};
   return forward_launch(p, a, nullptr, stream, &pa);
