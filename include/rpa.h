@@ -103,7 +103,12 @@ enum {
 typedef struct rpa_plan_options {
   int32_t struct_size;      /* sizeof(rpa_plan_options)                         */
   int32_t path;             /* RPA_PATH_*                                       */
-  int32_t q_block;          /* prefill query block, tokens (0: choose)          */
+  int32_t q_block;          /* prefill query block, tokens (0: choose).  At most
+                               one 128-row tile per CTA: 128 / G tokens (G =
+                               num_q_heads / num_kv_heads); twice that runs on
+                               SM pairs (as prefill_pairs = 2, half the block
+                               per SM, head_dim 128 or 256); larger blocks are
+                               refused with RPA_ERR_UNSUPPORTED             */
   int32_t kv_split;         /* decode split length, tokens (0: choose)          */
   int32_t num_sms;          /* SMs to plan for (0: ask the current device, else 152) */
   int32_t prefill_pairs;    /* tensor-core prefill on SM pairs (one M = 256 MMA
@@ -127,7 +132,8 @@ typedef struct rpa_plan_info {
   int32_t path;             /* RPA_PATH_SIMT or RPA_PATH_TC                     */
   int32_t num_decode_seqs;  /* sequences with q_len == 1                        */
   int32_t num_prefill_seqs; /* sequences with q_len > 1                         */
-  int32_t q_block;          /* prefill query block in tokens                    */
+  int32_t q_block;          /* prefill query block in tokens (query tokens of
+                               one work item; on SM pairs, of both CTAs)     */
   int32_t kv_split;         /* decode split length in tokens                    */
   int32_t max_splits;       /* largest split count of any decode sequence       */
   int32_t num_prefill_items;/* (sequence, query block, kv head) work items      */
@@ -203,9 +209,12 @@ rpa_status_t rpa_plan_get_info(const rpa_plan_t* plan, rpa_plan_info* info);
  *            zero; the rest is scratch the call overwrites).
  *            Scratch owned by the call while it runs; the error word lives at
  *            its start and is sticky until rpa_get_device_error clears it.
- *   Pages: the prefill kernel reads whole pages, so the slots of a sequence's
- *            last page past its kv_len must hold finite values (a
- *            zero-initialised pool satisfies this).
+ *   Pages: only the slots of keys some query of the batch sees are used;
+ *            every other slot (the free slots of a sequence's last page past
+ *            its kv_len, keys before every query's window, pages no sequence
+ *            owns) may hold anything, NaN and infinities included.  The
+ *            kernels load some of them along with the visible keys (whole
+ *            boxes of a page) but zero them before any product uses them.
  * The scalar arguments must equal the plan's, else RPA_ERR_PLAN_MISMATCH.
  * sm_scale multiplies q.k before the softmax (1/sqrt(head_dim) is usual).
  * Enqueues on `stream` the split-KV decode kernel and, where a sequence is
@@ -356,10 +365,13 @@ rpa_status_t rpa_forward_kv(const void* q, const void* k_new, const void* v_new,
  * Read the device error word at the start of `workspace` after everything
  * enqueued on `stream` so far (this call synchronises `stream`), store it in
  * *err (an RPA_DEVERR_* code) and reset it to RPA_DEVERR_NONE.
+ * workspace == NULL selects the fixed scratch of rpa_forward_decode_noalloc on
+ * the current device (its error word, sticky in the same way).
  */
 rpa_status_t rpa_get_device_error(void* workspace, rpa_stream_t stream, int32_t* err);
 
-/* Zero the workspace error word (enqueued on `stream`, no synchronisation). */
+/* Zero the workspace error word (enqueued on `stream`, no synchronisation);
+ * workspace == NULL: that of rpa_forward_decode_noalloc's fixed scratch. */
 rpa_status_t rpa_clear_device_error(void* workspace, rpa_stream_t stream);
 
 /*
@@ -377,13 +389,18 @@ rpa_status_t rpa_clear_device_error(void* workspace, rpa_stream_t stream);
  * RPA_ERR_UNSUPPORTED; a plan whose workspace_bytes exceeds
  * RPA_NOALLOC_SCRATCH_BYTES is rejected with RPA_ERR_WORKSPACE_TOO_SMALL.
  * The scratch is one fixed array inside the library (every GPU that loads the
- * library holds it until the process exits), shared by every call: each call
- * clears the parts that must start at zero, and calls that overlap on the GPU
- * (for example on two streams) race on it.  The first call on a device looks
- * up the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.  No device memory
- * is allocated or freed.  The device error word of this scratch is not
- * exposed; the call returns RPA_OK once its work is enqueued.
+ * library holds it until the process exits), shared by every call and keeping
+ * the last call's contents; calls that overlap on the GPU (for example on two
+ * streams) race on it.  Only its error word must start at zero: it does (the
+ * array is zero when the library loads) and, like a workspace's, it is sticky:
+ * a kernel that meets a bad page id or a length that disagrees with the plan
+ * sets it and skips the access, and rpa_get_device_error(NULL, stream, &err)
+ * reads and clears it.  The split partials are written before they are read
+ * within a call.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, once per device, thread-safe) with that
+ * device current; make that first call before any stream capture.  No device
+ * memory is allocated or freed.  The call returns RPA_OK once its work is
+ * enqueued (RPA_ERR_CUDA with rpa_last_cuda_error set if a CUDA call fails).
  */
 #define RPA_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
 
@@ -431,8 +448,8 @@ rpa_status_t rpa_trace_end(rpa_trace_record* records, int32_t* count);
 /* A static, human-readable name for a status code. */
 const char* rpa_status_string(rpa_status_t status);
 
-/* The cudaError_t behind the calling thread's last RPA_ERR_CUDA returned by a
- * forward call (0 if none): for diagnostics. */
+/* The cudaError_t behind the calling thread's last RPA_ERR_CUDA returned by
+ * any entry point (0 if none): for diagnostics. */
 int32_t rpa_last_cuda_error(void);
 
 #ifdef __cplusplus

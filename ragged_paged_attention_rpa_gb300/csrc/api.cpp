@@ -138,7 +138,8 @@ rpa_status_t rpa_plan_get_info(const rpa_plan_t* plan, rpa_plan_info* info) {
   info->path = p.path;
   info->num_decode_seqs = p.num_decode;
   info->num_prefill_seqs = p.num_prefill;
-  info->q_block = p.q_block;
+  // Query tokens per work item: on SM pairs each CTA holds half of them.
+  info->q_block = p.prefill_pairs ? 2 * p.q_block : p.q_block;
   info->kv_split = p.kv_split;
   info->max_splits = p.max_splits;
   info->num_prefill_items = static_cast<int32_t>(p.items.size());
@@ -304,7 +305,8 @@ rpa_status_t rpa_write_kv(const void* k_new, const void* v_new, void* k_pages, v
                       static_cast<unsigned char*>(workspace), num_seqs, total_q, num_kv_heads,
                       head_dim, esz, page_size, max_pages_per_seq, num_pages};
   rpa::trace_start(stream);
-  return rpa::launch_kv_write(kw, stream) == 0 ? RPA_OK : RPA_ERR_CUDA;
+  if (int err = rpa::launch_kv_write(kw, stream)) return cuda_failed(err);
+  return RPA_OK;
 }
 
 rpa_status_t rpa_qkv_prologue(const void* q, const void* k, const void* v,
@@ -338,7 +340,8 @@ rpa_status_t rpa_qkv_prologue(const void* q, const void* k, const void* v,
                        dtype == RPA_DTYPE_F32 ? 4 : 2, page_size, max_pages_per_seq,
                        num_pages};
   rpa::trace_start(stream);
-  return rpa::launch_prologue(pa, stream) == 0 ? RPA_OK : RPA_ERR_CUDA;
+  if (int err = rpa::launch_prologue(pa, stream)) return cuda_failed(err);
+  return RPA_OK;
 }
 
 rpa_status_t rpa_forward_qkv(const void* q, const void* k, const void* v,
@@ -403,37 +406,42 @@ rpa_status_t rpa_forward_decode_noalloc(const void* q, const void* k_pages,
       !aligned(kv_lens, 4) || !aligned(window, 4))
     return RPA_ERR_INVALID_ARG;
   void* scratch = nullptr;
-  if (rpa::noalloc_scratch(&scratch) != 0) return RPA_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // The error word must start at zero.
-  if (cudaMemsetAsync(scratch, 0, rpa::kHeaderBytes, s) != cudaSuccess) return RPA_ERR_CUDA;
+  if (int err = rpa::noalloc_scratch(&scratch)) return cuda_failed(err);
+  // The scratch's error word started at zero and stays sticky until
+  // rpa_get_device_error(NULL, ...) reads and clears it; nothing else in the
+  // scratch has to start at zero.
   rpa::Args a{q, k_pages, v_pages, page_table, cu_q_lens, kv_lens, window, sm_scale,
               out, static_cast<unsigned char*>(scratch)};
   rpa::trace_start(stream);
-  if (rpa::launch_decode(p, a, stream) != 0) return RPA_ERR_CUDA;
+  if (int err = rpa::launch_decode(p, a, stream)) return cuda_failed(err);
   return RPA_OK;
 }
 
 int32_t rpa_last_cuda_error(void) { return g_last_cuda_error; }
 
 rpa_status_t rpa_get_device_error(void* workspace, rpa_stream_t stream, int32_t* err) {
-  if (workspace == nullptr || err == nullptr) return RPA_ERR_INVALID_ARG;
+  if (err == nullptr) return RPA_ERR_INVALID_ARG;
+  if (workspace == nullptr) {
+    // The fixed scratch of rpa_forward_decode_noalloc on the current device.
+    if (int e = rpa::noalloc_scratch(&workspace)) return cuda_failed(e);
+  }
   int32_t v = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return RPA_ERR_CUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return RPA_ERR_CUDA;
-  if (cudaMemsetAsync(workspace, 0, 2 * sizeof(int32_t), s) != cudaSuccess)
-    return RPA_ERR_CUDA;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, 2 * sizeof(int32_t), s);
+  if (e != cudaSuccess) return cuda_failed(static_cast<int>(e));
   *err = v;
   return v == RPA_DEVERR_NONE ? RPA_OK : RPA_ERR_DEVICE;
 }
 
 rpa_status_t rpa_clear_device_error(void* workspace, rpa_stream_t stream) {
-  if (workspace == nullptr) return RPA_ERR_INVALID_ARG;
+  if (workspace == nullptr) {
+    if (int e = rpa::noalloc_scratch(&workspace)) return cuda_failed(e);
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, 2 * sizeof(int32_t), s) != cudaSuccess)
-    return RPA_ERR_CUDA;
+  if (cudaError_t e = cudaMemsetAsync(workspace, 0, 2 * sizeof(int32_t), s))
+    return cuda_failed(static_cast<int>(e));
   return RPA_OK;
 }
 

@@ -41,6 +41,7 @@
 // programmatic dependent, combines the partials of every cut segment:
 // out = sum_c 2^(lse_c - M) O_c / sum_c 2^(lse_c - M).
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "rpa_internal.h"
@@ -513,11 +514,31 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       {
         const int row = (lane & 7) + ((lane >> 4) << 3);
         const int hi = (lane >> 3) & 1;
+        if ((vmask & 0xffffu) == 0xffffu) {
 #pragma unroll
-        for (int mt = 0; mt < KT; ++mt) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(smem_u32(vt + swz(row, 2 * mt + hi)), a0, a1, a2, a3);
-          mma_t<FP8>(o[mt], a0, a1, a2, a3, b0, b1);
+          for (int mt = 0; mt < KT; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(smem_u32(vt + swz(row, 2 * mt + hi)), a0, a1, a2, a3);
+            mma_t<FP8>(o[mt], a0, a1, a2, a3, b0, b1);
+          }
+        } else {
+          // A block at a segment's edge: its masked keys have P = 0, but
+          // their V rows (free slots past the last key, keys before the
+          // window) may hold anything and 0 x NaN is NaN, so those keys'
+          // columns of the V^T fragments are zeroed.  In the m16n8k16 A
+          // fragment, a0 / a1 hold keys 2(lane % 4) + {0, 1}, a2 / a3 the
+          // same keys + 8 (the lower key in the lower half).
+          const int k0 = 2 * (lane & 3);
+          const uint32_t mlo = (((vmask >> k0) & 1u) ? 0x0000ffffu : 0u) |
+                               (((vmask >> (k0 + 1)) & 1u) ? 0xffff0000u : 0u);
+          const uint32_t mhi = (((vmask >> (k0 + 8)) & 1u) ? 0x0000ffffu : 0u) |
+                               (((vmask >> (k0 + 9)) & 1u) ? 0xffff0000u : 0u);
+#pragma unroll
+          for (int mt = 0; mt < KT; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(smem_u32(vt + swz(row, 2 * mt + hi)), a0, a1, a2, a3);
+            mma_t<FP8>(o[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, b0, b1);
+          }
         }
       }
       __syncwarp();
@@ -831,17 +852,21 @@ int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
 
 // ---------------------------------------------------------------------------
 // Fixed scratch for rpa_forward_decode_noalloc: the decode kernel's workspace
-// (error word, split partials, arrival counters) in a file-scope device array,
-// so that callers who cannot allocate device memory can still run decode.
-// Every GPU that loads this library holds the array until the process exits.
-// In host code `g_noalloc_scratch` names a host-side stand-in, never a device
-// address; the device address comes from cudaGetSymbolAddress, resolved once
-// per device (with that device current) on the first call on that device.
+// (error word and detail word, then the split partials) in a file-scope device
+// array, so that callers who cannot allocate device memory can still run
+// decode.  Every GPU that loads this library holds the array until the process
+// exits.  The array starts zeroed (a static device variable), so its error
+// word starts at zero and stays sticky until rpa_get_device_error reads it;
+// the partials are written before they are read within each call.  In host
+// code `g_noalloc_scratch` names a host-side stand-in, never a device address;
+// the device address comes from cudaGetSymbolAddress, looked up once per
+// device (with that device current, under a lock) by the first call on it.
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[RPA_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices] = {};
 }  // namespace
 
@@ -850,6 +875,7 @@ int noalloc_scratch(void** ptr) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return static_cast<int>(e);
   if (dev < 0 || dev >= kMaxDevices) return static_cast<int>(cudaErrorInvalidDevice);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (g_noalloc_ptr[dev] == nullptr) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);

@@ -263,8 +263,11 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
                   int32_t forced_q_block, int32_t forced_split) {
   const int32_t group = plan.hq / plan.hkv;
   const int32_t max_qb = prefill_tokens_per_block(plan.d, group);
+  // Query tokens per CTA: a requested block larger than one 128-row tile
+  // holds was refused or sent to SM pairs (half the block per SM) by the
+  // caller.
   int32_t qb = max_qb;
-  if (forced_q_block > 0) qb = std::min(forced_q_block, max_qb);
+  if (forced_q_block > 0) qb = plan.prefill_pairs ? forced_q_block / 2 : forced_q_block;
   plan.q_block = qb;
   struct Cost {
     int64_t cost;
@@ -496,9 +499,25 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
   plan.prefill_ctas = 0;
   const bool pairs_ok = tc_prefill && prefill_pair_supported(plan.d, plan.p, group);
   if (opts.prefill_pairs == 2 && plan.num_prefill > 0 && !pairs_ok) return RPA_ERR_UNSUPPORTED;
-  // Chosen only on request: on GB300 the pair kernel's cross-SM barrier
-  // round trips cost more per tile than its halved copy traffic saves.
-  plan.prefill_pairs = pairs_ok && plan.num_prefill > 0 && opts.prefill_pairs == 2;
+  // A requested query block is either one CTA's 128-row tile or less
+  // (128 / G tokens), or, on SM pairs, two such halves (one M = 256 MMA over
+  // both); anything larger would need several tiles per KV tile, which the
+  // tensor memory at these head sizes cannot hold, and is refused rather
+  // than silently shrunk.
+  const int32_t max_qb = prefill_tokens_per_block(plan.d, group);
+  bool want_pairs = opts.prefill_pairs == 2;
+  if (tc_prefill && plan.num_prefill > 0 && opts.q_block > 0) {
+    if (opts.q_block > 2 * max_qb) return RPA_ERR_UNSUPPORTED;
+    if (opts.q_block > max_qb) {
+      if (!pairs_ok) return RPA_ERR_UNSUPPORTED;
+      want_pairs = true;
+    }
+    if (want_pairs && (opts.q_block % 2 != 0)) return RPA_ERR_UNSUPPORTED;
+  }
+  // Chosen only on request (prefill_pairs = 2, or a query block of two
+  // tiles): on GB300 the pair kernel's cross-SM barrier round trips cost
+  // more per tile than its halved copy traffic saves.
+  plan.prefill_pairs = pairs_ok && plan.num_prefill > 0 && want_pairs;
   if (tc_prefill && plan.num_prefill > 0)
     plan_prefill(plan, cu, kv, win, opts.q_block, opts.prefill_split);
 

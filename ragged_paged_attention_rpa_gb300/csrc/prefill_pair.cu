@@ -107,6 +107,7 @@ static_assert(sizeof(Barriers) <= 512, "barrier block");
 struct Geom {
   int32_t seq, g, t0, ntok, pos_first;  // this CTA's block
   int32_t key_first, ntiles, pos_last;  // the pair: tiles and its last query
+  int32_t lo;                           // the pair: first key any query sees
   int32_t W;
   bool ok;
 };
@@ -132,7 +133,8 @@ __device__ __forceinline__ Geom pair_geom(const PairParams& p, const PrefillItem
   r.ntok = rank == 0 ? n0 : n1;
   r.pos_first = L - ql + qb * qbt;
   r.ok = n0 > 0 && first0 >= 0 && r.pos_last < L && (r.pos_last >> p.page_shift) < p.mpps;
-  r.key_first = first_visible(first0, r.W) / kTileAlign * kTileAlign;
+  r.lo = first_visible(first0, r.W);
+  r.key_first = r.lo / kTileAlign * kTileAlign;
   r.ntiles = r.ok ? (r.pos_last - r.key_first) / kBN + 1 : 0;
   return r;
 }
@@ -161,10 +163,12 @@ __device__ __forceinline__ float max_tree(const uint32_t* v) {
 }
 
 // TMA source row of the box of `rows` keys starting at `key` (-rows: wholly
-// past the pair's last query; the TMA fills it with zeros).
+// outside the keys the pair's queries see, past its last query or before its
+// first visible key; the TMA fills it with zeros and the page table is not
+// read).
 __device__ __forceinline__ int32_t box_row(const PairParams& p, const Geom& gm, int32_t key,
                                            int32_t rows) {
-  if (key > gm.pos_last) return -rows;
+  if (key > gm.pos_last || key + rows <= gm.lo) return -rows;
   const int32_t page = __ldg(p.page_table + static_cast<int64_t>(gm.seq) * p.mpps +
                              (key >> p.page_shift));
   if (page < 0 || page >= p.num_pages) {
@@ -327,13 +331,40 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
       // O += P V: per V stage (kVKeys keys), B = the pair's V split by
       // dimension (MN-major: 8-key groups 1024 B apart, 64-dimension chunks
       // kVKeys x 128 B apart); A = P from the S buffer's first 64 columns.
-      auto issue_pv = [&](uint32_t Tp, int jp) -> bool {
+      //
+      // A masked key has P = 0, but 0 x NaN is NaN: the V rows of keys no
+      // query of the pair sees (before its first visible key, past its last
+      // query) may hold anything, so they are zeroed in both CTAs' stages
+      // (the partner's through its cluster address) before the MMA reads
+      // them.  Boxes wholly outside those keys arrive as zeros already.
+      auto clear_v_edges = [&](const Geom& gm, int32_t kst, int vs) {
+        const int a = max(0, min(Lay::kVKeys, gm.lo - kst));              // rows [0, a)
+        const int b = max(0, min(Lay::kVKeys, gm.pos_last + 1 - kst));    // rows [b, kVKeys)
+        if ((a == 0 && b == Lay::kVKeys) || a == Lay::kVKeys || b == 0) return;
+        const uint32_t st0 = cluster_addr(smem + Lay::kVOff + vs * kStage, 0);
+        const uint32_t st1 = cluster_addr(smem + Lay::kVOff + vs * kStage, 1);
+        const int nrows = a + (Lay::kVKeys - b);
+        for (int u = lane; u < 2 * nrows * Lay::kVChunks * 8; u += 32) {
+          const int cta = u & 1, v = u >> 1;
+          const int rr = v / (Lay::kVChunks * 8), rem = v % (Lay::kVChunks * 8);
+          const int row = rr < a ? rr : b + (rr - a);
+          const uint32_t addr = (cta ? st1 : st0) + (rem >> 3) * (Lay::kVKeys * 128) + row * 128 +
+                                (rem & 7) * 16;
+          asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u)
+                       : "memory");
+        }
+        // The pair's MMA reads both stages through the async proxy.
+        asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+        __syncwarp();
+      };
+      auto issue_pv = [&](const Geom& gm, uint32_t Tp, int jp) -> bool {
         const int sb = Tp & 1;
         if (!wait(&B.p_full[sb], (Tp >> 1) & 1)) return false;
         if (jp == 0 && !wait(&B.o_free, (I & 1) ^ 1)) return false;
         for (int sgi = 0; sgi < kBN / Lay::kVKeys; ++sgi, ++CV) {
           const int vs = CV % kVS;
           if (!wait(&B.v_full[vs], (CV / kVS) & 1)) return false;
+          clear_v_edges(gm, gm.key_first + jp * kBN + sgi * Lay::kVKeys, vs);
           tc_fence_after();
           const uint32_t vb = v_base + vs * kStage;
 #pragma unroll
@@ -382,7 +413,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (!alive) break;
             if (j + 2 == n) mma_commit_pair(&B.q_empty);
           }
-          alive = issue_pv(T + j, j);
+          alive = issue_pv(gm, T + j, j);
         }
         T += n;
         ++I;

@@ -152,6 +152,7 @@ static_assert(sizeof(Barriers) <= 512, "barrier block");
 
 struct Geom {
   int32_t seq, g, t0, ntok, pos_first, key_first, ntiles, W;
+  int32_t lo;   // first key visible to any query of the item
   bool ok;
 };
 
@@ -176,6 +177,7 @@ __device__ __forceinline__ Geom item_geom(const PrefillParams& p, const PrefillI
   r.ok = r.ntok > 0 && r.pos_first >= 0 && pos_last < L &&
          (pos_last >> p.page_shift) < p.mpps;
   const int32_t klo = first_visible(r.pos_first, r.W);
+  r.lo = klo;
   // Tiles start on a 64-key boundary at or below the first visible key (a
   // 128-key boundary would mask up to 127 keys of a window's first tile).
   r.key_first = klo / kTileAlign * kTileAlign;
@@ -214,12 +216,13 @@ __device__ __forceinline__ float max_tree(const uint32_t* v) {
 }
 
 // TMA source row of the box of `rows` keys starting at `key` (a box never
-// crosses a page; -rows: a box wholly past the item's last query, which the
-// TMA fills with zeros).
+// crosses a page; -rows: a box wholly outside the keys the item's queries
+// see, past its last query or before its first visible key, which the TMA
+// fills with zeros without reading the page table).
 __device__ __forceinline__ int32_t box_row(const PrefillParams& p, const Geom& gm, int32_t key,
                                            int32_t rows) {
   const int32_t pos_last = gm.pos_first + gm.ntok - 1;
-  if (key > pos_last) return -rows;
+  if (key > pos_last || key + rows <= gm.lo) return -rows;
   const int32_t page = __ldg(p.page_table + static_cast<int64_t>(gm.seq) * p.mpps +
                              (key >> p.page_shift));
   if (page < 0 || page >= p.num_pages) {
@@ -378,13 +381,41 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // MN-major B operand: 8-key groups 1024 B apart (SBO), 64-dimension
     // chunks kVKeys x 128 B apart (LBO); 16 keys per MMA = 2048 B.  P (A)
     // sits in the first 64 columns of its S buffer, 8 columns per 16 keys.
-    auto issue_pv = [&](uint32_t Tp, int jp) -> bool {
+    //
+    // A masked key has P = 0, but 0 x NaN is NaN: the V rows of keys no query
+    // of the item sees (before its first visible key, past its last query)
+    // may hold anything (free slots of the last page, pages a sliding-window
+    // cache has let go), so they are zeroed in the stage before the MMA reads
+    // it.  Boxes wholly outside those keys arrive as zeros already; only the
+    // stages at the two ends of an item need this.
+    auto clear_v_edges = [&](const Geom& gm, int32_t kst, int vs) {
+      const int32_t last = gm.pos_first + gm.ntok - 1;
+      const int a = max(0, min(Lay::kVKeys, gm.lo - kst));        // rows [0, a): before
+      const int b = max(0, min(Lay::kVKeys, last + 1 - kst));     // rows [b, kVKeys): past
+      if ((a == 0 && b == Lay::kVKeys) || a == Lay::kVKeys || b == 0) return;
+      // A key row is D / 64 chunks of 128 bytes, kVKeys x 128 B apart; the
+      // swizzle permutes 16-byte units inside a row, so whole rows are
+      // cleared whatever it is.
+      uint8_t* st = reinterpret_cast<uint8_t*>(v_s) + vs * kStage;
+      const int nrows = a + (Lay::kVKeys - b);
+      for (int u = lane; u < nrows * Lay::kChunks * 8; u += 32) {
+        const int rr = u / (Lay::kChunks * 8), rem = u % (Lay::kChunks * 8);
+        const int row = rr < a ? rr : b + (rr - a);
+        *reinterpret_cast<uint4*>(st + (rem >> 3) * (Lay::kVKeys * 128) + row * 128 +
+                                  (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      // The tensor core reads the stage through the async proxy.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+    };
+    auto issue_pv = [&](const Geom& gm, uint32_t Tp, int jp) -> bool {
       const int sb = Tp & 1;
       if (!wait(&B.p_full[sb], (Tp >> 1) & 1)) return false;
       if (jp == 0 && !wait(&B.o_free, (I & 1) ^ 1)) return false;
       for (int sgi = 0; sgi < Lay::kChunks; ++sgi, ++CV) {
         const int vs = CV % kVS;
         if (!wait(&B.v_full[vs], (CV / kVS) & 1)) return false;
+        clear_v_edges(gm, gm.key_first + jp * kBN + sgi * Lay::kVKeys, vs);
         tc_fence_after();
         const uint32_t vb = v_base + vs * kStage;
 #pragma unroll
@@ -437,7 +468,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           if (!alive) break;
           if (j + 2 == n) mma_commit(&B.q_empty);
         }
-        alive = issue_pv(T + j, j);
+        alive = issue_pv(gm, T + j, j);
       }
       T += n;
       ++I;

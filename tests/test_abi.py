@@ -533,3 +533,28 @@ def test_plan_log_line_when_asked():
     assert on.returncode == 0 and off.returncode == 0, on.stderr + off.stderr
     assert on.stderr.count("librpa plan: 128 seqs (128 decode, 0 prefill)") == 1, on.stderr
     assert "librpa plan" not in off.stderr
+
+
+def test_q_block_is_honoured_or_refused():
+    """A requested prefill query block is used as asked: up to one 128-row
+    tile per CTA (128 / G tokens; G = 2 here, so 64), twice that on SM pairs
+    (half per SM), and anything larger is refused, never silently shrunk."""
+    b = workloads.WORKLOADS["swa_prefill"](meta_only=True)
+    for qb in (8, 16, 32, 64):
+        info = plan_of(b, q_block=qb).info()
+        assert info["q_block"] == qb and info["prefill_pairs"] == 0
+    info = plan_of(b, q_block=128).info()
+    assert info["q_block"] == 128 and info["prefill_pairs"] == 1
+    assert info["num_prefill_items"] == b.num_kv_heads * 8192 // 128
+    info = plan_of(b, q_block=64, prefill_pairs=2).info()
+    assert info["q_block"] == 64 and info["prefill_pairs"] == 1
+    for qb in (256, 512, 129, 96 + 1):
+        with pytest.raises(RpaError) as e:
+            plan_of(b, q_block=qb)
+        assert e.value.status == binding.RPA_ERR_UNSUPPORTED, qb
+    # Multi-token decode at G = 8: one tile holds 16 tokens, a pair 32.
+    s = workloads.spec_decode_batch(meta_only=True)
+    assert plan_of(s, q_block=16).info()["q_block"] == 16
+    assert plan_of(s, q_block=32).info()["prefill_pairs"] == 1
+    with pytest.raises(RpaError):
+        plan_of(s, q_block=64)

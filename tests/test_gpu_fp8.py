@@ -11,7 +11,7 @@ import torch
 import oracle
 from ragged_paged_attention_rpa_gb300 import binding, workloads
 
-from .test_gpu_parity import assert_bf16_close
+from .test_gpu_parity import assert_bf16_close, unseen_slots
 
 pytestmark = pytest.mark.gpu
 
@@ -38,6 +38,7 @@ def run_fp8(b):
     v8 = torch.from_numpy(b.v_fp8).cuda()
     ks = torch.from_numpy(b.k_scale).cuda()
     vs = torch.from_numpy(b.v_scale).cuda()
+    db.out.fill_(float("nan"))
     binding.rpa_forward_fp8kv(db.q, k8, v8, ks, vs, db.page_table, db.cu_q_lens, db.kv_lens,
                               db.window, b.sm_scale, db.out, plan, ws)
     err = binding.rpa_get_device_error(ws)
@@ -61,6 +62,25 @@ def test_fp8_decode_workload():
     got, err, _ = run_fp8(b)
     assert err == 0
     assert_bf16_close(got, fp8_oracle(b), "fp8 decode workload")
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_fp8_decode_poisoned(case):
+    """e4m3 NaN (S.1111.111) in every fp8 slot no query sees."""
+    kv, hq, hkv, d, p, win = CASES[case]
+    b = workloads.with_fp8_kv(workloads.make_batch([1] * len(kv), kv, num_q_heads=hq,
+                                                   num_kv_heads=hkv, head_dim=d, page_size=p,
+                                                   windows=win, pool_pages=sum(-(-x // p) for x in kv) + 3,
+                                                   seed=870 + case))
+    mask = unseen_slots(b)
+    assert mask.any()
+    k8, v8 = b.k_fp8.copy(), b.v_fp8.copy()
+    k8[mask] = 0x7F
+    v8[mask] = 0xFF
+    b = workloads.Batch(**{**b.__dict__, "k_fp8": k8, "v_fp8": v8})
+    got, err, _ = run_fp8(b)
+    assert err == 0
+    assert_bf16_close(got, fp8_oracle(b), "poisoned fp8 decode case %d" % case)
 
 
 def test_bf16_entry_point_refuses_an_fp8_plan():

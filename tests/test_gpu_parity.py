@@ -5,9 +5,12 @@ Tolerances:
     the compared outputs, the oracle in fp32 accumulation, unrounded;
   * fp32 debug build: max |gpu - oracle| / max |oracle| <= 1e-5 (normwise; an
     elementwise relative bound is meaningless near zero outputs).
-Small cases compare every output; the full-size workloads compare every decode
-row and a fixed sample of prefill rows (first, last and window-edge tokens plus
-seeded random ones), which the oracle computes one by one.
+Every test compares every output row, the five full-size workloads included;
+`out` is filled with NaN before each call, so a row the kernels never write
+fails.  Pool slots that no query of the batch sees (free slots past a
+sequence's last key, keys before every query's window, pages no sequence owns)
+are set to NaN in the `poisoned` tests: the definition never reads them, so
+neither may the result depend on them.
 """
 
 from __future__ import annotations
@@ -34,6 +37,7 @@ def run_gpu(b, **plan_kw):
     db = binding.Batch(b)
     plan = db.plan(**plan_kw)
     ws = binding.alloc_workspace(plan)
+    db.out.fill_(float("nan"))
     out = db.forward(plan, ws)
     err = binding.rpa_get_device_error(ws)
     torch.cuda.synchronize()
@@ -52,30 +56,34 @@ def assert_bf16_close(got, ref, what=""):
         "%s: max %.3g mean %.3g" % (what, e.max(), e.mean())
 
 
-def sample_rows(b, n_random=512, seed=0):
-    """Every row of decode tokens; for prefill sequences their first and last
-    tokens, tokens at the window edge, and seeded random tokens (all heads)."""
-    hq = b.num_q_heads
-    toks = set()
-    rng = np.random.default_rng(seed)
+BF16_NAN = np.uint16(0x7FC0)
+
+
+def unseen_slots(b):
+    """[num_pages, page_size] mask of the pool slots no query of the batch
+    sees: for sequence s the visible keys of its queries together are
+    max(0, L - q_len - W + 1) .. L - 1 (W <= 0: from 0)."""
+    seen = np.zeros((b.num_pages, b.page_size), dtype=bool)
     for s in range(b.num_seqs):
-        t0, t1 = int(b.cu_q_lens[s]), int(b.cu_q_lens[s + 1])
-        if t1 - t0 == 0:
+        ql = int(b.cu_q_lens[s + 1] - b.cu_q_lens[s])
+        if ql == 0:
             continue
-        if t1 - t0 == 1:
-            toks.add(t0)
-            continue
-        toks.update([t0, t0 + 1, t1 - 1, t1 - 2])
+        L = int(b.kv_lens[s])
         w = 0 if b.window is None else int(b.window[s])
-        if w > 0:
-            L = int(b.kv_lens[s])
-            for pos in (w - 1, w, w + 1, w + 127, 2 * w):
-                t = t0 + pos - (L - (t1 - t0))
-                if t0 <= t < t1:
-                    toks.add(t)
-        toks.update(int(x) for x in rng.integers(t0, t1, size=min(n_random, t1 - t0)))
-    toks = np.array(sorted(toks), dtype=np.int64)
-    return (toks[:, None] * hq + np.arange(hq)[None, :]).reshape(-1)
+        lo = max(0, L - ql - w + 1) if w > 0 else 0
+        j = np.arange(lo, L)
+        seen[b.page_table[s, j // b.page_size], j % b.page_size] = True
+    return ~seen
+
+
+def poisoned(b):
+    """The batch with NaN in every K and V slot no query sees."""
+    mask = unseen_slots(b)
+    k, v = b.k_pages.copy(), b.v_pages.copy()
+    nan = BF16_NAN if k.dtype == np.uint16 else np.float32("nan")
+    k[mask] = nan
+    v[mask] = nan
+    return workloads.Batch(**{**b.__dict__, "k_pages": k, "v_pages": v})
 
 
 # ---------------------------------------------------------------- small cases
@@ -276,24 +284,33 @@ def test_bad_page_id_sets_the_error_word_without_faulting():
     assert_bf16_close(got, oracle_rows(b))
 
 
-# ---------------------------------------------------------------- prefill, mixed
+# ---------------------------------------------------------------- the full-size workloads
 
 
 @pytest.mark.parametrize("name", ["swa_prefill", "causal_prefill"])
-def test_prefill_workloads_sampled(name):
+def test_prefill_workloads_full(name):
+    """The 8192-token prefills (32 q / 16 kv heads, D 256), every output row."""
     b = workloads.WORKLOADS[name]()
     got, err, _ = run_gpu(b)
     assert err == 0
-    rows = sample_rows(b, n_random=96)
-    assert_bf16_close(got[rows], oracle_rows(b, rows), name)
+    assert_bf16_close(got, oracle_rows(b), name)
 
 
-def test_mixed_workload_sampled():
-    b = workloads.mixed_batch(seed=4)
+@pytest.fixture(scope="module")
+def mixed_case():
+    b = poisoned(workloads.mixed_batch(seed=4))
+    return b, oracle_rows(b)
+
+
+def test_mixed_workload_full(mixed_case):
+    """512 decode sequences and 4 chunked prefills of 2048 tokens, half of
+    them windowed, every output row, with NaN in every slot no query sees."""
+    b, ref = mixed_case
     got, err, plan = run_gpu(b)
     assert err == 0
-    rows = sample_rows(b, n_random=64)
-    assert_bf16_close(got[rows], oracle_rows(b, rows), "mixed")
+    info = plan.info()
+    assert info["num_decode_seqs"] == 512 and info["num_prefill_seqs"] == 4
+    assert_bf16_close(got, ref, "mixed")
 
 
 # ---------------------------------------------------------------- multi-token decode
@@ -325,12 +342,11 @@ def test_multi_token_decode(case):
     assert_bf16_close(got, oracle_rows(b), "multi-token decode case %d" % case)
 
 
-def test_spec_decode_workload_sampled():
+def test_spec_decode_workload_full():
     b = workloads.WORKLOADS["spec_decode"]()
     got, err, _ = run_gpu(b)
     assert err == 0
-    rows = sample_rows(b, n_random=8)
-    assert_bf16_close(got[rows], oracle_rows(b, rows), "spec_decode")
+    assert_bf16_close(got, oracle_rows(b), "spec_decode")
 
 
 @pytest.mark.parametrize("case,tiles", [(0, 2), (1, 2), (2, 1), (3, 1), (5, 1), (7, 2), (8, 1)])
@@ -344,3 +360,79 @@ def test_prefill_split_parts(case, tiles):
     info = plan.info()
     assert err == 0 and info["prefill_split_items"] > 0
     assert_bf16_close(got, oracle_rows(b), "split prefill case %d" % case)
+
+
+# ---------------------------------------------------------------- unseen slots hold NaN
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_small_ragged_poisoned(case):
+    ql, kv, hq, hkv, d, p, win = SMALL[case]
+    b = poisoned(workloads.make_batch(ql, kv, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                                      page_size=p, windows=win, pool_pages=None,
+                                      seed=1300 + case))
+    got, err, plan = run_gpu(b)
+    assert err == 0
+    assert_bf16_close(got, oracle_rows(b), "poisoned case %d" % case)
+
+
+@pytest.mark.parametrize("case", range(len(PREFILL)))
+def test_prefill_tc_poisoned(case):
+    ql, kv, hq, hkv, d, p, win = PREFILL[case]
+    b = poisoned(workloads.make_batch(ql, kv, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                                      page_size=p, windows=win, seed=1400 + case))
+    assert unseen_slots(b).any()
+    got, err, plan = run_gpu(b)
+    assert err == 0 and plan.info()["path"] == RPA_PATH_TC
+    assert_bf16_close(got, oracle_rows(b), "poisoned prefill case %d" % case)
+
+
+@pytest.mark.parametrize("case", [0, 2, 3, 5, 7])
+def test_prefill_sm_pairs_poisoned(case):
+    ql, kv, hq, hkv, d, p, win = PREFILL[case]
+    b = poisoned(workloads.make_batch(ql, kv, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                                      page_size=p, windows=win, seed=1500 + case))
+    got, err, plan = run_gpu(b, prefill_pairs=2)
+    assert err == 0 and plan.info()["prefill_pairs"] == 1
+    assert_bf16_close(got, oracle_rows(b), "poisoned pair prefill case %d" % case)
+
+
+@pytest.mark.parametrize("case,tiles", [(2, 1), (3, 1), (8, 2)])
+def test_prefill_split_parts_poisoned(case, tiles):
+    ql, kv, hq, hkv, d, p, win = PREFILL[case]
+    b = poisoned(workloads.make_batch(ql, kv, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                                      page_size=p, windows=win, seed=1600 + case))
+    got, err, plan = run_gpu(b, prefill_split=tiles)
+    assert err == 0 and plan.info()["prefill_split_items"] > 0
+    assert_bf16_close(got, oracle_rows(b), "poisoned split prefill case %d" % case)
+
+
+def test_decode_workload_poisoned():
+    """The decode batch with NaN in the free slots of every last page, before
+    every window and in the 2900-odd pool pages no sequence owns."""
+    b = poisoned(workloads.decode_batch(seed=1))
+    got, err, plan = run_gpu(b)
+    assert err == 0
+    assert_bf16_close(got, oracle_rows(b), "poisoned decode")
+    windowed = poisoned(workloads.make_batch([1] * 40, list(range(100, 4100, 100)),
+                                             num_q_heads=8, num_kv_heads=1, head_dim=256,
+                                             page_size=128, windows=[300 + 7 * i for i in range(40)],
+                                             seed=17))
+    got, err, _ = run_gpu(windowed)
+    assert err == 0
+    assert_bf16_close(got, oracle_rows(windowed), "poisoned windowed decode")
+
+
+# ---------------------------------------------------------------- query blocks of two tiles
+
+
+@pytest.mark.parametrize("q_block", [128, 64])
+def test_prefill_q_block_on_sm_pairs(q_block):
+    """A 128-token query block at G = 2 (two 128-row tiles) runs on SM pairs;
+    same result as any other block size."""
+    b = workloads.make_batch([700, 300], [700, 900], num_q_heads=4, num_kv_heads=2,
+                             head_dim=256, page_size=128, windows=[0, 128], seed=77)
+    got, err, plan = run_gpu(b, q_block=q_block, prefill_pairs=2)
+    info = plan.info()
+    assert err == 0 and info["q_block"] == q_block and info["prefill_pairs"] == 1
+    assert_bf16_close(got, oracle_rows(b), "q_block %d on pairs" % q_block)
