@@ -125,6 +125,14 @@ typedef struct rpa_plan_options {
                                CTA; items crossing a range boundary run as
                                parts whose fp32 partials a combine kernel
                                merges                                           */
+  int32_t decode_sms;       /* batches with both decode and tensor-core prefill
+                               work: 0 let the planner split the SMs between
+                               the two persistent grids (HBM-bound decode,
+                               tensor-bound prefill) and run them side by side,
+                               or not when its cost model says one after the
+                               other is faster; n > 0: decode on n SMs,
+                               prefill on the rest; -1: one after the other,
+                               each on every SM                                 */
 } rpa_plan_options;
 
 /* What a plan chose; filled by rpa_plan_get_info. */
@@ -145,6 +153,9 @@ typedef struct rpa_plan_info {
   int32_t prefill_split_items; /* prefill items split across CTAs              */
   int32_t prefill_split_parts; /* parts those items became                     */
   int32_t prefill_max_tiles;   /* key tiles of the busiest prefill CTA        */
+  int32_t decode_sms;          /* mixed batch run side by side: SMs of the
+                                  decode grid (0: not side by side)          */
+  int32_t prefill_sms;         /* ... and of the prefill grid                 */
 } rpa_plan_info;
 
 typedef struct rpa_plan rpa_plan_t;

@@ -75,7 +75,8 @@ class _Options(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_int32), ("path", ctypes.c_int32),
                 ("q_block", ctypes.c_int32), ("kv_split", ctypes.c_int32),
                 ("num_sms", ctypes.c_int32), ("prefill_pairs", ctypes.c_int32),
-                ("kv_dtype", ctypes.c_int32), ("prefill_split", ctypes.c_int32)]
+                ("kv_dtype", ctypes.c_int32), ("prefill_split", ctypes.c_int32),
+                ("decode_sms", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -85,7 +86,8 @@ class PlanInfo(ctypes.Structure):
                 ("num_prefill_items", ctypes.c_int32), ("prefill_ctas", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("prefill_pairs", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("prefill_split_items", ctypes.c_int32),
-                ("prefill_split_parts", ctypes.c_int32), ("prefill_max_tiles", ctypes.c_int32)]
+                ("prefill_split_parts", ctypes.c_int32), ("prefill_max_tiles", ctypes.c_int32),
+                ("decode_sms", ctypes.c_int32), ("prefill_sms", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: int(getattr(self, name)) for name, _ in self._fields_}
@@ -202,7 +204,8 @@ def rpa_plan(cu_q_lens_host, kv_lens_host, window_host, num_q_heads: int,
              num_kv_heads: int, head_dim: int, page_size: int, max_pages_per_seq: int,
              num_pages: int, dtype: int = RPA_DTYPE_BF16, path: int = RPA_PATH_AUTO,
              q_block: int = 0, kv_split: int = 0, num_sms: int = 0,
-             prefill_pairs: int = 0, kv_dtype: int = 0, prefill_split: int = 0) -> Plan:
+             prefill_pairs: int = 0, kv_dtype: int = 0, prefill_split: int = 0,
+             decode_sms: int = 0) -> Plan:
     """rpa_plan from host (numpy) metadata; returns a Plan."""
     cu = _np_i32(cu_q_lens_host)
     kv = _np_i32(kv_lens_host)
@@ -213,7 +216,7 @@ def rpa_plan(cu_q_lens_host, kv_lens_host, window_host, num_q_heads: int,
     if win is not None and win.shape[0] != num_seqs:
         raise ValueError("window must have num_seqs entries")
     opts = _Options(ctypes.sizeof(_Options), path, q_block, kv_split, num_sms, prefill_pairs,
-                    kv_dtype, prefill_split)
+                    kv_dtype, prefill_split, decode_sms)
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     st = lib().rpa_plan(ctypes.byref(handle), _np_ptr(cu), _np_ptr(kv), _np_ptr(win),
@@ -493,8 +496,13 @@ class ForwardCall:
             workspace.numel() * workspace.element_size())
         self._fn = lib().rpa_forward
 
-    def __call__(self):
-        st = self._fn(*self._args)
+    def __call__(self, plan: Optional[Plan] = None):
+        """Enqueue the call; `plan` replaces the plan given at construction
+        (one built for the same metadata, e.g. anew for every step)."""
+        args = self._args
+        if plan is not None:
+            args = args[:15] + (plan.handle,) + args[16:]
+        st = self._fn(*args)
         if st != RPA_OK:
             raise RpaError(st, "rpa_forward")
 
@@ -522,8 +530,11 @@ class ForwardFp8Call(ForwardCall):
             _dptr(workspace, "workspace"), workspace.numel() * workspace.element_size())
         self._fn = lib().rpa_forward_fp8kv
 
-    def __call__(self):
-        st = self._fn(*self._args)
+    def __call__(self, plan: Optional[Plan] = None):
+        args = self._args
+        if plan is not None:
+            args = args[:17] + (plan.handle,) + args[18:]
+        st = self._fn(*args)
         if st != RPA_OK:
             raise RpaError(st, "rpa_forward_fp8kv")
 

@@ -94,7 +94,7 @@ rpa_status_t rpa_plan(rpa_plan_t** plan, const int32_t* cu_q_lens_host,
   }
   if (o.q_block < 0 || o.kv_split < 0 || o.num_sms < 0 || o.prefill_pairs < 0 ||
       o.prefill_pairs > 2 || o.kv_dtype < 0 || o.kv_dtype > RPA_DTYPE_FP8_E4M3 ||
-      o.prefill_split < -1 || o.prefill_split > 65535)
+      o.prefill_split < -1 || o.prefill_split > 65535 || o.decode_sms < -1)
     return RPA_ERR_INVALID_ARG;
   rpa_status_t st = rpa::validate_metadata(cu_q_lens_host, kv_lens_host, num_seqs,
                                            page_size, max_pages_per_seq);
@@ -150,6 +150,8 @@ rpa_status_t rpa_plan_get_info(const rpa_plan_t* plan, rpa_plan_info* info) {
   info->prefill_split_items = static_cast<int32_t>(p.psplit.size());
   info->prefill_split_parts = p.n_split_items;
   info->prefill_max_tiles = p.prefill_max_tiles;
+  info->decode_sms = p.overlap ? p.decode_sms : 0;
+  info->prefill_sms = p.overlap ? p.prefill_sms : 0;
   return RPA_OK;
 }
 
@@ -165,6 +167,39 @@ rpa_status_t cuda_failed(int err) {
   return RPA_ERR_CUDA;
 }
 
+// The second stream of a mixed batch's side-by-side grids: one per host
+// thread and device, created by the thread's first such call on the device
+// (non-blocking, so it never waits on the legacy default stream by itself),
+// with the two events that fork it from and join it back to the caller's
+// stream.  Under stream capture the fork and the join become graph edges.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  ~SideStream() {
+    if (fork) cudaEventDestroy(fork);
+    if (join) cudaEventDestroy(join);
+    if (stream) cudaStreamDestroy(stream);
+  }
+};
+constexpr int kMaxSideDevices = 64;
+
+int side_stream(SideStream** out) {
+  static thread_local SideStream side[kMaxSideDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  if (dev < 0 || dev >= kMaxSideDevices) return static_cast<int>(cudaErrorInvalidDevice);
+  SideStream& r = side[dev];
+  if (r.stream == nullptr) {
+    if ((e = cudaEventCreateWithFlags(&r.fork, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&r.join, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&r.stream, cudaStreamNonBlocking)) != cudaSuccess)
+      return static_cast<int>(e);
+  }
+  *out = &r;
+  return 0;
+}
+
 rpa_status_t forward_launch(const rpa::Plan& p, const rpa::Args& a,
                             const rpa::KvWriteArgs* kvw, rpa_stream_t stream,
                             const rpa::PrologueArgs* pro = nullptr) {
@@ -172,14 +207,41 @@ rpa_status_t forward_launch(const rpa::Plan& p, const rpa::Args& a,
   rpa::trace_start(stream);
   if (kvw != nullptr && (err = rpa::launch_kv_write(*kvw, stream)) != 0) return cuda_failed(err);
   if (pro != nullptr && (err = rpa::launch_prologue(*pro, stream)) != 0) return cuda_failed(err);
-  if (p.num_decode > 0 && !p.simt_decode) {
+  const bool decode = p.num_decode > 0 && !p.simt_decode;
+  const bool prefill = !p.items.empty();
+  if (decode && prefill && p.overlap) {
+    // Side by side: the prefill grid (prefill_sms CTAs) on the side stream,
+    // forked after everything enqueued so far, the decode grid (decode_sms
+    // CTAs) on the caller's stream; the caller's stream then waits for the
+    // prefill.  Together the grids fill the SMs once.
+    SideStream* side = nullptr;
+    if ((err = side_stream(&side)) != 0) return cuda_failed(err);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaEventRecord(side->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+    if (e != cudaSuccess) return cuda_failed(static_cast<int>(e));
+    rpa_stream_t ss = reinterpret_cast<rpa_stream_t>(side->stream);
+    rpa::trace_start(ss);
+    err = rpa::launch_prefill_tc(p, a, ss);
+    if (err) return cuda_failed(err);
+    if ((e = cudaEventRecord(side->join, side->stream)) != cudaSuccess)
+      return cuda_failed(static_cast<int>(e));
     err = rpa::launch_decode(p, a, stream);
+    // Join even when the decode launch failed, so that a capture in progress
+    // is left with every forked stream joined.
+    e = cudaStreamWaitEvent(s, side->join, 0);
     if (err) return cuda_failed(err);
-  }
-  if (!p.items.empty()) {
-    err = p.prefill_pairs ? rpa::launch_prefill_pair(p, a, stream)
-                          : rpa::launch_prefill_tc(p, a, stream);
-    if (err) return cuda_failed(err);
+    if (e != cudaSuccess) return cuda_failed(static_cast<int>(e));
+  } else {
+    if (decode) {
+      err = rpa::launch_decode(p, a, stream);
+      if (err) return cuda_failed(err);
+    }
+    if (prefill) {
+      err = p.prefill_pairs ? rpa::launch_prefill_pair(p, a, stream)
+                            : rpa::launch_prefill_tc(p, a, stream);
+      if (err) return cuda_failed(err);
+    }
   }
   if (p.simt_decode || p.simt_prefill) {
     err = rpa::launch_simt(p, a, stream);

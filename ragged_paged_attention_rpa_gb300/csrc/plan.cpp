@@ -95,6 +95,7 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
   const int32_t nseg = static_cast<int32_t>(plan.dseg_seqhead.size());
   if (nseg == 0) return;
   const std::vector<int32_t>& blk0 = plan.dseg_blk0;
+  const int32_t dec_sms = plan.decode_sms > 0 ? plan.decode_sms : plan.num_sms;
   const int32_t P = plan.p;
   int32_t pshift = 0;                      // page sizes are powers of two
   while ((1 << pshift) < P) ++pshift;
@@ -172,7 +173,7 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
     Plan::DecodeLaunch dl{sb, se, 0, 0, slot_base, 0, 0, 0};
     bool uniform = forced_tokens > 0;
     if (!uniform) {
-      const int32_t cap = std::min<int32_t>(plan.num_sms, kMaxDecodeGrid);
+      const int32_t cap = std::min<int32_t>(dec_sms, kMaxDecodeGrid);
       const int64_t segs = se - sb;
       // Bounds on the smallest feasible cap T: every segment costs at least
       // once, so cap ranges need T >= (blocks + cost x segments) / cap; and a
@@ -221,7 +222,7 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
     if (uniform) {
       int32_t bpc = forced_tokens > 0
                         ? static_cast<int32_t>(ceil_div(forced_tokens, 16))
-                        : static_cast<int32_t>(ceil_div(total, static_cast<int64_t>(plan.num_sms)));
+                        : static_cast<int32_t>(ceil_div(total, static_cast<int64_t>(dec_sms)));
       bpc = std::max<int32_t>(1, bpc);
       while (bpc > 1 && !fits(sb, se, bpc)) bpc = std::max<int32_t>(1, bpc * 3 / 4);
       dl.bpc = bpc;
@@ -309,7 +310,8 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
   plan.pcta0.clear();
   plan.n_split_items = 0;
   plan.prefill_max_tiles = 0;
-  const int64_t slots = static_cast<int64_t>(plan.num_sms) * prefill_ctas_per_sm(plan.d);
+  const int64_t slots = static_cast<int64_t>(plan.prefill_sms > 0 ? plan.prefill_sms : plan.num_sms) *
+                       prefill_ctas_per_sm(plan.d);
   // A persistent grid takes the items round-robin, longest first; its time
   // is set by the CTA with the most tiles.  On request (prefill_split = n),
   // lay every item's key tiles end to end and cut them into ranges of n
@@ -439,6 +441,57 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
       per_item * std::min<int64_t>(static_cast<int64_t>(plan.items.size()), slots / per_item));
 }
 
+// Key tiles of the prefill work items with `span` query tokens each (the
+// same geometry as plan_prefill): their sum, the largest, and the count.
+struct TileStats {
+  int64_t total = 0, largest = 0, items = 0;
+};
+TileStats prefill_tile_stats(const Plan& plan, const int32_t* cu, const int32_t* kv,
+                             const int32_t* win, int64_t span) {
+  TileStats t;
+  for (int32_t s = 0; s < plan.num_seqs; ++s) {
+    const int32_t ql = cu[s + 1] - cu[s];
+    if (ql <= 1) continue;
+    const int32_t L = kv[s];
+    const int32_t w = win ? win[s] : 0;
+    for (int64_t b = 0; b < ceil_div(ql, span); ++b) {
+      const int64_t pos0 = static_cast<int64_t>(L) - ql + b * span;
+      const int64_t pos1 = std::min<int64_t>(pos0 + span, L) - 1;
+      const int64_t lo = (w > 0 && pos0 - (w - 1) > 0) ? pos0 - (w - 1) : 0;
+      const int64_t tiles =
+          (pos1 - lo / kPrefillTileAlign * kPrefillTileAlign) / kPrefillTileKeys + 1;
+      t.total += tiles * plan.hkv;
+      t.largest = std::max(t.largest, tiles);
+      t.items += plan.hkv;
+    }
+  }
+  return t;
+}
+
+// Cost model of a mixed batch's two persistent grids (microseconds), from
+// GB300 measurements of the kernels alone: the decode grid streams its KV
+// bytes at up to kDecodeSmGBs per SM until HBM saturates at kDecodeHbmGBs,
+// plus its ramp and merge tail; the single-SM prefill kernel at D = 256 takes
+// ~1.9 us per 128-key tile and ~3.2 us per item epilogue (both scale with D),
+// its makespan set by the busier of the average CTA and the longest item.
+constexpr double kDecodeSmGBs = 75.0;
+constexpr double kDecodeHbmGBs = 6000.0;
+constexpr double kDecodeFixedUs = 7.0;
+constexpr double kPrefillTileUs256 = 1.9;
+constexpr double kPrefillItemUs256 = 3.2;
+constexpr double kPrefillFixedUs = 4.0;
+
+double decode_cost_us(double bytes, int32_t sms) {
+  return bytes / std::min(sms * kDecodeSmGBs, kDecodeHbmGBs) * 1e-3 + kDecodeFixedUs;
+}
+
+double prefill_cost_us(const TileStats& t, int32_t head_dim, int32_t sms) {
+  const double f = head_dim / 256.0;
+  const double tiles = std::max(static_cast<double>(t.total) / sms, static_cast<double>(t.largest));
+  return tiles * kPrefillTileUs256 * f + std::ceil(static_cast<double>(t.items) / sms) *
+         kPrefillItemUs256 * f + kPrefillFixedUs;
+}
+
 }  // namespace
 
 rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
@@ -492,7 +545,6 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
   plan.dseg_seqhead.clear();
   plan.dseg_blk0.clear();
   plan.dlaunch.clear();
-  if (tc_decode && ndec > 0) plan_decode(plan, cu, kv, win, opts.kv_split);
 
   plan.items.clear();
   plan.q_block = 0;
@@ -518,6 +570,55 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
   // tiles): on GB300 the pair kernel's cross-SM barrier round trips cost
   // more per tile than its halved copy traffic saves.
   plan.prefill_pairs = pairs_ok && plan.num_prefill > 0 && want_pairs;
+
+  // A mixed batch ("TPU Deep Dive" slides, chapter 8, "Continuous batching
+  // with static shapes": one step holds decoding and prefilling sequences)
+  // puts HBM-bound decode and tensor-bound prefill work in one call.  One
+  // after the other, each grid leaves the other's resource idle; side by
+  // side on disjoint SMs, decode streams from HBM while prefill keeps the
+  // tensor cores busy.  The split of the SMs evens the two grids' modelled
+  // times; it is taken when that beats running them one after the other.
+  plan.overlap = false;
+  plan.decode_sms = plan.prefill_sms = 0;
+  plan.est_decode_us = plan.est_prefill_us = 0.f;
+  if (opts.decode_sms < -1) return RPA_ERR_INVALID_ARG;
+  if (tc_decode && ndec > 0 && tc_prefill && plan.num_prefill > 0 && !plan.prefill_pairs &&
+      opts.decode_sms >= 0 && plan.num_sms >= 2) {
+    double dec_bytes = 0;
+    for (int32_t s = 0; s < plan.num_seqs; ++s) {
+      if (cu[s + 1] - cu[s] != 1) continue;
+      const int32_t w = win ? win[s] : 0;
+      const int32_t lo = (w > 0 && kv[s] - w > 0) ? kv[s] - w : 0;
+      dec_bytes += static_cast<double>(ceil_div(kv[s], 16) - lo / 16) * 16.0 * plan.hkv *
+                   plan.d * 2.0 * (plan.kv_fp8 ? 1.0 : 2.0);
+    }
+    const int32_t qb_cta = opts.q_block > 0 ? opts.q_block : max_qb;
+    const TileStats ts = prefill_tile_stats(plan, cu, kv, win, qb_cta);
+    const int32_t n = plan.num_sms;
+    int32_t best = 0;
+    double best_t = decode_cost_us(dec_bytes, n) + prefill_cost_us(ts, plan.d, n);
+    if (opts.decode_sms > 0) {
+      best = std::min(opts.decode_sms, n - 1);
+      best_t = std::max(decode_cost_us(dec_bytes, best), prefill_cost_us(ts, plan.d, n - best));
+    } else {
+      for (int32_t x = 1; x < n; ++x) {
+        const double t = std::max(decode_cost_us(dec_bytes, x), prefill_cost_us(ts, plan.d, n - x));
+        if (t < best_t) {
+          best_t = t;
+          best = x;
+        }
+      }
+    }
+    if (best > 0) {
+      plan.overlap = true;
+      plan.decode_sms = best;
+      plan.prefill_sms = n - best;
+      plan.est_decode_us = static_cast<float>(decode_cost_us(dec_bytes, best));
+      plan.est_prefill_us = static_cast<float>(prefill_cost_us(ts, plan.d, n - best));
+    }
+  }
+
+  if (tc_decode && ndec > 0) plan_decode(plan, cu, kv, win, opts.kv_split);
   if (tc_prefill && plan.num_prefill > 0)
     plan_prefill(plan, cu, kv, win, opts.q_block, opts.prefill_split);
 

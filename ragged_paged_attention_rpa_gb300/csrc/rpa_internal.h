@@ -95,6 +95,14 @@ struct Plan {
   bool simt_decode = false;          // decode sequences handled by the SIMT kernel
   bool simt_prefill = false;         // prefill sequences handled by the SIMT kernel
   int32_t num_sms = 152;
+  // Mixed batches (decode and tensor-core prefill work in one call): the two
+  // persistent grids run side by side on disjoint SMs, decode on
+  // decode_sms of them and prefill on prefill_sms (forked onto a second
+  // stream and joined back); 0: each grid takes every SM, one after the other.
+  bool overlap = false;
+  int32_t decode_sms = 0, prefill_sms = 0;
+  // The planner's cost estimates (microseconds) behind that choice.
+  float est_decode_us = 0.f, est_prefill_us = 0.f;
 
   // Decode (q_len == 1) on the split-KV kernel.  Segments = (sequence, KV
   // head) pairs in stream order; blocks are 16 keys; each launch cuts its

@@ -12,8 +12,9 @@ namespace rpa {
 namespace {
 
 struct Mark {
-  int kernel;        // -1: start of an rpa_forward call
+  int kernel;        // -1: start of an rpa_forward call on `stream`
   cudaEvent_t event;
+  void* stream;
 };
 
 bool g_on = false;
@@ -41,7 +42,7 @@ void record(int kernel, void* stream) {
   if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return;
   const unsigned flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0u;
   if (cudaEventRecordWithFlags(e, s, flags) != cudaSuccess) return;
-  g_marks.push_back({kernel, e});
+  g_marks.push_back({kernel, e, stream});
 }
 
 }  // namespace
@@ -79,9 +80,14 @@ rpa_status_t rpa_trace_end(rpa_trace_record* records, int32_t* count) {
     const rpa::Mark& m = rpa::g_marks[i];
     if (m.kernel < 0) continue;
     if (n >= *count) break;
+    // The previous mark on the same stream: a mixed batch's prefill runs on
+    // a second stream beside the decode.
+    size_t j = i - 1;
+    while (j > 0 && rpa::g_marks[j].stream != m.stream) --j;
+    if (rpa::g_marks[j].stream != m.stream) continue;
     float ms = 0.f;
     if (cudaEventSynchronize(m.event) != cudaSuccess ||
-        cudaEventElapsedTime(&ms, rpa::g_marks[i - 1].event, m.event) != cudaSuccess) {
+        cudaEventElapsedTime(&ms, rpa::g_marks[j].event, m.event) != cudaSuccess) {
       st = RPA_ERR_CUDA;
       break;
     }

@@ -355,7 +355,7 @@ def test_prefill_items_scheduled_longest_first_to_least_loaded(name):
     info = plan_of(b).info()
     items = [it for it in prefill_items(b, info["q_block"]) for _ in range(b.num_kv_heads)]
     tiles = [t for _, t in items]
-    n = min(len(tiles), 152)
+    n = min(len(tiles), info["prefill_sms"] or 152)
     assert info["prefill_ctas"] == n
     assert info["prefill_max_tiles"] == lpt_busiest(tiles, n, keys=[k for k, _ in items])
     # Striding the longest-first list would load the busiest CTA more.
@@ -558,3 +558,53 @@ def test_q_block_is_honoured_or_refused():
     assert plan_of(s, q_block=32).info()["prefill_pairs"] == 1
     with pytest.raises(RpaError):
         plan_of(s, q_block=64)
+
+
+# The planner's cost model of a mixed batch's two grids, restated: decode
+# streams its visible 16-key blocks' K and V at up to 75 GB/s per SM until
+# 6000 GB/s, plus 7 us; the prefill takes 1.9 us per key tile and 3.2 us per
+# item epilogue at D = 256 (scaled by D / 256), plus 4 us, its tiles per CTA
+# at least those of the longest item.
+def mixed_costs(b, n_sms=152):
+    ql = np.diff(b.cu_q_lens)
+    dec_bytes = 0.0
+    for s in np.where(ql == 1)[0]:
+        L = int(b.kv_lens[s])
+        w = 0 if b.window is None else int(b.window[s])
+        lo = L - w if (w > 0 and L - w > 0) else 0
+        dec_bytes += (ceil_div(L, 16) - lo // 16) * 16 * b.num_kv_heads * b.head_dim * 4
+    qb = 128 // (b.num_q_heads // b.num_kv_heads)
+    tiles = [t for _, t in prefill_items(b, qb) for _ in range(b.num_kv_heads)]
+    f = b.head_dim / 256
+
+    def dec(x):
+        return dec_bytes / min(x * 75.0, 6000.0) * 1e-3 + 7.0
+
+    def pre(y):
+        return (max(sum(tiles) / y, max(tiles)) * 1.9 * f + ceil_div(len(tiles), y) * 3.2 * f
+                + 4.0)
+    return dec, pre
+
+
+def test_mixed_batch_grids_split_the_sms_by_the_cost_model():
+    """A batch with decode and prefill sequences runs its two persistent grids
+    side by side on disjoint SMs, split where the modelled times of the two
+    are most even (the larger of the two smallest), when that beats running
+    them one after the other; -1 keeps them sequential, n > 0 forces the
+    split."""
+    b = workloads.mixed_batch(seed=4, meta_only=True)
+    dec, pre = mixed_costs(b)
+    best = min(range(1, 152), key=lambda x: (max(dec(x), pre(152 - x)), x))
+    assert max(dec(best), pre(152 - best)) < dec(152) + pre(152)
+    info = plan_of(b).info()
+    assert info["decode_sms"] == best and info["prefill_sms"] == 152 - best
+    assert info["prefill_ctas"] == min(152 - best, info["num_prefill_items"])
+    seq = plan_of(b, decode_sms=-1).info()
+    assert seq["decode_sms"] == 0 and seq["prefill_sms"] == 0 and seq["prefill_ctas"] == 152
+    forced = plan_of(b, decode_sms=100).info()
+    assert forced["decode_sms"] == 100 and forced["prefill_sms"] == 52
+    with pytest.raises(RpaError):
+        plan_of(b, decode_sms=-2)
+    # Decode-only and prefill-only batches have nothing to overlap.
+    assert plan_of(workloads.decode_batch(meta_only=True)).info()["decode_sms"] == 0
+    assert plan_of(workloads.WORKLOADS["swa_prefill"](meta_only=True)).info()["decode_sms"] == 0

@@ -397,7 +397,7 @@ def test_prefill_sm_pairs_poisoned(case):
     assert_bf16_close(got, oracle_rows(b), "poisoned pair prefill case %d" % case)
 
 
-@pytest.mark.parametrize("case,tiles", [(2, 1), (3, 1), (8, 2)])
+@pytest.mark.parametrize("case,tiles", [(2, 1), (3, 1), (7, 2), (8, 1)])
 def test_prefill_split_parts_poisoned(case, tiles):
     ql, kv, hq, hkv, d, p, win = PREFILL[case]
     b = poisoned(workloads.make_batch(ql, kv, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
