@@ -468,18 +468,20 @@ TileStats prefill_tile_stats(const Plan& plan, const int32_t* cu, const int32_t*
   return t;
 }
 
-// Cost model of a mixed batch's two persistent grids (microseconds), from
-// GB300 measurements of the kernels alone: the decode grid streams its KV
-// bytes at up to kDecodeSmGBs per SM until HBM saturates at kDecodeHbmGBs,
-// plus its ramp and merge tail; the single-SM prefill kernel at D = 256 takes
-// ~1.9 us per 128-key tile and ~3.2 us per item epilogue (both scale with D),
-// its makespan set by the busier of the average CTA and the longest item.
-constexpr double kDecodeSmGBs = 75.0;
-constexpr double kDecodeHbmGBs = 6000.0;
-constexpr double kDecodeFixedUs = 7.0;
-constexpr double kPrefillTileUs256 = 1.9;
+// Cost model of a mixed batch's two persistent grids (microseconds), fitted
+// to GB300 timings of the mixed batch's decode part on 30-152 SMs and its
+// prefill part on 40-152 SMs: the decode grid streams its KV bytes at ~55
+// GB/s per SM (each CTA's copy ring, not HBM, sets the pace) until ~5 TB/s,
+// plus its ramp, merges and combine; the single-SM prefill kernel at D = 256
+// takes ~2.0 us per 128-key tile and ~3.2 us per item epilogue (both scale
+// with D), its makespan set by the busier of the average CTA and the longest
+// item, plus its ramp and tail.
+constexpr double kDecodeSmGBs = 55.0;
+constexpr double kDecodeHbmGBs = 5000.0;
+constexpr double kDecodeFixedUs = 8.0;
+constexpr double kPrefillTileUs256 = 2.0;
 constexpr double kPrefillItemUs256 = 3.2;
-constexpr double kPrefillFixedUs = 4.0;
+constexpr double kPrefillFixedUs = 20.0;
 
 double decode_cost_us(double bytes, int32_t sms) {
   return bytes / std::min(sms * kDecodeSmGBs, kDecodeHbmGBs) * 1e-3 + kDecodeFixedUs;
