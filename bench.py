@@ -727,6 +727,13 @@ def bench_one(args, name, world, rank, local, dist, binding, torch, peaks, l2_by
                 "frac": achieved / peak}
     roof["kernel"] = dom
     roof["kernel_us"] = dom_us
+    if info.get("decode_sms", 0) > 0 and dom in ("decode_split", "prefill_tc"):
+        # A mixed batch's grids run side by side: the kernel had only its
+        # share of the SMs; its fraction of that share of the peak beside.
+        sms = info["decode_sms"] if dom == "decode_split" else info["prefill_sms"]
+        share = sms / float(info["decode_sms"] + info["prefill_sms"])
+        roof["sm_share"] = share
+        roof["frac_of_sm_share"] = roof["frac"] / share
     roof["peak_source"] = "of %s (%s)" % (peaks["source"], "MEASURED_PEAKS.json"
                                           if peaks["source"] == "measured" else
                                           "6.8 TB/s, 1.9 PFLOP/s")
@@ -754,7 +761,7 @@ def bench_one(args, name, world, rank, local, dist, binding, torch, peaks, l2_by
                          "round-robin, %.1f s" % (n_tok, b.num_q_heads, b.name, el)}
 
     config = workload_config(b, counts, l2_bytes, world, args.flush)
-    config.update({
+    method = {
         "launch": "stream (Python loop behind a GPU sleep)" if args.no_graph else
                   "CUDA graph of the K timed steps, replayed once",
         "step": "rpa_forward_qkv (q/k RMS norm + rotary embedding, v norm, KV "
@@ -763,13 +770,14 @@ def bench_one(args, name, world, rank, local, dist, binding, torch, peaks, l2_by
                 if args.kv_write else ("rpa_forward_fp8kv" if fp8 else "rpa_forward"),
         "kv_pages": "e4m3 bytes + fp32 scale per KV head (f16 products, fp32 "
                     "accumulation)" if fp8 else "bf16",
-    })
+    }
     return {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if b.dtype == "bf16" else "f32", "data": "synthetic",
         "config": config,
+        "method": method,
         "plan": info,
         "achieved_gbs": counts["bytes"] / step_s / 1e9,
         "achieved_tflops": counts["flops"] / step_s / 1e12,
@@ -824,13 +832,12 @@ def main():
         # Every configuration: its own step time, throughput, dominant
         # kernel's roofline (with the ncu traffic where a summary exists), the
         # whole step's roofline fraction, the CPU oracle and e2e.
-        keep = ("value", "unit", "ms_per_step", "config", "plan", "achieved_gbs",
+        keep = ("value", "unit", "ms_per_step", "config", "method", "plan", "achieved_gbs",
                 "achieved_tflops", "algorithmic", "kernels", "roofline", "step_roofline",
                 "cpu_baseline", "e2e", "gpu_launches", "clocks", "flushed_step_ms",
                 "step_ms_p50")
         line["workloads"] = {n: {k: r[k] for k in keep} for n, r in recs.items()}
-        line["gpu_launches"] = sum(r["gpu_launches"] for r in recs.values())
-        line["gpu_launches_headline"] = recs[head]["gpu_launches"]
+        line["gpu_launches_all_workloads"] = sum(r["gpu_launches"] for r in recs.values())
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
