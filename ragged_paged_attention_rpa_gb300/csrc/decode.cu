@@ -359,8 +359,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int32_t idx = si.pg_off + (key0 >> p.page_shift) - si.slot0;
     return idx < kMaxCtaPages ? s_pages[idx] : -1;
   };
-  // Boxes of 128-byte rows: 64 bf16 or 128 fp8 elements.
-  constexpr int kBoxElems = 128 / L::ESZ;
   // Issue cursor over this warp's blocks: segment ist, local block isj.
   int ist = 0, isj = warp;
   while (ist < nseg && isj >= s_seg[ist].nb) { ++ist; isj = warp; }
@@ -384,11 +382,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       // Earlier generic-proxy reads of this stage come before the async writes.
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       sm100::mbar_arrive_expect_tx(&full_bar[warp][st], static_cast<uint32_t>(L::kStageBytes));
-#pragma unroll
-      for (int c = 0; c < D / kBoxElems; ++c) {
-        sm100::tma_load_3d(kt + c * kBlk * 128, &tm_k, &full_bar[warp][st], c * kBoxElems, si.g, row);
-        sm100::tma_load_3d(vt + c * kBlk * 128, &tm_v, &full_bar[warp][st], c * kBoxElems, si.g, row);
-      }
+      // One box per K and per V block: every 128-byte chunk of the block's
+      // 16 rows ([chunk][row][128 B] in the stage).
+      sm100::tma_load_4d(kt, &tm_k, &full_bar[warp][st], 0, si.g, row, 0);
+      sm100::tma_load_4d(vt, &tm_v, &full_bar[warp][st], 0, si.g, row, 0);
     }
     ++issued;
     advance(ist, isj);
@@ -826,10 +823,8 @@ int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   CUtensorMap tk, tv;
   const uint64_t rows = static_cast<uint64_t>(plan.num_pages) * plan.p;
   const bool fp8 = plan.kv_fp8;
-  if (fp8 ? (!make_tmap_3d_u8(&tk, a.k_pages, D, plan.hkv, rows, 1, kBlk) ||
-             !make_tmap_3d_u8(&tv, a.v_pages, D, plan.hkv, rows, 1, kBlk))
-          : (!make_tmap_3d(&tk, a.k_pages, D, plan.hkv, rows, 1, kBlk) ||
-             !make_tmap_3d(&tv, a.v_pages, D, plan.hkv, rows, 1, kBlk)))
+  if (!make_tmap_4d_chunks(&tk, a.k_pages, D, plan.hkv, rows, 1, kBlk, fp8) ||
+      !make_tmap_4d_chunks(&tv, a.v_pages, D, plan.hkv, rows, 1, kBlk, fp8))
     return static_cast<int>(cudaErrorInvalidValue);
   for (const Plan::DecodeLaunch& dl : plan.dlaunch) {
     const int n = dl.seg_end - dl.seg_begin;

@@ -101,6 +101,7 @@ struct PrefillParams {
   float* ppart_o;      // [slot][kBM][D]
   float* ppart_lse;    // [slot][kBM]
   int32_t out_v8;      // `out` is 32-byte aligned: the epilogue stores 32 bytes at once
+  int32_t v_4d;        // tm_v is 4-D (chunks outermost): one box per V stage
 };
 
 // One 32-byte store (eight 32-bit words) to a 32-byte aligned address.
@@ -343,6 +344,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(ring + st * kStage) + lane * rows * 64;
             if (is_k) {
               tma_load_3d(dst, tm, &full[st], sgi * 64, gm.g, row);
+            } else if (p.v_4d) {
+              // The stage's keys in one box of every 64-dimension chunk.
+              tma_load_4d(dst, tm, &full[st], 0, gm.g, row, 0);
             } else {
               for (int c = 0; c < Lay::kChunks; ++c)
                 tma_load_3d(dst + c * Lay::kVKeys * 64, tm, &full[st], c * 64, gm.g, row);
@@ -795,11 +799,15 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   const int box_rows_k = std::min(plan.p, kTileAlign);   // boxes never cross a page
   const int box_rows_v = std::min(std::min(plan.p, Lay::kVKeys), kTileAlign);
   CUtensorMap tq, tk, tv;
+  // A V stage that is one box high (its kVKeys keys in one page) takes all
+  // its 64-dimension chunks in one 4-D box ([chunk][key][128 B], the stage's
+  // layout); otherwise one 3-D box per chunk and per page.
+  const uint64_t pool_rows = static_cast<uint64_t>(plan.num_pages) * plan.p;
+  const bool v_4d = Lay::kChunks > 1 && box_rows_v == Lay::kVKeys;
   if (!make_tmap_3d(&tq, a.q, D, plan.hq, static_cast<uint64_t>(plan.total_q), G, qb) ||
-      !make_tmap_3d(&tk, a.k_pages, D, plan.hkv, static_cast<uint64_t>(plan.num_pages) * plan.p, 1,
-                    box_rows_k) ||
-      !make_tmap_3d(&tv, a.v_pages, D, plan.hkv, static_cast<uint64_t>(plan.num_pages) * plan.p, 1,
-                    box_rows_v))
+      !make_tmap_3d(&tk, a.k_pages, D, plan.hkv, pool_rows, 1, box_rows_k) ||
+      !(v_4d ? make_tmap_4d_chunks(&tv, a.v_pages, D, plan.hkv, pool_rows, 1, box_rows_v, false)
+             : make_tmap_3d(&tv, a.v_pages, D, plan.hkv, pool_rows, 1, box_rows_v)))
     return static_cast<int>(cudaErrorInvalidValue);
   PrefillParams p;
   p.page_table = a.page_table;
@@ -817,6 +825,7 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   p.page_shift = shift;
   p.box_rows_k = box_rows_k;
   p.box_rows_v = box_rows_v;
+  p.v_4d = v_4d ? 1 : 0;
   p.mpps = plan.mpps;
   p.num_pages = plan.num_pages;
   p.scale_log2 = a.sm_scale * 1.4426950408889634f;

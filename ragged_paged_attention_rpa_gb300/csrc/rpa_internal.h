@@ -256,6 +256,10 @@ bool decode_supported(int32_t head_dim, int32_t group, int32_t page_size);
 bool tmap_available();
 bool make_tmap_3d(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid, uint64_t outer,
                   uint32_t box_mid, uint32_t box_outer);
+// The same tensor as 4-D (64-element chunks outermost): one box brings every
+// chunk of box_outer rows, landing as [chunk][row][128 B] (bytes for fp8).
+bool make_tmap_4d_chunks(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid,
+                         uint64_t outer, uint32_t box_mid, uint32_t box_outer, bool fp8);
 // The same over a byte tensor (fp8 pages), box (128, box_mid, box_outer).
 bool make_tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid, uint64_t outer,
                      uint32_t box_mid, uint32_t box_outer);
