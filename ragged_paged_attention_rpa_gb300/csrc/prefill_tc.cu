@@ -31,7 +31,8 @@
 //              at a time; tcgen05.commit onto mbarriers.  The score tile runs
 //              one ahead of the PV product (two S buffers; P is written over
 //              its own S);
-//   warps 3-10 softmax: two warps per 32 rows (a TMEM lane quarter), one
+//   warp 3     idle (completes the first warpgroup);
+//   warps 4-11 softmax: two warps per 32 rows (a TMEM lane quarter), one
 //              thread per row and 64 of the tile's 128 keys each; the pair
 //              swaps row maxima through shared memory every tile;
 //              reads S from TMEM, masks causal and window edges (interior
@@ -40,8 +41,15 @@
 //              with a polynomial on the FMA pipe (paired fp32 instructions),
 //              writes P (bf16) to TMEM, rescales O in TMEM only when the max
 //              grew by more than 2^8 (the result is the same; it bounds P by
-//              256); epilogue O / l -> bf16 -> global (32-byte stores),
-//              the next item's geometry read during the current item.
+//              256); at an item's end hands its row sums to the epilogue
+//              and goes straight on to the next item's first tile, the next
+//              item's geometry read during the current item;
+//   warps 12-15 epilogue: one thread per row; waits for the item's last PV,
+//              O / l -> bf16 -> global (32-byte stores), then frees O for the
+//              next item's first PV, so the softmax warps never wait for an
+//              item's last PV nor drain O themselves.
+// The warpgroups rebalance registers at the start (setmaxnreg): the
+// producers and the epilogue give registers to the softmax warps.
 // Every wait is bounded; on a timeout the CTA records RPA_DEVERR_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -63,7 +71,16 @@ constexpr int kTileAlign = 64;  // score tiles start on multiples of this many k
 constexpr int kStage = 16384;   // bytes per K or V ring stage
 constexpr int kKS = 5;          // K ring depth (stages)
 constexpr int kVS = 5;          // V ring depth (stages)
-constexpr int kThreads = 352;   // K producer, V producer, MMA, 8 softmax warps
+constexpr int kThreads = 512;   // 4 warpgroups: producers + MMA, 2 x softmax, epilogue
+constexpr int kSoftmaxWarp0 = 4;  // warps 4-11: softmax (two warpgroups)
+constexpr int kEpiWarp0 = 12;     // warps 12-15: epilogue (one warpgroup)
+// Register split (setmaxnreg) against the launch's 512 x 128: the producer /
+// MMA warpgroup and the epilogue warpgroup give back to 80 per thread, the
+// two softmax warpgroups grow to 176: 128 x 80 + 128 x 80 + 256 x 176 =
+// 65536.
+constexpr int kRegsLaunch = 128, kRegsCtl = 80, kRegsEpi = 80, kRegsSoftmax = 176;
+static_assert(128 * kRegsCtl + 128 * kRegsEpi + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
+              "register split exceeds the launch's registers");
 constexpr int kPolyEvery = 32;  // one pair of exponentials in 32 on the FMA pipe
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait, then give up
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
@@ -127,10 +144,12 @@ struct Layout {
   static constexpr int kVOff = kKOff + kKS * kStage;
   static constexpr int kBarOff = kVOff + kVS * kStage;
   static constexpr int kXchOff = kBarOff + 512;         // softmax pair exchange
-  static constexpr int kUsed = kXchOff + 2 * 2 * kBM * 4;
+  static constexpr int kLOff = kXchOff + 2 * 2 * kBM * 4;   // row sums, softmax -> epilogue
+  static constexpr int kUsed = kLOff + kBM * 4;
   // Ask for more than half an SM's shared memory so that exactly one CTA
   // (which owns the SM's tensor memory) is resident per SM.
   static constexpr int kBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
+  static_assert(kUsed <= 227 * 1024, "more shared memory than one CTA may have");
   // TMEM columns: O (D), then two S buffers of 128; P (bf16 pairs) is
   // written over the first 64 columns of its own S buffer.
   static constexpr int kOCol = 0;
@@ -142,7 +161,8 @@ struct Barriers {
   uint64_t q_full, q_empty;
   uint64_t k_full[kKS], k_empty[kKS], v_full[kVS], v_empty[kVS];
   uint64_t s_full[2], p_full[2], o_done[2];
-  uint64_t o_free;
+  uint64_t o_free;       // the epilogue has read O out of TMEM
+  uint64_t l_full, l_empty;  // an item's row sums handed over / taken
   uint64_t fin;          // all MMAs of this CTA complete (teardown)
   uint64_t xbar[4];      // softmax pair exchange, one per TMEM lane quarter
   uint32_t tmem_base;
@@ -273,7 +293,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(&B.p_full[i], 256);
       mbar_init(&B.o_done[i], 1);
     }
-    mbar_init(&B.o_free, 256);
+    mbar_init(&B.o_free, 128);
+    mbar_init(&B.l_full, 128);
+    mbar_init(&B.l_empty, 128);
     for (int i = 0; i < 4; ++i) mbar_init(&B.xbar[i], 64);
     mbar_init(&B.fin, 1);
     B.abort = 0;
@@ -291,7 +313,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_after();
   const uint32_t tmem = B.tmem_base;
   const int G = p.group;
-
+  // Each warpgroup rebalances its registers at the start of its branch (all
+  // four of its warps at the same instruction).
+  if (warp < kSoftmaxWarp0) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
   if (warp <= 1) {
     // ------------------------------------------------------------ producers
     // Warp 0 loads Q and K, warp 1 loads V; each keeps its own ring of
@@ -374,7 +399,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     constexpr uint32_t kIdS = idesc_bf16(kBN, 0);
     constexpr uint32_t kIdPV = idesc_bf16(D, 1);
     const uint32_t q_base = smem_addr(q_s), k_base = smem_addr(k_s), v_base = smem_addr(v_s);
-    uint32_t T = 0, I = 0, CK = 0, CV = 0;   // tiles, items, K / V stages
+    uint32_t T = 0, I = 0, IO = 0, CK = 0, CV = 0;   // tiles, items (with PV), K / V stages
     bool alive = true;
     // A wait the whole warp agrees on.
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -415,7 +440,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     auto issue_pv = [&](const Geom& gm, uint32_t Tp, int jp) -> bool {
       const int sb = Tp & 1;
       if (!wait(&B.p_full[sb], (Tp >> 1) & 1)) return false;
-      if (jp == 0 && !wait(&B.o_free, (I & 1) ^ 1)) return false;
+      if (jp == 0 && !wait(&B.o_free, (IO & 1) ^ 1)) return false;
       for (int sgi = 0; sgi < Lay::kChunks; ++sgi, ++CV) {
         const int vs = CV % kVS;
         if (!wait(&B.v_full[vs], (CV / kVS) & 1)) return false;
@@ -476,6 +501,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       T += n;
       ++I;
+      if (n > 0) ++IO;
     }
     // Every MMA issued must finish before TMEM is released.
     mma_commit(&B.fin);
@@ -483,22 +509,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mbar_wait(&B.fin, 0, &dummy, kDrainNs);
     __syncwarp();
     if (!alive && lane == 0) report_error(p.ws, RPA_DEVERR_TIMEOUT, blockIdx.x);
-  } else {
-    // ------------------------------------------------------------ softmax + epilogue
+  }
+  // (warp 3: nothing to do)
+  } else if (warp < kEpiWarp0) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    // ------------------------------------------------------------ softmax
     // Two warps per TMEM lane quarter (32 rows): half h takes keys
     // [64h, 64h + 64) of every tile and columns [hD/2, (h+1)D/2) of O.  The
     // pair swaps row maxima every tile (and row sums once per item) through
     // shared memory, paced by the quarter's mbarrier; both then take the
     // same decisions, so O and P stay consistent.
     const int q4 = warp & 3;                            // TMEM lane quarter of this warp
-    const int h = (warp - 3) >> 2;                      // key / column half
+    const int h = (warp - kSoftmaxWarp0) >> 2;          // key / column half
     const int r = 32 * q4 + lane;                       // TMEM lane = row
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q4) << 16);
-    const int tok = r / G, head = r % G;
+    const int tok = r / G;
     const float c = p.scale_log2;
     float* xch = reinterpret_cast<float*>(smem + Lay::kXchOff);   // [2][2][kBM]
     uint64_t* xbar = &B.xbar[q4];
-    uint32_t T = 0, X = 0;                              // tiles, exchanges
+    uint32_t T = 0, X = 0, L = 0;                       // tiles, exchanges, items handed over
     bool alive = true;
     // Publish v for this row, wait for the partner's, return it.
     auto swap = [&](float v) -> float {
@@ -628,28 +657,65 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           p.ppart_lse[static_cast<int64_t>(split_slot(items.items[it].split)) * kBM + r] = -INFINITY;
         continue;
       }
-      // Epilogue: the row sum over both halves, then wait for the last PV
-      // and write this half's columns: O / l -> bf16 -> out.
+      // The row sum over both halves; then the first half hands it to the
+      // epilogue warps (one slot, taken before the next item's sums come)
+      // and writes a split part's log2-sum-exp.
       l += swap(l);
       if (!alive) break;
+      if (h == 0) {
+        if (items.items[it].split != 0 && valid)
+          p.ppart_lse[static_cast<int64_t>(split_slot(items.items[it].split)) * kBM + r] =
+              (l > 0.f) ? m_ref + __log2f(l) : -INFINITY;
+        if (!mbar_wait(&B.l_empty, (L & 1) ^ 1, abort, kWaitNs)) {
+          alive = false;
+          break;
+        }
+        reinterpret_cast<float*>(smem + Lay::kLOff)[r] = l;
+        mbar_arrive(&B.l_full);
+      }
+      ++L;
+    }
+    if (!alive && lane == 0) report_error(p.ws, RPA_DEVERR_TIMEOUT, blockIdx.x);
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
+    // ------------------------------------------------------------ epilogue
+    // One thread per row (TMEM lane).  Per item with key tiles: take the row
+    // sums from the softmax warps, wait for the item's last PV, then O / l
+    // -> bf16 -> out (or fp32 O / l into a split part's slot) and free O for
+    // the next item's first PV.  Meanwhile the softmax warps already work on
+    // the next item's first score tile.
+    const int q4 = warp & 3;
+    const int r = 32 * q4 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+    const int tok = r / G, head = r % G;
+    const float* l_s = reinterpret_cast<const float*>(smem + Lay::kLOff);
+    uint32_t T = 0, L = 0;                              // tiles, items taken over
+    bool alive = true;
+    for (int it = mine.begin; it < mine.end && alive; it += mine.step) {
+      const Geom gm = item_geom(p, items.items[it]);
+      if (!gm.ok || gm.ntiles == 0) continue;
+      T += gm.ntiles;
       const uint32_t Tl = T - 1;
+      const bool valid = tok < gm.ntok && r < G * p.qb_tokens;
+      if (!mbar_wait(&B.l_full, L & 1, abort, kWaitNs)) {
+        alive = false;
+        break;
+      }
+      const float l = l_s[r];
+      mbar_arrive(&B.l_empty);
+      ++L;
       if (!mbar_wait(&B.o_done[Tl & 1], (Tl >> 1) & 1, abort, kWaitNs)) {
         alive = false;
         break;
       }
       tc_fence_after();
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      __nv_bfloat16* orow =
-          p.out + (static_cast<int64_t>(gm.t0 + tok) * p.hq + gm.g * G + head) * D;
       if (items.items[it].split != 0) {
-        // A part of a split item: fp32 O / l and the row's log2-sum-exp (a
-        // row with no visible key here: zeros and -inf).
-        const int64_t slot = split_slot(items.items[it].split);
-        float* prow = p.ppart_o + (slot * kBM + r) * D;
-        if (h == 0 && valid)
-          p.ppart_lse[slot * kBM + r] = (l > 0.f) ? m_ref + __log2f(l) : -INFINITY;
+        // A part of a split item: fp32 O / l (a row with no visible key
+        // here: zeros; its log2-sum-exp, -inf, came from the softmax warps).
+        float* prow = p.ppart_o + (static_cast<int64_t>(split_slot(items.items[it].split)) * kBM + r) * D;
 #pragma unroll 1
-        for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
+        for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
           tmem_ld32(lane_addr + Lay::kOCol + c0, o);
           tmem_wait_ld();
@@ -662,30 +728,30 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                    __uint_as_float(o[4 * q + 3]) * inv);
           }
         }
-        tc_fence_before();
-        mbar_arrive(&B.o_free);
-        continue;
-      }
+      } else {
+        __nv_bfloat16* orow =
+            p.out + (static_cast<int64_t>(gm.t0 + tok) * p.hq + gm.g * G + head) * D;
 #pragma unroll 1
-      for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(lane_addr + Lay::kOCol + c0, o);
-        tmem_wait_ld();
-        if (valid) {
-          // Each thread writes 64 bytes of its own row: two 32-byte stores
-          // when `out` is 32-byte aligned (half the store transactions of a
-          // warp that touches 32 rows at once), else four 16-byte ones.
-          uint32_t w[16];
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + Lay::kOCol + c0, o);
+          tmem_wait_ld();
+          if (valid) {
+            // Each thread writes 64 bytes of its own row: two 32-byte stores
+            // when `out` is 32-byte aligned, else four 16-byte ones.
+            uint32_t w[16];
 #pragma unroll
-          for (int q = 0; q < 16; ++q)
-            w[q] = pack_bf16x2(__uint_as_float(o[2 * q]) * inv, __uint_as_float(o[2 * q + 1]) * inv);
-          if (p.out_v8) {
-            st_global_v8(orow + c0, w);
-            st_global_v8(orow + c0 + 16, w + 8);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+            for (int q = 0; q < 16; ++q)
+              w[q] = pack_bf16x2(__uint_as_float(o[2 * q]) * inv, __uint_as_float(o[2 * q + 1]) * inv);
+            if (p.out_v8) {
+              st_global_v8(orow + c0, w);
+              st_global_v8(orow + c0 + 16, w + 8);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+              for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            }
           }
         }
       }
