@@ -19,42 +19,35 @@
 // (sequence, query block, KV head), given by the plan: items, longest first,
 // go to the CTA with the fewest key tiles so far.  On request an item's key
 // tiles are split across CTAs; each part writes an fp32 partial (O / l and
-// the log2-sum-exp per row) that prefill_combine_kernel merges.
-//
-// Tensor memory holds the item's Q block (A operand of the score MMAs, D / 2
-// columns of bf16 pairs), O (D columns, fp32) and two score buffers of 64
-// keys; the shared memory holds nothing but the K and V rings (7 + 7 stages
-// of 16 KB) and a few small exchange buffers.  At D = 256 a Q block in shared
-// memory would take 64 KB, leaving rings of 1.25 tiles of K and of V whose
-// copies (~1 us from L2) the tensor core then waits for; with Q in tensor
-// memory the rings hold 3.5 score tiles each, and the score MMAs read only K
-// from shared memory.  Warp roles:
-//   warp 0     TMA producer of the Q block (once per item, its 64-dimension
-//              chunks as K-ring stages) and of K, gathered page by page
-//              through the page table (a stage: 64 keys x 128 dimensions);
-//   warp 1     TMA producer of V into its own ring (a stage: 8192 / D keys,
-//              at most 64, x all D dimensions), so K runs ahead of V;
-//   warp 2     MMA issuer: copies each Q chunk stage into tensor memory
-//              (tcgen05.cp), S = Q K^T over 64-key tiles (Q from TMEM, K
-//              from SMEM, N = 64), O += P V (P from TMEM, V from SMEM), one
-//              ring stage at a time; tcgen05.commit onto mbarriers.  The
-//              score tile runs one ahead of the PV product (two S buffers; P
-//              is written over its own S);
+// the log2-sum-exp per row) that prefill_combine_kernel merges.  Warp roles:
+//   warp 0     TMA producer of the Q block (once per item) and of K, gathered
+//              page by page through the page table into a ring of 16 KB
+//              stages (one 64-dimension chunk of a 128-key tile each);
+//   warp 1     TMA producer of V into its own ring of 16 KB stages (8192 / D
+//              keys x all D dimensions each), so K runs ahead of V;
+//   warp 2     MMA issuer: S = Q K^T over 128-key tiles (SMEM x SMEM -> TMEM,
+//              N = 128: narrower score MMAs leave the tensor core partly
+//              idle) and O += P V (P from TMEM, V from SMEM), one ring stage
+//              at a time; tcgen05.commit onto mbarriers.  The score tile runs
+//              one ahead of the PV product (two S buffers; P is written over
+//              its own S);
 //   warp 3     idle (completes the first warpgroup);
 //   warps 4-11 softmax: two warps per 32 rows (a TMEM lane quarter), one
-//              thread per row and 32 of the tile's 64 keys each; the pair
+//              thread per row and 64 of the tile's 128 keys each; the pair
 //              swaps row maxima through shared memory every tile;
 //              reads S from TMEM, masks causal and window edges (interior
 //              tiles skip the mask), keeps the running max / sum in fp32,
-//              exponentiates with the MUFU unit and, for one pair in 16,
+//              exponentiates with the MUFU unit and, for one pair in 32,
 //              with a polynomial on the FMA pipe (paired fp32 instructions),
 //              writes P (bf16) to TMEM, rescales O in TMEM only when the max
 //              grew by more than 2^8 (the result is the same; it bounds P by
 //              256); at an item's end hands its row sums to the epilogue
-//              and goes straight on to the next item's first tile;
+//              and goes straight on to the next item's first tile, the next
+//              item's geometry read during the current item;
 //   warps 12-15 epilogue: one thread per row; waits for the item's last PV,
 //              O / l -> bf16 -> global (32-byte stores), then frees O for the
-//              next item's first PV.
+//              next item's first PV, so the softmax warps never wait for an
+//              item's last PV nor drain O themselves.
 // The warpgroups rebalance registers at the start (setmaxnreg): the
 // producers and the epilogue give registers to the softmax warps.
 // Every wait is bounded; on a timeout the CTA records RPA_DEVERR_TIMEOUT,
@@ -73,12 +66,11 @@ namespace {
 using namespace sm100;
 
 constexpr int kBM = 128;        // MMA rows per block
-constexpr int kBN = 64;         // keys per score tile (N of the score MMAs)
+constexpr int kBN = 128;        // keys per score tile (N of the score MMAs)
 constexpr int kTileAlign = 64;  // score tiles start on multiples of this many keys
 constexpr int kStage = 16384;   // bytes per K or V ring stage
-constexpr int kKS = 7;          // K ring depth (stages; Q chunks pass through it too)
-constexpr int kVS = 7;          // V ring depth (stages)
-static_assert(kBN == kPrefillTileKeys && kTileAlign == kPrefillTileAlign, "plan tile geometry");
+constexpr int kKS = 5;          // K ring depth (stages)
+constexpr int kVS = 5;          // V ring depth (stages)
 constexpr int kThreads = 512;   // 4 warpgroups: producers + MMA, 2 x softmax, epilogue
 constexpr int kSoftmaxWarp0 = 4;  // warps 4-11: softmax (two warpgroups)
 constexpr int kEpiWarp0 = 12;     // warps 12-15: epilogue (one warpgroup)
@@ -89,7 +81,7 @@ constexpr int kEpiWarp0 = 12;     // warps 12-15: epilogue (one warpgroup)
 constexpr int kRegsLaunch = 128, kRegsCtl = 80, kRegsEpi = 80, kRegsSoftmax = 176;
 static_assert(128 * kRegsCtl + 128 * kRegsEpi + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
               "register split exceeds the launch's registers");
-constexpr int kPolyEvery = 16;  // one pair of exponentials in 16 on the FMA pipe
+constexpr int kPolyEvery = 32;  // one pair of exponentials in 32 on the FMA pipe
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait, then give up
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
 
@@ -127,7 +119,6 @@ struct PrefillParams {
   float* ppart_lse;    // [slot][kBM]
   int32_t out_v8;      // `out` is 32-byte aligned: the epilogue stores 32 bytes at once
   int32_t v_4d;        // tm_v is 4-D (chunks outermost): one box per V stage
-  int32_t k_4d;        // tm_k is 4-D: one box per K stage (64 keys x two chunks)
 };
 
 // One 32-byte store (eight 32-bit words) to a 32-byte aligned address.
@@ -138,20 +129,18 @@ __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
                : "memory");
 }
 
-// A 64-key score tile's K streams through the K ring 128 dimensions (two
-// 64-dimension chunks) at a time (64 keys x 256 B = one stage at D >= 128);
-// its V streams through the V ring kVKeys keys at a time (all D dimensions).
-// One stage feeds whole MMAs, so the tensor core starts on a tile before all
-// of it has landed.  The item's Q block passes through the K ring as D / 64
-// stages of 128 rows x 64 dimensions on its way to tensor memory.
+// A score tile's K streams through the K ring one 64-dimension chunk at a
+// time (128 keys x 128 B = one stage); its V streams through the V ring
+// kVKeys keys at a time (all D dimensions, kVKeys x D x 2 B = one stage).
+// Either way a tile is D / 64 stages, and one stage feeds whole MMAs, so the
+// tensor core starts on a tile before all of it has landed.
 template <int D>
 struct Layout {
   static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms per row
-  static constexpr int kKChunks = kChunks < 2 ? kChunks : 2;   // chunks per K stage
-  static constexpr int kKStages = kChunks / kKChunks;    // K stages per tile
-  static constexpr int kVKeys = 8192 / D < kBN ? 8192 / D : kBN;   // keys per V stage
-  static constexpr int kVStages = kBN / kVKeys;          // V stages per tile
-  static constexpr int kKOff = 0;
+  static constexpr int kVKeys = 8192 / D;                // keys per V stage
+  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kQBytes;
   static constexpr int kVOff = kKOff + kKS * kStage;
   static constexpr int kBarOff = kVOff + kVS * kStage;
   static constexpr int kXchOff = kBarOff + 512;         // softmax pair exchange
@@ -161,17 +150,15 @@ struct Layout {
   // (which owns the SM's tensor memory) is resident per SM.
   static constexpr int kBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
   static_assert(kUsed <= 227 * 1024, "more shared memory than one CTA may have");
-  // TMEM columns: O (D, fp32), Q (D / 2: bf16 pairs), two S buffers of 64;
-  // P (bf16 pairs) is written over the first 32 columns of its own S buffer.
+  // TMEM columns: O (D), then two S buffers of 128; P (bf16 pairs) is
+  // written over the first 64 columns of its own S buffer.
   static constexpr int kOCol = 0;
-  static constexpr int kQCol = D;
-  static constexpr int kSCol = D + D / 2;
-  static constexpr int kCols = 512;
-  static_assert(kSCol + 2 * kBN <= kCols, "tensor memory");
+  static constexpr int kSCol = D;
+  static constexpr int kCols = 512;                      // D + 256 <= 512
 };
 
 struct Barriers {
-  uint64_t q_done;       // an item's last score MMA has read Q (TMEM) and completed
+  uint64_t q_full, q_empty;
   uint64_t k_full[kKS], k_empty[kKS], v_full[kVS], v_empty[kVS];
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t o_free;       // the epilogue has read O out of TMEM
@@ -283,6 +270,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   uint8_t* smem = smem_raw;
   const ItemRange mine = my_items(items);
+  __nv_bfloat16* q_s = reinterpret_cast<__nv_bfloat16*>(smem + Lay::kQOff);
   __nv_bfloat16* k_s = reinterpret_cast<__nv_bfloat16*>(smem + Lay::kKOff);
   __nv_bfloat16* v_s = reinterpret_cast<__nv_bfloat16*>(smem + Lay::kVOff);
   Barriers& B = *reinterpret_cast<Barriers*>(smem + Lay::kBarOff);
@@ -290,7 +278,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(&B.q_done, 1);
+    mbar_init(&B.q_full, 1);
+    mbar_init(&B.q_empty, 1);
     for (int i = 0; i < kKS; ++i) {
       mbar_init(&B.k_full[i], 1);
       mbar_init(&B.k_empty[i], 1);
@@ -330,8 +319,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
   if (warp <= 1) {
     // ------------------------------------------------------------ producers
-    // Warp 0 loads Q (D / 64 stages per item) and K, warp 1 loads V; each
-    // keeps its own ring of 16 KB stages, counted by C across tiles and items.
+    // Warp 0 loads Q and K, warp 1 loads V; each keeps its own ring of
+    // 16 KB stages, counted by C across tiles and items.
     const bool is_k = warp == 0;
     const int depth = is_k ? kKS : kVS;
     uint64_t* full = is_k ? B.k_full : B.v_full;
@@ -339,22 +328,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint8_t* ring = smem + (is_k ? Lay::kKOff : Lay::kVOff);
     const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
     const int rows = is_k ? p.box_rows_k : p.box_rows_v;
-    const int nbox = (is_k ? kBN : Lay::kVKeys) / rows;    // boxes per stage and chunk (<= 8)
-    const int tile_stages = is_k ? Lay::kKStages : Lay::kVStages;
-    const uint32_t stage_bytes = is_k ? static_cast<uint32_t>(kBN * Lay::kKChunks * 128)
-                                      : static_cast<uint32_t>(Lay::kVKeys * D * 2);
+    const int nbox = (is_k ? kBN : Lay::kVKeys) / rows;    // boxes per stage (<= 8)
+    uint32_t C = 0, I = 0, issued_q = 0;
     const uint32_t q_box_bytes = static_cast<uint32_t>(G * p.qb_tokens) * 128u;
-    uint32_t C = 0;
     bool alive = true;
-    // Wait for ring stage C to be free and arm its full barrier for `bytes`.
-    auto take = [&](uint32_t bytes) -> int {
-      const int st = C % depth;
-      if (lane == 0) alive = mbar_wait(&empty[st], ((C / depth) & 1) ^ 1, abort, kWaitNs);
-      alive = __shfl_sync(0xffffffffu, alive, 0);
-      if (alive && lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
-      __syncwarp();
-      return st;
-    };
     for (int it = mine.begin; it < mine.end && alive; it += mine.step) {
       const Geom gm = item_geom(p, items.items[it]);
       if (!gm.ok) {
@@ -362,43 +339,42 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           report_error(p.ws, RPA_DEVERR_LENGTHS, gm.seq);
         continue;
       }
-      if (is_k) {
-        // Q: one stage per 64-dimension chunk, (G heads x qb tokens) rows.
-        for (int c = 0; c < Lay::kChunks && alive; ++c, ++C) {
-          const int st = take(q_box_bytes);
-          if (!alive) break;
-          if (lane == 0)
-            tma_load_3d(ring + st * kStage, &tm_q, &full[st], c * 64, gm.g * G, gm.t0);
+      const uint32_t Icur = I++;
+      if (is_k && lane == 0) {
+        alive = mbar_wait(&B.q_empty, (Icur & 1) ^ 1, abort, kWaitNs);
+        if (alive) {
+          mbar_arrive_expect_tx(&B.q_full, q_box_bytes * Lay::kChunks);
+          for (int c = 0; c < Lay::kChunks; ++c)
+            tma_load_3d(q_s + c * kBM * 64, &tm_q, &B.q_full, c * 64, gm.g * G, gm.t0);
+          ++issued_q;
         }
       }
+      alive = __shfl_sync(0xffffffffu, alive, 0);
       for (int j = 0; j < gm.ntiles && alive; ++j) {
         const int32_t key0 = gm.key_first + j * kBN;
-        // K: the same 64 keys for every chunk of the tile.
+        // K: the same 128 keys for every chunk of the tile.
         const int32_t krow = (is_k && lane < nbox) ? box_row(p, gm, key0 + lane * rows, rows) : 0;
-        for (int sgi = 0; sgi < tile_stages && alive; ++sgi, ++C) {
+        for (int sgi = 0; sgi < Lay::kChunks; ++sgi, ++C) {
+          const int st = C % depth;
+          const uint32_t ph = (C / depth) & 1;
           const int32_t row = is_k ? krow
                               : (lane < nbox ? box_row(p, gm, key0 + sgi * Lay::kVKeys + lane * rows, rows)
                                              : 0);
-          const int st = take(stage_bytes);
+          if (lane == 0) alive = mbar_wait(&empty[st], ph ^ 1, abort, kWaitNs);
+          alive = __shfl_sync(0xffffffffu, alive, 0);
           if (!alive) break;
+          if (lane == 0) mbar_arrive_expect_tx(&full[st], kStage);
+          __syncwarp();
           if (lane < nbox) {
-            uint8_t* stage = ring + st * kStage;
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(ring + st * kStage) + lane * rows * 64;
             if (is_k) {
-              if (p.k_4d) {
-                // Both 64-dimension chunks of the stage's 64 keys in one box.
-                tma_load_4d(stage, tm, &full[st], 0, gm.g, row, sgi * Lay::kKChunks);
-              } else {
-                for (int c = 0; c < Lay::kKChunks; ++c)
-                  tma_load_3d(stage + c * (kBN * 128) + lane * rows * 128, tm, &full[st],
-                              (sgi * Lay::kKChunks + c) * 64, gm.g, row);
-              }
+              tma_load_3d(dst, tm, &full[st], sgi * 64, gm.g, row);
             } else if (p.v_4d) {
               // The stage's keys in one box of every 64-dimension chunk.
-              tma_load_4d(stage + lane * rows * 128, tm, &full[st], 0, gm.g, row, 0);
+              tma_load_4d(dst, tm, &full[st], 0, gm.g, row, 0);
             } else {
               for (int c = 0; c < Lay::kChunks; ++c)
-                tma_load_3d(stage + c * (Lay::kVKeys * 128) + lane * rows * 128, tm, &full[st],
-                            c * 64, gm.g, row);
+                tma_load_3d(dst + c * Lay::kVKeys * 64, tm, &full[st], c * 64, gm.g, row);
             }
           }
         }
@@ -411,15 +387,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         int dummy = 0;
         mbar_wait(&full[t % depth], (t / depth) & 1, &dummy, kDrainNs);
       }
+      if (is_k && issued_q > 0) {
+        int dummy = 0;
+        mbar_wait(&B.q_full, (issued_q - 1) & 1, &dummy, kDrainNs);
+      }
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp walks the schedule and waits; one elected lane issues
-    // every copy, MMA and commit (see mma_ss).
+    // every MMA and commit (see mma_ss).
     constexpr uint32_t kIdS = idesc_bf16(kBN, 0);
     constexpr uint32_t kIdPV = idesc_bf16(D, 1);
-    const uint32_t k_base = smem_addr(k_s), v_base = smem_addr(v_s);
-    uint32_t T = 0, IO = 0, IQ = 0, CK = 0, CV = 0;   // tiles, items with PV / with S, stages
+    const uint32_t q_base = smem_addr(q_s), k_base = smem_addr(k_s), v_base = smem_addr(v_s);
+    uint32_t T = 0, I = 0, IO = 0, CK = 0, CV = 0;   // tiles, items (with PV), K / V stages
     bool alive = true;
     // A wait the whole warp agrees on.
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -429,7 +409,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // O += P(Tp) V(Tp): one V stage (kVKeys keys x D) at a time.  V is the
     // MN-major B operand: 8-key groups 1024 B apart (SBO), 64-dimension
     // chunks kVKeys x 128 B apart (LBO); 16 keys per MMA = 2048 B.  P (A)
-    // sits in the first 32 columns of its S buffer, 8 columns per 16 keys.
+    // sits in the first 64 columns of its S buffer, 8 columns per 16 keys.
     //
     // A masked key has P = 0, but 0 x NaN is NaN: the V rows of keys no query
     // of the item sees (before its first visible key, past its last query)
@@ -461,7 +441,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const int sb = Tp & 1;
       if (!wait(&B.p_full[sb], (Tp >> 1) & 1)) return false;
       if (jp == 0 && !wait(&B.o_free, (IO & 1) ^ 1)) return false;
-      for (int sgi = 0; sgi < Lay::kVStages; ++sgi, ++CV) {
+      for (int sgi = 0; sgi < Lay::kChunks; ++sgi, ++CV) {
         const int vs = CV % kVS;
         if (!wait(&B.v_full[vs], (CV / kVS) & 1)) return false;
         clear_v_edges(gm, gm.key_first + jp * kBN + sgi * Lay::kVKeys, vs);
@@ -479,25 +459,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mma_commit(&B.o_done[sb]);
       return true;
     };
-    // S(Ts) into S buffer (Ts & 1): one K stage (64 keys x two 64-dimension
-    // chunks) at a time.  A = Q in TMEM (8 columns per 16 dimensions), B = K,
-    // K-major with the 128-byte swizzle: 16 elements = 32 B inside a chunk,
-    // chunks 64 x 128 B apart.
+    // S(Ts) into S buffer (Ts & 1): one K stage (a 64-dimension chunk of 128
+    // keys) at a time.  Q and K are K-major with the 128-byte swizzle: 16
+    // elements = 32 B inside a chunk; Q's chunks are 16 KB apart.
     auto issue_s = [&](uint32_t Ts) -> bool {
       const uint32_t sc = tmem + Lay::kSCol + (Ts & 1) * kBN;
-      for (int ks_i = 0; ks_i < Lay::kKStages; ++ks_i, ++CK) {
+      for (int c = 0; c < Lay::kChunks; ++c, ++CK) {
         const int ks = CK % kKS;
         if (!wait(&B.k_full[ks], (CK / kKS) & 1)) return false;
         tc_fence_after();
         const uint32_t kb = k_base + ks * kStage;
 #pragma unroll
-        for (int c = 0; c < Lay::kKChunks; ++c) {
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int d0 = (ks_i * Lay::kKChunks + c) * 64 + w * 16;   // first dimension
-            const uint64_t bdesc = smem_desc(kb + c * (kBN * 128) + w * 32, 16, 1024);
-            mma_ts(sc, tmem + Lay::kQCol + d0 / 2, bdesc, kIdS, (d0 > 0) ? 1u : 0u);
-          }
+        for (int w = 0; w < 4; ++w) {
+          const uint64_t adesc = smem_desc(q_base + c * (kBM * 128) + w * 32, 16, 1024);
+          const uint64_t bdesc = smem_desc(kb + w * 32, 16, 1024);
+          mma_ss(sc, adesc, bdesc, kIdS, (c > 0 || w > 0) ? 1u : 0u);
         }
         mma_commit(&B.k_empty[ks]);
       }
@@ -507,49 +483,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int it = mine.begin; it < mine.end && alive; it += mine.step) {
       const Geom gm = item_geom(p, items.items[it]);
       if (!gm.ok) continue;
-      const int n = gm.ntiles;
-      // Q: its chunks arrive as K-ring stages.  The previous item's score
-      // MMAs must have finished reading Q before it is overwritten.
-      if (n > 0 && IQ > 0 && !wait(&B.q_done, (IQ - 1) & 1)) {
-        alive = false;
-        break;
-      }
-      for (int c = 0; c < Lay::kChunks; ++c, ++CK) {
-        const int ks = CK % kKS;
-        if (!wait(&B.k_full[ks], (CK / kKS) & 1)) {
-          alive = false;
-          break;
-        }
-        tc_fence_after();
-        if (n > 0) {
-          // 128 rows x 64 dimensions, K-major: four 16-dimension slabs.
-          const uint32_t qb = k_base + ks * kStage;
-#pragma unroll
-          for (int w = 0; w < 4; ++w)
-            tmem_cp_128x256b(tmem + Lay::kQCol + c * 32 + w * 8, smem_desc(qb + w * 32, 16, 1024));
-        }
-        mma_commit(&B.k_empty[ks]);
-      }
+      alive = wait(&B.q_full, I & 1);
       if (!alive) break;
       // Order: S(0), then for each j: S(j + 1), PV(j).  S(j + 1) overwrites
       // the buffer holding P(j - 1), which PV(j - 1) (issued before it) read.
-      if (n > 0) {
-        alive = issue_s(T);
-        if (n == 1) mma_commit(&B.q_done);
-      }
+      // Q is released once the item's last score tile is issued.
+      const int n = gm.ntiles;
+      if (n > 0) alive = issue_s(T);
+      if (n <= 1) mma_commit(&B.q_empty);
       for (int j = 0; j < n && alive; ++j) {
         if (j + 1 < n) {
           alive = issue_s(T + j + 1);
           if (!alive) break;
-          if (j + 2 == n) mma_commit(&B.q_done);
+          if (j + 2 == n) mma_commit(&B.q_empty);
         }
         alive = issue_pv(gm, T + j, j);
       }
       T += n;
-      if (n > 0) {
-        ++IO;
-        ++IQ;
-      }
+      ++I;
+      if (n > 0) ++IO;
     }
     // Every MMA issued must finish before TMEM is released.
     mma_commit(&B.fin);
@@ -563,7 +515,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------ softmax
     // Two warps per TMEM lane quarter (32 rows): half h takes keys
-    // [32h, 32h + 32) of every tile and columns [hD/2, (h+1)D/2) of O.  The
+    // [64h, 64h + 64) of every tile and columns [hD/2, (h+1)D/2) of O.  The
     // pair swaps row maxima every tile (and row sums once per item) through
     // shared memory, paced by the quarter's mbarrier; both then take the
     // same decisions, so O and P stay consistent.
@@ -609,22 +561,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           break;
         }
         tc_fence_after();
-        uint32_t sr[32];
-        tmem_ld32(lane_addr + Lay::kSCol + sb * kBN + 32 * h, sr);
+        uint32_t sr[64];
+        tmem_ld32(lane_addr + Lay::kSCol + sb * kBN + 64 * h,
+                  *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(lane_addr + Lay::kSCol + sb * kBN + 64 * h + 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_wait_ld();
-        const int32_t key0 = gm.key_first + j * kBN + 32 * h;
+        const int32_t key0 = gm.key_first + j * kBN + 64 * h;
         // Interior halves (every key visible to every row of the warp) skip
         // the per-element mask; elsewhere masked scores become -inf.
-        const bool full = __all_sync(0xffffffffu, valid && key0 >= lo && key0 + 31 <= pos);
+        const bool full = __all_sync(0xffffffffu, valid && key0 >= lo && key0 + 63 <= pos);
         if (!full) {
 #pragma unroll
-          for (int cc = 0; cc < 32; ++cc) {
+          for (int cc = 0; cc < 64; ++cc) {
             const int32_t key = key0 + cc;
             const bool vis = valid && key >= lo && key <= pos;
             if (!vis) sr[cc] = 0xff800000u;   // -inf
           }
         }
-        float mx = max_tree<32>(sr);
+        float mx = max_tree<64>(sr);
         mx = fmaxf(mx, swap(mx));
         if (!alive) break;
         // Scaling after the max keeps the order (c >= 0).
@@ -658,18 +613,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           m_ref = m_new;
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        // P for this half's 32 keys: 16 packed columns over the S buffer's
-        // columns [16h, 16h + 16), scores of half 0 that both halves have
+        // P for this half's 64 keys: 32 packed columns over the S buffer's
+        // columns [32h, 32h + 32), scores of half 0 that both halves have
         // read before the exchange above.
         // Paired fp32 arithmetic (masked scores are -inf: 2^-inf = +0).
         // One pair in kPolyEvery takes its 2^x on the FMA pipe.
-        uint32_t pk[16];
+        uint32_t pk[32];
         float ls;
         {
           const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_use, -m_use);
           uint64_t acc = f2_pack(0.f, 0.f);
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc) {
+          for (int cc = 0; cc < 32; ++cc) {
             const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[2 * cc]),
                                                __uint_as_float(sr[2 * cc + 1])), c2, nm2);
             uint64_t p2;
@@ -690,7 +645,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           ls = a0 + a1;
         }
         l += ls;
-        tmem_st16(lane_addr + Lay::kSCol + sb * kBN + 16 * h, pk);
+        tmem_st32(lane_addr + Lay::kSCol + sb * kBN + 32 * h, pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&B.p_full[sb]);
@@ -915,12 +870,8 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   // layout); otherwise one 3-D box per chunk and per page.
   const uint64_t pool_rows = static_cast<uint64_t>(plan.num_pages) * plan.p;
   const bool v_4d = Lay::kChunks > 1 && box_rows_v == Lay::kVKeys;
-  // A K stage (64 keys, two chunks) one box high likewise takes one 4-D box.
-  const bool k_4d = Lay::kKChunks > 1 && box_rows_k == kBN;
   if (!make_tmap_3d(&tq, a.q, D, plan.hq, static_cast<uint64_t>(plan.total_q), G, qb) ||
-      !(k_4d ? make_tmap_4d_chunks(&tk, a.k_pages, D, plan.hkv, pool_rows, 1, box_rows_k, false,
-                                   Lay::kKChunks)
-             : make_tmap_3d(&tk, a.k_pages, D, plan.hkv, pool_rows, 1, box_rows_k)) ||
+      !make_tmap_3d(&tk, a.k_pages, D, plan.hkv, pool_rows, 1, box_rows_k) ||
       !(v_4d ? make_tmap_4d_chunks(&tv, a.v_pages, D, plan.hkv, pool_rows, 1, box_rows_v, false)
              : make_tmap_3d(&tv, a.v_pages, D, plan.hkv, pool_rows, 1, box_rows_v)))
     return static_cast<int>(cudaErrorInvalidValue);
@@ -941,7 +892,6 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
   p.box_rows_k = box_rows_k;
   p.box_rows_v = box_rows_v;
   p.v_4d = v_4d ? 1 : 0;
-  p.k_4d = k_4d ? 1 : 0;
   p.mpps = plan.mpps;
   p.num_pages = plan.num_pages;
   p.scale_log2 = a.sm_scale * 1.4426950408889634f;

@@ -53,9 +53,9 @@ RPA_HD constexpr int32_t split_tiles(int32_t c) {
 // longer lists are split over several launches.
 constexpr int kMaxItemsPerLaunch = 2048;
 
-// Score tiles of the tensor-core prefill: 64 keys, starting on multiples of
+// Score tiles of the tensor-core prefill: 128 keys, starting on multiples of
 // 64 keys at or below the first visible key.
-constexpr int kPrefillTileKeys = 64;
+constexpr int kPrefillTileKeys = 128;
 constexpr int kPrefillTileAlign = 64;
 
 // An item split into parts: its partial slots are [slot0, slot0 + nparts).
@@ -256,12 +256,10 @@ bool decode_supported(int32_t head_dim, int32_t group, int32_t page_size);
 bool tmap_available();
 bool make_tmap_3d(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid, uint64_t outer,
                   uint32_t box_mid, uint32_t box_outer);
-// The same tensor as 4-D (64-element chunks outermost): one box brings
-// box_chunks chunks (0: every chunk) of box_outer rows, landing as
-// [chunk][row][128 B] (bytes for fp8).
+// The same tensor as 4-D (64-element chunks outermost): one box brings every
+// chunk of box_outer rows, landing as [chunk][row][128 B] (bytes for fp8).
 bool make_tmap_4d_chunks(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid,
-                         uint64_t outer, uint32_t box_mid, uint32_t box_outer, bool fp8,
-                         uint32_t box_chunks = 0);
+                         uint64_t outer, uint32_t box_mid, uint32_t box_outer, bool fp8);
 // The same over a byte tensor (fp8 pages), box (128, box_mid, box_outer).
 bool make_tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid, uint64_t outer,
                      uint32_t box_mid, uint32_t box_outer);

@@ -154,18 +154,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
-// Shared memory -> tensor memory copy of a 128-row x 256-bit slab (16 bf16
-// per row): row r of the matrix the descriptor describes lands in TMEM lane
-// r, eight consecutive 32-bit columns from `taddr`.  Issued like an MMA (one
-// elected lane) and executed in order with the MMAs the same lane issues
-// after it.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
-  asm volatile(
-      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
-      " @e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n}\n" ::"r"(taddr), "l"(s_desc)
-      : "memory");
-}
-
 // Arrive on `bar` once every MMA the elected lane issued before has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(

@@ -62,23 +62,20 @@ bool make_tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid,
 
 // The same tensor seen as 4-D, (64, mid, outer, d / 64): the 64-element
 // chunks of a row become the outermost dimension (stride 128 bytes), so one
-// box (64, box_mid, box_outer, box_chunks) brings box_chunks chunks (0: all)
-// of box_outer rows and lands in shared memory as [chunk][row][128 B], the
-// layout that separate 3-D boxes of (64, box_mid, box_outer) give, in one
-// copy.
+// box (64, box_mid, box_outer, d / 64) brings every chunk of box_outer rows
+// and lands in shared memory as [chunk][row][128 B], the layout that d / 64
+// separate 3-D boxes of (64, box_mid, box_outer) give, in one copy.
 bool make_tmap_4d_chunks(CUtensorMap* m, const void* base, uint64_t d, uint64_t mid,
-                         uint64_t outer, uint32_t box_mid, uint32_t box_outer, bool fp8,
-                         uint32_t box_chunks) {
+                         uint64_t outer, uint32_t box_mid, uint32_t box_outer, bool fp8) {
   EncodeFn fn = encode_fn();
   if (fn == nullptr) return false;
   const uint64_t esz = fp8 ? 1 : 2;
   const uint64_t inner = 128 / esz;            // elements of one 128-byte chunk
   if (d % inner != 0) return false;
-  if (box_chunks == 0) box_chunks = static_cast<uint32_t>(d / inner);
-  if (box_chunks > d / inner) return false;
   cuuint64_t dims[4] = {inner, mid, outer, d / inner};
   cuuint64_t strides[3] = {d * esz, d * mid * esz, 128};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(inner), box_mid, box_outer, box_chunks};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(inner), box_mid, box_outer,
+                       static_cast<cuuint32_t>(d / inner)};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                   const_cast<void*>(base), dims, strides, box, estr,

@@ -254,7 +254,7 @@ def test_fp8_kv_plans_are_decode_only():
 def prefill_items(b, q_block):
     """(keys streamed, key tiles) of every prefill work item (sequence, query
     block): the keys from the first visible key of its first query to its last
-    query's position; the 64-key tiles starting on a multiple of 64 at or
+    query's position; the 128-key tiles starting on a multiple of 64 at or
     below that first key.  Restated from the attention's visibility rule."""
     items = []
     for s in range(b.num_seqs):
@@ -267,12 +267,12 @@ def prefill_items(b, q_block):
             pos0 = L - ql + blk * q_block
             pos1 = min(L - ql + (blk + 1) * q_block, L) - 1
             lo = pos0 - (w - 1) if (w > 0 and pos0 - (w - 1) > 0) else 0
-            items.append((pos1 - lo + 1, (pos1 - lo // 64 * 64) // 64 + 1))
+            items.append((pos1 - lo + 1, (pos1 - lo // 64 * 64) // 128 + 1))
     return items
 
 
 def prefill_tiles(b, q_block):
-    """Key tiles (64 keys, starting on a multiple of 64 at or below the first
+    """Key tiles (128 keys, starting on a multiple of 64 at or below the first
     visible key) of every prefill work item (sequence, query block), restated
     from the attention's visibility rule."""
     tiles = []
@@ -286,7 +286,7 @@ def prefill_tiles(b, q_block):
             pos0 = L - ql + blk * q_block
             pos1 = min(L - ql + (blk + 1) * q_block, L) - 1
             lo = pos0 - (w - 1) if (w > 0 and pos0 - (w - 1) > 0) else 0
-            tiles.append((pos1 - lo // 64 * 64) // 64 + 1)
+            tiles.append((pos1 - lo // 64 * 64) // 128 + 1)
     return tiles
 
 
@@ -562,7 +562,7 @@ def test_q_block_is_honoured_or_refused():
 
 # The planner's cost model of a mixed batch's two grids, restated: decode
 # streams its visible 16-key blocks' K and V at up to 68 GB/s per SM until
-# 5000 GB/s, plus 8 us; the prefill takes 1.0 us per 64-key tile and 3.2 us per
+# 5000 GB/s, plus 8 us; the prefill takes 2.0 us per key tile and 3.2 us per
 # item epilogue at D = 256 (scaled by D / 256), plus 20 us, its tiles per CTA
 # at least those of the longest item.
 def mixed_costs(b, n_sms=152):
@@ -581,7 +581,7 @@ def mixed_costs(b, n_sms=152):
         return dec_bytes / min(x * 68.0, 5000.0) * 1e-3 + 8.0
 
     def pre(y):
-        return (max(sum(tiles) / y, max(tiles)) * 1.0 * f + ceil_div(len(tiles), y) * 3.2 * f
+        return (max(sum(tiles) / y, max(tiles)) * 2.0 * f + ceil_div(len(tiles), y) * 3.2 * f
                 + 20.0)
     return dec, pre
 
