@@ -168,7 +168,8 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {
-    "decode_split": ["decode.cu"], "decode_combine": ["decode.cu"],
+    "decode_split": ["decode.cu", "decode_sched.cuh"],
+    "decode_combine": ["decode.cu", "decode_sched.cuh"],
     "prefill_tc": ["prefill_tc.cu"], "prefill_combine": ["prefill_tc.cu"],
     "simt": ["simt.cu"], "kv_write": ["kv_write.cu"], "prologue": ["prologue.cu"],
 }

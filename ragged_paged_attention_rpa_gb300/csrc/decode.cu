@@ -44,6 +44,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "decode_sched.cuh"
 #include "rpa_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -55,72 +56,6 @@ constexpr int kWarps = 4;
 constexpr int kBlk = 16;  // keys per warp block (the MMA's M)
 
 constexpr int stages_for(int D) { return D >= 256 ? 3 : 4; }
-
-struct DecodeParams {
-  const __nv_bfloat16* q;
-  const __nv_bfloat16* k;
-  const __nv_bfloat16* v;
-  const int32_t* page_table;
-  const int32_t* cu_q_lens;
-  const int32_t* kv_lens;
-  const int32_t* window;
-  __nv_bfloat16* out;
-  unsigned char* ws;
-  float* part_o;      // [2 * total CTAs][G][D]
-  float* part_lse;    // [2 * total CTAs][G]
-  int32_t hq, hkv, group, page_shift, mpps, num_pages;
-  float scale_log2;   // sm_scale * log2(e)
-  const float* k_scale;  // fp8 pages: per-KV-head scales (else unused)
-  const float* v_scale;
-};
-
-// One launch's share of the block stream.  seqhead[i] = (sequence << 8) | kv
-// head of segment i; blk0[i] = first block of segment i (blk0[n_seg] = total).
-// CTA c takes blocks [c * bpc, (c + 1) * bpc) where bpc > 0, else
-// [cta0[c], cta0[c + 1]).
-template <int NSEG>
-struct DecodeSched {
-  int32_t n_seg, bpc, n_blocks, slot_base, seg_base, n_ctas;
-  int32_t cta0[kMaxDecodeGrid + 1];
-  int32_t cta_seg[kMaxDecodeGrid];   // first segment | last segment << 16
-  int32_t seqhead[NSEG];
-  int32_t blk0[NSEG + 1];
-  // From the plan's host metadata (validated there): query token, first
-  // visible key and length of each segment's sequence.
-  int32_t q0[NSEG], lo[NSEG], len[NSEG];
-};
-
-template <int NSEG>
-__device__ __forceinline__ int32_t range_start(const DecodeSched<NSEG>& sc, int c) {
-  return sc.bpc > 0 ? min(c * sc.bpc, sc.n_blocks) : sc.cta0[c];
-}
-
-// The CTA whose range holds block x.
-template <int NSEG>
-__device__ __forceinline__ int cta_of(const DecodeSched<NSEG>& sc, int32_t x) {
-  if (sc.bpc > 0) return x / sc.bpc;
-  int lo = 0, hi = sc.n_ctas - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (sc.cta0[mid] <= x) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
-struct SegInfo {
-  int32_t s, g, q0;      // sequence, kv head, its query token
-  int32_t kb, ke;        // keys [kb, ke) of this CTA's part (kb on a 16-key boundary)
-  int32_t lo;            // first visible key of the sequence
-  int32_t nb;            // 16-key blocks in this CTA's part
-  int32_t slot0, pg_off; // first page-table slot; offset in the shared page list
-  int32_t npg;           // pages of this part
-  int32_t whole;         // the segment lies entirely in this CTA's range
-  int32_t gseg;          // segment index in the launch
-};
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
@@ -185,17 +120,6 @@ __device__ __forceinline__ uint32_t pack_t(float lo, float hi) {
 // 16-byte chunk index XORed with the row's low three bits).
 __device__ __forceinline__ int swz(int row, int chunk) {
   return (chunk >> 3) * (16 * 64) + row * 64 + (((chunk & 7) ^ (row & 7)) << 3);
-}
-
-// Largest i in [0, n) with a[i] <= x (a sorted ascending, a[0] <= x).
-template <int NSEG>
-__device__ __forceinline__ int seg_of(const DecodeSched<NSEG>& sc, int32_t x) {
-  int lo = 0, hi = sc.n_seg - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (sc.blk0[mid] <= x) lo = mid; else hi = mid - 1;
-  }
-  return lo;
 }
 
 // Shared memory of a decode CTA: per warp a ring of S stages (one 16-key
@@ -287,66 +211,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     sm100::prefetch_tmap(&tm_k);
     sm100::prefetch_tmap(&tm_v);
   }
-  // ---- Segment table of this CTA's range.  Segment t's entry (and, from
-  // the page counts of the segments before it, its offset in the page list)
-  // comes from the launch parameters alone, so one barrier publishes it.
-  auto seg_info = [&](int t) {
-    const int k = kfirst + t;
-    const int32_t sh = sc.seqhead[k];
-    SegInfo si;
-    si.s = sh >> 8;
-    si.g = sh & 255;
-    si.gseg = k;
-    si.q0 = sc.q0[k];
-    const int32_t Lk = sc.len[k];
-    const int32_t lo = sc.lo[k];
-    const int32_t nb_plan = sc.blk0[k + 1] - sc.blk0[k];
-    const int32_t jb = max(cb0, sc.blk0[k]) - sc.blk0[k];
-    const int32_t je = min(cb1, sc.blk0[k + 1]) - sc.blk0[k];
-    si.lo = lo;
-    si.kb = (lo / kBlk + jb) * kBlk;
-    si.ke = min(Lk, (lo / kBlk + je) * kBlk);
-    if (si.ke < si.kb) si.ke = si.kb;
-    si.nb = je - jb;
-    si.whole = (jb == 0 && je == nb_plan) ? 1 : 0;
-    si.slot0 = si.kb >> p.page_shift;
-    si.npg = (si.ke > si.kb) ? ((si.ke - 1) >> p.page_shift) - si.slot0 + 1 : 0;
-    si.pg_off = 0;
-    return si;
-  };
-  for (int t = tid; t <= nseg; t += kWarps * 32) {
-    int off = 0;
-    for (int u = 0; u < t; ++u) off += seg_info(u).npg;
-    if (t < nseg) {
-      SegInfo si = seg_info(t);
-      si.pg_off = off;
-      s_seg[t] = si;
-    } else {
-      // One past the last segment: the length of the page list.
-      s_npages = min(off, kMaxCtaPages);
-      if (off > kMaxCtaPages) report_error(p.ws, RPA_DEVERR_LENGTHS, c);
-    }
-  }
-  __syncthreads();
-  // ---- Page ids of the range, read once (all loads in one round).
-  for (int i = tid; i < s_npages; i += kWarps * 32) {
-    int t = 0;
-    while (t + 1 < nseg && s_seg[t + 1].pg_off <= i) ++t;
-    const SegInfo& si = s_seg[t];
-    const int32_t slot = si.slot0 + (i - si.pg_off);
-    int32_t page = -1;
-    if (slot >= p.mpps) {
-      report_error(p.ws, RPA_DEVERR_LENGTHS, si.s);
-    } else {
-      page = __ldg(p.page_table + static_cast<int64_t>(si.s) * p.mpps + slot);
-      if (page < 0 || page >= p.num_pages) {
-        report_error(p.ws, RPA_DEVERR_PAGE_ID, si.s);
-        page = -1;
-      }
-    }
-    s_pages[i] = page;
-  }
-  __syncthreads();
+  load_range_tables(sc, p, c, cb0, cb1, kfirst, nseg, s_seg, s_pages, &s_npages);
 
   unsigned char* ring = smem_raw + warp * S * L::kStageBytes;
   volatile int* abort = &s_abort;
@@ -879,6 +744,17 @@ int noalloc_scratch(void** ptr) {
   }
   *ptr = g_noalloc_ptr[dev];
   return 0;
+}
+
+int launch_decode_combine(const Plan& plan, const DecodeParams& p, const Plan::DecodeLaunch& dl,
+                          int head_dim, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  switch (head_dim) {
+    case 64: return launch_combine<64>(plan, p, dl, s);
+    case 128: return launch_combine<128>(plan, p, dl, s);
+    case 256: return launch_combine<256>(plan, p, dl, s);
+    default: return static_cast<int>(cudaErrorInvalidValue);
+  }
 }
 
 bool decode_supported(int32_t head_dim, int32_t group, int32_t page_size) {
