@@ -335,6 +335,9 @@ def parse():
     ap.add_argument("--decode-sms", type=int, default=0,
                     help="plan option for mixed batches: 0 choose, -1 run decode and prefill "
                          "one after the other, n > 0 decode on n SMs beside the prefill")
+    ap.add_argument("--decode-kernel", type=int, default=0,
+                    help="plan option: 0 choose, 1 CUDA-core decode kernel, 2 tensor-core "
+                         "decode kernel")
     ap.add_argument("--flush", action="store_true",
                     help="flush L2 before every step and time each step with its own "
                          "event pair, even when a step's inputs exceed L2")
@@ -482,7 +485,8 @@ def bench_one(args, name, world, rank, local, dist, binding, torch, peaks, l2_by
     fp8 = b.k_fp8 is not None
     plan_kw = dict(q_block=args.q_block, kv_split=args.kv_split,
                    kv_dtype=binding.RPA_DTYPE_FP8_E4M3 if fp8 else 0,
-                   prefill_split=args.prefill_split, decode_sms=args.decode_sms)
+                   prefill_split=args.prefill_split, decode_sms=args.decode_sms,
+                   decode_kernel=0 if fp8 else args.decode_kernel)
     plan = db.plan(**plan_kw)
     info = plan.info()
     ws = binding.alloc_workspace(plan)

@@ -99,6 +99,17 @@ enum {
   RPA_PATH_TC = 2      /* tensor-core paths; RPA_ERR_UNSUPPORTED if impossible  */
 };
 
+/* Split-KV decode kernels (rpa_plan_options.decode_kernel). */
+enum {
+  RPA_DECODE_KERNEL_AUTO = 0, /* the planner's choice                            */
+  RPA_DECODE_KERNEL_MMA = 1,  /* CUDA-core warp MMAs (mma.sync): every decode
+                                 shape of the tensor-core path, fp8 pages too   */
+  RPA_DECODE_KERNEL_TC = 2    /* tensor cores (tcgen05.mma, accumulators in
+                                 tensor memory): bf16 pages, head_dim 128 or
+                                 256, G <= 8, page_size >= 16; else
+                                 RPA_ERR_UNSUPPORTED                            */
+};
+
 /* Optional knobs for rpa_plan.  Zero-initialise and set struct_size. */
 typedef struct rpa_plan_options {
   int32_t struct_size;      /* sizeof(rpa_plan_options)                         */
@@ -133,6 +144,7 @@ typedef struct rpa_plan_options {
                                other is faster; n > 0: decode on n SMs,
                                prefill on the rest; -1: one after the other,
                                each on every SM                                 */
+  int32_t decode_kernel;    /* RPA_DECODE_KERNEL_* for the split-KV decode      */
 } rpa_plan_options;
 
 /* What a plan chose; filled by rpa_plan_get_info. */
@@ -156,6 +168,8 @@ typedef struct rpa_plan_info {
   int32_t decode_sms;          /* mixed batch run side by side: SMs of the
                                   decode grid (0: not side by side)          */
   int32_t prefill_sms;         /* ... and of the prefill grid                 */
+  int32_t decode_kernel;       /* RPA_DECODE_KERNEL_MMA or _TC for the
+                                  split-KV decode (0: no such decode)         */
 } rpa_plan_info;
 
 typedef struct rpa_plan rpa_plan_t;

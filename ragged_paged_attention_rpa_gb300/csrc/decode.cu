@@ -622,37 +622,7 @@ int launch_one(const Plan& plan, const DecodeParams& p, const CUtensorMap& tk,
     return e;
   // Host staging, copied into the launch parameters.
   DecodeSched<NSEG>& sc = thread_staging<DecodeSched<NSEG>>();
-  const int n = dl.seg_end - dl.seg_begin;
-  sc.n_seg = n;
-  sc.bpc = dl.bpc;
-  sc.n_ctas = dl.n_ctas;
-  if (dl.bpc == 0) {
-    if (dl.n_ctas > kMaxDecodeGrid) return static_cast<int>(cudaErrorInvalidValue);
-    for (int i = 0; i <= dl.n_ctas; ++i) sc.cta0[i] = plan.dcta_blk0[dl.cta_begin + i];
-  }
-  sc.slot_base = dl.slot_base;
-  sc.seg_base = dl.seg_begin;
-  const int32_t base = plan.dseg_blk0[dl.seg_begin];
-  for (int i = 0; i < n; ++i) {
-    const int k = dl.seg_begin + i;
-    sc.seqhead[i] = plan.dseg_seqhead[k];
-    sc.blk0[i] = plan.dseg_blk0[k] - base;
-    sc.q0[i] = plan.dseg_q0[k];
-    sc.lo[i] = plan.dseg_lo[k];
-    sc.len[i] = plan.dseg_len[k];
-  }
-  sc.blk0[n] = plan.dseg_blk0[dl.seg_end] - base;
-  sc.n_blocks = sc.blk0[n];
-  if (dl.bpc == 0) {
-    // Segment of a block: last k with blk0[k] <= x (segments may be empty).
-    auto seg_at = [&](int32_t x) {
-      return static_cast<int32_t>(std::upper_bound(sc.blk0, sc.blk0 + n, x) - sc.blk0) - 1;
-    };
-    for (int i = 0; i < dl.n_ctas; ++i) {
-      const int32_t b0 = sc.cta0[i], b1 = sc.cta0[i + 1];
-      sc.cta_seg[i] = b0 < b1 ? (seg_at(b0) | (seg_at(b1 - 1) << 16)) : 0;
-    }
-  }
+  if (int e = fill_decode_sched(plan, dl, sc)) return e;
   decode_kernel<D, NSEG, FP8><<<dl.n_ctas, kWarps * 32, smem, stream>>>(tk, tv, p, sc);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return static_cast<int>(e);
@@ -662,29 +632,7 @@ int launch_one(const Plan& plan, const DecodeParams& p, const CUtensorMap& tk,
 
 template <int D>
 int launch_decode_t(const Plan& plan, const Args& a, cudaStream_t stream) {
-  DecodeParams p;
-  p.q = static_cast<const __nv_bfloat16*>(a.q);
-  p.k = static_cast<const __nv_bfloat16*>(a.k_pages);
-  p.v = static_cast<const __nv_bfloat16*>(a.v_pages);
-  p.page_table = a.page_table;
-  p.cu_q_lens = a.cu_q_lens;
-  p.kv_lens = a.kv_lens;
-  p.window = a.window;
-  p.out = static_cast<__nv_bfloat16*>(a.out);
-  p.ws = a.workspace;
-  p.part_o = reinterpret_cast<float*>(a.workspace + plan.off_partial_o);
-  p.part_lse = reinterpret_cast<float*>(a.workspace + plan.off_partial_lse);
-  p.hq = plan.hq;
-  p.hkv = plan.hkv;
-  p.group = plan.hq / plan.hkv;
-  int shift = 0;
-  while ((1 << shift) < plan.p) ++shift;
-  p.page_shift = shift;
-  p.mpps = plan.mpps;
-  p.num_pages = plan.num_pages;
-  p.scale_log2 = a.sm_scale * 1.4426950408889634f;
-  p.k_scale = a.k_scale;
-  p.v_scale = a.v_scale;
+  const DecodeParams p = make_decode_params(plan, a);
   CUtensorMap tk, tv;
   const uint64_t rows = static_cast<uint64_t>(plan.num_pages) * plan.p;
   const bool fp8 = plan.kv_fp8;
@@ -765,6 +713,7 @@ bool decode_supported(int32_t head_dim, int32_t group, int32_t page_size) {
 int decode_ctas_per_sm(int32_t) { return 1; }
 
 int launch_decode(const Plan& plan, const Args& a, void* stream) {
+  if (plan.decode_tc) return launch_decode_tc(plan, a, stream);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (plan.d) {
     case 64: return launch_decode_t<64>(plan, a, s);

@@ -6,7 +6,10 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "rpa_internal.h"
@@ -169,5 +172,73 @@ __device__ __forceinline__ void load_range_tables(const DecodeSched<NSEG>& sc,
 // Launch the log-sum-exp combine of launch dl's cut segments (decode.cu).
 int launch_decode_combine(const Plan& plan, const DecodeParams& p, const Plan::DecodeLaunch& dl,
                           int head_dim, void* stream);
+
+// Host: the decode kernels' parameters for a call's arguments.
+inline DecodeParams make_decode_params(const Plan& plan, const Args& a) {
+  DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.k = static_cast<const __nv_bfloat16*>(a.k_pages);
+  p.v = static_cast<const __nv_bfloat16*>(a.v_pages);
+  p.page_table = a.page_table;
+  p.cu_q_lens = a.cu_q_lens;
+  p.kv_lens = a.kv_lens;
+  p.window = a.window;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.ws = a.workspace;
+  p.part_o = reinterpret_cast<float*>(a.workspace + plan.off_partial_o);
+  p.part_lse = reinterpret_cast<float*>(a.workspace + plan.off_partial_lse);
+  p.hq = plan.hq;
+  p.hkv = plan.hkv;
+  p.group = plan.hq / plan.hkv;
+  int shift = 0;
+  while ((1 << shift) < plan.p) ++shift;
+  p.page_shift = shift;
+  p.mpps = plan.mpps;
+  p.num_pages = plan.num_pages;
+  p.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
+  return p;
+}
+
+// Host: launch dl's schedule from the plan's host copies (segments relative
+// to the launch, the per-CTA range table and each range's first and last
+// segment).  Returns a cudaError_t.
+template <int NSEG>
+int fill_decode_sched(const Plan& plan, const Plan::DecodeLaunch& dl, DecodeSched<NSEG>& sc) {
+  const int n = dl.seg_end - dl.seg_begin;
+  if (n > NSEG) return static_cast<int>(cudaErrorInvalidValue);
+  sc.n_seg = n;
+  sc.bpc = dl.bpc;
+  sc.n_ctas = dl.n_ctas;
+  if (dl.bpc == 0) {
+    if (dl.n_ctas > kMaxDecodeGrid) return static_cast<int>(cudaErrorInvalidValue);
+    for (int i = 0; i <= dl.n_ctas; ++i) sc.cta0[i] = plan.dcta_blk0[dl.cta_begin + i];
+  }
+  sc.slot_base = dl.slot_base;
+  sc.seg_base = dl.seg_begin;
+  const int32_t base = plan.dseg_blk0[dl.seg_begin];
+  for (int i = 0; i < n; ++i) {
+    const int k = dl.seg_begin + i;
+    sc.seqhead[i] = plan.dseg_seqhead[k];
+    sc.blk0[i] = plan.dseg_blk0[k] - base;
+    sc.q0[i] = plan.dseg_q0[k];
+    sc.lo[i] = plan.dseg_lo[k];
+    sc.len[i] = plan.dseg_len[k];
+  }
+  sc.blk0[n] = plan.dseg_blk0[dl.seg_end] - base;
+  sc.n_blocks = sc.blk0[n];
+  if (dl.bpc == 0) {
+    // Segment of a block: last k with blk0[k] <= x (segments may be empty).
+    auto seg_at = [&](int32_t x) {
+      return static_cast<int32_t>(std::upper_bound(sc.blk0, sc.blk0 + n, x) - sc.blk0) - 1;
+    };
+    for (int i = 0; i < dl.n_ctas; ++i) {
+      const int32_t b0 = sc.cta0[i], b1 = sc.cta0[i + 1];
+      sc.cta_seg[i] = b0 < b1 ? (seg_at(b0) | (seg_at(b1 - 1) << 16)) : 0;
+    }
+  }
+  return 0;
+}
 
 }  // namespace rpa

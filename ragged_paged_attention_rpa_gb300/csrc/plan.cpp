@@ -483,6 +483,9 @@ constexpr double kPrefillTileUs256 = 2.0;
 constexpr double kPrefillItemUs256 = 3.2;
 constexpr double kPrefillFixedUs = 20.0;
 
+// RPA_DECODE_KERNEL_AUTO takes the tensor-core decode kernel where it applies.
+constexpr bool kDecodeTcByDefault = false;
+
 double decode_cost_us(double bytes, int32_t sms) {
   return bytes / std::min(sms * kDecodeSmGBs, kDecodeHbmGBs) * 1e-3 + kDecodeFixedUs;
 }
@@ -525,6 +528,17 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
       return RPA_ERR_UNSUPPORTED;
   }
   plan.kv_fp8 = opts.kv_dtype == RPA_DTYPE_FP8_E4M3;
+  // Which split-KV decode kernel: the tensor-core one where it applies,
+  // unless the CUDA-core one is asked for.
+  if (opts.decode_kernel < RPA_DECODE_KERNEL_AUTO || opts.decode_kernel > RPA_DECODE_KERNEL_TC)
+    return RPA_ERR_INVALID_ARG;
+  const bool tcgen_decode =
+      tc_decode && decode_tc_supported(plan.d, group, plan.p, plan.kv_fp8);
+  if (opts.decode_kernel == RPA_DECODE_KERNEL_TC && ndec > 0 && !tcgen_decode)
+    return RPA_ERR_UNSUPPORTED;
+  plan.decode_tc = ndec > 0 && tcgen_decode &&
+                   (opts.decode_kernel == RPA_DECODE_KERNEL_TC ||
+                    (opts.decode_kernel == RPA_DECODE_KERNEL_AUTO && kDecodeTcByDefault));
   if (want == RPA_PATH_TC) {
     if ((ndec > 0 && !tc_decode) || (plan.num_prefill > 0 && !tc_prefill))
       return RPA_ERR_UNSUPPORTED;

@@ -94,6 +94,7 @@ struct Plan {
   int32_t path = RPA_PATH_SIMT;     // path actually used
   bool simt_decode = false;          // decode sequences handled by the SIMT kernel
   bool simt_prefill = false;         // prefill sequences handled by the SIMT kernel
+  bool decode_tc = false;            // split-KV decode on the tensor-core kernel
   int32_t num_sms = 152;
   // Mixed batches (decode and tensor-core prefill work in one call): the two
   // persistent grids run side by side on disjoint SMs, decode on
@@ -250,6 +251,10 @@ int noalloc_scratch(void** ptr);
 
 // Whether the split-KV decode supports this shape (decode.cu).
 bool decode_supported(int32_t head_dim, int32_t group, int32_t page_size);
+// Whether its tensor-core kernel does (decode_tc.cu), and that kernel's
+// launcher (launch_decode hands over to it when plan.decode_tc is set).
+bool decode_tc_supported(int32_t head_dim, int32_t group, int32_t page_size, bool kv_fp8);
+int launch_decode_tc(const Plan& plan, const Args& a, void* stream);
 
 // TMA tensor maps (tmap.cpp): a 3-D bf16 tensor [outer][mid][d] with a
 // 128-byte-swizzled box of (64, box_mid, box_outer) elements.

@@ -608,3 +608,34 @@ def test_mixed_batch_grids_split_the_sms_by_the_cost_model():
     # Decode-only and prefill-only batches have nothing to overlap.
     assert plan_of(workloads.decode_batch(meta_only=True)).info()["decode_sms"] == 0
     assert plan_of(workloads.WORKLOADS["swa_prefill"](meta_only=True)).info()["decode_sms"] == 0
+
+
+def test_decode_kernel_option():
+    """decode_kernel picks the split-KV decode kernel: 1 the CUDA-core one (any
+    tensor-core decode shape, fp8 pages too), 2 the tensor-core one (bf16
+    pages, head_dim 128 or 256, G <= 8, pages of >= 16 tokens) or
+    RPA_ERR_UNSUPPORTED; 0 the planner's choice.  The plan reports which."""
+    b = workloads.decode_batch(meta_only=True)
+    assert plan_of(b, decode_kernel=1).info()["decode_kernel"] == 1
+    assert plan_of(b, decode_kernel=2).info()["decode_kernel"] == 2
+    assert plan_of(b).info()["decode_kernel"] in (1, 2)
+    for bad in (-1, 3):
+        with pytest.raises(RpaError) as e:
+            plan_of(b, decode_kernel=bad)
+        assert e.value.status == binding.RPA_ERR_INVALID_ARG
+    with pytest.raises(RpaError) as e:
+        plan_of(b, decode_kernel=2, kv_dtype=binding.RPA_DTYPE_FP8_E4M3)
+    assert e.value.status == binding.RPA_ERR_UNSUPPORTED
+    fp8 = plan_of(b, decode_kernel=1, kv_dtype=binding.RPA_DTYPE_FP8_E4M3).info()
+    assert fp8["decode_kernel"] == 1
+    d64 = workloads.make_batch([1, 1], [40, 9], num_q_heads=8, num_kv_heads=1, head_dim=64,
+                               page_size=16, meta_only=True)
+    with pytest.raises(RpaError) as e:
+        plan_of(d64, decode_kernel=2)
+    assert e.value.status == binding.RPA_ERR_UNSUPPORTED
+    assert plan_of(d64).info()["decode_kernel"] == 1
+    # No decode sequence: no decode kernel, whatever was asked.
+    pre = workloads.WORKLOADS["swa_prefill"](meta_only=True)
+    assert plan_of(pre, decode_kernel=2).info()["decode_kernel"] == 0
+    # The CUDA-core (SIMT) path: no split-KV decode either.
+    assert plan_of(b, path=binding.RPA_PATH_SIMT).info()["decode_kernel"] == 0
