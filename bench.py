@@ -335,6 +335,9 @@ def parse():
     ap.add_argument("--decode-sms", type=int, default=0,
                     help="plan option for mixed batches: 0 choose, -1 run decode and prefill "
                          "one after the other, n > 0 decode on n SMs beside the prefill")
+    ap.add_argument("--prefill-dynamic", type=int, default=0,
+                    help="plan option: 0 prefill CTAs take items as they get free, -1 each "
+                         "CTA runs the planner's list")
     ap.add_argument("--decode-kernel", type=int, default=0,
                     help="plan option: 0 choose, 1 CUDA-core decode kernel, 2 tensor-core "
                          "decode kernel")
@@ -486,7 +489,8 @@ def bench_one(args, name, world, rank, local, dist, binding, torch, peaks, l2_by
     plan_kw = dict(q_block=args.q_block, kv_split=args.kv_split,
                    kv_dtype=binding.RPA_DTYPE_FP8_E4M3 if fp8 else 0,
                    prefill_split=args.prefill_split, decode_sms=args.decode_sms,
-                   decode_kernel=0 if fp8 else args.decode_kernel)
+                   decode_kernel=0 if fp8 else args.decode_kernel,
+                   prefill_dynamic=args.prefill_dynamic)
     plan = db.plan(**plan_kw)
     info = plan.info()
     ws = binding.alloc_workspace(plan)
@@ -619,8 +623,9 @@ def bench_one(args, name, world, rank, local, dist, binding, torch, peaks, l2_by
             dist.barrier()
         torch.cuda.synchronize()
         if R:
-            if graph is None:
-                torch.cuda._sleep(int(2e6))
+            # The device sleeps while the host enqueues the steps, so the
+            # timed region opens on queued work, not on host launch latency.
+            torch.cuda._sleep(int(2e6))
             e_start.record(stream)
             if graph is not None:
                 graph.replay()

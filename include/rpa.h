@@ -145,6 +145,11 @@ typedef struct rpa_plan_options {
                                prefill on the rest; -1: one after the other,
                                each on every SM                                 */
   int32_t decode_kernel;    /* RPA_DECODE_KERNEL_* for the split-KV decode      */
+  int32_t prefill_dynamic;  /* tensor-core prefill (single-SM kernel, whole
+                               items): 0 items taken longest first by whichever
+                               CTA gets free (a work counter in the workspace
+                               header), -1 each CTA runs the list the planner
+                               gave it (longest processing time first)         */
 } rpa_plan_options;
 
 /* What a plan chose; filled by rpa_plan_get_info. */
@@ -170,6 +175,7 @@ typedef struct rpa_plan_info {
   int32_t prefill_sms;         /* ... and of the prefill grid                 */
   int32_t decode_kernel;       /* RPA_DECODE_KERNEL_MMA or _TC for the
                                   split-KV decode (0: no such decode)         */
+  int32_t prefill_dynamic;     /* 1: prefill CTAs take items as they get free */
 } rpa_plan_info;
 
 typedef struct rpa_plan rpa_plan_t;

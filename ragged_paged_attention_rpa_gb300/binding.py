@@ -76,7 +76,8 @@ class _Options(ctypes.Structure):
                 ("q_block", ctypes.c_int32), ("kv_split", ctypes.c_int32),
                 ("num_sms", ctypes.c_int32), ("prefill_pairs", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("prefill_split", ctypes.c_int32),
-                ("decode_sms", ctypes.c_int32), ("decode_kernel", ctypes.c_int32)]
+                ("decode_sms", ctypes.c_int32), ("decode_kernel", ctypes.c_int32),
+                ("prefill_dynamic", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -88,7 +89,7 @@ class PlanInfo(ctypes.Structure):
                 ("kv_dtype", ctypes.c_int32), ("prefill_split_items", ctypes.c_int32),
                 ("prefill_split_parts", ctypes.c_int32), ("prefill_max_tiles", ctypes.c_int32),
                 ("decode_sms", ctypes.c_int32), ("prefill_sms", ctypes.c_int32),
-                ("decode_kernel", ctypes.c_int32)]
+                ("decode_kernel", ctypes.c_int32), ("prefill_dynamic", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: int(getattr(self, name)) for name, _ in self._fields_}
@@ -206,7 +207,8 @@ def rpa_plan(cu_q_lens_host, kv_lens_host, window_host, num_q_heads: int,
              num_pages: int, dtype: int = RPA_DTYPE_BF16, path: int = RPA_PATH_AUTO,
              q_block: int = 0, kv_split: int = 0, num_sms: int = 0,
              prefill_pairs: int = 0, kv_dtype: int = 0, prefill_split: int = 0,
-             decode_sms: int = 0, decode_kernel: int = 0) -> Plan:
+             decode_sms: int = 0, decode_kernel: int = 0,
+             prefill_dynamic: int = 0) -> Plan:
     """rpa_plan from host (numpy) metadata; returns a Plan."""
     cu = _np_i32(cu_q_lens_host)
     kv = _np_i32(kv_lens_host)
@@ -217,7 +219,7 @@ def rpa_plan(cu_q_lens_host, kv_lens_host, window_host, num_q_heads: int,
     if win is not None and win.shape[0] != num_seqs:
         raise ValueError("window must have num_seqs entries")
     opts = _Options(ctypes.sizeof(_Options), path, q_block, kv_split, num_sms, prefill_pairs,
-                    kv_dtype, prefill_split, decode_sms, decode_kernel)
+                    kv_dtype, prefill_split, decode_sms, decode_kernel, prefill_dynamic)
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     st = lib().rpa_plan(ctypes.byref(handle), _np_ptr(cu), _np_ptr(kv), _np_ptr(win),

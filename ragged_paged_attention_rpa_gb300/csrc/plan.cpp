@@ -261,7 +261,7 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
 // block, KV head), or with SM pairs (sequence, pair of adjacent query blocks,
 // KV head), costed by the keys the item streams.
 void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t* win,
-                  int32_t forced_q_block, int32_t forced_split) {
+                  int32_t forced_q_block, int32_t forced_split, bool dynamic) {
   const int32_t group = plan.hq / plan.hkv;
   const int32_t max_qb = prefill_tokens_per_block(plan.d, group);
   // Query tokens per CTA: a requested block larger than one 128-row tile
@@ -308,6 +308,7 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
   plan.items.clear();
   plan.psplit.clear();
   plan.pcta0.clear();
+  plan.prefill_dynamic = false;
   plan.n_split_items = 0;
   plan.prefill_max_tiles = 0;
   const int64_t slots = static_cast<int64_t>(plan.prefill_sms > 0 ? plan.prefill_sms : plan.num_sms) *
@@ -417,12 +418,24 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
       }
       heap[j] = v;
     }
-    // CTA-major placement, each CTA's items in assignment (longest-first) order.
-    for (size_t c = 0; c < static_cast<size_t>(grid); ++c) plan.pcta0[c + 1] += plan.pcta0[c];
-    plan.items.resize(all.size());
-    std::vector<int32_t> fill(plan.pcta0.begin(), plan.pcta0.end() - 1);
-    for (size_t i = 0; i < all.size(); ++i) plan.items[static_cast<size_t>(fill[owner[i]]++)] = all[i].item;
     plan.prefill_ctas = static_cast<int32_t>(grid);
+    if (dynamic) {
+      // The same order, each item taken by whichever CTA gets free first:
+      // on SMs of equal speed that is this assignment; where some SMs
+      // stream faster than others (their share of HBM and L2 differs by
+      // ~10% on GB300), the faster ones take more items instead of the
+      // slowest setting the makespan.
+      for (const Cost& c : all) plan.items.push_back(c.item);
+      plan.pcta0.clear();
+      plan.prefill_dynamic = true;
+    } else {
+      // CTA-major placement, each CTA's items in assignment (longest-first) order.
+      for (size_t c = 0; c < static_cast<size_t>(grid); ++c) plan.pcta0[c + 1] += plan.pcta0[c];
+      plan.items.resize(all.size());
+      std::vector<int32_t> fill(plan.pcta0.begin(), plan.pcta0.end() - 1);
+      for (size_t i = 0; i < all.size(); ++i)
+        plan.items[static_cast<size_t>(fill[owner[i]]++)] = all[i].item;
+    }
     uint64_t busiest = 0;
     for (const uint64_t v : heap) busiest = std::max(busiest, v >> 16);
     plan.prefill_max_tiles = static_cast<int32_t>(busiest);
@@ -636,7 +649,8 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
 
   if (tc_decode && ndec > 0) plan_decode(plan, cu, kv, win, opts.kv_split);
   if (tc_prefill && plan.num_prefill > 0)
-    plan_prefill(plan, cu, kv, win, opts.q_block, opts.prefill_split);
+    plan_prefill(plan, cu, kv, win, opts.q_block, opts.prefill_split,
+                 opts.prefill_dynamic == 0);
 
   // Workspace: header, then the decode partials (two slots per decode CTA,
   // G x D fp32 each, plus G log2-sum-exps).

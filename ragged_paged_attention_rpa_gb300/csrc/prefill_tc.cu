@@ -90,6 +90,10 @@ constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
 struct ItemList {
   int32_t n;
   int32_t n_ctas;
+  // 1: items in longest-first order, taken as CTAs get free: CTA c starts on
+  // item c, then takes item gridDim.x + (a work counter in the workspace
+  // header, incremented atomically); the last CTA to finish resets it.
+  int32_t dyn;
   int32_t cta0[kMaxPrefillGrid + 1];
   PrefillItem items[kMaxItemsPerLaunch];
 };
@@ -157,6 +161,24 @@ struct Layout {
   static constexpr int kCols = 512;                      // D + 256 <= 512
 };
 
+struct Geom {
+  int32_t seq, g, t0, ntok, pos_first, key_first, ntiles, W;
+  int32_t lo;   // first key visible to any query of the item
+  bool ok;
+};
+
+// An item as the K producer hands it to the other warps: its geometry, its
+// split code and whether the stream of items has ended.
+struct ItemSlot {
+  Geom gm;
+  int32_t split;
+  int32_t end;
+};
+constexpr int kItemRing = 3;
+// Warps that take each item from the ring: V producer, MMA issuer, eight
+// softmax warps, four epilogue warps.
+constexpr int kItemReaders = 14;
+
 struct Barriers {
   uint64_t q_full, q_empty;
   uint64_t k_full[kKS], k_empty[kKS], v_full[kVS], v_empty[kVS];
@@ -165,17 +187,14 @@ struct Barriers {
   uint64_t l_full, l_empty;  // an item's row sums handed over / taken
   uint64_t fin;          // all MMAs of this CTA complete (teardown)
   uint64_t xbar[4];      // softmax pair exchange, one per TMEM lane quarter
+  uint64_t item_full[kItemRing], item_empty[kItemRing];
+  ItemSlot item[kItemRing];
   uint32_t tmem_base;
   int abort;
 };
 
 static_assert(sizeof(Barriers) <= 512, "barrier block");
 
-struct Geom {
-  int32_t seq, g, t0, ntok, pos_first, key_first, ntiles, W;
-  int32_t lo;   // first key visible to any query of the item
-  bool ok;
-};
 
 __device__ __forceinline__ Geom item_geom(const PrefillParams& p, const PrefillItem& it) {
   Geom r;
@@ -253,6 +272,33 @@ __device__ __forceinline__ int32_t box_row(const PrefillParams& p, const Geom& g
   return page * p.page_size + (key & (p.page_size - 1));
 }
 
+// The workspace header's work counter of a dynamic item list: [0] items
+// taken beyond the first wave, [1] CTAs finished.  The last CTA to finish
+// sets both back to zero for the next launch (every CTA's last take comes
+// before its own finish).
+__device__ __forceinline__ void leave_item_counter(unsigned char* ws) {
+  int32_t* ctr = reinterpret_cast<int32_t*>(ws + kPrefillCounterOff);
+  __threadfence();
+  if (atomicAdd(&ctr[1], 1) == static_cast<int32_t>(gridDim.x) - 1) {
+    atomicExch(&ctr[0], 0);
+    atomicExch(&ctr[1], 0);
+  }
+}
+
+// A warp takes item number R from the ring (every lane waits and reads;
+// lane 0 releases the slot).  False when the wait gave up.
+__device__ __forceinline__ bool take_item(Barriers& B, uint32_t& R, ItemSlot& e,
+                                          volatile int* abort, int lane) {
+  const int sl = R % kItemRing;
+  const bool ok = mbar_wait(&B.item_full[sl], (R / kItemRing) & 1, abort, kWaitNs);
+  if (!__all_sync(0xffffffffu, ok)) return false;
+  e = B.item[sl];
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&B.item_empty[sl]);
+  ++R;
+  return true;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -263,7 +309,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // the shared memory with no slack, so a misaligned base ends the launch.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_addr(smem_raw) & 1023u) {
-    if (threadIdx.x == 0) report_error(p.ws, RPA_DEVERR_LAUNCH, blockIdx.x);
+    if (threadIdx.x == 0) {
+      report_error(p.ws, RPA_DEVERR_LAUNCH, blockIdx.x);
+      if (items.dyn) leave_item_counter(p.ws);
+    }
     return;
   }
   // A combine of split items may be scheduled now; it waits for this grid.
@@ -297,6 +346,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mbar_init(&B.l_full, 128);
     mbar_init(&B.l_empty, 128);
     for (int i = 0; i < 4; ++i) mbar_init(&B.xbar[i], 64);
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(&B.item_full[i], 1);
+      mbar_init(&B.item_empty[i], kItemReaders);
+    }
     mbar_init(&B.fin, 1);
     B.abort = 0;
     fence_barrier_init();
@@ -329,16 +382,61 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
     const int rows = is_k ? p.box_rows_k : p.box_rows_v;
     const int nbox = (is_k ? kBN : Lay::kVKeys) / rows;    // boxes per stage (<= 8)
-    uint32_t C = 0, I = 0, issued_q = 0;
+    uint32_t C = 0, I = 0, issued_q = 0, R = 0;
     const uint32_t q_box_bytes = static_cast<uint32_t>(G * p.qb_tokens) * 128u;
     bool alive = true;
-    for (int it = mine.begin; it < mine.end && alive; it += mine.step) {
-      const Geom gm = item_geom(p, items.items[it]);
-      if (!gm.ok) {
-        if (lane == 0 && is_k && items.items[it].seq >= 0)
-          report_error(p.ws, RPA_DEVERR_LENGTHS, gm.seq);
-        continue;
+    int32_t* ctr = reinterpret_cast<int32_t*>(p.ws + kPrefillCounterOff);
+    // K producer: the item after `it` (lane 0).
+    auto next_item = [&](int32_t it) -> int32_t {
+      if (!items.dyn) return it + mine.step;
+      return static_cast<int32_t>(gridDim.x) + atomicAdd(&ctr[0], 1);
+    };
+    int32_t it = items.dyn ? static_cast<int32_t>(blockIdx.x) : mine.begin;
+    const int32_t it_end = items.dyn ? items.n : mine.end;
+    for (;;) {
+      Geom gm;
+      bool end = false;
+      if (is_k) {
+        // Lane 0 takes the next item with work in it and hands it to the
+        // other warps through the ring.
+        if (lane == 0) {
+          int32_t split = 0;
+          for (;;) {
+            if (it >= it_end) {
+              end = true;
+              break;
+            }
+            gm = item_geom(p, items.items[it]);
+            split = items.items[it].split;
+            if (gm.ok) break;
+            if (items.items[it].seq >= 0) report_error(p.ws, RPA_DEVERR_LENGTHS, gm.seq);
+            it = next_item(it);
+          }
+          const int sl = R % kItemRing;
+          alive = mbar_wait(&B.item_empty[sl], ((R / kItemRing) & 1) ^ 1, abort, kWaitNs);
+          if (alive) {
+            B.item[sl].gm = gm;
+            B.item[sl].split = split;
+            B.item[sl].end = end ? 1 : 0;
+            mbar_arrive(&B.item_full[sl]);
+            if (!end) it = next_item(it);
+          }
+        }
+        ++R;
+        alive = __shfl_sync(0xffffffffu, alive, 0);
+        if (!alive) break;
+        __syncwarp();
+        // Every lane reads the item back (the copies below need it).
+        const ItemSlot e = B.item[(R - 1) % kItemRing];
+        gm = e.gm;
+        end = e.end != 0;
+      } else {
+        ItemSlot e;
+        if (!(alive = take_item(B, R, e, abort, lane))) break;
+        gm = e.gm;
+        end = e.end != 0;
       }
+      if (end) break;
       const uint32_t Icur = I++;
       if (is_k && lane == 0) {
         alive = mbar_wait(&B.q_empty, (Icur & 1) ^ 1, abort, kWaitNs);
@@ -379,6 +477,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           }
         }
       }
+      if (!alive) break;
     }
     if (!alive && lane == 0) {
       // Let every copy this warp started land before its shared memory goes.
@@ -480,9 +579,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mma_commit(&B.s_full[Ts & 1]);
       return true;
     };
-    for (int it = mine.begin; it < mine.end && alive; it += mine.step) {
-      const Geom gm = item_geom(p, items.items[it]);
-      if (!gm.ok) continue;
+    uint32_t R = 0;
+    for (;;) {
+      ItemSlot e;
+      if (!(alive = take_item(B, R, e, abort, lane))) break;
+      if (e.end) break;
+      const Geom gm = e.gm;
       alive = wait(&B.q_full, I & 1);
       if (!alive) break;
       // Order: S(0), then for each j: S(j + 1), PV(j).  S(j + 1) overwrites
@@ -502,6 +604,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       T += n;
       ++I;
       if (n > 0) ++IO;
+      if (!alive) break;
     }
     // Every MMA issued must finish before TMEM is released.
     mma_commit(&B.fin);
@@ -541,15 +644,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (!ok) alive = false;
       return o;
     };
-    // The next item's geometry is read while this one runs (its loads
-    // would otherwise sit between this item's epilogue and the next tile).
-    Geom gm_next;
-    gm_next.ok = false;
-    if (mine.begin < mine.end) gm_next = item_geom(p, items.items[mine.begin]);
-    for (int it = mine.begin; it < mine.end && alive; it += mine.step) {
-      const Geom gm = gm_next;
-      if (it + mine.step < mine.end) gm_next = item_geom(p, items.items[it + mine.step]);
-      if (!gm.ok) continue;
+    uint32_t R = 0;
+    while (alive) {
+      ItemSlot e;
+      if (!take_item(B, R, e, abort, lane)) {
+        alive = false;
+        break;
+      }
+      if (e.end) break;
+      const Geom gm = e.gm;
       const bool valid = tok < gm.ntok && r < G * p.qb_tokens;
       const int32_t pos = gm.pos_first + tok;
       const int32_t lo = first_visible(pos, gm.W);
@@ -653,8 +756,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (!alive) break;
       if (gm.ntiles == 0) {
         // An empty part still tells the combine that it holds nothing.
-        if (items.items[it].split != 0 && h == 0 && valid)
-          p.ppart_lse[static_cast<int64_t>(split_slot(items.items[it].split)) * kBM + r] = -INFINITY;
+        if (e.split != 0 && h == 0 && valid)
+          p.ppart_lse[static_cast<int64_t>(split_slot(e.split)) * kBM + r] = -INFINITY;
         continue;
       }
       // The row sum over both halves; then the first half hands it to the
@@ -663,8 +766,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       l += swap(l);
       if (!alive) break;
       if (h == 0) {
-        if (items.items[it].split != 0 && valid)
-          p.ppart_lse[static_cast<int64_t>(split_slot(items.items[it].split)) * kBM + r] =
+        if (e.split != 0 && valid)
+          p.ppart_lse[static_cast<int64_t>(split_slot(e.split)) * kBM + r] =
               (l > 0.f) ? m_ref + __log2f(l) : -INFINITY;
         if (!mbar_wait(&B.l_empty, (L & 1) ^ 1, abort, kWaitNs)) {
           alive = false;
@@ -691,9 +794,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const float* l_s = reinterpret_cast<const float*>(smem + Lay::kLOff);
     uint32_t T = 0, L = 0;                              // tiles, items taken over
     bool alive = true;
-    for (int it = mine.begin; it < mine.end && alive; it += mine.step) {
-      const Geom gm = item_geom(p, items.items[it]);
-      if (!gm.ok || gm.ntiles == 0) continue;
+    uint32_t R = 0;
+    while (alive) {
+      ItemSlot e;
+      if (!take_item(B, R, e, abort, lane)) {
+        alive = false;
+        break;
+      }
+      if (e.end) break;
+      const Geom gm = e.gm;
+      if (gm.ntiles == 0) continue;
       T += gm.ntiles;
       const uint32_t Tl = T - 1;
       const bool valid = tok < gm.ntok && r < G * p.qb_tokens;
@@ -710,10 +820,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       tc_fence_after();
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      if (items.items[it].split != 0) {
+      if (e.split != 0) {
         // A part of a split item: fp32 O / l (a row with no visible key
         // here: zeros; its log2-sum-exp, -inf, came from the softmax warps).
-        float* prow = p.ppart_o + (static_cast<int64_t>(split_slot(items.items[it].split)) * kBM + r) * D;
+        float* prow = p.ppart_o + (static_cast<int64_t>(split_slot(e.split)) * kBM + r) * D;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
@@ -768,6 +878,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc_fence_after();
     tmem_dealloc(tmem, Lay::kCols);
   }
+  if (threadIdx.x == 0 && items.dyn) leave_item_counter(p.ws);
 }
 
 struct SplitList {
@@ -906,6 +1017,9 @@ int launch_prefill_t(const Plan& plan, const Args& a, cudaStream_t stream) {
     for (int i = 0; i < cnt; ++i) list.items[i] = plan.items[off + i];
     int grid = std::min(cnt, plan.prefill_ctas);
     list.n_ctas = 0;
+    list.dyn = plan.prefill_dynamic ? 1 : 0;
+    if (plan.prefill_dynamic && (off != 0 || cnt != static_cast<int>(n)))
+      return static_cast<int>(cudaErrorInvalidValue);
     if (!plan.pcta0.empty()) {
       // Per-CTA lists (the plan keeps them to one launch).
       if (off != 0 || plan.pcta0.back() != cnt ||

@@ -22,6 +22,9 @@ namespace rpa {
 // Workspace layout: a 256-byte header (error word first), then the decode
 // split partials.  Offsets are multiples of 256 bytes.
 constexpr size_t kHeaderBytes = 256;
+// Offset in the header of the dynamic prefill item counter (two int32: items
+// taken, CTAs finished), zero between launches.
+constexpr size_t kPrefillCounterOff = 64;
 
 // One prefill work item: query block `qb` (of plan.q_block tokens) of
 // sequence `seq`, for KV head `head`.  Ordered longest first in the plan.
@@ -140,6 +143,9 @@ struct Plan {
   int32_t num_prefill = 0;
   int32_t q_block = 0;
   bool prefill_pairs = false;      // items are pairs of query blocks (SM-pair kernel)
+  // Items in longest-first order, each taken by the next CTA to get free
+  // (else CTA c runs its own list, pcta0).
+  bool prefill_dynamic = false;
   std::vector<PrefillItem> items;  // longest first, or per-CTA lists (pcta0)
   // Per-CTA item lists: CTA c runs items [pcta0[c], pcta0[c + 1]) in order;
   // empty: CTA c runs items c, c + grid, ... (a list too long for one launch).

@@ -639,3 +639,30 @@ def test_decode_kernel_option():
     assert plan_of(pre, decode_kernel=2).info()["decode_kernel"] == 0
     # The CUDA-core (SIMT) path: no split-KV decode either.
     assert plan_of(b, path=binding.RPA_PATH_SIMT).info()["decode_kernel"] == 0
+
+
+@pytest.mark.parametrize("name", ["causal_prefill", "swa_prefill", "mixed"])
+def test_prefill_items_taken_dynamically_by_default(name):
+    """Single-SM prefill items are taken longest first by whichever CTA gets
+    free (prefill_dynamic = 0, the default); -1 keeps the planner's per-CTA
+    lists.  Both plans hold the same items, grid and LPT makespan estimate."""
+    b = workloads.WORKLOADS[name](meta_only=True)
+    dyn = plan_of(b).info()
+    fixed = plan_of(b, prefill_dynamic=-1).info()
+    assert dyn["prefill_dynamic"] == 1 and fixed["prefill_dynamic"] == 0
+    for k in ("num_prefill_items", "prefill_ctas", "prefill_max_tiles", "q_block"):
+        assert dyn[k] == fixed[k], k
+    for bad in (-2, 1):
+        with pytest.raises(RpaError) as e:
+            plan_of(b, prefill_dynamic=bad)
+        assert e.value.status == binding.RPA_ERR_INVALID_ARG
+    # Split items and SM pairs keep fixed lists (a split that does not fit
+    # one launch falls back to whole items).
+    sp = plan_of(b, prefill_split=3).info()
+    assert sp["prefill_dynamic"] == (0 if sp["prefill_split_items"] > 0 else 1)
+    small = workloads.make_batch([700, 300], [700, 900], num_q_heads=4, num_kv_heads=2,
+                                 head_dim=256, page_size=128, windows=[0, 128], meta_only=True)
+    sp = plan_of(small, prefill_split=3).info()
+    assert sp["prefill_split_items"] > 0 and sp["prefill_dynamic"] == 0
+    if name != "mixed":
+        assert plan_of(b, prefill_pairs=2).info()["prefill_dynamic"] == 0

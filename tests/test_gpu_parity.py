@@ -436,3 +436,34 @@ def test_prefill_q_block_on_sm_pairs(q_block):
     info = plan.info()
     assert err == 0 and info["q_block"] == q_block and info["prefill_pairs"] == 1
     assert_bf16_close(got, oracle_rows(b), "q_block %d on pairs" % q_block)
+
+
+# ---------------------------------------------------------------- dynamic item order
+
+
+@pytest.mark.parametrize("case", [0, 2, 5, 7])
+def test_prefill_dynamic_items_match_fixed_lists_bitwise(case):
+    """Items taken dynamically (work counter in the workspace header) give
+    the same bits as the planner's fixed per-CTA lists: each item's
+    arithmetic does not depend on which CTA runs it.  Two calls in a row on
+    one workspace check that the counter is left at zero."""
+    ql, kv, hq, hkv, d, p, win = PREFILL[case]
+    b = poisoned(workloads.make_batch(ql, kv, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                                      page_size=p, windows=win, seed=1700 + case))
+    db = binding.Batch(b)
+    plan = db.plan()
+    assert plan.info()["prefill_dynamic"] == 1
+    ws = binding.alloc_workspace(plan)
+    outs = []
+    for _ in range(2):
+        db.out.fill_(float("nan"))
+        outs.append(db.forward(plan, ws).clone())
+    assert binding.rpa_get_device_error(ws) == 0
+    counters = ws[64:72].view(torch.int32).cpu().tolist()
+    assert counters == [0, 0]
+    fixed, err, fplan = run_gpu(b, prefill_dynamic=-1)
+    assert err == 0 and fplan.info()["prefill_dynamic"] == 0
+    got = outs[0].float().cpu().numpy().reshape(-1, b.head_dim).astype(np.float64)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert np.array_equal(got, fixed)
+    assert_bf16_close(got, oracle_rows(b), "dynamic prefill case %d" % case)
