@@ -448,16 +448,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
       }
       alive = __shfl_sync(0xffffffffu, alive, 0);
-      for (int j = 0; j < gm.ntiles && alive; ++j) {
+      // Source rows of a tile's boxes (lane < nbox: one box per stage), each
+      // a page-table load.  They are read a tile ahead, all at once: read
+      // one by one just before their stage, their latency (~600 cycles
+      // each) paced the ring at more than the tile's MMA time.
+      auto tile_rows = [&](int j, int32_t (&rw)[Lay::kChunks]) {
         const int32_t key0 = gm.key_first + j * kBN;
-        // K: the same 128 keys for every chunk of the tile.
-        const int32_t krow = (is_k && lane < nbox) ? box_row(p, gm, key0 + lane * rows, rows) : 0;
+        if (is_k) {
+          // K: the same 128 keys for every chunk of the tile.
+          const int32_t kr = lane < nbox ? box_row(p, gm, key0 + lane * rows, rows) : 0;
+#pragma unroll
+          for (int sgi = 0; sgi < Lay::kChunks; ++sgi) rw[sgi] = kr;
+        } else {
+#pragma unroll
+          for (int sgi = 0; sgi < Lay::kChunks; ++sgi)
+            rw[sgi] = lane < nbox ? box_row(p, gm, key0 + sgi * Lay::kVKeys + lane * rows, rows) : 0;
+        }
+      };
+      int32_t rcur[Lay::kChunks], rnext[Lay::kChunks];
+      if (gm.ntiles > 0) tile_rows(0, rcur);
+      for (int j = 0; j < gm.ntiles && alive; ++j) {
+        if (j + 1 < gm.ntiles) tile_rows(j + 1, rnext);
+#pragma unroll
         for (int sgi = 0; sgi < Lay::kChunks; ++sgi, ++C) {
           const int st = C % depth;
           const uint32_t ph = (C / depth) & 1;
-          const int32_t row = is_k ? krow
-                              : (lane < nbox ? box_row(p, gm, key0 + sgi * Lay::kVKeys + lane * rows, rows)
-                                             : 0);
+          const int32_t row = rcur[sgi];
           if (lane == 0) alive = mbar_wait(&empty[st], ph ^ 1, abort, kWaitNs);
           alive = __shfl_sync(0xffffffffu, alive, 0);
           if (!alive) break;
@@ -476,6 +492,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
           }
         }
+#pragma unroll
+        for (int sgi = 0; sgi < Lay::kChunks; ++sgi) rcur[sgi] = rnext[sgi];
       }
       if (!alive) break;
     }
