@@ -469,7 +469,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (gm.ntiles > 0) tile_rows(0, rcur);
       for (int j = 0; j < gm.ntiles && alive; ++j) {
         if (j + 1 < gm.ntiles) tile_rows(j + 1, rnext);
-#pragma unroll
+        // Rolled: unrolled, this loop's copies of the three TMA paths made
+        // the kernel's code large enough to cost ~4% of its time.
+#pragma unroll 1
         for (int sgi = 0; sgi < Lay::kChunks; ++sgi, ++C) {
           const int st = C % depth;
           const uint32_t ph = (C / depth) & 1;
@@ -516,7 +518,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     constexpr uint32_t kIdS = idesc_bf16(kBN, 0);
     constexpr uint32_t kIdPV = idesc_bf16(D, 1);
     const uint32_t q_base = smem_addr(q_s), k_base = smem_addr(k_s), v_base = smem_addr(v_s);
-    uint32_t T = 0, I = 0, IO = 0, CK = 0, CV = 0;   // tiles, items (with PV), K / V stages
+    uint32_t T = 0, I = 0, IO = 0;    // tiles, items (with PV)
+    // Ring slot and phase of the next K / V stage.
+    int ks = 0, vs = 0;
+    uint32_t kph = 0, vph = 0;
+    // Shared-memory descriptors differ between operands of one kind only in
+    // the start-address field (bits 0-13: the byte address / 16), and every
+    // operand lies below 256 KB, so the operand at byte offset `off` from a
+    // base has the base's descriptor + off / 16.  Built once here: rebuilt
+    // for every MMA, their 64-bit arithmetic made this warp's issue, not the
+    // tensor core, set the pace of a tile.  (The chunk and stage loops stay
+    // rolled: unrolled, the larger code ran the kernel ~20% slower.)
+    const uint64_t q_d0 = smem_desc(q_base, 16, 1024);
+    const uint64_t k_d0 = smem_desc(k_base, 16, 1024);
+    const uint64_t v_d0 = smem_desc(v_base, Lay::kVKeys * 128, 1024);
     bool alive = true;
     // A wait the whole warp agrees on.
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -558,20 +573,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const int sb = Tp & 1;
       if (!wait(&B.p_full[sb], (Tp >> 1) & 1)) return false;
       if (jp == 0 && !wait(&B.o_free, (IO & 1) ^ 1)) return false;
-      for (int sgi = 0; sgi < Lay::kChunks; ++sgi, ++CV) {
-        const int vs = CV % kVS;
-        if (!wait(&B.v_full[vs], (CV / kVS) & 1)) return false;
+      const uint32_t p_col = tmem + Lay::kSCol + sb * kBN;
+#pragma unroll 1
+      for (int sgi = 0; sgi < Lay::kChunks; ++sgi) {
+        if (!wait(&B.v_full[vs], vph)) return false;
         clear_v_edges(gm, gm.key_first + jp * kBN + sgi * Lay::kVKeys, vs);
         tc_fence_after();
-        const uint32_t vb = v_base + vs * kStage;
+        const uint64_t vd = v_d0 + static_cast<uint64_t>(vs * (kStage >> 4));
 #pragma unroll
         for (int kk = 0; kk < Lay::kVKeys / 16; ++kk) {
           const int kg = sgi * (Lay::kVKeys / 16) + kk;     // 16-key group of the tile
-          const uint64_t bdesc = smem_desc(vb + kk * 2048, Lay::kVKeys * 128, 1024);
-          mma_ts(tmem + Lay::kOCol, tmem + Lay::kSCol + sb * kBN + kg * 8, bdesc, kIdPV,
+          mma_ts(tmem + Lay::kOCol, p_col + kg * 8, vd + ((kk * 2048) >> 4), kIdPV,
                  (jp > 0 || kg > 0) ? 1u : 0u);
         }
         mma_commit(&B.v_empty[vs]);
+        if (++vs == kVS) {
+          vs = 0;
+          vph ^= 1;
+        }
       }
       mma_commit(&B.o_done[sb]);
       return true;
@@ -581,18 +600,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // elements = 32 B inside a chunk; Q's chunks are 16 KB apart.
     auto issue_s = [&](uint32_t Ts) -> bool {
       const uint32_t sc = tmem + Lay::kSCol + (Ts & 1) * kBN;
-      for (int c = 0; c < Lay::kChunks; ++c, ++CK) {
-        const int ks = CK % kKS;
-        if (!wait(&B.k_full[ks], (CK / kKS) & 1)) return false;
+#pragma unroll 1
+      for (int c = 0; c < Lay::kChunks; ++c) {
+        if (!wait(&B.k_full[ks], kph)) return false;
         tc_fence_after();
-        const uint32_t kb = k_base + ks * kStage;
+        const uint64_t kd = k_d0 + static_cast<uint64_t>(ks * (kStage >> 4));
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const uint64_t adesc = smem_desc(q_base + c * (kBM * 128) + w * 32, 16, 1024);
-          const uint64_t bdesc = smem_desc(kb + w * 32, 16, 1024);
-          mma_ss(sc, adesc, bdesc, kIdS, (c > 0 || w > 0) ? 1u : 0u);
-        }
+        for (int w = 0; w < 4; ++w)
+          mma_ss(sc, q_d0 + ((c * (kBM * 128) + w * 32) >> 4), kd + ((w * 32) >> 4), kIdS,
+                 (c > 0 || w > 0) ? 1u : 0u);
         mma_commit(&B.k_empty[ks]);
+        if (++ks == kKS) {
+          ks = 0;
+          kph ^= 1;
+        }
       }
       mma_commit(&B.s_full[Ts & 1]);
       return true;
