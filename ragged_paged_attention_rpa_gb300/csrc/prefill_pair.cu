@@ -322,7 +322,15 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
       constexpr uint32_t kIdPV = idesc_bf16_m(2 * kBM, D, 1);
       const uint32_t q_base = smem_addr(q_s);
       const uint32_t k_base = smem_addr(smem + Lay::kKOff), v_base = smem_addr(smem + Lay::kVOff);
-      uint32_t T = 0, I = 0, CK = 0, CV = 0;
+      uint32_t T = 0, I = 0;
+      // Ring slot and phase of the next K / V stage.
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0;
+      // Descriptors as base + byte offset / 16 (the start-address field;
+      // every operand lies below 256 KB), built once rather than per MMA.
+      const uint64_t q_d0 = smem_desc(q_base, 16, 1024);
+      const uint64_t k_d0 = smem_desc(k_base, 16, 1024);
+      const uint64_t v_d0 = smem_desc(v_base, Lay::kVKeys * 128, 1024);
       bool alive = true;
       auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
         const bool ok = mbar_wait_cluster(bar, parity, abort, kWaitNs);
@@ -361,20 +369,24 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int sb = Tp & 1;
         if (!wait(&B.p_full[sb], (Tp >> 1) & 1)) return false;
         if (jp == 0 && !wait(&B.o_free, (I & 1) ^ 1)) return false;
-        for (int sgi = 0; sgi < kBN / Lay::kVKeys; ++sgi, ++CV) {
-          const int vs = CV % kVS;
-          if (!wait(&B.v_full[vs], (CV / kVS) & 1)) return false;
+        const uint32_t p_col = tmem + Lay::kSCol + sb * kBN;
+#pragma unroll 1
+        for (int sgi = 0; sgi < kBN / Lay::kVKeys; ++sgi) {
+          if (!wait(&B.v_full[vs], vph)) return false;
           clear_v_edges(gm, gm.key_first + jp * kBN + sgi * Lay::kVKeys, vs);
           tc_fence_after();
-          const uint32_t vb = v_base + vs * kStage;
+          const uint64_t vd = v_d0 + static_cast<uint64_t>(vs * (kStage >> 4));
 #pragma unroll
           for (int kk = 0; kk < Lay::kVKeys / 16; ++kk) {
             const int kg = sgi * (Lay::kVKeys / 16) + kk;
-            const uint64_t bdesc = smem_desc(vb + kk * 2048, Lay::kVKeys * 128, 1024);
-            mma_ts_pair(tmem + Lay::kOCol, tmem + Lay::kSCol + sb * kBN + kg * 8, bdesc, kIdPV,
+            mma_ts_pair(tmem + Lay::kOCol, p_col + kg * 8, vd + ((kk * 2048) >> 4), kIdPV,
                         (jp > 0 || kg > 0) ? 1u : 0u);
           }
           mma_commit_pair(&B.v_empty[vs]);
+          if (++vs == kVS) {
+            vs = 0;
+            vph ^= 1;
+          }
         }
         mma_commit_pair(&B.o_done[sb]);
         return true;
@@ -383,18 +395,20 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
       // (K-major, chunks 16 KB apart), B = its 64 keys of the tile.
       auto issue_s = [&](uint32_t Ts) -> bool {
         const uint32_t sc = tmem + Lay::kSCol + (Ts & 1) * kBN;
-        for (int c = 0; c < Lay::kChunks; ++c, ++CK) {
-          const int ks = CK % kKS;
-          if (!wait(&B.k_full[ks], (CK / kKS) & 1)) return false;
+#pragma unroll 1
+        for (int c = 0; c < Lay::kChunks; ++c) {
+          if (!wait(&B.k_full[ks], kph)) return false;
           tc_fence_after();
-          const uint32_t kb = k_base + ks * kStage;
+          const uint64_t kd = k_d0 + static_cast<uint64_t>(ks * (kStage >> 4));
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const uint64_t adesc = smem_desc(q_base + c * (kBM * 128) + w * 32, 16, 1024);
-            const uint64_t bdesc = smem_desc(kb + w * 32, 16, 1024);
-            mma_ss_pair(sc, adesc, bdesc, kIdS, (c > 0 || w > 0) ? 1u : 0u);
-          }
+          for (int w = 0; w < 4; ++w)
+            mma_ss_pair(sc, q_d0 + ((c * (kBM * 128) + w * 32) >> 4), kd + ((w * 32) >> 4), kIdS,
+                        (c > 0 || w > 0) ? 1u : 0u);
           mma_commit_pair(&B.k_empty[ks]);
+          if (++ks == kKS) {
+            ks = 0;
+            kph ^= 1;
+          }
         }
         mma_commit_pair(&B.s_full[Ts & 1]);
         return true;
