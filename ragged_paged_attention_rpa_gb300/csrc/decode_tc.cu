@@ -384,7 +384,14 @@ decode_tc_kernel(const __grid_constant__ TcMaps maps, const DecodeParams p,
     const bool is_s = warp == 1;
     const uint32_t q_base = smem_u32(smem + L::kQOff), p_base = smem_u32(smem + L::kPOff);
     const uint32_t k_base = smem_u32(smem + L::kKOff), v_base = smem_u32(smem + L::kVOff);
-    uint32_t j = 0, CK = 0, CV = 0;
+    // Descriptors as base + byte offset / 16 (the start-address field;
+    // every operand lies below 256 KB), built once rather than per MMA.
+    const uint64_t q_d0 = smem_desc(q_base, 16, 1024), p_d0 = smem_desc(p_base, 16, 1024);
+    const uint64_t k_d0 = smem_desc(k_base, 16, 1024);
+    const uint64_t v_d0 = smem_desc(v_base, L::kVKeys * 128, 1024);
+    uint32_t j = 0;
+    int ks = 0, vs = 0;          // ring slot and phase of the next K / V stage
+    uint32_t kph = 0, vph = 0;
     int u = 0;
     bool alive = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -419,30 +426,33 @@ decode_tc_kernel(const __grid_constant__ TcMaps maps, const DecodeParams p,
       if (!wait(&B.p_full[b], (jp >> 1) & 1)) return false;
       if (!wait(&B.o_empty[b], ((jp >> 1) & 1) ^ 1)) return false;
       uint32_t acc = 0;
+#pragma unroll 1
       for (int sv = 0; sv < L::kChunks; ++sv) {
         const int a = max(tg.u0, sv * L::kVUnits);
         const int e = min(tg.u1, (sv + 1) * L::kVUnits);
         if (a >= e) continue;
-        const int vs = CV % L::kVS;
-        if (!wait(&B.v_full[vs], (CV / L::kVS) & 1)) return false;
-        ++CV;
+        if (!wait(&B.v_full[vs], vph)) return false;
         clear_v_edges(si, tg.key0 + sv * L::kVKeys, vs);
         tc_fence_after();
-        const uint32_t vb = v_base + vs * kStage;
+        const uint64_t vd = v_d0 + static_cast<uint64_t>(vs * (kStage >> 4));
+        const uint64_t pd = p_d0 + static_cast<uint64_t>((b * L::kPBytes) >> 4);
 #pragma unroll
         for (int dh = 0; dh < L::kHalves; ++dh) {
 #pragma unroll
           for (int kk = 0; kk < L::kVUnits; ++kk) {
             const int kg = sv * L::kVUnits + kk;   // 16-key group of the tile
-            const uint64_t adesc =
-                smem_desc(vb + dh * 2 * (L::kVKeys * 128) + kk * 2048, L::kVKeys * 128, 1024);
-            const uint64_t bdesc =
-                smem_desc(p_base + b * L::kPBytes + (kg >> 2) * 2048 + (kg & 3) * 32, 16, 1024);
-            mma_ss(tmem + 32 + 32 * b + 16 * dh, adesc, bdesc, kIdPV, (acc >> dh) & 1u);
+            mma_ss(tmem + 32 + 32 * b + 16 * dh,
+                   vd + static_cast<uint64_t>((dh * 2 * (L::kVKeys * 128) + kk * 2048) >> 4),
+                   pd + static_cast<uint64_t>(((kg >> 2) * 2048 + (kg & 3) * 32) >> 4), kIdPV,
+                   (acc >> dh) & 1u);
             acc |= 1u << dh;
           }
         }
         mma_commit(&B.v_empty[vs]);
+        if (++vs == L::kVS) {
+          vs = 0;
+          vph ^= 1;
+        }
       }
       mma_commit(&B.o_full[b]);
       mma_commit(&B.p_free[b]);
@@ -465,16 +475,21 @@ decode_tc_kernel(const __grid_constant__ TcMaps maps, const DecodeParams p,
         // time; K (A) and Q (B) K-major, 16 dimensions = 32 B per MMA.
         if (!(alive = wait(&B.s_empty[b], ((j >> 1) & 1) ^ 1))) break;
         tc_fence_after();
-        for (int ch = 0; ch < L::kChunks; ++ch, ++CK) {
-          const int ks = CK % L::kKS;
-          if (!(alive = wait(&B.k_full[ks], (CK / L::kKS) & 1))) break;
+#pragma unroll 1
+        for (int ch = 0; ch < L::kChunks; ++ch) {
+          if (!(alive = wait(&B.k_full[ks], kph))) break;
           tc_fence_after();
-          const uint32_t kb = k_base + ks * kStage;
+          const uint64_t kd = k_d0 + static_cast<uint64_t>(ks * (kStage >> 4));
+          const uint64_t qd = q_d0 + static_cast<uint64_t>(((qb - q_base) + ch * 2048) >> 4);
 #pragma unroll
           for (int w = 0; w < 4; ++w)
-            mma_ss(tmem + 16 * b, smem_desc(kb + w * 32, 16, 1024),
-                   smem_desc(qb + ch * 2048 + w * 32, 16, 1024), kIdS, (ch | w) ? 1u : 0u);
+            mma_ss(tmem + 16 * b, kd + ((w * 32) >> 4), qd + ((w * 32) >> 4), kIdS,
+                   (ch | w) ? 1u : 0u);
           mma_commit(&B.k_empty[ks]);
+          if (++ks == L::kKS) {
+            ks = 0;
+            kph ^= 1;
+          }
         }
         if (!alive) break;
         mma_commit(&B.s_full[b]);
