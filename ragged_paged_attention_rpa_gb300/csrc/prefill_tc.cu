@@ -580,13 +580,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         clear_v_edges(gm, gm.key_first + jp * kBN + sgi * Lay::kVKeys, vs);
         tc_fence_after();
         const uint64_t vd = v_d0 + static_cast<uint64_t>(vs * (kStage >> 4));
+        // kVKeys / 16 MMAs of 16 keys (P: 8 columns, V: 2048 B = 128
+        // descriptor units apart), in pairs; the stage's commit with the last.
+        constexpr int kPairs = Lay::kVKeys / 32;
+        const uint32_t pc = p_col + sgi * (Lay::kVKeys / 2);
 #pragma unroll
-        for (int kk = 0; kk < Lay::kVKeys / 16; ++kk) {
-          const int kg = sgi * (Lay::kVKeys / 16) + kk;     // 16-key group of the tile
-          mma_ts(tmem + Lay::kOCol, p_col + kg * 8, vd + ((kk * 2048) >> 4), kIdPV,
-                 (jp > 0 || kg > 0) ? 1u : 0u);
-        }
-        mma_commit(&B.v_empty[vs]);
+        for (int q = 0; q < kPairs - 1; ++q)
+          mma_ts2(tmem + Lay::kOCol, pc + 16 * q, pc + 16 * q + 8, vd + 256 * q, vd + 256 * q + 128,
+                  kIdPV, (jp > 0 || sgi > 0 || q > 0) ? 1u : 0u);
+        mma_ts2_commit(tmem + Lay::kOCol, pc + 16 * (kPairs - 1), pc + 16 * (kPairs - 1) + 8,
+                       vd + 256 * (kPairs - 1), vd + 256 * (kPairs - 1) + 128, kIdPV,
+                       (jp > 0 || sgi > 0 || kPairs > 1) ? 1u : 0u, &B.v_empty[vs]);
         if (++vs == kVS) {
           vs = 0;
           vph ^= 1;
@@ -605,11 +609,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (!wait(&B.k_full[ks], kph)) return false;
         tc_fence_after();
         const uint64_t kd = k_d0 + static_cast<uint64_t>(ks * (kStage >> 4));
-#pragma unroll
-        for (int w = 0; w < 4; ++w)
-          mma_ss(sc, q_d0 + ((c * (kBM * 128) + w * 32) >> 4), kd + ((w * 32) >> 4), kIdS,
-                 (c > 0 || w > 0) ? 1u : 0u);
-        mma_commit(&B.k_empty[ks]);
+        // Four MMAs of 16 dimensions (32 B = 2 descriptor units apart).
+        const uint64_t qd = q_d0 + static_cast<uint64_t>((c * (kBM * 128)) >> 4);
+        mma_ss4_commit(sc, qd, qd + 2, qd + 4, qd + 6, kd, kd + 2, kd + 4, kd + 6, kIdS,
+                       c > 0 ? 1u : 0u, &B.k_empty[ks]);
         if (++ks == kKS) {
           ks = 0;
           kph ^= 1;
