@@ -522,6 +522,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // Ring slot and phase of the next K / V stage.
     int ks = 0, vs = 0;
     uint32_t kph = 0, vph = 0;
+    // Whether the next K / V stage has landed, as tested (mbar_test) while
+    // the current stage's MMAs were issued; false: wait for it.
+    bool k_ready = false, v_ready = false;
     // Shared-memory descriptors differ between operands of one kind only in
     // the start-address field (bits 0-13: the byte address / 16), and every
     // operand lies below 256 KB, so the operand at byte offset `off` from a
@@ -576,10 +579,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const uint32_t p_col = tmem + Lay::kSCol + sb * kBN;
 #pragma unroll 1
       for (int sgi = 0; sgi < Lay::kChunks; ++sgi) {
-        if (!wait(&B.v_full[vs], vph)) return false;
+        if (!v_ready && !wait(&B.v_full[vs], vph)) return false;
         clear_v_edges(gm, gm.key_first + jp * kBN + sgi * Lay::kVKeys, vs);
         tc_fence_after();
+        const int vcur = vs;
         const uint64_t vd = v_d0 + static_cast<uint64_t>(vs * (kStage >> 4));
+        if (++vs == kVS) {
+          vs = 0;
+          vph ^= 1;
+        }
+        v_ready = __all_sync(0xffffffffu, mbar_test(&B.v_full[vs], vph));
         // kVKeys / 16 MMAs of 16 keys (P: 8 columns, V: 2048 B = 128
         // descriptor units apart), in pairs; the stage's commit with the last.
         constexpr int kPairs = Lay::kVKeys / 32;
@@ -590,11 +599,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                   kIdPV, (jp > 0 || sgi > 0 || q > 0) ? 1u : 0u);
         mma_ts2_commit(tmem + Lay::kOCol, pc + 16 * (kPairs - 1), pc + 16 * (kPairs - 1) + 8,
                        vd + 256 * (kPairs - 1), vd + 256 * (kPairs - 1) + 128, kIdPV,
-                       (jp > 0 || sgi > 0 || kPairs > 1) ? 1u : 0u, &B.v_empty[vs]);
-        if (++vs == kVS) {
-          vs = 0;
-          vph ^= 1;
-        }
+                       (jp > 0 || sgi > 0 || kPairs > 1) ? 1u : 0u, &B.v_empty[vcur]);
       }
       mma_commit(&B.o_done[sb]);
       return true;
@@ -606,17 +611,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const uint32_t sc = tmem + Lay::kSCol + (Ts & 1) * kBN;
 #pragma unroll 1
       for (int c = 0; c < Lay::kChunks; ++c) {
-        if (!wait(&B.k_full[ks], kph)) return false;
+        if (!k_ready && !wait(&B.k_full[ks], kph)) return false;
         tc_fence_after();
+        const int kcur = ks;
         const uint64_t kd = k_d0 + static_cast<uint64_t>(ks * (kStage >> 4));
-        // Four MMAs of 16 dimensions (32 B = 2 descriptor units apart).
-        const uint64_t qd = q_d0 + static_cast<uint64_t>((c * (kBM * 128)) >> 4);
-        mma_ss4_commit(sc, qd, qd + 2, qd + 4, qd + 6, kd, kd + 2, kd + 4, kd + 6, kIdS,
-                       c > 0 ? 1u : 0u, &B.k_empty[ks]);
         if (++ks == kKS) {
           ks = 0;
           kph ^= 1;
         }
+        k_ready = __all_sync(0xffffffffu, mbar_test(&B.k_full[ks], kph));
+        // Four MMAs of 16 dimensions (32 B = 2 descriptor units apart).
+        const uint64_t qd = q_d0 + static_cast<uint64_t>((c * (kBM * 128)) >> 4);
+        mma_ss4_commit(sc, qd, qd + 2, qd + 4, qd + 6, kd, kd + 2, kd + 4, kd + 6, kIdS,
+                       c > 0 ? 1u : 0u, &B.k_empty[kcur]);
       }
       mma_commit(&B.s_full[Ts & 1]);
       return true;

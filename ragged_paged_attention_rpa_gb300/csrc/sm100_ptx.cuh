@@ -51,6 +51,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// A non-blocking look at an mbarrier: true if the phase with parity `parity`
+// has completed (acquire semantics, as a wait that returns).  A wait whose
+// result is branched on costs its full latency (~70 cycles even when the
+// phase is complete); testing the next stage's barrier ahead of its use,
+// while the current stage's MMAs are issued, hides that.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Wait for the phase of `bar` with parity `parity` to complete.  Gives up
 // (returns false) when `*abort` is set by another thread or after `limit_ns`
 // nanoseconds, in which case it sets `*abort` itself.  Never spins forever.
