@@ -273,6 +273,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   __syncthreads();
 
   int count = 0;  // blocks consumed by this warp
+  // Whether block `count` has landed, as tested (mbar_test) during the
+  // previous block's math; false: wait for it.  A wait whose result is
+  // branched on costs its full latency even when the block is there.
+  bool next_ready = false;
   for (int t = 0; t < nseg; ++t) {
     const SegInfo si = s_seg[t];
     if (!sm100::mbar_wait(&q_bar[t & 1], (t >> 1) & 1, abort, 2000000000ull)) {
@@ -311,7 +315,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     for (int j = warp; j < si.nb; j += kWarps, ++count) {
       issue((count + S - 1) % S);
       const int st = count % S;
-      if (!sm100::mbar_wait(&full_bar[warp][st], (count / S) & 1, abort, 2000000000ull)) {
+      if (!next_ready &&
+          !sm100::mbar_wait(&full_bar[warp][st], (count / S) & 1, abort, 2000000000ull)) {
         if (lane == 0) report_error(p.ws, RPA_DEVERR_TIMEOUT, c);
         break;
       }
@@ -342,6 +347,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
           else mma_t<FP8>(sa, a0, a1, a2, a3, qf[kt2][0], qf[kt2][1]);
         }
       }
+      // The next block's copy (this warp's blocks run on across segments).
+      next_ready = sm100::mbar_test(&full_bar[warp][(count + 1) % S], ((count + 1) / S) & 1);
       const int r_top = lane >> 2, r_bot = r_top + 8;
       const bool v_top = (vmask >> r_top) & 1u, v_bot = (vmask >> r_bot) & 1u;
       float x[4];

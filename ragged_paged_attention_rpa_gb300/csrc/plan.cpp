@@ -486,13 +486,13 @@ TileStats prefill_tile_stats(const Plan& plan, const int32_t* cu, const int32_t*
 // prefill part on 40-152 SMs: the decode grid streams its KV bytes at ~68
 // GB/s per SM (each CTA's copy ring, not HBM, sets the pace) until ~5 TB/s,
 // plus its ramp, merges and combine; the single-SM prefill kernel at D = 256
-// takes ~1.8 us per 128-key tile and ~3.2 us per item epilogue (both scale
+// takes ~1.6 us per 128-key tile and ~3.2 us per item epilogue (both scale
 // with D), its makespan set by the busier of the average CTA and the longest
 // item, plus its ramp and tail.
 constexpr double kDecodeSmGBs = 68.0;
 constexpr double kDecodeHbmGBs = 5000.0;
 constexpr double kDecodeFixedUs = 8.0;
-constexpr double kPrefillTileUs256 = 1.8;
+constexpr double kPrefillTileUs256 = 1.6;
 constexpr double kPrefillItemUs256 = 3.2;
 constexpr double kPrefillFixedUs = 20.0;
 

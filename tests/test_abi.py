@@ -581,7 +581,7 @@ def mixed_costs(b, n_sms=152):
         return dec_bytes / min(x * 68.0, 5000.0) * 1e-3 + 8.0
 
     def pre(y):
-        return (max(sum(tiles) / y, max(tiles)) * 1.8 * f + ceil_div(len(tiles), y) * 3.2 * f
+        return (max(sum(tiles) / y, max(tiles)) * 1.6 * f + ceil_div(len(tiles), y) * 3.2 * f
                 + 20.0)
     return dec, pre
 
