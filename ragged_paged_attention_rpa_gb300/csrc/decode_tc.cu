@@ -392,6 +392,9 @@ decode_tc_kernel(const __grid_constant__ TcMaps maps, const DecodeParams p,
     uint32_t j = 0;
     int ks = 0, vs = 0;          // ring slot and phase of the next K / V stage
     uint32_t kph = 0, vph = 0;
+    // Whether the next K / V stage has landed, tested (mbar_test) while the
+    // current stage's MMAs were issued; false: wait for it.
+    bool k_ready = false, v_ready = false;
     int u = 0;
     bool alive = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -431,10 +434,16 @@ decode_tc_kernel(const __grid_constant__ TcMaps maps, const DecodeParams p,
         const int a = max(tg.u0, sv * L::kVUnits);
         const int e = min(tg.u1, (sv + 1) * L::kVUnits);
         if (a >= e) continue;
-        if (!wait(&B.v_full[vs], vph)) return false;
+        if (!v_ready && !wait(&B.v_full[vs], vph)) return false;
         clear_v_edges(si, tg.key0 + sv * L::kVKeys, vs);
         tc_fence_after();
+        const int vcur = vs;
         const uint64_t vd = v_d0 + static_cast<uint64_t>(vs * (kStage >> 4));
+        if (++vs == L::kVS) {
+          vs = 0;
+          vph ^= 1;
+        }
+        v_ready = __all_sync(0xffffffffu, mbar_test(&B.v_full[vs], vph));
         const uint64_t pd = p_d0 + static_cast<uint64_t>((b * L::kPBytes) >> 4);
 #pragma unroll
         for (int dh = 0; dh < L::kHalves; ++dh) {
@@ -448,11 +457,7 @@ decode_tc_kernel(const __grid_constant__ TcMaps maps, const DecodeParams p,
             acc |= 1u << dh;
           }
         }
-        mma_commit(&B.v_empty[vs]);
-        if (++vs == L::kVS) {
-          vs = 0;
-          vph ^= 1;
-        }
+        mma_commit(&B.v_empty[vcur]);
       }
       mma_commit(&B.o_full[b]);
       mma_commit(&B.p_free[b]);
@@ -477,19 +482,18 @@ decode_tc_kernel(const __grid_constant__ TcMaps maps, const DecodeParams p,
         tc_fence_after();
 #pragma unroll 1
         for (int ch = 0; ch < L::kChunks; ++ch) {
-          if (!(alive = wait(&B.k_full[ks], kph))) break;
+          if (!k_ready && !(alive = wait(&B.k_full[ks], kph))) break;
           tc_fence_after();
+          const int kcur = ks;
           const uint64_t kd = k_d0 + static_cast<uint64_t>(ks * (kStage >> 4));
           const uint64_t qd = q_d0 + static_cast<uint64_t>(((qb - q_base) + ch * 2048) >> 4);
-#pragma unroll
-          for (int w = 0; w < 4; ++w)
-            mma_ss(tmem + 16 * b, kd + ((w * 32) >> 4), qd + ((w * 32) >> 4), kIdS,
-                   (ch | w) ? 1u : 0u);
-          mma_commit(&B.k_empty[ks]);
           if (++ks == L::kKS) {
             ks = 0;
             kph ^= 1;
           }
+          k_ready = __all_sync(0xffffffffu, mbar_test(&B.k_full[ks], kph));
+          mma_ss4_commit(tmem + 16 * b, kd, kd + 2, kd + 4, kd + 6, qd, qd + 2, qd + 4, qd + 6,
+                         kIdS, ch > 0 ? 1u : 0u, &B.k_empty[kcur]);
         }
         if (!alive) break;
         mma_commit(&B.s_full[b]);
