@@ -285,6 +285,26 @@ __device__ __forceinline__ void leave_item_counter(unsigned char* ws) {
   }
 }
 
+// Zero rows [0, a) and [b, kVKeys) of a V stage ([chunk][kVKeys rows][128 B]),
+// then order the stores before the tensor core's reads (whole warp).  Out of
+// line: inlined into the MMA warp's stage loop, this rarely taken code cost
+// ~3% of the prefill's time.  A key row is D / 64 chunks of 128 bytes,
+// kVKeys x 128 B apart; the swizzle permutes 16-byte units inside a row, so
+// whole rows are cleared whatever it is.
+template <int kVKeys, int kChunks>
+__device__ __noinline__ void zero_v_rows(uint8_t* st, int a, int b, int lane) {
+  const int nrows = a + (kVKeys - b);
+  for (int u = lane; u < nrows * kChunks * 8; u += 32) {
+    const int rr = u / (kChunks * 8), rem = u % (kChunks * 8);
+    const int row = rr < a ? rr : b + (rr - a);
+    *reinterpret_cast<uint4*>(st + (rem >> 3) * (kVKeys * 128) + row * 128 + (rem & 7) * 16) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+  // The tensor core reads the stage through the async proxy.
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+}
+
 // A warp takes item number R from the ring (every lane waits and reads;
 // lane 0 releases the slot).  False when the wait gave up.
 __device__ __forceinline__ bool take_item(Barriers& B, uint32_t& R, ItemSlot& e,
@@ -554,23 +574,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // stages at the two ends of an item need this.
     auto clear_v_edges = [&](const Geom& gm, int32_t kst, int vs) {
       const int32_t last = gm.pos_first + gm.ntok - 1;
+      // Interior stages (every key visible to some query of the item): nothing.
+      if (kst >= gm.lo && kst + Lay::kVKeys <= last + 1) return;
       const int a = max(0, min(Lay::kVKeys, gm.lo - kst));        // rows [0, a): before
       const int b = max(0, min(Lay::kVKeys, last + 1 - kst));     // rows [b, kVKeys): past
-      if ((a == 0 && b == Lay::kVKeys) || a == Lay::kVKeys || b == 0) return;
-      // A key row is D / 64 chunks of 128 bytes, kVKeys x 128 B apart; the
-      // swizzle permutes 16-byte units inside a row, so whole rows are
-      // cleared whatever it is.
-      uint8_t* st = reinterpret_cast<uint8_t*>(v_s) + vs * kStage;
-      const int nrows = a + (Lay::kVKeys - b);
-      for (int u = lane; u < nrows * Lay::kChunks * 8; u += 32) {
-        const int rr = u / (Lay::kChunks * 8), rem = u % (Lay::kChunks * 8);
-        const int row = rr < a ? rr : b + (rr - a);
-        *reinterpret_cast<uint4*>(st + (rem >> 3) * (Lay::kVKeys * 128) + row * 128 +
-                                  (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      // The tensor core reads the stage through the async proxy.
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
+      if (a == Lay::kVKeys || b == 0) return;   // the whole stage arrived as zeros
+      zero_v_rows<Lay::kVKeys, Lay::kChunks>(reinterpret_cast<uint8_t*>(v_s) + vs * kStage, a, b,
+                                             lane);
     };
     auto issue_pv = [&](const Geom& gm, uint32_t Tp, int jp) -> bool {
       const int sb = Tp & 1;
