@@ -291,15 +291,20 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       const __nv_bfloat16* qr = qs + (t & 1) * 8 * D + (hv ? h : 0) * D;
 #pragma unroll
       for (int kt = 0; kt < KT; ++kt) {
-        const int d0 = kt * 16 + 2 * (lane & 3);
-        qf[kt][0] = hv ? *reinterpret_cast<const uint32_t*>(qr + d0) : 0u;
-        qf[kt][1] = hv ? *reinterpret_cast<const uint32_t*>(qr + d0 + 8) : 0u;
         if constexpr (FP8) {
-          // bf16 pairs -> f16 pairs for the f16 products with the fp8 pages.
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-            qf[kt][i] = pack_f16x2(__uint_as_float(qf[kt][i] << 16),
-                                   __uint_as_float(qf[kt][i] & 0xffff0000u));
+          // The K fragments of fp8 pages are read four bytes at a time (see
+          // below): fragment dimensions {2c, 2c + 1} and {2c + 8, 2c + 9} of
+          // each 16 (c = lane % 4) hold dimensions 4c .. 4c + 3; q's take the
+          // same order, which leaves every score unchanged.  bf16 pairs ->
+          // f16 pairs for the f16 products with the fp8 pages.
+          const int d0 = kt * 16 + 4 * (lane & 3);
+          const uint2 q4 = hv ? *reinterpret_cast<const uint2*>(qr + d0) : make_uint2(0u, 0u);
+          qf[kt][0] = pack_f16x2(__uint_as_float(q4.x << 16), __uint_as_float(q4.x & 0xffff0000u));
+          qf[kt][1] = pack_f16x2(__uint_as_float(q4.y << 16), __uint_as_float(q4.y & 0xffff0000u));
+        } else {
+          const int d0 = kt * 16 + 2 * (lane & 3);
+          qf[kt][0] = hv ? *reinterpret_cast<const uint32_t*>(qr + d0) : 0u;
+          qf[kt][1] = hv ? *reinterpret_cast<const uint32_t*>(qr + d0 + 8) : 0u;
         }
       }
     }
@@ -323,9 +328,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       const __nv_bfloat16* kt;
       const __nv_bfloat16* vt;
       if constexpr (FP8) {
-        // The block as f16 in this warp's copy (the stage is then free).
+        // V as f16 in this warp's copy (its fragments need a transpose,
+        // which ldmatrix does on 16-bit data); K is read in place below.
         __nv_bfloat16* ck = conv + warp * 2 * TILE;
-        fp8_tile_to_f16<D>(ring + st * L::kStageBytes, ck, lane);
         fp8_tile_to_f16<D>(ring + st * L::kStageBytes + TILE, ck + TILE, lane);
         __syncwarp();
         kt = ck;
@@ -336,7 +341,27 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       }
       const uint32_t vmask = valid_mask[warp][st];
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-      {
+      if constexpr (FP8) {
+        // K fragments straight from the e4m3 stage ([128-dimension chunk]
+        // [16 rows][128 B], 128-byte swizzled): lane (g = lane / 4, c =
+        // lane % 4) reads dimensions 16 kt + 4c .. + 3 of rows g and g + 8
+        // as one word each and widens them in registers (exact), in the
+        // dimension order q's fragments were built in.
+        const unsigned char* kraw = ring + st * L::kStageBytes;
+        const int g = lane >> 2, c4 = 4 * (lane & 3);
+#pragma unroll
+        for (int kt2 = 0; kt2 < KT; ++kt2) {
+          const int d = kt2 * 16;
+          const unsigned char* base = kraw + (d >> 7) * (kBlk * 128) + g * 128 +
+                                      ((((d & 127) >> 4) ^ (g & 7)) << 4) + c4;
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(base);
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(base + 8 * 128);
+          const uint32_t a0 = e4m3x2_to_f16x2(w0 & 0xffffu), a2 = e4m3x2_to_f16x2(w0 >> 16);
+          const uint32_t a1 = e4m3x2_to_f16x2(w1 & 0xffffu), a3 = e4m3x2_to_f16x2(w1 >> 16);
+          if (kt2 & 1) mma_t<FP8>(sb, a0, a1, a2, a3, qf[kt2][0], qf[kt2][1]);
+          else mma_t<FP8>(sa, a0, a1, a2, a3, qf[kt2][0], qf[kt2][1]);
+        }
+      } else {
         const int row = lane & 15;
         const int hi = lane >> 4;
 #pragma unroll
