@@ -21,14 +21,17 @@
 // so every CTA finishes at about the same time whatever the length mix.  A
 // CTA's range may start or end inside a segment.
 //
-// CTA.  Four independent warps take the range's blocks round-robin (warp w:
-// blocks w, w+4, ... of each segment).  Blocks sit on absolute 16-key
-// boundaries, so with pages of 16 tokens or more a block is 16 consecutive
-// rows of one page: one lane of the warp fetches it with TMA (a 3-D tensor map
-// over the pool, 128-byte swizzled boxes of 64 dims x 16 rows) into the
-// warp's own shared-memory ring, completion on an mbarrier.  The page ids of
-// the CTA's whole range are read into shared memory once, first, in one round
-// of loads (the range's first and last segment come from the plan).  Per block a
+// CTA.  Four independent compute warps take the range's blocks round-robin
+// (warp w: blocks w, w+4, ... of each segment).  Blocks sit on absolute
+// 16-key boundaries, so with pages of 16 tokens or more a block is 16
+// consecutive rows of one page.  A fifth warp does all the copying: its lane
+// w fetches warp w's blocks with TMA (one 4-D box over the pool per K or V
+// block: every 128-byte chunk of the block's 16 rows, 128-byte swizzled) into
+// w's own shared-memory ring, completion on the stage's full mbarrier, and
+// refills a stage once w has released it on its empty mbarrier, so the
+// compute warps only wait and compute.  The page ids of the CTA's whole range
+// are read into shared memory once, first, in one round of loads (the
+// range's first and last segment come from the plan).  Per block a compute
 // warp runs
 //     S^T[16 keys x 8 heads] = K . Q^T     (mma.m16n8k16, bf16 -> fp32)
 //     O^T[D x 8 heads]     += V^T . P^T   (P^T rebuilt in registers by a
@@ -52,7 +55,7 @@ namespace rpa {
 
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 4;  // compute warps; one more warp issues their copies
 constexpr int kBlk = 16;  // keys per warp block (the MMA's M)
 
 constexpr int stages_for(int D) { return D >= 256 ? 3 : 4; }
@@ -163,7 +166,7 @@ __device__ __forceinline__ void fp8_tile_to_f16(const unsigned char* src, __nv_b
 }
 
 template <int D, int NSEG, bool FP8>
-__global__ void __launch_bounds__(kWarps * 32, 1)
+__global__ void __launch_bounds__((kWarps + 1) * 32, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const DecodeParams p, const __grid_constant__ DecodeSched<NSEG> sc) {
   using L = DecodeSmem<D, FP8>;
@@ -182,6 +185,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   __shared__ float wm[kWarps][8], wl[kWarps][8];
   __shared__ int s_npages, s_abort;
   __shared__ __align__(8) uint64_t full_bar[kWarps][S];
+  __shared__ __align__(8) uint64_t empty_bar[kWarps][S];   // stage consumed
   __shared__ __align__(8) uint64_t q_bar[2];   // Q buffer t & 1 holds segment t's queries
 
   // The combine kernel may be scheduled now; it waits for this grid's end.
@@ -203,7 +207,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   }
 
   if (tid == 0) {
-    for (int i = 0; i < kWarps * S; ++i) sm100::mbar_init(&full_bar[i / S][i % S], 1);
+    for (int i = 0; i < kWarps * S; ++i) {
+      sm100::mbar_init(&full_bar[i / S][i % S], 1);
+      sm100::mbar_init(&empty_bar[i / S][i % S], 1);
+    }
     sm100::mbar_init(&q_bar[0], 1);
     sm100::mbar_init(&q_bar[1], 1);
     s_abort = 0;
@@ -213,51 +220,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   }
   load_range_tables(sc, p, c, cb0, cb1, kfirst, nseg, s_seg, s_pages, &s_npages);
 
-  unsigned char* ring = smem_raw + warp * S * L::kStageBytes;
   volatile int* abort = &s_abort;
-  // A warp's blocks in order: segment t, local blocks warp, warp + 4, ...
-  auto advance = [&](int& st_, int& j_) {
-    j_ += kWarps;
-    while (st_ < nseg && j_ >= s_seg[st_].nb) { ++st_; j_ = warp; }
-  };
   auto page_of = [&](const SegInfo& si, int32_t key0) {
     const int32_t idx = si.pg_off + (key0 >> p.page_shift) - si.slot0;
     return idx < kMaxCtaPages ? s_pages[idx] : -1;
   };
-  // Issue cursor over this warp's blocks: segment ist, local block isj.
-  int ist = 0, isj = warp;
-  while (ist < nseg && isj >= s_seg[ist].nb) { ++ist; isj = warp; }
-  int issued = 0;
-  auto issue = [&](int st) {
-    if (ist >= nseg) return;
-    const SegInfo& si = s_seg[ist];
-    const int32_t key0 = si.kb + isj * kBlk;
-    // Lanes 0..15: validity of one key each (visible and on a good page).
-    const int32_t page = page_of(si, key0);
-    const int32_t key = key0 + lane;
-    const bool ok = lane < kBlk && page >= 0 && key >= si.lo && key < si.ke;
-    const uint32_t vmask = __ballot_sync(0xffffffffu, ok);
-    if (lane == 0) {
-      valid_mask[warp][st] = vmask;
-      // Rows of the block: page * P + (key0 % P); a bad page reads zeros.
-      const int32_t row = page >= 0 ? page * (1 << p.page_shift) + (key0 & ((1 << p.page_shift) - 1))
-                                    : -kBlk;
-      unsigned char* kt = ring + st * L::kStageBytes;
-      unsigned char* vt = kt + TILE * L::ESZ;
-      // Earlier generic-proxy reads of this stage come before the async writes.
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      sm100::mbar_arrive_expect_tx(&full_bar[warp][st], static_cast<uint32_t>(L::kStageBytes));
-      // One box per K and per V block: every 128-byte chunk of the block's
-      // 16 rows ([chunk][row][128 B] in the stage).
-      sm100::tma_load_4d(kt, &tm_k, &full_bar[warp][st], 0, si.g, row, 0);
-      sm100::tma_load_4d(vt, &tm_v, &full_bar[warp][st], 0, si.g, row, 0);
-    }
-    ++issued;
-    advance(ist, isj);
-  };
-  __syncwarp();
-#pragma unroll
-  for (int i = 0; i < S - 1; ++i) issue(i);
   // Q of segment t: G x D contiguous bf16 (the G heads of KV head g are
   // adjacent), one bulk copy into buffer t & 1 on q_bar[t & 1].
   int q_last0 = -1, q_last1 = -1;   // (thread 0) last segment copied into buffer 0 / 1
@@ -271,6 +238,60 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   if (tid == 0)
     for (int t = 0; t < 2 && t < nseg; ++t) load_q(t);
   __syncthreads();
+
+  if (warp == kWarps) {
+    // ---- Copy warp: lane w (< 4) streams compute warp w's blocks (segment
+    // t, local blocks w, w + 4, ...) through w's ring, a stage at a time as
+    // w releases it.  Per block: its keys' validity mask (visible and on a
+    // good page) into shared memory, then one 4-D TMA box each for K and V
+    // (a bad page reads zeros), completion on the stage's full barrier.
+    if (lane < kWarps) {
+      const int w = lane;
+      unsigned char* ring = smem_raw + w * S * L::kStageBytes;
+      int ist = 0, isj = w;
+      while (ist < nseg && isj >= s_seg[ist].nb) { ++ist; isj = w; }
+      int i = 0;
+      for (; ist < nseg; ++i) {
+        const int st = i % S;
+        if (i >= S && !sm100::mbar_wait(&empty_bar[w][st], ((i / S) - 1) & 1, abort, 2000000000ull)) {
+          report_error(p.ws, RPA_DEVERR_TIMEOUT, c);
+          break;
+        }
+        const SegInfo& si = s_seg[ist];
+        const int32_t key0 = si.kb + isj * kBlk;
+        const int32_t page = page_of(si, key0);
+        uint32_t vmask = 0;
+        if (page >= 0) {
+          const int32_t a = max(si.lo - key0, 0), b = min(si.ke - key0, kBlk);
+          if (b > a) vmask = ((1u << b) - 1u) & ~((1u << a) - 1u);
+        }
+        valid_mask[w][st] = vmask;
+        // Rows of the block: page * P + (key0 % P); a bad page reads zeros.
+        const int32_t row = page >= 0 ? page * (1 << p.page_shift) + (key0 & ((1 << p.page_shift) - 1))
+                                      : -kBlk;
+        unsigned char* kt = ring + st * L::kStageBytes;
+        unsigned char* vt = kt + TILE * L::ESZ;
+        sm100::mbar_arrive_expect_tx(&full_bar[w][st], static_cast<uint32_t>(L::kStageBytes));
+        // One box per K and per V block: every 128-byte chunk of the block's
+        // 16 rows ([chunk][row][128 B] in the stage).
+        sm100::tma_load_4d(kt, &tm_k, &full_bar[w][st], 0, si.g, row, 0);
+        sm100::tma_load_4d(vt, &tm_v, &full_bar[w][st], 0, si.g, row, 0);
+        isj += kWarps;
+        while (ist < nseg && isj >= s_seg[ist].nb) { ++ist; isj = w; }
+      }
+      if (*abort) {
+        // Let every copy still in flight land before the CTA exits.
+        for (int k = max(i - S, 0); k < i; ++k) {
+          int dummy = 0;
+          sm100::mbar_wait(&full_bar[w][k % S], (k / S) & 1, &dummy, 200000000ull);
+        }
+      }
+    }
+    return;
+  }
+  // The compute warps synchronise among themselves (named barrier 1).
+  auto compute_sync = []() { asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory"); };
+  unsigned char* ring = smem_raw + warp * S * L::kStageBytes;
 
   int count = 0;  // blocks consumed by this warp
   // Whether block `count` has landed, as tested (mbar_test) during the
@@ -318,7 +339,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     for (int mt = 0; mt < KT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
     for (int j = warp; j < si.nb; j += kWarps, ++count) {
-      issue((count + S - 1) % S);
       const int st = count % S;
       if (!next_ready &&
           !sm100::mbar_wait(&full_bar[warp][st], (count / S) & 1, abort, 2000000000ull)) {
@@ -435,7 +455,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
           }
         }
       }
+      // Every lane's reads of the stage are done: hand it back to the copy warp.
       __syncwarp();
+      if (lane == 0) sm100::mbar_arrive(&empty_bar[warp][st]);
     }
 
     // ---- Merge the four warps' states for segment t.
@@ -450,7 +472,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       wl[warp][2 * lane] = l[0];
       wl[warp][2 * lane + 1] = l[1];
     }
-    __syncthreads();
+    compute_sync();
     // Every warp holds segment t's queries in registers now: buffer t & 1
     // takes segment t + 2's (the async copy is ordered after those reads).
     if (tid == 0 && t + 2 < nseg) {
@@ -502,10 +524,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             }
           }
         }
-        if (round == 0) __syncthreads();
+        if (round == 0) compute_sync();
       }
     }
-    __syncthreads();
+    compute_sync();
     // Write the output (whole segment) or this CTA's partial (O / L).
     for (int e = tid * 4; e < G * D; e += kWarps * 32 * 4) {
       const int h = e / D, d = e % D;
@@ -521,14 +543,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         *reinterpret_cast<float4*>(p.part_o + (static_cast<int64_t>(slot) * G + h) * D + d) = u;
       }
     }
-    __syncthreads();
+    compute_sync();
   }
   if (*abort) {
-    // Let every copy this warp started land before the CTA exits.
-    for (int i = count; i < issued; ++i) {
-      int dummy = 0;
-      sm100::mbar_wait(&full_bar[warp][i % S], (i / S) & 1, &dummy, 200000000ull);
-    }
+    // (The copy warp drains its own K / V copies.)
     if (tid == 0)
       for (int b = 0; b < 2; ++b) {
         const int last = b ? q_last1 : q_last0;
@@ -655,7 +673,7 @@ int launch_one(const Plan& plan, const DecodeParams& p, const CUtensorMap& tk,
   // Host staging, copied into the launch parameters.
   DecodeSched<NSEG>& sc = thread_staging<DecodeSched<NSEG>>();
   if (int e = fill_decode_sched(plan, dl, sc)) return e;
-  decode_kernel<D, NSEG, FP8><<<dl.n_ctas, kWarps * 32, smem, stream>>>(tk, tv, p, sc);
+  decode_kernel<D, NSEG, FP8><<<dl.n_ctas, (kWarps + 1) * 32, smem, stream>>>(tk, tv, p, sc);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return static_cast<int>(e);
   trace_mark(RPA_KERNEL_DECODE_SPLIT, stream);
