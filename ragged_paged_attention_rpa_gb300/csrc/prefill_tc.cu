@@ -900,28 +900,34 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       } else {
         __nv_bfloat16* orow =
             p.out + (static_cast<int64_t>(gm.t0 + tok) * p.hq + gm.g * G + head) * D;
+        // Each thread writes 32 bytes of its own row per 16 columns (one
+        // store when `out` is 32-byte aligned, else two), while the next 16
+        // columns load from TMEM.
+        auto store16 = [&](const uint32_t (&o)[16], int col) {
+          if (!valid) return;
+          uint32_t w[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            w[q] = pack_bf16x2(__uint_as_float(o[2 * q]) * inv, __uint_as_float(o[2 * q + 1]) * inv);
+          if (p.out_v8) {
+            st_global_v8(orow + col, w);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + col);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+        };
+        uint32_t oa[16], ob[16];
+        tmem_ld16(lane_addr + Lay::kOCol, oa);
+        tmem_wait_ld();
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(lane_addr + Lay::kOCol + c0, o);
+          tmem_ld16(lane_addr + Lay::kOCol + c0 + 16, ob);
+          store16(oa, c0);
           tmem_wait_ld();
-          if (valid) {
-            // Each thread writes 64 bytes of its own row: two 32-byte stores
-            // when `out` is 32-byte aligned, else four 16-byte ones.
-            uint32_t w[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-              w[q] = pack_bf16x2(__uint_as_float(o[2 * q]) * inv, __uint_as_float(o[2 * q + 1]) * inv);
-            if (p.out_v8) {
-              st_global_v8(orow + c0, w);
-              st_global_v8(orow + c0 + 16, w + 8);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-            }
-          }
+          if (c0 + 32 < D) tmem_ld16(lane_addr + Lay::kOCol + c0 + 32, oa);
+          store16(ob, c0 + 16);
+          tmem_wait_ld();
         }
       }
       tc_fence_before();
