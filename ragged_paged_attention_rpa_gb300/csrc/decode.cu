@@ -125,18 +125,21 @@ __device__ __forceinline__ int swz(int row, int chunk) {
   return (chunk >> 3) * (16 * 64) + row * 64 + (((chunk & 7) ^ (row & 7)) << 3);
 }
 
-// Shared memory of a decode CTA: per warp a ring of S stages (one 16-key
-// block of K and of V each, as TMA writes them: 128-byte swizzled rows), for
-// fp8 pages a per-warp f16 copy of the block being consumed, two Q tiles and
-// the merge buffers.
+// Shared memory of a decode CTA: per warp a ring of S K slots and S V slots
+// (one 16-key block of K or of V each, as TMA writes them: 128-byte swizzled
+// rows; K slot s, then V slot s at S slots further), for fp8 pages a per-warp
+// f16 copy of the V block being consumed, two Q tiles and the merge buffers.
+// K and V have slots of their own so that a block's K slot is refilled as
+// soon as its scores are out, before its V is used.
 template <int D, bool FP8>
 struct DecodeSmem {
   static constexpr int S = FP8 ? 4 : stages_for(D);
   static constexpr int TILE = kBlk * D;                         // elements of a K (or V) tile
   static constexpr int ESZ = FP8 ? 1 : 2;                       // bytes per element as stored
-  static constexpr size_t kStageBytes = size_t(2) * TILE * ESZ;
+  static constexpr size_t kSlotBytes = size_t(TILE) * ESZ;     // one K or V block
+  static constexpr size_t kStageBytes = 2 * kSlotBytes;
   static constexpr size_t kRing = size_t(kWarps) * S * kStageBytes;
-  static constexpr size_t kConv = FP8 ? size_t(kWarps) * 2 * TILE * 2 : 0;
+  static constexpr size_t kConv = FP8 ? size_t(kWarps) * TILE * 2 : 0;
   static constexpr size_t kQ = 2 * 8 * D * 2;                   // two Q tiles (G <= 8)
   static constexpr int kORow = D + 4;                           // padded row of the merge buffer
   static constexpr size_t kO = 2 * 8 * kORow * 4;               // two merge buffers
@@ -184,8 +187,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   __shared__ uint32_t valid_mask[kWarps][S];
   __shared__ float wm[kWarps][8], wl[kWarps][8];
   __shared__ int s_npages, s_abort;
-  __shared__ __align__(8) uint64_t full_bar[kWarps][S];
-  __shared__ __align__(8) uint64_t empty_bar[kWarps][S];   // stage consumed
+  __shared__ __align__(8) uint64_t kfull_bar[kWarps][S], vfull_bar[kWarps][S];    // slot landed
+  __shared__ __align__(8) uint64_t kempty_bar[kWarps][S], vempty_bar[kWarps][S];  // slot consumed
   __shared__ __align__(8) uint64_t q_bar[2];   // Q buffer t & 1 holds segment t's queries
 
   // The combine kernel may be scheduled now; it waits for this grid's end.
@@ -208,8 +211,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
   if (tid == 0) {
     for (int i = 0; i < kWarps * S; ++i) {
-      sm100::mbar_init(&full_bar[i / S][i % S], 1);
-      sm100::mbar_init(&empty_bar[i / S][i % S], 1);
+      sm100::mbar_init(&kfull_bar[i / S][i % S], 1);
+      sm100::mbar_init(&vfull_bar[i / S][i % S], 1);
+      sm100::mbar_init(&kempty_bar[i / S][i % S], 1);
+      sm100::mbar_init(&vempty_bar[i / S][i % S], 1);
     }
     sm100::mbar_init(&q_bar[0], 1);
     sm100::mbar_init(&q_bar[1], 1);
@@ -241,19 +246,19 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
   if (warp == kWarps) {
     // ---- Copy warp: lane w (< 4) streams compute warp w's blocks (segment
-    // t, local blocks w, w + 4, ...) through w's ring, a stage at a time as
-    // w releases it.  Per block: its keys' validity mask (visible and on a
-    // good page) into shared memory, then one 4-D TMA box each for K and V
-    // (a bad page reads zeros), completion on the stage's full barrier.
+    // t, local blocks w, w + 4, ...) through w's K and V slots, each as w
+    // releases it.  Per block: its keys' validity mask (visible and on a good
+    // page) into shared memory, then one 4-D TMA box each for K and V (a bad
+    // page reads zeros), completion on the slot's full barrier.
     if (lane < kWarps) {
       const int w = lane;
       unsigned char* ring = smem_raw + w * S * L::kStageBytes;
       int ist = 0, isj = w;
       while (ist < nseg && isj >= s_seg[ist].nb) { ++ist; isj = w; }
-      int i = 0;
+      int i = 0, nk = 0, nv = 0;   // blocks taken; K and V copies issued
       for (; ist < nseg; ++i) {
         const int st = i % S;
-        if (i >= S && !sm100::mbar_wait(&empty_bar[w][st], ((i / S) - 1) & 1, abort, 2000000000ull)) {
+        if (i >= S && !sm100::mbar_wait(&kempty_bar[w][st], ((i / S) - 1) & 1, abort, 2000000000ull)) {
           report_error(p.ws, RPA_DEVERR_TIMEOUT, c);
           break;
         }
@@ -269,21 +274,42 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // Rows of the block: page * P + (key0 % P); a bad page reads zeros.
         const int32_t row = page >= 0 ? page * (1 << p.page_shift) + (key0 & ((1 << p.page_shift) - 1))
                                       : -kBlk;
-        unsigned char* kt = ring + st * L::kStageBytes;
-        unsigned char* vt = kt + TILE * L::ESZ;
-        sm100::mbar_arrive_expect_tx(&full_bar[w][st], static_cast<uint32_t>(L::kStageBytes));
         // One box per K and per V block: every 128-byte chunk of the block's
-        // 16 rows ([chunk][row][128 B] in the stage).
-        sm100::tma_load_4d(kt, &tm_k, &full_bar[w][st], 0, si.g, row, 0);
-        sm100::tma_load_4d(vt, &tm_v, &full_bar[w][st], 0, si.g, row, 0);
+        // 16 rows ([chunk][row][128 B] in the slot).
+        unsigned char* kt = ring + st * L::kSlotBytes;
+        unsigned char* vt = ring + (S + st) * L::kSlotBytes;
+        if constexpr (FP8) {
+          // fp8 pages: the compute warp copies V out (widened) before its
+          // score MMAs, so K and V share the K slot's barriers.
+          sm100::mbar_arrive_expect_tx(&kfull_bar[w][st], static_cast<uint32_t>(2 * L::kSlotBytes));
+          sm100::tma_load_4d(kt, &tm_k, &kfull_bar[w][st], 0, si.g, row, 0);
+          sm100::tma_load_4d(vt, &tm_v, &kfull_bar[w][st], 0, si.g, row, 0);
+          ++nk;
+        } else {
+          sm100::mbar_arrive_expect_tx(&kfull_bar[w][st], static_cast<uint32_t>(L::kSlotBytes));
+          sm100::tma_load_4d(kt, &tm_k, &kfull_bar[w][st], 0, si.g, row, 0);
+          ++nk;
+          if (i >= S && !sm100::mbar_wait(&vempty_bar[w][st], ((i / S) - 1) & 1, abort, 2000000000ull)) {
+            report_error(p.ws, RPA_DEVERR_TIMEOUT, c);
+            break;
+          }
+          sm100::mbar_arrive_expect_tx(&vfull_bar[w][st], static_cast<uint32_t>(L::kSlotBytes));
+          sm100::tma_load_4d(vt, &tm_v, &vfull_bar[w][st], 0, si.g, row, 0);
+          ++nv;
+        }
         isj += kWarps;
         while (ist < nseg && isj >= s_seg[ist].nb) { ++ist; isj = w; }
       }
       if (*abort) {
-        // Let every copy still in flight land before the CTA exits.
-        for (int k = max(i - S, 0); k < i; ++k) {
+        // Let every copy still in flight land before the CTA exits: the last
+        // S K and V copies issued (one per slot).
+        for (int k = max(nk - S, 0); k < nk; ++k) {
           int dummy = 0;
-          sm100::mbar_wait(&full_bar[w][k % S], (k / S) & 1, &dummy, 200000000ull);
+          sm100::mbar_wait(&kfull_bar[w][k % S], (k / S) & 1, &dummy, 200000000ull);
+        }
+        for (int k = max(nv - S, 0); k < nv; ++k) {
+          int dummy = 0;
+          sm100::mbar_wait(&vfull_bar[w][k % S], (k / S) & 1, &dummy, 200000000ull);
         }
       }
     }
@@ -340,26 +366,26 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     for (int j = warp; j < si.nb; j += kWarps, ++count) {
       const int st = count % S;
-      if (!next_ready &&
-          !sm100::mbar_wait(&full_bar[warp][st], (count / S) & 1, abort, 2000000000ull)) {
+      const uint32_t par = (count / S) & 1;
+      if (!next_ready && !sm100::mbar_wait(&kfull_bar[warp][st], par, abort, 2000000000ull)) {
         if (lane == 0) report_error(p.ws, RPA_DEVERR_TIMEOUT, c);
         break;
       }
-      const __nv_bfloat16* kt;
+      const __nv_bfloat16* kt = reinterpret_cast<const __nv_bfloat16*>(ring + st * L::kSlotBytes);
+      const unsigned char* vraw = ring + (S + st) * L::kSlotBytes;
+      const uint32_t vmask = valid_mask[warp][st];
       const __nv_bfloat16* vt;
       if constexpr (FP8) {
         // V as f16 in this warp's copy (its fragments need a transpose,
-        // which ldmatrix does on 16-bit data); K is read in place below.
-        __nv_bfloat16* ck = conv + warp * 2 * TILE;
-        fp8_tile_to_f16<D>(ring + st * L::kStageBytes + TILE, ck + TILE, lane);
+        // which ldmatrix does on 16-bit data), made first (K and V landed
+        // together); both slots go back to the copy warp after the scores.
+        __nv_bfloat16* cv = conv + warp * TILE;
+        fp8_tile_to_f16<D>(vraw, cv, lane);
         __syncwarp();
-        kt = ck;
-        vt = ck + TILE;
+        vt = cv;
       } else {
-        kt = reinterpret_cast<const __nv_bfloat16*>(ring + st * L::kStageBytes);
-        vt = kt + TILE;
+        vt = reinterpret_cast<const __nv_bfloat16*>(vraw);
       }
-      const uint32_t vmask = valid_mask[warp][st];
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (FP8) {
         // K fragments straight from the e4m3 stage ([128-dimension chunk]
@@ -367,7 +393,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // lane % 4) reads dimensions 16 kt + 4c .. + 3 of rows g and g + 8
         // as one word each and widens them in registers (exact), in the
         // dimension order q's fragments were built in.
-        const unsigned char* kraw = ring + st * L::kStageBytes;
+        const unsigned char* kraw = ring + st * L::kSlotBytes;
         const int g = lane >> 2, c4 = 4 * (lane & 3);
 #pragma unroll
         for (int kt2 = 0; kt2 < KT; ++kt2) {
@@ -392,8 +418,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
           else mma_t<FP8>(sa, a0, a1, a2, a3, qf[kt2][0], qf[kt2][1]);
         }
       }
-      // The next block's copy (this warp's blocks run on across segments).
-      next_ready = sm100::mbar_test(&full_bar[warp][(count + 1) % S], ((count + 1) / S) & 1);
+      // The scores are out: the K slot (fp8: and the V slot) goes back to
+      // the copy warp.  Then a look at this block's V and the next block's K
+      // (this warp's blocks run on across segments).
+      __syncwarp();
+      if (lane == 0) sm100::mbar_arrive(&kempty_bar[warp][st]);
+      const bool v_ready = FP8 || sm100::mbar_test(&vfull_bar[warp][st], par);
+      next_ready = sm100::mbar_test(&kfull_bar[warp][(count + 1) % S], ((count + 1) / S) & 1);
       const int r_top = lane >> 2, r_bot = r_top + 8;
       const bool v_top = (vmask >> r_top) & 1u, v_bot = (vmask >> r_bot) & 1u;
       float x[4];
@@ -425,6 +456,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       }
       const uint32_t b0 = transpose8x8(pack_t<FP8>(p0, p1));
       const uint32_t b1 = transpose8x8(pack_t<FP8>(p2, p3));
+      if (!v_ready && !sm100::mbar_wait(&vfull_bar[warp][st], par, abort, 2000000000ull)) {
+        if (lane == 0) report_error(p.ws, RPA_DEVERR_TIMEOUT, c);
+        break;
+      }
       {
         const int row = (lane & 7) + ((lane >> 4) << 3);
         const int hi = (lane >> 3) & 1;
@@ -455,9 +490,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
           }
         }
       }
-      // Every lane's reads of the stage are done: hand it back to the copy warp.
+      // Every lane's reads of the V slot are done: hand it back to the copy warp.
       __syncwarp();
-      if (lane == 0) sm100::mbar_arrive(&empty_bar[warp][st]);
+      if (!FP8 && lane == 0) sm100::mbar_arrive(&vempty_bar[warp][st]);
     }
 
     // ---- Merge the four warps' states for segment t.

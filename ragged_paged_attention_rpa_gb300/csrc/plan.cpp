@@ -483,14 +483,14 @@ TileStats prefill_tile_stats(const Plan& plan, const int32_t* cu, const int32_t*
 
 // Cost model of a mixed batch's two persistent grids (microseconds), fitted
 // to GB300 timings of the mixed batch's decode part on 30-152 SMs and its
-// prefill part on 40-152 SMs: the decode grid streams its KV bytes at ~74
+// prefill part on 40-152 SMs: the decode grid streams its KV bytes at ~78
 // GB/s per SM (each CTA's copy ring, not HBM, sets the pace; the rate that
 // puts the split where a sweep of it measured the shortest step) until ~5 TB/s,
 // plus its ramp, merges and combine; the single-SM prefill kernel at D = 256
 // takes ~1.6 us per 128-key tile and ~3.2 us per item epilogue (both scale
 // with D), its makespan set by the busier of the average CTA and the longest
 // item, plus its ramp and tail.
-constexpr double kDecodeSmGBs = 74.0;
+constexpr double kDecodeSmGBs = 78.0;
 constexpr double kDecodeHbmGBs = 5000.0;
 constexpr double kDecodeFixedUs = 8.0;
 constexpr double kPrefillTileUs256 = 1.6;

@@ -561,7 +561,7 @@ def test_q_block_is_honoured_or_refused():
 
 
 # The planner's cost model of a mixed batch's two grids, restated: decode
-# streams its visible 16-key blocks' K and V at up to 74 GB/s per SM until
+# streams its visible 16-key blocks' K and V at up to 78 GB/s per SM until
 # 5000 GB/s, plus 8 us; the prefill takes 1.6 us per key tile and 3.2 us per
 # item epilogue at D = 256 (scaled by D / 256), plus 20 us, its tiles per CTA
 # at least those of the longest item.
@@ -578,7 +578,7 @@ def mixed_costs(b, n_sms=152):
     f = b.head_dim / 256
 
     def dec(x):
-        return dec_bytes / min(x * 74.0, 5000.0) * 1e-3 + 8.0
+        return dec_bytes / min(x * 78.0, 5000.0) * 1e-3 + 8.0
 
     def pre(y):
         return (max(sum(tiles) / y, max(tiles)) * 1.6 * f + ceil_div(len(tiles), y) * 3.2 * f
