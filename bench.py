@@ -167,18 +167,21 @@ def load_peaks():
                 source="measured" if hbm else "fallback")
 
 
+# A kernel's device source, and for the persistent kernels the planner whose
+# schedule (ranges, item order) decides how often they re-read keys.
 KERNEL_SOURCES = {
-    "decode_split": ["decode.cu", "decode_sched.cuh"],
-    "decode_combine": ["decode.cu", "decode_sched.cuh"],
-    "prefill_tc": ["prefill_tc.cu"], "prefill_combine": ["prefill_tc.cu"],
+    "decode_split": ["decode.cu", "decode_sched.cuh", "plan.cpp"],
+    "decode_combine": ["decode.cu", "decode_sched.cuh", "plan.cpp"],
+    "prefill_tc": ["prefill_tc.cu", "plan.cpp"], "prefill_combine": ["prefill_tc.cu", "plan.cpp"],
     "simt": ["simt.cu"], "kv_write": ["kv_write.cu"], "prologue": ["prologue.cu"],
 }
 
 
 def kernel_source_hash(kernel: str):
-    """First 16 hex digits of the SHA-256 of a kernel's source with comments,
-    blank lines and runs of white space removed (so edits of comments alone
-    keep it), together with the device headers every kernel includes."""
+    """First 16 hex digits of the SHA-256 of a kernel's sources (KERNEL_SOURCES)
+    with comments, blank lines and runs of white space removed (so edits of
+    comments alone keep it), together with the device headers every kernel
+    includes."""
     names = KERNEL_SOURCES.get(kernel)
     if names is None:
         return None
@@ -338,6 +341,9 @@ def parse():
     ap.add_argument("--prefill-dynamic", type=int, default=0,
                     help="plan option: 0 prefill CTAs take items as they get free, -1 each "
                          "CTA runs the planner's list")
+    ap.add_argument("--prefill-grouping", type=int, default=0,
+                    help="plan option: 0 group the prefill list by (sequence, KV head) when "
+                         "its K and V outgrow L2, -1 longest first over the whole batch")
     ap.add_argument("--decode-kernel", type=int, default=0,
                     help="plan option: 0 choose, 1 CUDA-core decode kernel, 2 tensor-core "
                          "decode kernel")
@@ -490,7 +496,8 @@ def bench_one(args, name, world, rank, local, dist, binding, torch, peaks, l2_by
                    kv_dtype=binding.RPA_DTYPE_FP8_E4M3 if fp8 else 0,
                    prefill_split=args.prefill_split, decode_sms=args.decode_sms,
                    decode_kernel=0 if fp8 else args.decode_kernel,
-                   prefill_dynamic=args.prefill_dynamic)
+                   prefill_dynamic=args.prefill_dynamic,
+                   prefill_grouping=args.prefill_grouping)
     plan = db.plan(**plan_kw)
     info = plan.info()
     ws = binding.alloc_workspace(plan)

@@ -150,6 +150,13 @@ typedef struct rpa_plan_options {
                                CTA gets free (a work counter in the workspace
                                header), -1 each CTA runs the list the planner
                                gave it (longest processing time first)         */
+  int32_t prefill_grouping; /* dynamic prefill list: 0 group the (sequence, KV
+                               head) pairs so that items sharing keys run
+                               together when every prefill sequence sees its
+                               whole prefix and their K and V outgrow L2
+                               (DRAM reads near the algorithmic bytes, ~1%
+                               longer on the causal 8k prefill), -1 longest
+                               first over the whole batch                      */
 } rpa_plan_options;
 
 /* What a plan chose; filled by rpa_plan_get_info. */
@@ -176,6 +183,10 @@ typedef struct rpa_plan_info {
   int32_t decode_kernel;       /* RPA_DECODE_KERNEL_MMA or _TC for the
                                   split-KV decode (0: no such decode)         */
   int32_t prefill_dynamic;     /* 1: prefill CTAs take items as they get free */
+  int32_t prefill_groups;      /* dynamic prefill list: groups of (sequence,
+                                  KV head) pairs run one after the other so
+                                  that items sharing keys find them in L2
+                                  (1: one group, longest first throughout)    */
 } rpa_plan_info;
 
 typedef struct rpa_plan rpa_plan_t;

@@ -77,7 +77,7 @@ class _Options(ctypes.Structure):
                 ("num_sms", ctypes.c_int32), ("prefill_pairs", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("prefill_split", ctypes.c_int32),
                 ("decode_sms", ctypes.c_int32), ("decode_kernel", ctypes.c_int32),
-                ("prefill_dynamic", ctypes.c_int32)]
+                ("prefill_dynamic", ctypes.c_int32), ("prefill_grouping", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -89,7 +89,8 @@ class PlanInfo(ctypes.Structure):
                 ("kv_dtype", ctypes.c_int32), ("prefill_split_items", ctypes.c_int32),
                 ("prefill_split_parts", ctypes.c_int32), ("prefill_max_tiles", ctypes.c_int32),
                 ("decode_sms", ctypes.c_int32), ("prefill_sms", ctypes.c_int32),
-                ("decode_kernel", ctypes.c_int32), ("prefill_dynamic", ctypes.c_int32)]
+                ("decode_kernel", ctypes.c_int32), ("prefill_dynamic", ctypes.c_int32),
+                ("prefill_groups", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: int(getattr(self, name)) for name, _ in self._fields_}
@@ -208,7 +209,7 @@ def rpa_plan(cu_q_lens_host, kv_lens_host, window_host, num_q_heads: int,
              q_block: int = 0, kv_split: int = 0, num_sms: int = 0,
              prefill_pairs: int = 0, kv_dtype: int = 0, prefill_split: int = 0,
              decode_sms: int = 0, decode_kernel: int = 0,
-             prefill_dynamic: int = 0) -> Plan:
+             prefill_dynamic: int = 0, prefill_grouping: int = 0) -> Plan:
     """rpa_plan from host (numpy) metadata; returns a Plan."""
     cu = _np_i32(cu_q_lens_host)
     kv = _np_i32(kv_lens_host)
@@ -219,7 +220,8 @@ def rpa_plan(cu_q_lens_host, kv_lens_host, window_host, num_q_heads: int,
     if win is not None and win.shape[0] != num_seqs:
         raise ValueError("window must have num_seqs entries")
     opts = _Options(ctypes.sizeof(_Options), path, q_block, kv_split, num_sms, prefill_pairs,
-                    kv_dtype, prefill_split, decode_sms, decode_kernel, prefill_dynamic)
+                    kv_dtype, prefill_split, decode_sms, decode_kernel, prefill_dynamic,
+                    prefill_grouping)
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     st = lib().rpa_plan(ctypes.byref(handle), _np_ptr(cu), _np_ptr(kv), _np_ptr(win),

@@ -96,7 +96,7 @@ rpa_status_t rpa_plan(rpa_plan_t** plan, const int32_t* cu_q_lens_host,
       o.prefill_pairs > 2 || o.kv_dtype < 0 || o.kv_dtype > RPA_DTYPE_FP8_E4M3 ||
       o.prefill_split < -1 || o.prefill_split > 65535 || o.decode_sms < -1 ||
       o.decode_kernel < 0 || o.decode_kernel > RPA_DECODE_KERNEL_TC || o.prefill_dynamic < -1 ||
-      o.prefill_dynamic > 0)
+      o.prefill_dynamic > 0 || o.prefill_grouping < -1 || o.prefill_grouping > 0)
     return RPA_ERR_INVALID_ARG;
   rpa_status_t st = rpa::validate_metadata(cu_q_lens_host, kv_lens_host, num_seqs,
                                            page_size, max_pages_per_seq);
@@ -155,6 +155,7 @@ rpa_status_t rpa_plan_get_info(const rpa_plan_t* plan, rpa_plan_info* info) {
   info->decode_sms = p.overlap ? p.decode_sms : 0;
   info->prefill_sms = p.overlap ? p.prefill_sms : 0;
   info->prefill_dynamic = p.prefill_dynamic ? 1 : 0;
+  info->prefill_groups = p.prefill_groups;
   info->decode_kernel = (p.num_decode > 0 && !p.simt_decode)
                             ? (p.decode_tc ? RPA_DECODE_KERNEL_TC : RPA_DECODE_KERNEL_MMA)
                             : 0;

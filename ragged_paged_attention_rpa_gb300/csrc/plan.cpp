@@ -260,8 +260,12 @@ void plan_decode(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t
 // Prefill work items, longest first for a persistent grid: (sequence, query
 // block, KV head), or with SM pairs (sequence, pair of adjacent query blocks,
 // KV head), costed by the keys the item streams.
+// K and V bytes per group of (sequence, KV head) pairs in the dynamic
+// prefill list: about a third of the 126 MB L2.
+constexpr double kL2GroupBytes = 40.0 * 1024 * 1024;
+
 void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_t* win,
-                  int32_t forced_q_block, int32_t forced_split, bool dynamic) {
+                  int32_t forced_q_block, int32_t forced_split, bool dynamic, bool grouping) {
   const int32_t group = plan.hq / plan.hkv;
   const int32_t max_qb = prefill_tokens_per_block(plan.d, group);
   // Query tokens per CTA: a requested block larger than one 128-row tile
@@ -309,6 +313,7 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
   plan.psplit.clear();
   plan.pcta0.clear();
   plan.prefill_dynamic = false;
+  plan.prefill_groups = 0;
   plan.n_split_items = 0;
   plan.prefill_max_tiles = 0;
   const int64_t slots = static_cast<int64_t>(plan.prefill_sms > 0 ? plan.prefill_sms : plan.num_sms) *
@@ -425,7 +430,51 @@ void plan_prefill(Plan& plan, const int32_t* cu, const int32_t* kv, const int32_
       // stream faster than others (their share of HBM and L2 differs by
       // ~10% on GB300), the faster ones take more items instead of the
       // slowest setting the makespan.
-      for (const Cost& c : all) plan.items.push_back(c.item);
+      //
+      // When the prefill's K and V outgrow L2 and each (sequence, KV head)
+      // is read by several items, the list runs in groups of (sequence, KV
+      // head) pairs of at most kL2GroupBytes of K and V, longest first within
+      // each group: the items that share keys then run close together and
+      // find them in L2, where longest first over the whole batch would
+      // stream every head's keys at once and read each from HBM again and
+      // again (2.7x the algorithmic bytes on the causal 8k prefill).
+      const int64_t pairs = static_cast<int64_t>(plan.num_prefill) * plan.hkv;
+      // Sliding windows reuse keys only between neighbouring query blocks,
+      // which longest first keeps together already: only batches whose
+      // prefill sequences all see their whole prefix are grouped.  Groups of
+      // equal bytes (ceil(total / kL2GroupBytes) of them): a small last group
+      // would start its longest items late and leave a tail.
+      double total = 0;
+      bool whole_prefix = true;
+      for (int32_t sq = 0; sq < plan.num_seqs; ++sq) {
+        if (cu[sq + 1] - cu[sq] <= 1) continue;
+        total += static_cast<double>(kv[sq]) * plan.d * 2.0 * 2.0 * plan.hkv;
+        const int32_t w = win ? win[sq] : 0;
+        if (w > 0 && w < kv[sq]) whole_prefix = false;
+      }
+      const int32_t ngroups = std::max<int32_t>(1, static_cast<int32_t>(std::ceil(total / kL2GroupBytes)));
+      std::vector<int32_t> gid(static_cast<size_t>(plan.num_seqs) * plan.hkv, 0);
+      double acc = 0;
+      for (int32_t sq = 0; sq < plan.num_seqs; ++sq) {
+        if (cu[sq + 1] - cu[sq] <= 1) continue;
+        for (int32_t h = 0; h < plan.hkv; ++h) {
+          gid[static_cast<size_t>(sq) * plan.hkv + h] =
+              std::min(ngroups - 1, static_cast<int32_t>(acc * ngroups / total));
+          acc += static_cast<double>(kv[sq]) * plan.d * 2.0 * 2.0;
+        }
+      }
+      std::vector<Cost> order = all;
+      plan.prefill_groups = 1;
+      if (grouping && whole_prefix && total > 1.5 * kL2GroupBytes &&
+          static_cast<int64_t>(all.size()) >= 4 * pairs) {
+        plan.prefill_groups = ngroups;
+        auto g_of = [&](const Cost& c) {
+          return gid[static_cast<size_t>(c.item.seq) * plan.hkv + (c.item.qb_head & 255)];
+        };
+        std::stable_sort(order.begin(), order.end(),
+                         [&](const Cost& a, const Cost& b) { return g_of(a) < g_of(b); });
+      }
+      for (const Cost& c : order) plan.items.push_back(c.item);
       plan.pcta0.clear();
       plan.prefill_dynamic = true;
     } else {
@@ -651,7 +700,7 @@ rpa_status_t build_schedule(Plan& plan, const int32_t* cu, const int32_t* kv,
   if (tc_decode && ndec > 0) plan_decode(plan, cu, kv, win, opts.kv_split);
   if (tc_prefill && plan.num_prefill > 0)
     plan_prefill(plan, cu, kv, win, opts.q_block, opts.prefill_split,
-                 opts.prefill_dynamic == 0);
+                 opts.prefill_dynamic == 0, opts.prefill_grouping == 0);
 
   // Workspace: header, then the decode partials (two slots per decode CTA,
   // G x D fp32 each, plus G log2-sum-exps).

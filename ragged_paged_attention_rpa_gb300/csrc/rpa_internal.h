@@ -146,6 +146,7 @@ struct Plan {
   // Items in longest-first order, each taken by the next CTA to get free
   // (else CTA c runs its own list, pcta0).
   bool prefill_dynamic = false;
+  int32_t prefill_groups = 0;         // groups of the dynamic prefill list
   std::vector<PrefillItem> items;  // longest first, or per-CTA lists (pcta0)
   // Per-CTA item lists: CTA c runs items [pcta0[c], pcta0[c + 1]) in order;
   // empty: CTA c runs items c, c + grid, ... (a list too long for one launch).

@@ -666,3 +666,42 @@ def test_prefill_items_taken_dynamically_by_default(name):
     assert sp["prefill_split_items"] > 0 and sp["prefill_dynamic"] == 0
     if name != "mixed":
         assert plan_of(b, prefill_pairs=2).info()["prefill_dynamic"] == 0
+
+
+def test_dynamic_prefill_list_runs_in_l2_sized_groups():
+    """When every prefill sequence sees its whole prefix (no window shorter
+    than its KV), their K and V (kv_len x D x 2 x 2 bytes per (sequence, KV
+    head)) exceed 1.5 x 40 MiB and every pair is read by at least four items
+    on average, the dynamic list runs the pairs in ceil(total / 40 MiB)
+    groups of equal bytes (pair order), longest first within each group;
+    otherwise one group."""
+    def want(b):
+        ql = np.diff(b.cu_q_lens)
+        pre = [s for s in range(b.num_seqs) if ql[s] > 1]
+        per = [int(b.kv_lens[s]) * b.head_dim * 4 for s in pre for _ in range(b.num_kv_heads)]
+        total = float(sum(per))
+        items = len(prefill_items(b, plan_of(b).info()["q_block"])) * b.num_kv_heads
+        windowed = any(b.window is not None and 0 < int(b.window[s]) < int(b.kv_lens[s])
+                       for s in pre)
+        if windowed or not (total > 1.5 * 40 * 2**20 and items >= 4 * len(per)):
+            return 1
+        return max(1, -(-int(total) // (40 * 2**20)))
+    for name in ("causal_prefill", "swa_prefill", "mixed", "spec_decode"):
+        b = workloads.WORKLOADS[name](meta_only=True)
+        info = plan_of(b).info()
+        assert info["prefill_groups"] == want(b), name
+    # The causal 8k prefill: 16 heads x 8 MiB in four groups of four heads;
+    # the sliding-window one, the mixed batch's four chunks (24 MiB) and
+    # multi-token decode (one item per pair) in one.
+    assert plan_of(workloads.WORKLOADS["causal_prefill"](meta_only=True)).info()["prefill_groups"] == 4
+    assert plan_of(workloads.WORKLOADS["swa_prefill"](meta_only=True)).info()["prefill_groups"] == 1
+    assert plan_of(workloads.WORKLOADS["mixed"](meta_only=True)).info()["prefill_groups"] == 1
+    assert plan_of(workloads.WORKLOADS["spec_decode"](meta_only=True)).info()["prefill_groups"] == 1
+    # Fixed lists have no groups; prefill_grouping = -1 keeps one.
+    b = workloads.WORKLOADS["causal_prefill"](meta_only=True)
+    assert plan_of(b, prefill_dynamic=-1).info()["prefill_groups"] == 0
+    assert plan_of(b, prefill_grouping=-1).info()["prefill_groups"] == 1
+    for bad in (-2, 1):
+        with pytest.raises(RpaError) as e:
+            plan_of(b, prefill_grouping=bad)
+        assert e.value.status == binding.RPA_ERR_INVALID_ARG
