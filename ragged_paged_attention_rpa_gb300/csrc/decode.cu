@@ -130,7 +130,8 @@ __device__ __forceinline__ int swz(int row, int chunk) {
 // rows; K slot s, then V slot s at S slots further), for fp8 pages a per-warp
 // f16 copy of the V block being consumed, two Q tiles and the merge buffers.
 // K and V have slots of their own so that a block's K slot is refilled as
-// soon as its scores are out, before its V is used.
+// soon as its scores are out, before its V is used (fp8 pages: V is copied
+// out first, and both slots go back after the scores).
 template <int D, bool FP8>
 struct DecodeSmem {
   static constexpr int S = FP8 ? 4 : stages_for(D);
