@@ -296,6 +296,18 @@ def test_prefill_workloads_full(name):
     assert_bf16_close(got, oracle_rows(b), name)
 
 
+def test_prefill_l2_groups_change_order_not_bits():
+    """The causal 8k prefill's dynamic list in four L2-sized groups of KV
+    heads (the default) and longest first over all heads (prefill_grouping =
+    -1) give the same bits: the grouping only reorders whole items."""
+    b = workloads.WORKLOADS["causal_prefill"]()
+    grouped, err, plan = run_gpu(b)
+    assert err == 0 and plan.info()["prefill_groups"] == 4
+    flat, err, fplan = run_gpu(b, prefill_grouping=-1)
+    assert err == 0 and fplan.info()["prefill_groups"] == 1
+    assert np.array_equal(grouped, flat)
+
+
 @pytest.fixture(scope="module")
 def mixed_case():
     b = poisoned(workloads.mixed_batch(seed=4))
